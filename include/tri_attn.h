@@ -1,0 +1,131 @@
+/*
+ * tri_attn.h -- C ABI of libtriattn: the forward pass of starting-node
+ * triangular self-attention over a pair representation, on one GB300 GPU.
+ *
+ * Operation (POPCORNBENCH "Kimi-K2.6 l2_p6", forward op list steps 1-18, and
+ * "FW-GLM-5-1 l2_p6", the quoted reference Model.forward), for each cell
+ * (b, r, c) of the B x N x N pair grid with D channels, h heads, d = D / h:
+ *
+ *   x_hat = LayerNorm(pair_repr[b,r,c,:])            (eps 1e-5, biased variance)
+ *   q, k, v = Wq x_hat, Wk x_hat, Wv x_hat            (no bias)
+ *   g = sigmoid(Wg x_hat + bg)
+ *   bias[b,t,r,c] = (Wb x_hat)[t]                     (no bias; shared by all rows)
+ *   for each row i, head t, query j:
+ *     l_k = q[b,i,j,t].k[b,i,k,t] / sqrt(d) + bias[b,t,j,k]
+ *     l_k = -1e9 where the mask drops key k           (replacement, not addition)
+ *     o[b,i,j,t] = sum_k softmax_k(l) v[b,i,k,t]
+ *   out[b,i,j,:] = Wo (g * o) + bo                    (dropout is the identity)
+ *
+ * Mask readings (the pages disagree; both are offered):
+ *   TRI_ATTN_MASK_ROW_KEY   key k of row i is dropped when pair_mask[b,i,k] == 0
+ *   TRI_ATTN_MASK_QUERY_KEY key k of query j is dropped when pair_mask[b,j,k] == 0
+ *                           (the quoted code's broadcast of pair_mask over rows i)
+ * A softmax row whose keys are all dropped gets the uniform weight 1/N.
+ *
+ * Conventions for every entry point:
+ *   - Tensors are dense, row-major (C order), of the element type given by
+ *     `dtype` (float for TRI_ATTN_F32, bfloat16 for TRI_ATTN_BF16); pair_mask is
+ *     int32 with any nonzero entry meaning "keep". Linear weights use the
+ *     nn.Linear layout (out_features, in_features).
+ *   - Device pointers are addresses in the current CUDA context's device memory,
+ *     16-byte aligned. `stream` is a cudaStream_t (NULL = legacy default stream).
+ *   - Status codes are returned; nothing aborts, throws or traps across the ABI.
+ *     Errors detected on the device (a bounded wait that ran out, a failed
+ *     bounds check) are recorded in the handle and reported by
+ *     tri_attn_sync_check.
+ *   - A handle may be used from one stream at a time: its workspace is shared
+ *     by all calls.
+ */
+#ifndef TRI_ATTN_H
+#define TRI_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct tri_attn_s* tri_attn_t;
+
+enum { TRI_ATTN_F32 = 0, TRI_ATTN_BF16 = 1 };
+enum { TRI_ATTN_MASK_ROW_KEY = 0, TRI_ATTN_MASK_QUERY_KEY = 1 };
+
+enum {
+  TRI_ATTN_OK = 0,
+  TRI_ATTN_ERR_INVALID_ARG = 1,    /* bad pointer, shape, alignment or handle       */
+  TRI_ATTN_ERR_UNSUPPORTED = 2,    /* valid but not built (e.g. bf16 with D != 128) */
+  TRI_ATTN_ERR_CUDA = 3,           /* a CUDA runtime call failed                     */
+  TRI_ATTN_ERR_OOM = 4,            /* device allocation failed                       */
+  TRI_ATTN_ERR_DEVICE_TIMEOUT = 5, /* a kernel's bounded wait ran out                */
+  TRI_ATTN_ERR_DEVICE_CHECK = 6    /* a kernel's own bounds/alignment check failed   */
+};
+
+/* Build a handle for one problem shape and one set of weights.
+ *
+ * B, N, D, h: batch, pair-grid side, channels, heads; D % h == 0. Supported:
+ *   TRI_ATTN_F32  any B, N >= 1, D <= 256 with d = D/h <= 64;
+ *   TRI_ATTN_BF16 the tensor-core path: D == 128, h in {4} (d == 32), any B, N >= 1.
+ *   Other shapes return TRI_ATTN_ERR_UNSUPPORTED (there is no fallback path).
+ * mask_mode: TRI_ATTN_MASK_ROW_KEY or TRI_ATTN_MASK_QUERY_KEY (see above).
+ * Weights (device pointers, element type `dtype`), nn.Linear layout:
+ *   ln_gamma, ln_beta [D]; Wq, Wk, Wv, Wg [D][D]; bg [D]; Wb [h][D]; Wo [D][D]; bo [D].
+ *   Which Linear carries a bias follows the layer definitions on
+ *   "Kimi-K2.6 l2_p6": gate and out_proj do; query, key, value and bias_proj
+ *   do not.
+ * The weights are copied and repacked into memory the handle owns, on `stream`,
+ * and the call synchronises `stream` before returning, so the caller may free
+ * its weight buffers afterwards. The handle also owns the workspace for the
+ * intermediates (q, k, v, g, the bias plane and the attention output).
+ * On success *out receives the handle; on failure *out is NULL and nothing
+ * is leaked. */
+int tri_attn_create(tri_attn_t* out, int B, int N, int D, int h, int dtype, int mask_mode,
+                    const void* ln_gamma, const void* ln_beta,
+                    const void* Wq, const void* Wk, const void* Wv,
+                    const void* Wg, const void* bg, const void* Wb,
+                    const void* Wo, const void* bo, void* stream);
+
+/* One forward pass, asynchronous on `stream`; allocates nothing.
+ *
+ * pair_repr: device (B, N, N, D) of the handle's dtype, 16-byte aligned.
+ * pair_mask: device (B, N, N) int32, nonzero = keep.
+ * out:       device (B, N, N, D) of the handle's dtype; must not overlap the inputs.
+ * The inputs must stay valid until the stream work completes. Argument and
+ * launch errors are returned at once; device-side errors surface through
+ * tri_attn_sync_check. */
+int tri_attn_forward(tri_attn_t t, void* stream, const void* pair_repr,
+                     const int32_t* pair_mask, void* out);
+
+/* The same forward pass on HOST buffers: copies pair_repr and pair_mask to the
+ * device (into staging buffers the handle owns; allocated at the first call),
+ * runs the forward pass and copies the result back into `out_host`, all on
+ * `stream`, then synchronises `stream` and reports device-side errors like
+ * tri_attn_sync_check. Host buffers should be page-locked for full copy speed;
+ * pageable memory works but copies synchronously. */
+int tri_attn_forward_host(tri_attn_t t, void* stream, const void* pair_repr_host,
+                          const int32_t* pair_mask_host, void* out_host);
+
+/* Synchronise `stream`, then report any error the handle's kernels recorded on
+ * the device since the last check (and clear it). */
+int tri_attn_sync_check(tri_attn_t t, void* stream);
+
+/* Release everything the handle owns. The caller must make sure no work that
+ * uses the handle is still running. NULL is accepted. */
+int tri_attn_destroy(tri_attn_t t);
+
+/* Human-readable name of a status code (static storage). */
+const char* tri_attn_status_string(int status);
+
+/* Bytes of device memory a handle of this shape owns (weights + workspace). */
+int tri_attn_workspace_bytes(int B, int N, int D, int h, int dtype, size_t* bytes);
+
+/* Test hook: cap every bounded device-side wait of this handle's kernels at
+ * `spins` polls (0 restores the default of about one second). A cap of 1
+ * makes the first wait that is not already complete give up, so the timeout
+ * path can be exercised without hanging the GPU. */
+int tri_attn_set_wait_limit(tri_attn_t t, long long spins);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TRI_ATTN_H */

@@ -1,0 +1,56 @@
+// Shared declarations of the CUDA library: the handle, device error codes and
+// the kernel launchers of each path.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/tri_attn.h"
+
+// Codes written into the handle's device error word (bitwise OR of causes).
+#define TRI_DEV_ERR_TIMEOUT 1u
+#define TRI_DEV_ERR_CHECK 2u
+
+// Default cap of a bounded spin-wait, in polls (each poll is a try_wait with a
+// hardware suspend hint, so this is on the order of a second).
+#define TRI_DEFAULT_WAIT_LIMIT (1ll << 24)
+
+struct tri_attn_s {
+  int B, N, D, h, d, dtype, mask_mode;
+  long long cells;                 // B * N * N
+  int device;
+  // Packed weights (owned).
+  void* w_proj;                    // f32: [D][4D+h] (in, out); bf16: [n_proj_pad][D] (out, in)
+  void* w_out;                     // f32: [D][D] (in, out);    bf16: [D][D] (out, in)
+  float* gamma; float* beta; float* bg; float* bo;   // fp32 copies
+  float* wb_f32;                   // bf16 path: Wb as fp32 [h][D]
+  // Workspace (owned).
+  void* q; void* k; void* v; void* g; void* o;       // [cells][D], handle dtype
+  float* bias;                     // [B][h][N][N]
+  unsigned int* dev_err;           // device error word
+  long long wait_limit;
+  // Host-buffer staging (forward_host), allocated on first use.
+  void* stage_x; int32_t* stage_mask; void* stage_out;
+  // Tensor-core path state (opaque to the f32 path).
+  void* tc;
+  size_t bytes_owned;
+};
+
+size_t tri_elem_size(int dtype);
+
+// ---- fp32 SIMT path (kernels_f32.cu)
+cudaError_t tri_f32_pack_weights(tri_attn_s* t, const void* Wq, const void* Wk, const void* Wv,
+                                 const void* Wg, const void* Wb, const void* Wo,
+                                 cudaStream_t s);
+cudaError_t tri_f32_forward(tri_attn_s* t, cudaStream_t s, const float* x,
+                            const int32_t* mask, float* out);
+
+// ---- bf16 tensor-core path (kernels_tc.cu)
+bool tri_tc_supported(int B, int N, int D, int h);
+cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const void* Wv,
+                        const void* Wg, const void* Wb, const void* Wo, cudaStream_t s);
+void tri_tc_release(tri_attn_s* t);
+cudaError_t tri_tc_forward(tri_attn_s* t, cudaStream_t s, const void* x,
+                           const int32_t* mask, void* out);
+size_t tri_tc_extra_bytes(int B, int N, int D, int h);

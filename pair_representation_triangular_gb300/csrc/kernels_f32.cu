@@ -1,0 +1,260 @@
+// fp32 SIMT path of starting-node triangular self-attention.
+//
+// Three kernels, in the split of the "Kimi-K2.6 l2_p6" POPCORNBENCH page
+// (preprocess / attention / finalize), written for fp32 accuracy rather than
+// tensor-core throughput:
+//   ln_proj_f32    LayerNorm + the five projections of every cell, gate sigmoid,
+//                  pair bias scattered to its (B, h, N, N) plane;
+//   row_attn_f32   per (row i, head, 128 queries): logits with the shared pair
+//                  bias, mask replacement by -1e9, online softmax over keys
+//                  staged 32 at a time, P.V;
+//   gate_out_f32   g * o followed by the output projection and its bias.
+#include <math.h>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int kCellsPerBlock = 32;   // cells per block in the two projection kernels
+constexpr int kProjThreads = 256;
+constexpr int kQueriesPerBlock = 128;
+constexpr int kKeyChunk = 32;
+
+// Transpose-pack W (rows x D, nn.Linear layout) into dst[e * ld + col0 + r].
+__global__ void pack_transpose_f32(const float* __restrict__ W, int rows, int D,
+                                   float* __restrict__ dst, int ld, int col0) {
+  int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= rows * D) return;
+  int r = idx / D, e = idx % D;
+  dst[(size_t)e * ld + col0 + r] = W[idx];
+}
+
+// LayerNorm ("FW-GLM-5-1 l2_p6", self.layer_norm) and the concatenated
+// projection [Wq|Wk|Wv|Wg|Wb] ("Kimi-K2.6 l2_p6", op list steps 1-3 and 5-7).
+__global__ void __launch_bounds__(kProjThreads)
+ln_proj_f32(const float* __restrict__ x, long long cells, int N, int D, int h,
+            const float* __restrict__ gamma, const float* __restrict__ beta,
+            const float* __restrict__ Wt,      // [D][4D + h]
+            const float* __restrict__ bg,
+            float* __restrict__ q, float* __restrict__ k, float* __restrict__ v,
+            float* __restrict__ g, float* __restrict__ bias) {
+  extern __shared__ float xs[];            // [kCellsPerBlock][D]
+  const long long cell0 = (long long)blockIdx.x * kCellsPerBlock;
+  const int ncell = (int)min((long long)kCellsPerBlock, cells - cell0);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  for (int idx = tid; idx < kCellsPerBlock * D; idx += kProjThreads) {
+    int c = idx / D;
+    xs[idx] = (c < ncell) ? x[(cell0 + c) * D + (idx % D)] : 0.f;
+  }
+  __syncthreads();
+
+  // Mean and biased variance over D, eps 1e-5 inside the square root.
+  for (int c = warp; c < kCellsPerBlock; c += kProjThreads / 32) {
+    float* row = xs + c * D;
+    float s = 0.f;
+    for (int e = lane; e < D; e += 32) s += row[e];
+    for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    const float mean = s / D;
+    float ss = 0.f;
+    for (int e = lane; e < D; e += 32) { float t = row[e] - mean; ss += t * t; }
+    for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float rstd = 1.0f / sqrtf(ss / D + 1e-5f);
+    for (int e = lane; e < D; e += 32) row[e] = (row[e] - mean) * rstd * gamma[e] + beta[e];
+  }
+  __syncthreads();
+
+  const int nout = 4 * D + h;
+  const long long NN = (long long)N * N;
+  for (int o = tid; o < nout; o += kProjThreads) {
+    float acc[kCellsPerBlock];
+#pragma unroll
+    for (int c = 0; c < kCellsPerBlock; ++c) acc[c] = 0.f;
+    for (int e = 0; e < D; ++e) {
+      const float w = Wt[(size_t)e * nout + o];
+#pragma unroll
+      for (int c = 0; c < kCellsPerBlock; ++c) acc[c] = fmaf(xs[c * D + e], w, acc[c]);
+    }
+    const int sect = o / D, col = o % D;
+    if (sect < 4) {
+      float* dst = sect == 0 ? q : sect == 1 ? k : sect == 2 ? v : g;
+      const float add = sect == 3 ? bg[col] : 0.f;
+#pragma unroll
+      for (int c = 0; c < kCellsPerBlock; ++c) {
+        float val = acc[c];
+        if (sect == 3) val = 1.0f / (1.0f + expf(-(val + add)));
+        if (c < ncell) dst[(cell0 + c) * D + col] = val;
+      }
+    } else {
+      const int t = o - 4 * D;
+#pragma unroll
+      for (int c = 0; c < kCellsPerBlock; ++c) {
+        const long long cell = cell0 + c;
+        const long long b = cell / NN;
+        if (c < ncell) bias[(b * h + t) * NN + (cell - b * NN)] = acc[c];   // bias[b, t, r, c]
+      }
+    }
+  }
+}
+
+// Row attention ("Kimi-K2.6 l2_p6", op list steps 8-16): block = (128 queries
+// j, head t, row (b, i)); one thread per query, keys in chunks of KC.
+template <int MAXD, int KC>
+__global__ void __launch_bounds__(kQueriesPerBlock)
+row_attn_f32(const float* __restrict__ q, const float* __restrict__ k,
+             const float* __restrict__ v, const float* __restrict__ bias,
+             const int32_t* __restrict__ mask, int mask_mode,
+             int N, int D, int h, int d, float* __restrict__ o) {
+  __shared__ float Ks[KC][MAXD];
+  __shared__ float Vs[KC][MAXD];
+  __shared__ float Bs[kQueriesPerBlock][KC + 1];
+  __shared__ unsigned char Ms[kQueriesPerBlock][KC + 1];
+  __shared__ int Mrow[KC];
+
+  const int tid = threadIdx.x;
+  const long long row = blockIdx.x;              // b * N + i
+  const int t = blockIdx.y;
+  const long long b = row / N;
+  const int j0 = blockIdx.z * kQueriesPerBlock;
+  const int j = j0 + tid;
+  const bool active = j < N;
+  const long long NN = (long long)N * N;
+  const float scale = 1.0f / sqrtf((float)d);
+
+  float qv[MAXD], acc[MAXD];
+#pragma unroll
+  for (int e = 0; e < MAXD; ++e) {
+    qv[e] = (active && e < d) ? q[(row * N + j) * D + t * d + e] : 0.f;
+    acc[e] = 0.f;
+  }
+  float m = -INFINITY, l = 0.f;
+
+  for (int k0 = 0; k0 < N; k0 += KC) {
+    const int nk = min(KC, N - k0);
+    __syncthreads();
+    for (int idx = tid; idx < KC * MAXD; idx += kQueriesPerBlock) {
+      const int kk = idx / MAXD, e = idx % MAXD;
+      const bool in = kk < nk && e < d;
+      const long long src = (row * N + k0 + kk) * D + t * d + e;
+      Ks[kk][e] = in ? k[src] : 0.f;
+      Vs[kk][e] = in ? v[src] : 0.f;
+    }
+    for (int idx = tid; idx < kQueriesPerBlock * KC; idx += kQueriesPerBlock) {
+      const int jj = idx / KC, kk = idx % KC;
+      const bool in = (j0 + jj) < N && kk < nk;
+      Bs[jj][kk] = in ? bias[(b * h + t) * NN + (long long)(j0 + jj) * N + k0 + kk] : 0.f;
+      if (mask_mode == TRI_ATTN_MASK_QUERY_KEY)
+        Ms[jj][kk] = (in && mask[b * NN + (long long)(j0 + jj) * N + k0 + kk] != 0) ? 1 : 0;
+    }
+    if (mask_mode == TRI_ATTN_MASK_ROW_KEY && tid < KC)
+      Mrow[tid] = tid < nk ? mask[row * N + k0 + tid] : 0;
+    __syncthreads();
+
+#pragma unroll 1
+    for (int kk = 0; kk < nk; ++kk) {
+      float dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < MAXD; ++e) dot = fmaf(qv[e], Ks[kk][e], dot);
+      float lg = dot * scale + Bs[tid][kk];
+      const int keep = mask_mode == TRI_ATTN_MASK_ROW_KEY ? Mrow[kk] : Ms[tid][kk];
+      if (!keep) lg = -1e9f;                      // replacement by -1e9
+      if (lg > m) {                               // running maximum moved: rescale
+        const float alpha = expf(m - lg);         // exp(-inf) = 0 before the first key
+        l *= alpha;
+#pragma unroll
+        for (int e = 0; e < MAXD; ++e) acc[e] *= alpha;
+        m = lg;
+      }
+      const float p = expf(lg - m);
+      l += p;
+#pragma unroll
+      for (int e = 0; e < MAXD; ++e) acc[e] = fmaf(p, Vs[kk][e], acc[e]);
+    }
+  }
+  if (active) {
+    const float inv = 1.0f / l;
+#pragma unroll
+    for (int e = 0; e < MAXD; ++e)
+      if (e < d) o[(row * N + j) * D + t * d + e] = acc[e] * inv;
+  }
+}
+
+// Gate and output projection ("Kimi-K2.6 l2_p6", op list steps 17-18).
+__global__ void __launch_bounds__(kProjThreads)
+gate_out_f32(const float* __restrict__ g, const float* __restrict__ o, long long cells, int D,
+             const float* __restrict__ Wot,     // [D][D] (in, out)
+             const float* __restrict__ bo, float* __restrict__ out) {
+  extern __shared__ float as[];               // [kCellsPerBlock][D]
+  const long long cell0 = (long long)blockIdx.x * kCellsPerBlock;
+  const int ncell = (int)min((long long)kCellsPerBlock, cells - cell0);
+  for (int idx = threadIdx.x; idx < kCellsPerBlock * D; idx += kProjThreads) {
+    const int c = idx / D;
+    const long long src = (cell0 + c) * D + (idx % D);
+    as[idx] = (c < ncell) ? g[src] * o[src] : 0.f;
+  }
+  __syncthreads();
+  for (int col = threadIdx.x; col < D; col += kProjThreads) {
+    float acc[kCellsPerBlock];
+#pragma unroll
+    for (int c = 0; c < kCellsPerBlock; ++c) acc[c] = 0.f;
+    for (int e = 0; e < D; ++e) {
+      const float w = Wot[(size_t)e * D + col];
+#pragma unroll
+      for (int c = 0; c < kCellsPerBlock; ++c) acc[c] = fmaf(as[c * D + e], w, acc[c]);
+    }
+    const float add = bo[col];
+#pragma unroll
+    for (int c = 0; c < kCellsPerBlock; ++c)
+      if (c < ncell) out[(cell0 + c) * D + col] = acc[c] + add;
+  }
+}
+
+}  // namespace
+
+cudaError_t tri_f32_pack_weights(tri_attn_s* t, const void* Wq, const void* Wk, const void* Wv,
+                                 const void* Wg, const void* Wb, const void* Wo,
+                                 cudaStream_t s) {
+  const int D = t->D, h = t->h, nout = 4 * D + h;
+  float* wp = (float*)t->w_proj;
+  const void* mats[5] = {Wq, Wk, Wv, Wg, Wb};
+  for (int m = 0; m < 5; ++m) {
+    const int rows = m < 4 ? D : h;
+    const int n = rows * D;
+    pack_transpose_f32<<<(n + 255) / 256, 256, 0, s>>>((const float*)mats[m], rows, D, wp, nout,
+                                                       m * D);
+  }
+  pack_transpose_f32<<<(D * D + 255) / 256, 256, 0, s>>>((const float*)Wo, D, D,
+                                                         (float*)t->w_out, D, 0);
+  return cudaGetLastError();
+}
+
+cudaError_t tri_f32_forward(tri_attn_s* t, cudaStream_t s, const float* x,
+                            const int32_t* mask, float* out) {
+  const long long cells = t->cells;
+  const int D = t->D, h = t->h, d = t->d, N = t->N;
+  const unsigned nblk = (unsigned)((cells + kCellsPerBlock - 1) / kCellsPerBlock);
+  const size_t smem = (size_t)kCellsPerBlock * D * sizeof(float);
+  float *q = (float*)t->q, *k = (float*)t->k, *v = (float*)t->v, *g = (float*)t->g,
+        *o = (float*)t->o;
+  ln_proj_f32<<<nblk, kProjThreads, smem, s>>>(x, cells, N, D, h, t->gamma, t->beta,
+                                               (const float*)t->w_proj, t->bg, q, k, v, g,
+                                               t->bias);
+  dim3 grid((unsigned)(t->B * (long long)N), h, (N + kQueriesPerBlock - 1) / kQueriesPerBlock);
+#define TRI_ATTN_F32_CASE(MD)                                                              \
+  case MD:                                                                                 \
+    row_attn_f32<MD, (MD >= 128 ? 16 : kKeyChunk)><<<grid, kQueriesPerBlock, 0, s>>>(q, k, v, t->bias, mask, t->mask_mode, \
+                                                       N, D, h, d, o);                     \
+    break;
+  const int md = d <= 8 ? 8 : d <= 16 ? 16 : d <= 32 ? 32 : d <= 64 ? 64 : 128;
+  switch (md) {
+    TRI_ATTN_F32_CASE(8)
+    TRI_ATTN_F32_CASE(16)
+    TRI_ATTN_F32_CASE(32)
+    TRI_ATTN_F32_CASE(64)
+    TRI_ATTN_F32_CASE(128)
+  }
+#undef TRI_ATTN_F32_CASE
+  gate_out_f32<<<nblk, kProjThreads, smem, s>>>(g, o, cells, D, (const float*)t->w_out, t->bo,
+                                                out);
+  return cudaGetLastError();
+}

@@ -1,0 +1,78 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every entry point
+declared in include/tri_attn.h, and rejects bad arguments before touching CUDA.
+Also checks that the product package never reaches the CPU oracle."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from pair_representation_triangular_gb300 import binding as tb
+from pair_representation_triangular_gb300 import build as tbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tbuild.build()
+    return tb.load_library()
+
+
+def test_exports_every_declared_entry_point(lib):
+    names = tb.exported_names()
+    assert "tri_attn_create" in names and "tri_attn_forward" in names
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in include/tri_attn.h but not exported"
+
+
+def test_status_strings(lib):
+    assert tb.tri_attn_status_string(tb.TRI_ATTN_OK) == "ok"
+    assert "timed out" in tb.tri_attn_status_string(tb.TRI_ATTN_ERR_DEVICE_TIMEOUT)
+    assert tb.tri_attn_status_string(99) == "unknown status"
+
+
+def _create(lib, B, N, D, h, dtype, mode=0, ptr=16, out=True):
+    handle = ctypes.c_void_p()
+    args = [ctypes.byref(handle) if out else None, B, N, D, h, dtype, mode] + [ptr] * 10 + [None]
+    return lib.tri_attn_create(*args)
+
+
+def test_create_rejects_bad_arguments_before_cuda(lib):
+    assert _create(lib, 1, 8, 64, 4, 0, out=False) == tb.TRI_ATTN_ERR_INVALID_ARG
+    assert _create(lib, 1, 8, 65, 4, 0) == tb.TRI_ATTN_ERR_INVALID_ARG      # D % h
+    assert _create(lib, 0, 8, 64, 4, 0) == tb.TRI_ATTN_ERR_INVALID_ARG      # B < 1
+    assert _create(lib, 1, 0, 64, 4, 0) == tb.TRI_ATTN_ERR_INVALID_ARG      # N < 1
+    assert _create(lib, 1, 8, 64, 4, 7) == tb.TRI_ATTN_ERR_INVALID_ARG      # dtype
+    assert _create(lib, 1, 8, 64, 4, 0, mode=3) == tb.TRI_ATTN_ERR_INVALID_ARG
+    assert _create(lib, 1, 8, 64, 4, 0, ptr=0) == tb.TRI_ATTN_ERR_INVALID_ARG  # NULL weights
+    assert _create(lib, 1, 8, 64, 4, 0, ptr=24) == tb.TRI_ATTN_ERR_INVALID_ARG  # misaligned
+    assert _create(lib, 1, 8, 512, 4, 0) == tb.TRI_ATTN_ERR_UNSUPPORTED     # f32 D > 256
+    assert _create(lib, 1, 8, 96, 4, 1) == tb.TRI_ATTN_ERR_UNSUPPORTED      # bf16 needs D=128
+
+
+def test_null_handle_calls(lib):
+    assert lib.tri_attn_forward(None, None, 16, 16, 16) == tb.TRI_ATTN_ERR_INVALID_ARG
+    assert lib.tri_attn_forward_host(None, None, 16, 16, 16) == tb.TRI_ATTN_ERR_INVALID_ARG
+    assert lib.tri_attn_sync_check(None, None) == tb.TRI_ATTN_ERR_INVALID_ARG
+    assert lib.tri_attn_set_wait_limit(None, 5) == tb.TRI_ATTN_ERR_INVALID_ARG
+    assert lib.tri_attn_destroy(None) == tb.TRI_ATTN_OK
+
+
+def test_workspace_bytes(lib):
+    n = tb.tri_attn_workspace_bytes(2, 32, 64, 4, tb.TRI_ATTN_F32)
+    cells = 2 * 32 * 32
+    assert n >= 5 * cells * 64 * 4 + 2 * 4 * 32 * 32 * 4
+    with pytest.raises(tb.TriAttnError):
+        tb.tri_attn_workspace_bytes(2, 32, 65, 4, tb.TRI_ATTN_F32)
+
+
+def test_product_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "pair_representation_triangular_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                with open(os.path.join(dirpath, f)) as fh:
+                    src = fh.read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), f
+                assert "tri_attn_oracle" not in src, f
