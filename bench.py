@@ -1,0 +1,398 @@
+"""Benchmark: forward passes of starting-node triangular self-attention on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step is one full forward pass (LayerNorm + projections, row attention, gate +
+output projection) over one batch of seeded synthetic input, the default being
+the B=1, N=768, D=128, h=4 bf16 workload with a padded-sequence mask (700 of 768
+residues kept). Prints one JSON line (rank 0).
+
+value      pair-cells/s = B*N^2 / (device time per forward), inputs resident in
+           HBM, L2 flushed (256 MB write) before every timed step.
+e2e        the same metric through tri_attn_forward_host: pageable->pinned
+           host buffers are reused; every step copies pair_repr and pair_mask
+           host->device and the output device->host inside the timed region.
+roofline   the dominant kernel (largest share of device time) against its
+           algorithmic bytes or FLOPs per launch.
+cpu_baseline  the CPU oracle (fp64 numpy) on a bounded sample of the same
+           workload, timed on this host's cores.
+
+--impl reference times the CPU oracle alone (the reference arm of this
+benchmark) and prints the same JSON line with "impl": "reference".
+Under torchrun every rank runs its own independent forward passes (weak
+scaling over independent problems, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "b1-n768-d128-h4-bf16-pad700"
+METRIC = "pair-cells/s per forward (B*N^2/s)"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--mask-mode", type=int, default=0)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ workload math
+def algorithmic_work(w):
+    """Per-kernel algorithmic FLOPs and HBM bytes of one forward (bf16 path):
+    K1 reads x and writes q, k, v, g (bf16) and the fp32 bias plane; K2 reads
+    q, k, v, the bias plane and the mask, writes o; K3 reads g and o, writes out."""
+    P, D, h, N, B = w.cells, w.D, w.h, w.N, w.B
+    s = 2 if w.dtype == "bf16" else 4
+    return {
+        "ln_proj": {"flops": 2.0 * P * D * (4 * D + h),
+                    "bytes": P * D * s + 4 * P * D * s + 4 * P * h},
+        "row_attn": {"flops": 4.0 * B * N ** 3 * D,
+                     "bytes": 3 * P * D * s + 4 * P * h + 4 * P + P * D * s},
+        "gate_out": {"flops": 2.0 * P * D * D, "bytes": 3 * P * D * s},
+    }
+
+
+def kernel_key(name: str) -> str:
+    for k in ("ln_proj", "row_attn", "gate_out"):
+        if name.startswith(k):
+            return k
+    return name
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
+        sm = [float(r[1]) for r in self.rows if len(r) > 2 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) > 2 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = []
+        for r in self.rows:
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active" and n not in reasons:
+                    reasons.append(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+# ------------------------------------------------------------------ CPU oracle baseline
+def _oracle_rows_worker(args):
+    """Rows of the oracle forward in a spawned worker (single-threaded BLAS)."""
+    x_rows, mask, params, h, rows, mode, bias_b = args
+    import numpy as np
+    import oracle.tri_attn_oracle as O
+    P = {k: np.asarray(v, np.float64) for k, v in params.items()}
+    out = []
+    for n, (b, i) in enumerate(rows):
+        x_hat = O.layer_norm(np.asarray(x_rows[n], np.float64), P["gamma"], P["beta"])
+        q, k, v, g, _ = O.project(x_hat, P)
+        keep = O.keep_matrix(mask, b, i, mode)
+        o = O.row_attention(q, k, v, bias_b, keep, h)
+        out.append(O.output_projection(g, o, P))
+    return len(out)
+
+
+def _oracle_bias_worker(args):
+    x_cells, params, = args
+    import numpy as np
+    import oracle.tri_attn_oracle as O
+    P = {k: np.asarray(v, np.float64) for k, v in params.items()}
+    x_hat = O.layer_norm(np.asarray(x_cells, np.float64), P["gamma"], P["beta"])
+    return O.linear(x_hat, P["Wb"])
+
+
+def cpu_oracle_sample(w, inp, mode, budget_s=20.0, cores=None):
+    """Time the oracle on this host: the full bias plane (every cell) plus as many
+    rows as fit in about `budget_s`, spread over `cores` spawned processes; the
+    full-forward time is extrapolated from the per-row time. Returns the JSON
+    object of the baseline."""
+    import numpy as np
+    cores = cores or os.cpu_count() or 1
+    env_keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+    saved = {k: os.environ.get(k) for k in env_keys}
+    for k in env_keys:
+        os.environ[k] = "1"
+    ctx = mp.get_context("spawn")
+    B, N = w.B, w.N
+    try:
+        with ctx.Pool(cores) as pool:
+            t0 = time.perf_counter()
+            xs = inp["x"].reshape(B * N, N, w.D)
+            parts = pool.map(_oracle_bias_worker, [(xs[r], inp["params"]) for r in range(B * N)],
+                             chunksize=max(1, (B * N) // (4 * cores)))
+            bias = np.stack(parts).reshape(B, N, N, w.h).transpose(0, 3, 1, 2)
+            t_bias = time.perf_counter() - t0
+            # rows: one per worker first to measure, then as many as the budget allows
+            rows_all = [(b, i) for b in range(B) for i in range(N)]
+            done = 0
+            t_rows = 0.0
+            batch = cores
+            while done < len(rows_all):
+                chunk = rows_all[done:done + batch]
+                jobs = [((inp["x"][b, i],), inp["pair_mask"], inp["params"], w.h, [(b, i)], mode,
+                         bias[b]) for b, i in chunk]
+                jobs = [(j[0], j[1], j[2], j[3], j[4], j[5], j[6]) for j in jobs]
+                t1 = time.perf_counter()
+                pool.map(_oracle_rows_worker, jobs, chunksize=1)
+                t_rows += time.perf_counter() - t1
+                done += len(chunk)
+                if t_bias + t_rows > budget_s:
+                    break
+                batch = min(len(rows_all) - done, max(cores, int(done * (budget_s - t_bias - t_rows)
+                                                                  / max(t_rows, 1e-9) * 0.5)))
+                batch = max(batch, 1)
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    t_full = t_bias + t_rows * (len(rows_all) / done)
+    value = B * N * N / t_full
+    return {"value": value, "unit": "pair-cells/s", "cores": cores, "kind": "oracle",
+            "sample": (f"fp64 numpy oracle, {cores} spawned single-thread processes: full bias "
+                       f"plane ({B * N * N} cells, {t_bias:.2f} s) + {done} of {len(rows_all)} "
+                       f"rows ({t_rows:.2f} s); full-forward time extrapolated linearly "
+                       f"in rows: {t_full:.1f} s")}
+
+
+# ------------------------------------------------------------------ native arm
+def run_native(args, rank, world):
+    import numpy as np
+    import torch
+    from pair_representation_triangular_gb300 import binding as tb
+    from pair_representation_triangular_gb300 import build as tbuild
+    from pair_representation_triangular_gb300 import workloads as W
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    tbuild.build()
+    tb.load_library()
+    w = W.WORKLOADS[args.workload]
+    inp = W.make_inputs(w)
+    td = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    dt = tb.TRI_ATTN_BF16 if w.dtype == "bf16" else tb.TRI_ATTN_F32
+    params = {k: torch.from_numpy(v).to(dev, td) for k, v in inp["params"].items()}
+    x = torch.from_numpy(inp["x"]).to(dev, td)
+    m = torch.from_numpy(inp["pair_mask"]).to(dev)
+    out = torch.empty_like(x)
+    mod = tb.TriangularAttention(w.B, w.N, w.D, w.h, dt, args.mask_mode, params)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    tb.tri_attn_enable_kernel_timing(mod.handle, True)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        mod.forward(x, m, out)
+    st = mod.sync_check()
+    if st != tb.TRI_ATTN_OK:
+        raise RuntimeError(f"warm-up forward failed: {tb.tri_attn_status_string(st)}")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    kernel_ms = {}
+    launches = 0
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        for s in range(args.steps):
+            flush.fill_(float(s))                       # evict L2 (outside the timed pair)
+            ev[s][0].record(stream)
+            mod.forward(x, m, out)
+            ev[s][1].record(stream)
+            for name, ms in tb.tri_attn_kernel_times(mod.handle):
+                kernel_ms.setdefault(name, []).append(ms)
+                launches += 1
+        torch.cuda.synchronize(dev)
+    barrier()
+    st = mod.sync_check()
+    if st != tb.TRI_ATTN_OK:
+        raise RuntimeError(f"timed forward failed: {tb.tri_attn_status_string(st)}")
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms_total = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_per_step = ms_total / args.steps
+    value = world * w.cells / (ms_per_step / 1e3)
+
+    # e2e: host buffers through the C ABI (copies inside the timed region)
+    tb.tri_attn_enable_kernel_timing(mod.handle, False)
+    xh = torch.from_numpy(inp["x"]).to(td).pin_memory()
+    mh = torch.from_numpy(inp["pair_mask"]).pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    mod.forward_host(xh, mh, oh)
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        mod.forward_host(xh, mh, oh)
+    e2e_s = (time.perf_counter() - t0) / args.e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    h2d = xh.numel() * xh.element_size() + mh.numel() * mh.element_size()
+    d2h = oh.numel() * oh.element_size()
+
+    # roofline of the dominant kernel
+    work = algorithmic_work(w)
+    avg = {k: sum(v) / len(v) for k, v in kernel_ms.items()}
+    total = sum(avg.values())
+    top = max(avg, key=avg.get)
+    kw = work[kernel_key(top)]
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+        peak_src = "measured"
+    except OSError:
+        peak_src = "fallback"
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    tflops = peaks.get("bf16_tflops", 1900.0)
+    t_s = avg[top] / 1e3
+    t_bytes = kw["bytes"] / (hbm * 1e9)
+    t_flops = kw["flops"] / (tflops * 1e12)
+    if t_flops >= t_bytes:
+        roof = {"bound": "tensor", "achieved": kw["flops"] / t_s / 1e12, "peak": tflops,
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": kw["bytes"] / t_s / 1e9, "peak": hbm, "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = top
+    roof["peak_source"] = peak_src + " (burst)"
+    roof["traffic"] = None
+    roof["kernel_ms"] = {k: round(v, 5) for k, v in avg.items()}
+    roof["kernel_share"] = {k: round(v / total, 4) for k, v in avg.items()}
+    roof["kernel_roofline_frac"] = {}
+    for k, v in avg.items():
+        kk = work[kernel_key(k)]
+        t_roof = max(kk["bytes"] / (hbm * 1e9), kk["flops"] / (tflops * 1e12))
+        roof["kernel_roofline_frac"][k] = round(t_roof / (v / 1e3), 4)
+
+    result = {
+        "metric": METRIC, "value": value, "unit": "pair-cells/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "B": w.B, "N": w.N, "D": w.D, "h": w.h,
+                   "mask_mode": "row-key" if args.mask_mode == 0 else "query-key",
+                   "l2": "flushed (256 MB write) before each timed step; x is 151 MB",
+                   "parallelism": f"{world} independent problems, one per GPU"},
+        "e2e": {"value": world * w.cells / e2e_s, "unit": "pair-cells/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "roofline": roof,
+        "clocks": clk.summary(),
+    }
+    mod.close()
+    return result, w, inp
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        from pair_representation_triangular_gb300 import workloads as W
+        w = W.WORKLOADS[args.workload]
+        inp = W.make_inputs(w)
+        vals = []
+        base = None
+        for s in range(args.warmup + args.steps):
+            budget = 2.0 if s < args.warmup else max(2.0, 150.0 / max(args.steps, 1))
+            r = cpu_oracle_sample(w, inp, args.mask_mode, budget_s=budget)
+            if s >= args.warmup:
+                vals.append(r["value"])
+                base = r
+        value = statistics.mean(vals)
+        base["value"] = value
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": value, "unit": "pair-cells/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": w.cells / value * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "B": w.B, "N": w.N, "D": w.D, "h": w.h},
+            "cpu_baseline": base,
+            "e2e": {"value": value, "unit": "pair-cells/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+        }))
+        return
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    result, w, inp = run_native(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            result["cpu_baseline"] = cpu_oracle_sample(w, inp, args.mask_mode, budget_s=20.0)
+        print(json.dumps(result))
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -119,6 +119,19 @@ const char* tri_attn_status_string(int status);
 /* Bytes of device memory a handle of this shape owns (weights + workspace). */
 int tri_attn_workspace_bytes(int B, int N, int D, int h, int dtype, size_t* bytes);
 
+/* Per-kernel timing. With `enable` nonzero, every later tri_attn_forward records
+ * a CUDA event on its stream before its first kernel and after each kernel
+ * (events the handle owns; a few microseconds of stream work per forward).
+ * tri_attn_kernel_times then reports the duration of each kernel of the most
+ * recent forward. */
+int tri_attn_enable_kernel_timing(tri_attn_t t, int enable);
+
+/* Durations (milliseconds) of the kernels of the most recent forward, in launch
+ * order; waits for that forward to finish. On entry *n is the capacity of `ms`
+ * (and of `names`, which may be NULL); on return it is the number of kernels
+ * (0 when timing is off or nothing ran). names[i] receives a static string. */
+int tri_attn_kernel_times(tri_attn_t t, float* ms, const char** names, int* n);
+
 /* Test hook: cap every bounded device-side wait of this handle's kernels at
  * `spins` polls (0 restores the default of about one second). A cap of 1
  * makes the first wait that is not already complete give up, so the timeout

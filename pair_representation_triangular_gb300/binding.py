@@ -71,9 +71,13 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.tri_attn_status_string.restype = ctypes.c_char_p
     lib.tri_attn_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_size_t)]
     lib.tri_attn_set_wait_limit.argtypes = [vp, i64]
+    lib.tri_attn_enable_kernel_timing.argtypes = [vp, i32]
+    lib.tri_attn_kernel_times.argtypes = [vp, ctypes.POINTER(ctypes.c_float),
+                                          ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(i32)]
     for name in ("tri_attn_create", "tri_attn_forward", "tri_attn_forward_host",
                  "tri_attn_sync_check", "tri_attn_destroy", "tri_attn_workspace_bytes",
-                 "tri_attn_set_wait_limit"):
+                 "tri_attn_set_wait_limit", "tri_attn_enable_kernel_timing",
+                 "tri_attn_kernel_times"):
         getattr(lib, name).restype = i32
     if path == library_path():
         _lib = lib
@@ -145,6 +149,22 @@ def tri_attn_destroy(handle) -> None:
 
 def tri_attn_set_wait_limit(handle, spins: int) -> None:
     _check(load_library().tri_attn_set_wait_limit(handle, spins), "tri_attn_set_wait_limit")
+
+
+def tri_attn_enable_kernel_timing(handle, enable: bool) -> None:
+    _check(load_library().tri_attn_enable_kernel_timing(handle, int(enable)),
+           "tri_attn_enable_kernel_timing")
+
+
+def tri_attn_kernel_times(handle) -> list:
+    """[(kernel name, ms), ...] for the most recent forward of the handle."""
+    cap = 8
+    ms = (ctypes.c_float * cap)()
+    names = (ctypes.c_char_p * cap)()
+    n = ctypes.c_int(cap)
+    _check(load_library().tri_attn_kernel_times(handle, ms, names, ctypes.byref(n)),
+           "tri_attn_kernel_times")
+    return [(names[i].decode(), float(ms[i])) for i in range(n.value)]
 
 
 class TriangularAttention:

@@ -35,7 +35,21 @@ struct tri_attn_s {
   // Tensor-core path state (opaque to the f32 path).
   void* tc;
   size_t bytes_owned;
+  // Optional per-kernel timing: events recorded around each kernel of a forward.
+  int timing;
+  int n_marks;
+  cudaEvent_t marks[8];
+  const char* mark_names[8];
 };
+
+// Record timing mark `idx` (0 = before the first kernel; idx > 0 = after the
+// kernel named `name`) when kernel timing is enabled on the handle.
+inline void tri_mark(tri_attn_s* t, cudaStream_t s, int idx, const char* name) {
+  if (!t->timing || idx >= 8) return;
+  cudaEventRecord(t->marks[idx], s);
+  t->mark_names[idx] = name;
+  t->n_marks = idx + 1;
+}
 
 size_t tri_elem_size(int dtype);
 

@@ -236,9 +236,11 @@ cudaError_t tri_f32_forward(tri_attn_s* t, cudaStream_t s, const float* x,
   const size_t smem = (size_t)kCellsPerBlock * D * sizeof(float);
   float *q = (float*)t->q, *k = (float*)t->k, *v = (float*)t->v, *g = (float*)t->g,
         *o = (float*)t->o;
+  tri_mark(t, s, 0, nullptr);
   ln_proj_f32<<<nblk, kProjThreads, smem, s>>>(x, cells, N, D, h, t->gamma, t->beta,
                                                (const float*)t->w_proj, t->bg, q, k, v, g,
                                                t->bias);
+  tri_mark(t, s, 1, "ln_proj_f32");
   dim3 grid((unsigned)(t->B * (long long)N), h, (N + kQueriesPerBlock - 1) / kQueriesPerBlock);
 #define TRI_ATTN_F32_CASE(MD)                                                              \
   case MD:                                                                                 \
@@ -254,7 +256,9 @@ cudaError_t tri_f32_forward(tri_attn_s* t, cudaStream_t s, const float* x,
     TRI_ATTN_F32_CASE(128)
   }
 #undef TRI_ATTN_F32_CASE
+  tri_mark(t, s, 2, "row_attn_f32");
   gate_out_f32<<<nblk, kProjThreads, smem, s>>>(g, o, cells, D, (const float*)t->w_out, t->bo,
                                                 out);
+  tri_mark(t, s, 3, "gate_out_f32");
   return cudaGetLastError();
 }

@@ -1,13 +1,1010 @@
-// bf16 tensor-core path (placeholder until the tcgen05 kernels land).
-#include "common.cuh"
+// bf16 tensor-core path of starting-node triangular self-attention (sm_103a).
+//
+// Three kernels, each built on tcgen05 MMAs with operands staged by TMA in
+// swizzled shared memory and accumulators in tensor memory (TMEM):
+//
+//   ln_proj_tc   LayerNorm as the prologue of one concatenated projection GEMM
+//                x_hat [128 cells x 128] . [Wq|Wk|Wv|Wg]^T -> 512 TMEM columns;
+//                the epilogue writes q, k, v and sigmoid(g + bg) in bf16; the
+//                h pair-bias outputs (Wb x_hat) are computed on the CUDA cores
+//                from the same bf16 x_hat and written, scaled by log2(e), to
+//                the fp32 bias plane (B, h, N, Nb).
+//   row_attn_tc  flash-style row attention: a CTA owns (b, head t, 128 queries
+//                j, R rows i) and streams 64-key tiles; per tile S = Q K^T goes
+//                to TMEM, two softmax warpgroups add the shared pair bias
+//                (one smem tile serves all R rows), apply the key mask, run an
+//                online softmax in registers and write P (bf16) to smem;
+//                O_tile = P V goes to TMEM and is folded into a register
+//                accumulator. The (B, N, h, N, N) logits never exist.
+//   gate_out_tc  g * o formed in shared memory as the A operand of the output
+//                projection GEMM; the epilogue adds bo and stores bf16.
+//
+// Passages followed: POPCORNBENCH "Kimi-K2.6 l2_p6", forward op list steps
+// 1-18 and layer definitions; "FW-GLM-5-1 l2_p6", quoted Model.forward.
+#include <math.h>
+#include <stdio.h>
 
-bool tri_tc_supported(int, int, int, int) { return false; }
-size_t tri_tc_extra_bytes(int, int, int, int) { return 0; }
-cudaError_t tri_tc_init(tri_attn_s*, const void*, const void*, const void*, const void*,
-                        const void*, const void*, cudaStream_t) {
-  return cudaErrorNotSupported;
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------------------
+// Shared helpers
+// ---------------------------------------------------------------------------
+
+struct Abort {
+  int* flag;              // shared-memory flag: nonzero once any role gave up
+  unsigned int* dev_err;  // handle's device error word
+  long long polls;        // poll cap of ordinary waits
+};
+
+// Bounded wait; on time-out or when another role has already aborted, raises
+// the abort flag (and records a time-out) and returns false.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const Abort& a) {
+  if (tc::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = tc::global_timer_ns();
+  for (long long n = 1; n < a.polls; ++n) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if (*(volatile int*)a.flag) return false;
+    if ((n & 255) == 0 && tc::global_timer_ns() - t0 > 2000000000ull) break;
+  }
+  *(volatile int*)a.flag = 1;
+  atomicOr(a.dev_err, TRI_DEV_ERR_TIMEOUT);
+  return false;
 }
-void tri_tc_release(tri_attn_s*) {}
-cudaError_t tri_tc_forward(tri_attn_s*, cudaStream_t, const void*, const int32_t*, void*) {
-  return cudaErrorNotSupported;
+
+// Warp-uniform form for warps that go on to issue warp-collective tcgen05
+// loads: every lane waits, and the warp proceeds only if all lanes succeeded.
+__device__ __forceinline__ bool warp_wait_or_abort(uint64_t* bar, uint32_t parity, const Abort& a) {
+  const bool ok = wait_or_abort(bar, parity, a);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Drain wait used at teardown: ignores the abort flag and the poll cap so that
+// copies and MMAs still in flight land before the CTA releases its memory.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  tc::mbar_wait(bar, parity, 1ll << 40);
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
+}
+
+// ---------------------------------------------------------------------------
+// K1: LayerNorm + concatenated projection
+// ---------------------------------------------------------------------------
+namespace k1 {
+constexpr int BM = 128;                 // cells per tile
+constexpr int KD = 128;                 // channels (GEMM K)
+constexpr int NQ = 512;                 // q|k|v|g columns
+constexpr int kThreads = 192;           // warps 0-3 LN + epilogue, 4 TMA, 5 MMA
+constexpr uint32_t W_BYTES = NQ * KD * 2;           // 128 KB, two K-halves of 64 KB
+constexpr uint32_t X_BYTES = BM * KD * 2;           // 32 KB, two K-halves of 16 KB
+constexpr uint32_t OFF_W = 0;
+constexpr uint32_t OFF_X = OFF_W + W_BYTES;
+constexpr uint32_t OFF_PAR = OFF_X + 2 * X_BYTES;   // gamma, beta, bg [128] + Wb [4][128] fp32
+constexpr uint32_t PAR_BYTES = (3 * KD + 4 * KD) * 4;
+constexpr uint32_t OFF_BAR = OFF_PAR + PAR_BYTES;
+constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;     // + alignment slack
+
+struct Bars {
+  uint64_t w_full, x_full[2], x_empty[2], a_ready[2], tmem_full, tmem_empty, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct Params {
+  long long cells;
+  int N, Nb, h, mask_mode, ntiles;
+  const float* gamma; const float* beta; const float* bg; const float* wb;   // fp32
+  const int32_t* mask;
+  __nv_bfloat16 *q, *k, *v, *g;
+  float* bias;                 // (B, h, N, Nb), scaled by log2(e)
+  unsigned int* dev_err;
+  long long polls;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+           const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  Bars* bars = (Bars*)(smem + OFF_BAR);
+  float* s_gamma = (float*)(smem + OFF_PAR);
+  float* s_beta = s_gamma + KD;
+  float* s_bg = s_beta + KD;
+  float* s_wb = s_bg + KD;                 // [4][128]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const Abort ab{&bars->abort, p.dev_err, p.polls};
+
+  if (tid == 0) {
+    tc::mbar_init(&bars->w_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&bars->x_full[b], 1);
+      tc::mbar_init(&bars->x_empty[b], 1);
+      tc::mbar_init(&bars->a_ready[b], 128);
+    }
+    tc::mbar_init(&bars->tmem_full, 1);
+    tc::mbar_init(&bars->tmem_empty, 128);
+    tc::mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    tc::fence_mbar_init();
+  }
+  for (int i = tid; i < KD; i += kThreads) {
+    s_gamma[i] = p.gamma[i];
+    s_beta[i] = p.beta[i];
+    s_bg[i] = p.bg[i];
+  }
+  for (int i = tid; i < 4 * KD; i += kThreads) s_wb[i] = i < p.h * KD ? p.wb[i] : 0.f;
+  if (warp == 5) {
+    tc::tmem_alloc(&bars->tmem_base, 512);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const int ntiles = p.ntiles;
+  int my_tiles = 0;
+  for (int t = blockIdx.x; t < ntiles; t += gridDim.x) ++my_tiles;
+  int issued = 0;                          // tile loads issued (producer thread)
+
+  if (warp == 4) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&map_x);
+      tc::tma_prefetch_desc(&map_w);
+      tc::mbar_arrive_expect_tx(&bars->w_full, W_BYTES);
+      for (int kh = 0; kh < 2; ++kh)
+        for (int nh = 0; nh < 2; ++nh)
+          tc::tma_load_2d(smem + OFF_W + kh * 65536 + nh * 32768, &map_w, &bars->w_full,
+                          kh * 64, nh * 256);
+      for (int it = 0; it < my_tiles; ++it) {
+        const int b = it & 1;
+        if (it >= 2 && !wait_or_abort(&bars->x_empty[b], ((it >> 1) - 1) & 1, ab)) break;
+        const int tile = blockIdx.x + it * gridDim.x;
+        uint8_t* xs = smem + OFF_X + b * X_BYTES;
+        tc::mbar_arrive_expect_tx(&bars->x_full[b], X_BYTES);
+        tc::tma_load_2d(xs, &map_x, &bars->x_full[b], 0, tile * BM);
+        tc::tma_load_2d(xs + 16384, &map_x, &bars->x_full[b], 64, tile * BM);
+        issued = it + 1;
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 256, 0, 0);
+      const uint32_t w0 = tc::smem_addr(smem + OFF_W);
+      bool ok = wait_or_abort(&bars->w_full, 0, ab);
+      for (int it = 0; ok && it < my_tiles; ++it) {
+        const int b = it & 1;
+        if (!wait_or_abort(&bars->a_ready[b], (it >> 1) & 1, ab)) break;
+        if (it >= 1 && !wait_or_abort(&bars->tmem_empty, (it - 1) & 1, ab)) break;
+        tc::tc_fence_after();
+        const uint32_t a0 = tc::smem_addr(smem + OFF_X + b * X_BYTES);
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
+          const uint64_t ad = tc::smem_desc(a0 + ko, 16, 1024, tc::SWZ_128B);
+          for (int nh = 0; nh < 2; ++nh) {
+            const uint64_t bd = tc::smem_desc(w0 + (ks >> 2) * 65536 + nh * 32768 + (ks & 3) * 32,
+                                              16, 1024, tc::SWZ_128B);
+            tc::mma_bf16_ss(tmem + nh * 256, ad, bd, idesc, ks > 0);
+          }
+        }
+        tc::mma_commit(&bars->tmem_full);
+        tc::mma_commit(&bars->x_empty[b]);
+      }
+      tc::mma_commit(&bars->drain);
+      drain_wait(&bars->drain, 0);
+    }
+  } else {
+    // ---------------- LayerNorm + bias (prologue) and epilogue: thread = cell row
+    const int r = tid;                      // 0..127, TMEM lane r
+    const long long NN = (long long)p.N * p.N;
+    auto epilogue = [&](int it) -> bool {
+      if (!warp_wait_or_abort(&bars->tmem_full, it & 1, ab)) return false;
+      tc::tc_fence_after();
+      const int tile = blockIdx.x + it * gridDim.x;
+      const long long cell = (long long)tile * BM + r;
+      const bool valid = cell < p.cells;
+#pragma unroll 1
+      for (int ch = 0; ch < 16; ++ch) {
+        uint32_t acc[32];
+        tc::tmem_ld32(tc::tmem_addr(tmem, (warp & 3) * 32, ch * 32), acc);
+        tc::tmem_ld_wait();
+        const int sect = ch >> 2, col0 = (ch & 3) * 32;
+        uint32_t packed[16];
+        if (sect == 3) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float z0 = __uint_as_float(acc[2 * e]) + s_bg[col0 + 2 * e];
+            const float z1 = __uint_as_float(acc[2 * e + 1]) + s_bg[col0 + 2 * e + 1];
+            packed[e] = tc::pack_bf16x2(1.0f / (1.0f + __expf(-z0)), 1.0f / (1.0f + __expf(-z1)));
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            packed[e] = tc::pack_bf16x2(__uint_as_float(acc[2 * e]), __uint_as_float(acc[2 * e + 1]));
+        }
+        if (valid) {
+          __nv_bfloat16* base = sect == 0 ? p.q : sect == 1 ? p.k : sect == 2 ? p.v : p.g;
+          uint4* dst = (uint4*)(base + cell * KD + col0);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
+        }
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(&bars->tmem_empty);
+      return true;
+    };
+    bool ok = true;
+    for (int it = 0; ok && it < my_tiles; ++it) {
+      const int b = it & 1;
+      if (!warp_wait_or_abort(&bars->x_full[b], (it >> 1) & 1, ab)) { ok = false; break; }
+      const int tile = blockIdx.x + it * gridDim.x;
+      const long long cell = (long long)tile * BM + r;
+      uint8_t* xs = smem + OFF_X + b * X_BYTES;
+      // Row r of the tile: 16 chunks of 8 bf16, chunk c in K-half c/8 at a swizzled slot.
+      float xv[KD];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint4 u = *(const uint4*)(xs + (c >> 3) * 16384 + tc::swz_offset(r, c & 7, 128));
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          xv[c * 8 + 2 * e] = bf16_lo(w4[e]);
+          xv[c * 8 + 2 * e + 1] = bf16_hi(w4[e]);
+        }
+      }
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < KD; ++e) s += xv[e];
+      const float mean = s * (1.0f / KD);
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < KD; ++e) { const float d = xv[e] - mean; ss = fmaf(d, d, ss); }
+      const float rstd = rsqrtf(ss * (1.0f / KD) + 1e-5f);
+      float bsum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i0 = c * 8 + 2 * e;
+          const float y0 = (xv[i0] - mean) * rstd * s_gamma[i0] + s_beta[i0];
+          const float y1 = (xv[i0 + 1] - mean) * rstd * s_gamma[i0 + 1] + s_beta[i0 + 1];
+          w4[e] = tc::pack_bf16x2(y0, y1);
+          const float r0 = bf16_lo(w4[e]), r1 = bf16_hi(w4[e]);
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            bsum[t] = fmaf(r1, s_wb[t * KD + i0 + 1], fmaf(r0, s_wb[t * KD + i0], bsum[t]));
+        }
+        *(uint4*)(xs + (c >> 3) * 16384 + tc::swz_offset(r, c & 7, 128)) =
+            make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      }
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&bars->a_ready[b]);
+      if (cell < p.cells) {
+        const long long bb = cell / NN;
+        const long long rc = cell - bb * NN;
+        const long long rr = rc / p.N, cc = rc - rr * p.N;
+        bool keep = true;
+        if (p.mask_mode == TRI_ATTN_MASK_QUERY_KEY) keep = p.mask[cell] != 0;
+        for (int t = 0; t < p.h; ++t)
+          p.bias[((bb * p.h + t) * p.N + rr) * p.Nb + cc] = keep ? bsum[t] * kLog2e : -INFINITY;
+      }
+      if (it >= 1 && !epilogue(it - 1)) { ok = false; break; }
+    }
+    if (ok && my_tiles > 0) epilogue(my_tiles - 1);
+  }
+
+  // ---------------- teardown: every issued copy lands, every MMA completes
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 4 && lane == 0) {
+    drain_wait(&bars->w_full, 0);
+    for (int it = issued - 1; it >= 0 && it >= issued - 2; --it)
+      drain_wait(&bars->x_full[it & 1], (it >> 1) & 1);
+  }
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == 5) tc::tmem_dealloc(tmem, 512);
+}
+}  // namespace k1
+
+
+// ---------------------------------------------------------------------------
+// K2: flash row attention
+// ---------------------------------------------------------------------------
+namespace k2 {
+constexpr int R = 4;                    // rows i per CTA (share each bias tile)
+constexpr int BQ = 128;                 // queries j per CTA
+constexpr int BK = 64;                  // keys per tile
+constexpr int DH = 32;                  // head dim
+constexpr int STAGES = 2;
+constexpr int MAXW = 256;               // mask words per row (N <= 8192)
+constexpr int kThreads = 320;           // warp 0 TMA, 1 MMA, 2-5 softmax WG0, 6-9 WG1
+constexpr uint32_t Q_BYTES = BQ * DH * 2;          // 8 KB
+constexpr uint32_t KV_BYTES = BK * DH * 2;         // 4 KB each of K and V
+constexpr uint32_t BIAS_BYTES = BQ * BK * 4;       // 32 KB (two 16 KB boxes of 32 keys)
+constexpr uint32_t P_BYTES = BQ * BK * 2;          // 16 KB
+constexpr uint32_t OFF_Q = 0;
+constexpr uint32_t OFF_KV = OFF_Q + R * Q_BYTES;                 // [stage][r] K then V
+constexpr uint32_t STAGE_KV = R * 2 * KV_BYTES;
+constexpr uint32_t OFF_BIAS = OFF_KV + STAGES * STAGE_KV;
+constexpr uint32_t OFF_P = OFF_BIAS + STAGES * BIAS_BYTES;
+constexpr uint32_t OFF_MASK = OFF_P + 2 * P_BYTES;
+constexpr uint32_t OFF_BAR = OFF_MASK + R * MAXW * 4 + 64;
+constexpr uint32_t SMEM = OFF_BAR + 512 + 1024;
+
+struct Bars {
+  uint64_t q_full, kv_full[STAGES], kv_empty[STAGES];
+  uint64_t s_ready[2], s_free[2], p_full[2], p_free[2], o_ready[2], o_free[2], drain;
+  uint32_t tmem_base;
+  int abort;
+  int row_any[R];
+};
+
+struct Params {
+  int B, N, h, mask_mode, row_groups;
+  const int32_t* mask;
+  const unsigned char* q_any;     // mode query-key: per (b, j) any kept key
+  __nv_bfloat16* o;
+  unsigned int* dev_err;
+  long long polls;
+  float scale_log2;               // log2(e) / sqrt(d)
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+            const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_b,
+            const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  Bars* bars = (Bars*)(smem + OFF_BAR);
+  uint32_t* mbits = (uint32_t*)(smem + OFF_MASK);       // [R][MAXW]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const Abort ab{&bars->abort, p.dev_err, p.polls};
+
+  const int N = p.N;
+  const int rg = blockIdx.x % p.row_groups;
+  const int b = blockIdx.x / p.row_groups;
+  const int t = blockIdx.y;
+  const int j0 = blockIdx.z * BQ;
+  const int i0 = rg * R;
+  const int KT = (N + BK - 1) / BK;
+  const int nitems = KT * R;
+
+  if (tid == 0) {
+    tc::mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(&bars->kv_full[s], 1);
+      tc::mbar_init(&bars->kv_empty[s], 1);
+    }
+    for (int w = 0; w < 2; ++w) {
+      tc::mbar_init(&bars->s_ready[w], 1);
+      tc::mbar_init(&bars->s_free[w], 128);
+      tc::mbar_init(&bars->p_full[w], 128);
+      tc::mbar_init(&bars->p_free[w], 1);
+      tc::mbar_init(&bars->o_ready[w], 1);
+      tc::mbar_init(&bars->o_free[w], 128);
+    }
+    tc::mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&bars->tmem_base, 256);
+    tc::tmem_relinquish();
+  }
+  // Key-mask bits of the R rows (row-key mode): bit k of row r = pair_mask[b, i0+r, k] != 0.
+  if (warp >= 2) {
+    const int W = 2 * KT;                   // words of whole 64-key tiles; bits k >= N are 0
+    for (int item = warp - 2; item < R * W; item += 8) {
+      const int r = item / W, wd = item % W;
+      const int i = i0 + r, k = wd * 32 + lane;
+      bool keep = false;
+      if (p.mask_mode == TRI_ATTN_MASK_ROW_KEY)
+        keep = i < N && k < N && p.mask[((long long)b * N + i) * N + k] != 0;
+      else
+        keep = k < N;                       // query-key mode: only padding keys drop here
+      const unsigned bits = __ballot_sync(0xffffffffu, keep);
+      if (lane == 0) mbits[r * MAXW + wd] = bits;
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (tid < R) {
+    const int W = 2 * KT;
+    unsigned any = 0;
+    for (int wd = 0; wd < W; ++wd) any |= mbits[tid * MAXW + wd];
+    bars->row_any[tid] = any != 0;
+  }
+  __syncthreads();
+  const uint32_t tmem = bars->tmem_base;
+  int issued_kt = 0;                        // producer: k-tiles whose loads were issued
+
+  if (warp == 0) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&map_q);
+      tc::tma_prefetch_desc(&map_k);
+      tc::tma_prefetch_desc(&map_v);
+      tc::tma_prefetch_desc(&map_b);
+      const int row0 = b * N + i0;
+      tc::mbar_arrive_expect_tx(&bars->q_full, R * Q_BYTES);
+      for (int r = 0; r < R; ++r)
+        tc::tma_load_3d(smem + OFF_Q + r * Q_BYTES, &map_q, &bars->q_full, t * DH, j0, row0 + r);
+      for (int kt = 0; kt < KT; ++kt) {
+        const int s = kt % STAGES;
+        if (kt >= STAGES && !wait_or_abort(&bars->kv_empty[s], ((kt / STAGES) - 1) & 1, ab)) break;
+        uint8_t* kv = smem + OFF_KV + s * STAGE_KV;
+        uint8_t* bs = smem + OFF_BIAS + s * BIAS_BYTES;
+        tc::mbar_arrive_expect_tx(&bars->kv_full[s], STAGE_KV + BIAS_BYTES);
+        for (int r = 0; r < R; ++r) {
+          tc::tma_load_3d(kv + r * 2 * KV_BYTES, &map_k, &bars->kv_full[s], t * DH, kt * BK, row0 + r);
+          tc::tma_load_3d(kv + r * 2 * KV_BYTES + KV_BYTES, &map_v, &bars->kv_full[s], t * DH,
+                          kt * BK, row0 + r);
+        }
+        tc::tma_load_3d(bs, &map_b, &bars->kv_full[s], kt * BK, j0, b * p.h + t);
+        tc::tma_load_3d(bs + 16384, &map_b, &bars->kv_full[s], kt * BK + 32, j0, b * p.h + t);
+        issued_kt = kt + 1;
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_qk = tc::idesc_bf16_f32(128, BK, 0, 0);
+      constexpr uint32_t id_pv = tc::idesc_bf16_f32(128, DH, 0, 1);
+      const uint32_t q0 = tc::smem_addr(smem + OFF_Q);
+      const uint32_t kv0 = tc::smem_addr(smem + OFF_KV);
+      const uint32_t p0 = tc::smem_addr(smem + OFF_P);
+      auto pv = [&](int m) -> bool {
+        const int km = m / R, rm = m % R, wm = m & 1, sm = km % STAGES, u = m >> 1;
+        if (!wait_or_abort(&bars->p_full[wm], u & 1, ab)) return false;
+        if (u >= 1 && !wait_or_abort(&bars->o_free[wm], (u - 1) & 1, ab)) return false;
+        tc::tc_fence_after();
+        const uint32_t vaddr = kv0 + sm * STAGE_KV + rm * 2 * KV_BYTES + KV_BYTES;
+        for (int ks = 0; ks < BK / 16; ++ks) {
+          const uint64_t ad = tc::smem_desc(p0 + wm * P_BYTES + ks * 32, 16, 1024, tc::SWZ_128B);
+          const uint64_t bd = tc::smem_desc(vaddr + ks * 1024, 16, 512, tc::SWZ_64B);
+          tc::mma_bf16_ss(tmem + 128 + wm * 32, ad, bd, id_pv, ks > 0);
+        }
+        tc::mma_commit(&bars->o_ready[wm]);
+        tc::mma_commit(&bars->p_free[wm]);
+        if (rm == R - 1) tc::mma_commit(&bars->kv_empty[sm]);
+        return true;
+      };
+      bool ok = wait_or_abort(&bars->q_full, 0, ab);
+      for (int n = 0; ok && n < nitems; ++n) {
+        const int kt = n / R, r = n % R, w = n & 1, s = kt % STAGES, u = n >> 1;
+        if (r == 0 && !wait_or_abort(&bars->kv_full[s], (kt / STAGES) & 1, ab)) { ok = false; break; }
+        if (u >= 1 && !wait_or_abort(&bars->s_free[w], (u - 1) & 1, ab)) { ok = false; break; }
+        tc::tc_fence_after();
+        const uint32_t kaddr = kv0 + s * STAGE_KV + r * 2 * KV_BYTES;
+        for (int ks = 0; ks < DH / 16; ++ks) {
+          const uint64_t ad = tc::smem_desc(q0 + r * Q_BYTES + ks * 32, 16, 512, tc::SWZ_64B);
+          const uint64_t bd = tc::smem_desc(kaddr + ks * 32, 16, 512, tc::SWZ_64B);
+          tc::mma_bf16_ss(tmem + w * BK, ad, bd, id_qk, ks > 0);
+        }
+        tc::mma_commit(&bars->s_ready[w]);
+        if (n >= 1 && !pv(n - 1)) { ok = false; break; }
+      }
+      if (ok && nitems > 0) pv(nitems - 1);
+      tc::mma_commit(&bars->drain);
+      drain_wait(&bars->drain, 0);
+    }
+  } else {
+    // ---------------- softmax warpgroups: WG w handles rows r = w and w + 2
+    const int w = (warp - 2) >> 2;
+    const int jr = (warp & 3) * 32 + lane;          // query row in the tile = TMEM lane
+    const int j = j0 + jr;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t s_col = tmem + lane_base + w * BK;
+    const uint32_t o_col = tmem + lane_base + 128 + w * 32;
+    uint8_t* p_buf = smem + OFF_P + w * P_BYTES;
+    bool uni_q = false;                               // query-key mode: query j keeps no key
+    if (p.mask_mode == TRI_ATTN_MASK_QUERY_KEY && j < N) uni_q = !p.q_any[(long long)b * N + j];
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    float oacc[2][DH];
+#pragma unroll
+    for (int lr = 0; lr < 2; ++lr)
+#pragma unroll
+      for (int e = 0; e < DH; ++e) oacc[lr][e] = 0.f;
+    float pend_alpha = 0.f;
+    bool ok = true;
+    int step = 0;                                     // items done by this WG (= u)
+
+    auto fold_pending = [&](int lr_p) -> bool {       // O_tile of item step-1 into oacc[lr_p]
+      const int u = step - 1;
+      if (!warp_wait_or_abort(&bars->o_ready[w], u & 1, ab)) return false;
+      tc::tc_fence_after();
+      uint32_t ov[32];
+      tc::tmem_ld32(o_col, ov);
+      tc::tmem_ld_wait();
+      tc::tc_fence_before();
+      tc::mbar_arrive(&bars->o_free[w]);
+#pragma unroll
+      for (int e = 0; e < DH; ++e)
+        oacc[lr_p][e] = fmaf(oacc[lr_p][e], pend_alpha, __uint_as_float(ov[e]));
+      return true;
+    };
+
+    for (int kt = 0; ok && kt < KT; ++kt) {
+      const int s = kt % STAGES;
+#pragma unroll
+      for (int lr = 0; lr < 2; ++lr) {
+        if (!ok) break;
+        const int r = w + 2 * lr;
+        const int u = step;
+        // S tile of item (kt, r)
+        if (!warp_wait_or_abort(&bars->s_ready[w], u & 1, ab)) { ok = false; break; }
+        tc::tc_fence_after();
+        uint32_t sv[BK];
+        tc::tmem_ld32(s_col, *(uint32_t(*)[32])&sv[0]);
+        tc::tmem_ld32(s_col + 32, *(uint32_t(*)[32])&sv[32]);
+        tc::tmem_ld_wait();
+        tc::tc_fence_before();
+        tc::mbar_arrive(&bars->s_free[w]);
+        if (!warp_wait_or_abort(&bars->kv_full[s], (kt / STAGES) & 1, ab)) { ok = false; break; }
+        const uint32_t bw0 = mbits[r * MAXW + 2 * kt], bw1 = mbits[r * MAXW + 2 * kt + 1];
+        const bool uni = uni_q || !bars->row_any[r];
+        float x[BK];
+        if (uni) {
+#pragma unroll
+          for (int k = 0; k < BK; ++k) x[k] = (kt * BK + k < N) ? 0.f : -INFINITY;
+        } else {
+          const uint8_t* bsm = smem + OFF_BIAS + s * BIAS_BYTES;
+#pragma unroll
+          for (int c = 0; c < BK / 4; ++c) {
+            const float4 bv = *(const float4*)(bsm + (c >> 3) * 16384 + tc::swz_offset(jr, c & 7, 128));
+            x[4 * c + 0] = fmaf(__uint_as_float(sv[4 * c + 0]), p.scale_log2, bv.x);
+            x[4 * c + 1] = fmaf(__uint_as_float(sv[4 * c + 1]), p.scale_log2, bv.y);
+            x[4 * c + 2] = fmaf(__uint_as_float(sv[4 * c + 2]), p.scale_log2, bv.z);
+            x[4 * c + 3] = fmaf(__uint_as_float(sv[4 * c + 3]), p.scale_log2, bv.w);
+          }
+          if ((bw0 & bw1) != 0xffffffffu) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              if (!((bw0 >> k) & 1u)) x[k] = -INFINITY;
+              if (!((bw1 >> k) & 1u)) x[32 + k] = -INFINITY;
+            }
+          }
+        }
+        float mt = x[0];
+#pragma unroll
+        for (int k = 1; k < BK; ++k) mt = fmaxf(mt, x[k]);
+        const float m_new = fmaxf(m_run[lr], mt);
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = ex2_approx(m_run[lr] - m_use);
+        m_run[lr] = m_new;
+        float rs = 0.f;
+        uint32_t pk[BK / 2];
+#pragma unroll
+        for (int k = 0; k < BK; k += 2) {
+          const float p0 = ex2_approx(x[k] - m_use), p1 = ex2_approx(x[k + 1] - m_use);
+          rs += p0 + p1;
+          pk[k / 2] = tc::pack_bf16x2(p0, p1);
+        }
+        l_run[lr] = fmaf(l_run[lr], alpha, rs);
+        // P (bf16) into smem buffer w once PV of this WG's previous item has read it.
+        if (u >= 1 && !warp_wait_or_abort(&bars->p_free[w], (u - 1) & 1, ab)) { ok = false; break; }
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *(uint4*)(p_buf + tc::swz_offset(jr, c, 128)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(&bars->p_full[w]);
+        // Fold the previous item's O tile (the other local row) while this PV runs.
+        if (step >= 1 && !fold_pending(1 - lr)) { ok = false; break; }
+        pend_alpha = alpha;
+        ++step;
+      }
+    }
+    if (ok && step >= 1) {
+      // The last item of this WG is local row 1 (R = 4 keeps the lr order 0,1,0,1,...).
+      ok = fold_pending(1);
+    }
+    if (ok && j < N) {
+#pragma unroll
+      for (int lr = 0; lr < 2; ++lr) {
+        const int i = i0 + w + 2 * lr;
+        if (i >= N) continue;
+        const float inv = 1.0f / l_run[lr];
+        uint32_t pk[DH / 2];
+#pragma unroll
+        for (int e = 0; e < DH; e += 2) pk[e / 2] = tc::pack_bf16x2(oacc[lr][e] * inv, oacc[lr][e + 1] * inv);
+        uint4* dst = (uint4*)(p.o + (((long long)b * N + i) * N + j) * (p.h * DH) + t * DH);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      }
+    }
+  }
+
+  // ---------------- teardown
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0 && lane == 0) {
+    drain_wait(&bars->q_full, 0);
+    for (int kt = issued_kt - 1; kt >= 0 && kt >= issued_kt - STAGES; --kt)
+      drain_wait(&bars->kv_full[kt % STAGES], (kt / STAGES) & 1);
+  }
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == 1) tc::tmem_dealloc(tmem, 256);
+}
+
+// Per (b, r): does row r of pair_mask[b] keep any key? (query-key mode)
+__global__ void mask_rows_any(const int32_t* __restrict__ mask, int N, long long rows,
+                              unsigned char* __restrict__ any) {
+  const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int lane = threadIdx.x & 31;
+  int found = 0;
+  for (int k = lane; k < N; k += 32) found |= mask[row * N + k] != 0;
+  found = __any_sync(0xffffffffu, found);
+  if (lane == 0) any[row] = (unsigned char)found;
+}
+}  // namespace k2
+
+
+// ---------------------------------------------------------------------------
+// K3: gate multiply (prologue) + output projection
+// ---------------------------------------------------------------------------
+namespace k3 {
+constexpr int BM = 128;
+constexpr int KD = 128;
+constexpr int kThreads = 192;           // warps 0-3 gate + epilogue, 4 TMA, 5 MMA
+constexpr uint32_t T_BYTES = BM * KD * 2;           // 32 KB tile (two K-halves)
+constexpr uint32_t OFF_W = 0;                       // Wo, 32 KB
+constexpr uint32_t OFF_G = OFF_W + T_BYTES;         // g tiles [2]; become the A operand
+constexpr uint32_t OFF_O = OFF_G + 2 * T_BYTES;     // o tiles [2]
+constexpr uint32_t OFF_BO = OFF_O + 2 * T_BYTES;    // bo fp32 [128]
+constexpr uint32_t OFF_BAR = OFF_BO + KD * 4;
+constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
+
+struct Bars {
+  uint64_t w_full, in_full[2], in_empty[2], a_ready[2], acc_full[2], acc_empty[2], drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct Params {
+  long long cells;
+  int ntiles;
+  const float* bo;
+  __nv_bfloat16* out;
+  unsigned int* dev_err;
+  long long polls;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+gate_out_tc(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUtensorMap map_o,
+            const __grid_constant__ CUtensorMap map_wo, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  Bars* bars = (Bars*)(smem + OFF_BAR);
+  float* s_bo = (float*)(smem + OFF_BO);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const Abort ab{&bars->abort, p.dev_err, p.polls};
+  if (tid == 0) {
+    tc::mbar_init(&bars->w_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&bars->in_full[b], 1);
+      tc::mbar_init(&bars->in_empty[b], 1);
+      tc::mbar_init(&bars->a_ready[b], 128);
+      tc::mbar_init(&bars->acc_full[b], 1);
+      tc::mbar_init(&bars->acc_empty[b], 128);
+    }
+    tc::mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    tc::fence_mbar_init();
+  }
+  for (int i = tid; i < KD; i += kThreads) s_bo[i] = p.bo[i];
+  if (warp == 5) {
+    tc::tmem_alloc(&bars->tmem_base, 256);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  int my_tiles = 0;
+  for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) ++my_tiles;
+  int issued = 0;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&map_g);
+      tc::tma_prefetch_desc(&map_o);
+      tc::tma_prefetch_desc(&map_wo);
+      tc::mbar_arrive_expect_tx(&bars->w_full, T_BYTES);
+      tc::tma_load_2d(smem + OFF_W, &map_wo, &bars->w_full, 0, 0);
+      tc::tma_load_2d(smem + OFF_W + 16384, &map_wo, &bars->w_full, 64, 0);
+      for (int it = 0; it < my_tiles; ++it) {
+        const int b = it & 1;
+        if (it >= 2 && !wait_or_abort(&bars->in_empty[b], ((it >> 1) - 1) & 1, ab)) break;
+        const int row = (blockIdx.x + it * gridDim.x) * BM;
+        uint8_t* gs = smem + OFF_G + b * T_BYTES;
+        uint8_t* os = smem + OFF_O + b * T_BYTES;
+        tc::mbar_arrive_expect_tx(&bars->in_full[b], 2 * T_BYTES);
+        tc::tma_load_2d(gs, &map_g, &bars->in_full[b], 0, row);
+        tc::tma_load_2d(gs + 16384, &map_g, &bars->in_full[b], 64, row);
+        tc::tma_load_2d(os, &map_o, &bars->in_full[b], 0, row);
+        tc::tma_load_2d(os + 16384, &map_o, &bars->in_full[b], 64, row);
+        issued = it + 1;
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 128, 0, 0);
+      const uint32_t w0 = tc::smem_addr(smem + OFF_W);
+      bool ok = wait_or_abort(&bars->w_full, 0, ab);
+      for (int it = 0; ok && it < my_tiles; ++it) {
+        const int b = it & 1;
+        if (!wait_or_abort(&bars->a_ready[b], (it >> 1) & 1, ab)) break;
+        if (it >= 2 && !wait_or_abort(&bars->acc_empty[b], ((it >> 1) - 1) & 1, ab)) break;
+        tc::tc_fence_after();
+        const uint32_t a0 = tc::smem_addr(smem + OFF_G + b * T_BYTES);
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
+          tc::mma_bf16_ss(tmem + b * 128, tc::smem_desc(a0 + ko, 16, 1024, tc::SWZ_128B),
+                          tc::smem_desc(w0 + ko, 16, 1024, tc::SWZ_128B), idesc, ks > 0);
+        }
+        tc::mma_commit(&bars->acc_full[b]);
+        tc::mma_commit(&bars->in_empty[b]);
+      }
+      tc::mma_commit(&bars->drain);
+      drain_wait(&bars->drain, 0);
+    }
+  } else {
+    const int r = tid;
+    auto epilogue = [&](int it) -> bool {
+      const int b = it & 1;
+      if (!warp_wait_or_abort(&bars->acc_full[b], (it >> 1) & 1, ab)) return false;
+      tc::tc_fence_after();
+      const long long cell = (long long)(blockIdx.x + it * gridDim.x) * BM + r;
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t acc[32];
+        tc::tmem_ld32(tc::tmem_addr(tmem, (warp & 3) * 32, b * 128 + ch * 32), acc);
+        tc::tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = tc::pack_bf16x2(__uint_as_float(acc[2 * e]) + s_bo[ch * 32 + 2 * e],
+                                  __uint_as_float(acc[2 * e + 1]) + s_bo[ch * 32 + 2 * e + 1]);
+        if (cell < p.cells) {
+          uint4* dst = (uint4*)(p.out + cell * KD + ch * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(&bars->acc_empty[b]);
+      return true;
+    };
+    bool ok = true;
+    for (int it = 0; ok && it < my_tiles; ++it) {
+      const int b = it & 1;
+      if (!warp_wait_or_abort(&bars->in_full[b], (it >> 1) & 1, ab)) { ok = false; break; }
+      uint8_t* gs = smem + OFF_G + b * T_BYTES;
+      const uint8_t* os = smem + OFF_O + b * T_BYTES;
+#pragma unroll 4
+      for (int c = 0; c < 16; ++c) {
+        const uint32_t off = (c >> 3) * 16384 + tc::swz_offset(r, c & 7, 128);
+        const uint4 gu = *(const uint4*)(gs + off);
+        const uint4 ou = *(const uint4*)(os + off);
+        const uint32_t ga[4] = {gu.x, gu.y, gu.z, gu.w}, oa[4] = {ou.x, ou.y, ou.z, ou.w};
+        uint32_t res[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          res[e] = tc::pack_bf16x2(bf16_lo(ga[e]) * bf16_lo(oa[e]), bf16_hi(ga[e]) * bf16_hi(oa[e]));
+        *(uint4*)(gs + off) = make_uint4(res[0], res[1], res[2], res[3]);
+      }
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&bars->a_ready[b]);
+      if (it >= 1 && !epilogue(it - 1)) { ok = false; break; }
+    }
+    if (ok && my_tiles > 0) epilogue(my_tiles - 1);
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 4 && lane == 0) {
+    drain_wait(&bars->w_full, 0);
+    for (int it = issued - 1; it >= 0 && it >= issued - 2; --it)
+      drain_wait(&bars->in_full[it & 1], (it >> 1) & 1);
+  }
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == 5) tc::tmem_dealloc(tmem, 256);
+}
+}  // namespace k3
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)f;
+  }
+  return fn;
+}
+
+// Tiled map over a row-major tensor of `rank` dims (dims[0] innermost).
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
+              const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box,
+              CUtensorMapSwizzle swz) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, dt, rank, const_cast<void*>(base), dims, strides_bytes, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool map_rows_bf16(CUtensorMap* m, const void* base, long long rows, int box_rows) {
+  cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// (B*N rows, N cells, 128 channels) bf16, box of one head (32 ch) x box_j cells.
+bool map_heads(CUtensorMap* m, const void* base, int B, int N, int box_j) {
+  cuuint64_t dims[3] = {128, (cuuint64_t)N, (cuuint64_t)B * N};
+  cuuint64_t strides[2] = {256, (cuuint64_t)N * 256};
+  cuuint32_t box[3] = {32, (cuuint32_t)box_j, 1};
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box,
+                  CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+struct TcState {
+  CUtensorMap map_w, map_q, map_k, map_v, map_b, map_g, map_o, map_wo;
+  unsigned char* q_any;
+  int num_sms;
+  int Nb;
+};
+
+int round_up(int a, int b) { return (a + b - 1) / b * b; }
+
+
+}  // namespace
+
+bool tri_tc_supported(int B, int N, int D, int h) {
+  const long long cells = (long long)B * N * N;
+  return D == 128 && h == 4 && N >= 1 && N <= k2::MAXW * 32 && cells < (1ll << 31) &&
+         (long long)B * N < (1ll << 31) / 8;
+}
+
+size_t tri_tc_extra_bytes(int B, int N, int, int h) {
+  // bias-plane row padding and the per-row mask summary
+  const size_t Nb = (size_t)round_up(N, 4);
+  return (size_t)B * h * N * (Nb - N) * sizeof(float) + (size_t)B * N + 256;
+}
+
+cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const void* Wv,
+                        const void* Wg, const void*, const void* Wo, cudaStream_t s) {
+  TcState* st = (TcState*)calloc(1, sizeof(TcState));
+  if (!st) return cudaErrorMemoryAllocation;
+  t->tc = st;
+  const int B = t->B, N = t->N, D = t->D, h = t->h;
+  st->Nb = round_up(N, 4);
+  cudaError_t e = cudaDeviceGetAttribute(&st->num_sms, cudaDevAttrMultiProcessorCount, t->device);
+  // The bias plane of the base workspace is (B, h, N, N); this path pads rows to Nb.
+  if (e == cudaSuccess && st->Nb != N) {
+    cudaFree(t->bias);
+    t->bias = nullptr;
+    e = cudaMalloc((void**)&t->bias, (size_t)B * h * N * st->Nb * sizeof(float));
+  }
+  if (e == cudaSuccess) e = cudaMalloc((void**)&st->q_any, (size_t)B * N);
+  const size_t wbytes = (size_t)D * D * 2;
+  const void* mats[4] = {Wq, Wk, Wv, Wg};
+  for (int m = 0; m < 4 && e == cudaSuccess; ++m)
+    e = cudaMemcpyAsync((char*)t->w_proj + m * wbytes, mats[m], wbytes, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(t->w_out, Wo, wbytes, cudaMemcpyDeviceToDevice, s);
+  if (e != cudaSuccess) return e;
+
+  const long long cells = t->cells;
+  bool ok = map_rows_bf16(&st->map_w, t->w_proj, 512, 256);
+  ok = ok && map_heads(&st->map_q, t->q, B, N, k2::BQ);
+  ok = ok && map_heads(&st->map_k, t->k, B, N, k2::BK);
+  ok = ok && map_heads(&st->map_v, t->v, B, N, k2::BK);
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)N, (cuuint64_t)B * h};
+    cuuint64_t strides[2] = {(cuuint64_t)st->Nb * 4, (cuuint64_t)N * st->Nb * 4};
+    cuuint32_t box[3] = {32, (cuuint32_t)k2::BQ, 1};
+    ok = ok && make_map(&st->map_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, t->bias, dims, strides,
+                        box, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  ok = ok && map_rows_bf16(&st->map_g, t->g, cells, 128);
+  ok = ok && map_rows_bf16(&st->map_o, t->o, cells, 128);
+  ok = ok && map_rows_bf16(&st->map_wo, t->w_out, 128, 128);
+  if (!ok) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(k1::ln_proj_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, k1::SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k2::row_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, k2::SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k3::gate_out_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, k3::SMEM);
+  return e;
+}
+
+void tri_tc_release(tri_attn_s* t) {
+  TcState* st = (TcState*)t->tc;
+  if (!st) return;
+  if (st->q_any) cudaFree(st->q_any);
+  free(st);
+  t->tc = nullptr;
+}
+
+cudaError_t tri_tc_forward(tri_attn_s* t, cudaStream_t s, const void* x, const int32_t* mask,
+                           void* out) {
+  TcState* st = (TcState*)t->tc;
+  const int B = t->B, N = t->N, h = t->h;
+  const long long cells = t->cells;
+  const int ntiles = (int)((cells + 127) / 128);
+  const int grid_rows = ntiles < st->num_sms ? ntiles : st->num_sms;
+  CUtensorMap map_x;
+  if (!map_rows_bf16(&map_x, x, cells, 128)) return cudaErrorInvalidValue;
+
+  k1::Params p1;
+  p1.cells = cells; p1.N = N; p1.Nb = st->Nb; p1.h = h; p1.mask_mode = t->mask_mode;
+  p1.ntiles = ntiles;
+  p1.gamma = t->gamma; p1.beta = t->beta; p1.bg = t->bg; p1.wb = t->wb_f32; p1.mask = mask;
+  p1.q = (__nv_bfloat16*)t->q; p1.k = (__nv_bfloat16*)t->k; p1.v = (__nv_bfloat16*)t->v;
+  p1.g = (__nv_bfloat16*)t->g; p1.bias = t->bias; p1.dev_err = t->dev_err;
+  p1.polls = t->wait_limit;
+  int mark = 0;
+  tri_mark(t, s, mark++, nullptr);
+  k1::ln_proj_tc<<<grid_rows, k1::kThreads, k1::SMEM, s>>>(map_x, st->map_w, p1);
+  tri_mark(t, s, mark++, "ln_proj_tc");
+
+  if (t->mask_mode == TRI_ATTN_MASK_QUERY_KEY) {
+    const long long rows = (long long)B * N;
+    k2::mask_rows_any<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(mask, N, rows, st->q_any);
+    tri_mark(t, s, mark++, "mask_rows_any");
+  }
+  k2::Params p2;
+  p2.B = B; p2.N = N; p2.h = h; p2.mask_mode = t->mask_mode;
+  p2.row_groups = (N + k2::R - 1) / k2::R;
+  p2.mask = mask; p2.q_any = st->q_any; p2.o = (__nv_bfloat16*)t->o; p2.dev_err = t->dev_err;
+  p2.polls = t->wait_limit;
+  p2.scale_log2 = kLog2e / sqrtf((float)t->d);
+  dim3 g2((unsigned)(B * p2.row_groups), h, (N + k2::BQ - 1) / k2::BQ);
+  k2::row_attn_tc<<<g2, k2::kThreads, k2::SMEM, s>>>(st->map_q, st->map_k, st->map_v, st->map_b, p2);
+  tri_mark(t, s, mark++, "row_attn_tc");
+
+  k3::Params p3;
+  p3.cells = cells; p3.ntiles = ntiles; p3.bo = t->bo; p3.out = (__nv_bfloat16*)out;
+  p3.dev_err = t->dev_err; p3.polls = t->wait_limit;
+  k3::gate_out_tc<<<grid_rows, k3::kThreads, k3::SMEM, s>>>(st->map_g, st->map_o, st->map_wo, p3);
+  tri_mark(t, s, mark++, "gate_out_tc");
+  return cudaGetLastError();
 }

@@ -31,6 +31,8 @@ cudaError_t to_f32(const void* src, int dtype, int n, float* dst, cudaStream_t s
 void free_all(tri_attn_s* t) {
   if (!t) return;
   if (t->tc) tri_tc_release(t);
+  if (t->timing)
+    for (int i = 0; i < 8; ++i) cudaEventDestroy(t->marks[i]);
   void* ptrs[] = {t->w_proj, t->w_out, t->gamma, t->beta, t->bg, t->bo, t->wb_f32,
                   t->q, t->k, t->v, t->g, t->o, t->bias, t->dev_err,
                   t->stage_x, t->stage_mask, t->stage_out};
@@ -213,6 +215,44 @@ int tri_attn_forward_host(tri_attn_t t, void* stream, const void* pair_repr_host
 
 int tri_attn_destroy(tri_attn_t t) {
   free_all(t);
+  return TRI_ATTN_OK;
+}
+
+int tri_attn_enable_kernel_timing(tri_attn_t t, int enable) {
+  if (!t) return TRI_ATTN_ERR_INVALID_ARG;
+  if (enable && !t->timing) {
+    for (int i = 0; i < 8; ++i) {
+      cudaError_t e = cudaEventCreate(&t->marks[i]);
+      if (e != cudaSuccess) {
+        for (int k = 0; k < i; ++k) cudaEventDestroy(t->marks[k]);
+        return cuda_status(e);
+      }
+    }
+    t->timing = 1;
+    t->n_marks = 0;
+  } else if (!enable && t->timing) {
+    for (int i = 0; i < 8; ++i) cudaEventDestroy(t->marks[i]);
+    t->timing = 0;
+    t->n_marks = 0;
+  }
+  return TRI_ATTN_OK;
+}
+
+int tri_attn_kernel_times(tri_attn_t t, float* ms, const char** names, int* n) {
+  if (!t || !ms || !n || *n < 0) return TRI_ATTN_ERR_INVALID_ARG;
+  if (!t->timing || t->n_marks < 2) {
+    *n = 0;
+    return TRI_ATTN_OK;
+  }
+  const int k = t->n_marks - 1;
+  if (*n < k) return TRI_ATTN_ERR_INVALID_ARG;
+  cudaError_t e = cudaEventSynchronize(t->marks[k]);
+  for (int i = 0; i < k && e == cudaSuccess; ++i) {
+    e = cudaEventElapsedTime(&ms[i], t->marks[i], t->marks[i + 1]);
+    if (names) names[i] = t->mark_names[i + 1];
+  }
+  if (e != cudaSuccess) return cuda_status(e);
+  *n = k;
   return TRI_ATTN_OK;
 }
 
