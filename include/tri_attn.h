@@ -64,8 +64,9 @@ enum {
 /* Build a handle for one problem shape and one set of weights.
  *
  * B, N, D, h: batch, pair-grid side, channels, heads; D % h == 0. Supported:
- *   TRI_ATTN_F32  any B, N >= 1, D <= 256 with d = D/h <= 64;
- *   TRI_ATTN_BF16 the tensor-core path: D == 128, h in {4} (d == 32), any B, N >= 1.
+ *   TRI_ATTN_F32  any B, N >= 1, D <= 256 with d = D/h <= 128;
+ *   TRI_ATTN_BF16 the tensor-core path: D == 128, h == 4 (d == 32), any B,
+ *                 1 <= N <= 8192, B*N*N < 2^31.
  *   Other shapes return TRI_ATTN_ERR_UNSUPPORTED (there is no fallback path).
  * mask_mode: TRI_ATTN_MASK_ROW_KEY or TRI_ATTN_MASK_QUERY_KEY (see above).
  * Weights (device pointers, element type `dtype`), nn.Linear layout:
@@ -131,6 +132,18 @@ int tri_attn_enable_kernel_timing(tri_attn_t t, int enable);
  * (and of `names`, which may be NULL); on return it is the number of kernels
  * (0 when timing is off or nothing ran). names[i] receives a static string. */
 int tri_attn_kernel_times(tri_attn_t t, float* ms, const char** names, int* n);
+
+/* Diagnostic access to the handle's intermediates (valid until destroy; they
+ * hold the results of the most recent forward once it has finished):
+ *   "q", "k", "v", "g", "o"  (B*N*N, D) in the handle's dtype: per cell the
+ *                           projections, the post-sigmoid gate and the
+ *                           attention output before the gate;
+ *   "bias"                  (B, h, N, row_stride) fp32 pair-bias plane; on the
+ *                           bf16 path it holds log2(e) * bias, and -inf where
+ *                           the query-key mask drops (j, k).
+ * Returns the device pointer, or NULL for an unknown name or handle;
+ * *row_stride (may be NULL) receives the innermost row stride in elements. */
+void* tri_attn_debug_tensor(tri_attn_t t, const char* name, int64_t* row_stride);
 
 /* Test hook: cap every bounded device-side wait of this handle's kernels at
  * `spins` polls (0 restores the default of about one second). A cap of 1

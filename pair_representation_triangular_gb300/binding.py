@@ -72,6 +72,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.tri_attn_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_size_t)]
     lib.tri_attn_set_wait_limit.argtypes = [vp, i64]
     lib.tri_attn_enable_kernel_timing.argtypes = [vp, i32]
+    lib.tri_attn_debug_tensor.argtypes = [vp, ctypes.c_char_p, ctypes.POINTER(i64)]
+    lib.tri_attn_debug_tensor.restype = vp
     lib.tri_attn_kernel_times.argtypes = [vp, ctypes.POINTER(ctypes.c_float),
                                           ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(i32)]
     for name in ("tri_attn_create", "tri_attn_forward", "tri_attn_forward_host",
@@ -167,6 +169,22 @@ def tri_attn_kernel_times(handle) -> list:
     return [(names[i].decode(), float(ms[i])) for i in range(n.value)]
 
 
+def tri_attn_debug_tensor(handle, name: str):
+    """(device pointer, innermost row stride in elements) of an intermediate;
+    (None, 0) for an unknown name."""
+    ld = ctypes.c_longlong(0)
+    ptr = load_library().tri_attn_debug_tensor(handle, name.encode(), ctypes.byref(ld))
+    return ptr, ld.value
+
+
+class _DeviceView:
+    """A __cuda_array_interface__ view of library-owned device memory."""
+
+    def __init__(self, ptr: int, shape: tuple, typestr: str):
+        self.__cuda_array_interface__ = {"data": (ptr, True), "shape": shape,
+                                         "typestr": typestr, "version": 2}
+
+
 class TriangularAttention:
     """Owns one handle: ``TriangularAttention(B, N, D, h, dtype, mask_mode, params)``,
     then ``forward(pair_repr, pair_mask)`` returns a new output tensor."""
@@ -203,6 +221,23 @@ class TriangularAttention:
         self._check_inputs(pair_repr, pair_mask, out, False)
         tri_attn_forward_host(self.handle, stream, pair_repr, pair_mask, out)
         return out
+
+    def intermediate(self, name: str) -> torch.Tensor:
+        """Copy of an intermediate of the most recent forward (see
+        tri_attn_debug_tensor): q, k, v, g, o as (B, N, N, D) in the handle's dtype
+        (bf16 is returned as its raw bits reinterpreted); bias as (B, h, N, N) fp32."""
+        ptr, ld = tri_attn_debug_tensor(self.handle, name)
+        if not ptr:
+            raise KeyError(name)
+        torch.cuda.synchronize()
+        if name == "bias":
+            view = _DeviceView(ptr, (self.B, self.h, self.N, ld), "<f4")
+            return torch.as_tensor(view, device="cuda")[..., :self.N].clone()
+        shape = (self.B, self.N, self.N, self.D)
+        if self.torch_dtype == torch.float32:
+            return torch.as_tensor(_DeviceView(ptr, shape, "<f4"), device="cuda").clone()
+        raw = torch.as_tensor(_DeviceView(ptr, shape, "<i2"), device="cuda").clone()
+        return raw.view(torch.bfloat16)
 
     def sync_check(self, stream=None) -> int:
         return tri_attn_sync_check(self.handle, stream)

@@ -68,3 +68,4 @@ void tri_tc_release(tri_attn_s* t);
 cudaError_t tri_tc_forward(tri_attn_s* t, cudaStream_t s, const void* x,
                            const int32_t* mask, void* out);
 size_t tri_tc_extra_bytes(int B, int N, int D, int h);
+int tri_tc_bias_row_stride(const tri_attn_s* t);

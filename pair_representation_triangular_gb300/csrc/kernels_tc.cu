@@ -956,6 +956,11 @@ cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const voi
   return e;
 }
 
+int tri_tc_bias_row_stride(const tri_attn_s* t) {
+  const TcState* st = (const TcState*)t->tc;
+  return st ? st->Nb : t->N;
+}
+
 void tri_tc_release(tri_attn_s* t) {
   TcState* st = (TcState*)t->tc;
   if (!st) return;

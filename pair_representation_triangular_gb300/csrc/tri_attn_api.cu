@@ -256,6 +256,23 @@ int tri_attn_kernel_times(tri_attn_t t, float* ms, const char** names, int* n) {
   return TRI_ATTN_OK;
 }
 
+void* tri_attn_debug_tensor(tri_attn_t t, const char* name, int64_t* row_stride) {
+  if (!t || !name) return nullptr;
+  int64_t ld = t->D;
+  void* p = nullptr;
+  if (!strcmp(name, "q")) p = t->q;
+  else if (!strcmp(name, "k")) p = t->k;
+  else if (!strcmp(name, "v")) p = t->v;
+  else if (!strcmp(name, "g")) p = t->g;
+  else if (!strcmp(name, "o")) p = t->o;
+  else if (!strcmp(name, "bias")) {
+    p = t->bias;
+    ld = t->dtype == TRI_ATTN_BF16 ? tri_tc_bias_row_stride(t) : t->N;
+  }
+  if (p && row_stride) *row_stride = ld;
+  return p;
+}
+
 int tri_attn_set_wait_limit(tri_attn_t t, long long spins) {
   if (!t || spins < 0) return TRI_ATTN_ERR_INVALID_ARG;
   t->wait_limit = spins ? spins : TRI_DEFAULT_WAIT_LIMIT;
