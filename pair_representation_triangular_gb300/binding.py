@@ -181,7 +181,7 @@ class _DeviceView:
     """A __cuda_array_interface__ view of library-owned device memory."""
 
     def __init__(self, ptr: int, shape: tuple, typestr: str):
-        self.__cuda_array_interface__ = {"data": (ptr, True), "shape": shape,
+        self.__cuda_array_interface__ = {"data": (ptr, False), "shape": shape,
                                          "typestr": typestr, "version": 2}
 
 
