@@ -151,6 +151,38 @@ void* tri_attn_debug_tensor(tri_attn_t t, const char* name, int64_t* row_stride)
  * path can be exercised without hanging the GPU. */
 int tri_attn_set_wait_limit(tri_attn_t t, long long spins);
 
+/* fp32 forward pass that allocates no device memory. The pages have no
+ * counterpart to this entry point; it exists for callers that cannot call
+ * cudaMalloc when they need a forward pass (code running inside a memory pool
+ * or custom allocator that forbids outside allocations, plugins that are handed
+ * only their input and output buffers, loops where an allocation and the
+ * synchronisation it may cause are not allowed), so they cannot use
+ * tri_attn_create, which allocates its weights and workspace.
+ *
+ * Everything is a caller pointer (device, fp32, 16-byte aligned; pair_mask
+ * int32): the weights in nn.Linear layout as for tri_attn_create, pair_repr
+ * (B, N, N, D), pair_mask (B, N, N) and out (B, N, N, D). The intermediates live
+ * in one fixed 16 MiB device array inside the library, which every GPU that
+ * loads the library holds until the process exits. A problem needs
+ *   4 * ((4D + h) * D + D * D + 5 * B * N * N * D + B * h * N * N) bytes
+ * (each of those seven regions rounded up to 256); larger problems return
+ * TRI_ATTN_ERR_UNSUPPORTED without launching anything. Other shape rules are
+ * those of TRI_ATTN_F32 in tri_attn_create; the mask mode is as there.
+ *
+ * The call is asynchronous on `stream`. The first call on each device looks up
+ * the array's device address (cudaGetSymbolAddress, with that device current),
+ * so make that first call before any stream capture. All calls share the one
+ * array and it keeps the previous call's contents (every byte a call reads is
+ * written earlier in the same call, so nothing is cleared): calls that can
+ * overlap on the GPU, on different streams or from different threads, race on
+ * it and must be serialised by the caller. */
+int tri_attn_forward_noalloc(int B, int N, int D, int h, int mask_mode,
+                             const float* ln_gamma, const float* ln_beta,
+                             const float* Wq, const float* Wk, const float* Wv,
+                             const float* Wg, const float* bg, const float* Wb,
+                             const float* Wo, const float* bo, void* stream,
+                             const float* pair_repr, const int32_t* pair_mask, float* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -74,6 +74,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.tri_attn_enable_kernel_timing.argtypes = [vp, i32]
     lib.tri_attn_debug_tensor.argtypes = [vp, ctypes.c_char_p, ctypes.POINTER(i64)]
     lib.tri_attn_debug_tensor.restype = vp
+    lib.tri_attn_forward_noalloc.argtypes = [i32, i32, i32, i32, i32] + [vp] * 14
+    lib.tri_attn_forward_noalloc.restype = i32
     lib.tri_attn_kernel_times.argtypes = [vp, ctypes.POINTER(ctypes.c_float),
                                           ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(i32)]
     for name in ("tri_attn_create", "tri_attn_forward", "tri_attn_forward_host",
@@ -167,6 +169,19 @@ def tri_attn_kernel_times(handle) -> list:
     _check(load_library().tri_attn_kernel_times(handle, ms, names, ctypes.byref(n)),
            "tri_attn_kernel_times")
     return [(names[i].decode(), float(ms[i])) for i in range(n.value)]
+
+
+def tri_attn_forward_noalloc(B, N, D, h, mask_mode, params: dict, stream,
+                             pair_repr: torch.Tensor, pair_mask: torch.Tensor,
+                             out: torch.Tensor) -> None:
+    """fp32 forward that allocates nothing on the device (see include/tri_attn.h):
+    for callers that may not allocate; intermediates use the library's fixed
+    16 MiB scratch, so problems beyond it raise TriAttnError (UNSUPPORTED)."""
+    ptrs = [params[name].data_ptr() for name in PARAM_ORDER]
+    _check(load_library().tri_attn_forward_noalloc(B, N, D, h, mask_mode, *ptrs,
+                                                   _stream_ptr(stream), pair_repr.data_ptr(),
+                                                   pair_mask.data_ptr(), out.data_ptr()),
+           "tri_attn_forward_noalloc")
 
 
 def tri_attn_debug_tensor(handle, name: str):

@@ -60,6 +60,18 @@ cudaError_t tri_f32_pack_weights(tri_attn_s* t, const void* Wq, const void* Wk, 
 cudaError_t tri_f32_forward(tri_attn_s* t, cudaStream_t s, const float* x,
                             const int32_t* mask, float* out);
 
+// fp32 forward on caller-provided buffers (no handle): weights in nn.Linear
+// layout are packed into w_proj / w_out, intermediates go to q..o and bias.
+struct TriF32Raw {
+  int B, N, D, h, mask_mode;
+  const float *gamma, *beta, *Wq, *Wk, *Wv, *Wg, *bg, *Wb, *Wo, *bo;
+  const float* x;
+  const int32_t* mask;
+  float* out;
+  float *w_proj, *w_out, *q, *k, *v, *g, *o, *bias;
+};
+cudaError_t tri_f32_forward_raw(const TriF32Raw& a, cudaStream_t s);
+
 // ---- bf16 tensor-core path (kernels_tc.cu)
 bool tri_tc_supported(int B, int N, int D, int h);
 cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const void* Wv,

@@ -262,3 +262,36 @@ cudaError_t tri_f32_forward(tri_attn_s* t, cudaStream_t s, const float* x,
   tri_mark(t, s, 3, "gate_out_f32");
   return cudaGetLastError();
 }
+
+cudaError_t tri_f32_forward_raw(const TriF32Raw& a, cudaStream_t s) {
+  const long long cells = (long long)a.B * a.N * a.N;
+  const int D = a.D, h = a.h, d = a.D / a.h, N = a.N, nout = 4 * D + h;
+  const void* mats[5] = {a.Wq, a.Wk, a.Wv, a.Wg, a.Wb};
+  for (int m = 0; m < 5; ++m) {
+    const int rows = m < 4 ? D : h;
+    const int n = rows * D;
+    pack_transpose_f32<<<(n + 255) / 256, 256, 0, s>>>((const float*)mats[m], rows, D, a.w_proj,
+                                                       nout, m * D);
+  }
+  pack_transpose_f32<<<(D * D + 255) / 256, 256, 0, s>>>(a.Wo, D, D, a.w_out, D, 0);
+  const unsigned nblk = (unsigned)((cells + kCellsPerBlock - 1) / kCellsPerBlock);
+  const size_t smem = (size_t)kCellsPerBlock * D * sizeof(float);
+  ln_proj_f32<<<nblk, kProjThreads, smem, s>>>(a.x, cells, N, D, h, a.gamma, a.beta, a.w_proj,
+                                               a.bg, a.q, a.k, a.v, a.g, a.bias);
+  dim3 grid((unsigned)(a.B * (long long)N), h, (N + kQueriesPerBlock - 1) / kQueriesPerBlock);
+  const int md = d <= 8 ? 8 : d <= 16 ? 16 : d <= 32 ? 32 : d <= 64 ? 64 : 128;
+  switch (md) {
+    case 8: row_attn_f32<8, kKeyChunk><<<grid, kQueriesPerBlock, 0, s>>>(
+        a.q, a.k, a.v, a.bias, a.mask, a.mask_mode, N, D, h, d, a.o); break;
+    case 16: row_attn_f32<16, kKeyChunk><<<grid, kQueriesPerBlock, 0, s>>>(
+        a.q, a.k, a.v, a.bias, a.mask, a.mask_mode, N, D, h, d, a.o); break;
+    case 32: row_attn_f32<32, kKeyChunk><<<grid, kQueriesPerBlock, 0, s>>>(
+        a.q, a.k, a.v, a.bias, a.mask, a.mask_mode, N, D, h, d, a.o); break;
+    case 64: row_attn_f32<64, kKeyChunk><<<grid, kQueriesPerBlock, 0, s>>>(
+        a.q, a.k, a.v, a.bias, a.mask, a.mask_mode, N, D, h, d, a.o); break;
+    default: row_attn_f32<128, 16><<<grid, kQueriesPerBlock, 0, s>>>(
+        a.q, a.k, a.v, a.bias, a.mask, a.mask_mode, N, D, h, d, a.o); break;
+  }
+  gate_out_f32<<<nblk, kProjThreads, smem, s>>>(a.g, a.o, cells, D, a.w_out, a.bo, a.out);
+  return cudaGetLastError();
+}
