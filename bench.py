@@ -70,11 +70,13 @@ def algorithmic_work(w):
         "row_attn": {"flops": 4.0 * B * N ** 3 * D,
                      "bytes": 3 * P * D * s + 4 * P * h + 4 * P + P * D * s},
         "gate_out": {"flops": 2.0 * P * D * D, "bytes": 3 * P * D * s},
+        "mask_summary": {"flops": 0.0,
+                         "bytes": 4 * P + B * N * (1 + 8 * ((N + 63) // 64))},
     }
 
 
 def kernel_key(name: str) -> str:
-    for k in ("ln_proj", "row_attn", "gate_out"):
+    for k in ("ln_proj", "row_attn", "gate_out", "mask_summary"):
         if name.startswith(k):
             return k
     return name

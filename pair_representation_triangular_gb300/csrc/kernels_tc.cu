@@ -359,9 +359,9 @@ struct Bars {
 };
 
 struct Params {
-  int B, N, h, mask_mode, row_groups;
-  const int32_t* mask;
-  const unsigned char* q_any;     // mode query-key: per (b, j) any kept key
+  int B, N, h, mask_mode, row_groups, jtiles, words;
+  const uint32_t* mbits;          // (B*N rows, words): bit k = pair_mask[b, r, k] != 0, k < N
+  const unsigned char* row_any;   // (B*N rows): the mask row keeps some key
   __nv_bfloat16* o;
   unsigned int* dev_err;
   long long polls;
@@ -380,10 +380,14 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
   const Abort ab{&bars->abort, p.dev_err, p.polls};
 
   const int N = p.N;
-  const int rg = blockIdx.x % p.row_groups;
-  const int b = blockIdx.x / p.row_groups;
-  const int t = blockIdx.y;
-  const int j0 = blockIdx.z * BQ;
+  // Block order: query tile fastest, then head, then row group, so the CTAs that
+  // share one row group's K/V tiles run side by side and hit them in L2.
+  const int jt = blockIdx.x % p.jtiles;
+  const int t = (blockIdx.x / p.jtiles) % p.h;
+  const int rgb = blockIdx.x / (p.jtiles * p.h);
+  const int rg = rgb % p.row_groups;
+  const int b = rgb / p.row_groups;
+  const int j0 = jt * BQ;
   const int i0 = rg * R;
   const int KT = (N + BK - 1) / BK;
   const int nitems = KT * R;
@@ -410,31 +414,32 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     tc::tmem_alloc(&bars->tmem_base, 256);
     tc::tmem_relinquish();
   }
-  // Key-mask bits of the R rows (row-key mode): bit k of row r = pair_mask[b, i0+r, k] != 0.
-  if (warp >= 2) {
-    const int W = 2 * KT;                   // words of whole 64-key tiles; bits k >= N are 0
-    for (int item = warp - 2; item < R * W; item += 8) {
-      const int r = item / W, wd = item % W;
-      const int i = i0 + r, k = wd * 32 + lane;
-      bool keep = false;
-      if (p.mask_mode == TRI_ATTN_MASK_ROW_KEY)
-        keep = i < N && k < N && p.mask[((long long)b * N + i) * N + k] != 0;
-      else
-        keep = k < N;                       // query-key mode: only padding keys drop here
-      const unsigned bits = __ballot_sync(0xffffffffu, keep);
-      if (lane == 0) mbits[r * MAXW + wd] = bits;
+  // Key bits of the R rows for every 64-key tile. Row-key mode: the rows' own
+  // mask bits (precomputed by mask_summary); query-key mode: only keys k >= N
+  // drop here (the mask itself is folded into the bias plane).
+  {
+    const int W = 2 * KT;
+    for (int idx = tid; idx < R * W; idx += kThreads) {
+      const int r = idx / W, wd = idx % W;
+      const int i = i0 + r;
+      uint32_t bits;
+      if (p.mask_mode == TRI_ATTN_MASK_ROW_KEY) {
+        bits = i < N ? p.mbits[((long long)b * N + i) * p.words + wd] : 0u;
+      } else {
+        const int left = N - wd * 32;
+        bits = left >= 32 ? 0xffffffffu : left <= 0 ? 0u : ((1u << left) - 1u);
+      }
+      mbits[r * MAXW + wd] = bits;
+    }
+    if (tid < R) {
+      const int i = i0 + tid;
+      bars->row_any[tid] = p.mask_mode == TRI_ATTN_MASK_ROW_KEY
+                               ? (i < N && p.row_any[(long long)b * N + i] != 0) : 1;
     }
   }
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  if (tid < R) {
-    const int W = 2 * KT;
-    unsigned any = 0;
-    for (int wd = 0; wd < W; ++wd) any |= mbits[tid * MAXW + wd];
-    bars->row_any[tid] = any != 0;
-  }
-  __syncthreads();
   const uint32_t tmem = bars->tmem_base;
   int issued_kt = 0;                        // producer: k-tiles whose loads were issued
 
@@ -489,11 +494,10 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         if (rm == R - 1) tc::mma_commit(&bars->kv_empty[sm]);
         return true;
       };
-      bool ok = wait_or_abort(&bars->q_full, 0, ab);
-      for (int n = 0; ok && n < nitems; ++n) {
+      auto qk = [&](int n) -> bool {
         const int kt = n / R, r = n % R, w = n & 1, s = kt % STAGES, u = n >> 1;
-        if (r == 0 && !wait_or_abort(&bars->kv_full[s], (kt / STAGES) & 1, ab)) { ok = false; break; }
-        if (u >= 1 && !wait_or_abort(&bars->s_free[w], (u - 1) & 1, ab)) { ok = false; break; }
+        if (r == 0 && !wait_or_abort(&bars->kv_full[s], (kt / STAGES) & 1, ab)) return false;
+        if (u >= 1 && !wait_or_abort(&bars->s_free[w], (u - 1) & 1, ab)) return false;
         tc::tc_fence_after();
         const uint32_t kaddr = kv0 + s * STAGE_KV + r * 2 * KV_BYTES;
         for (int ks = 0; ks < DH / 16; ++ks) {
@@ -502,9 +506,16 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
           tc::mma_bf16_ss(tmem + w * BK, ad, bd, id_qk, ks > 0);
         }
         tc::mma_commit(&bars->s_ready[w]);
-        if (n >= 1 && !pv(n - 1)) { ok = false; break; }
+        return true;
+      };
+      // S(n+2) is computed as soon as the softmax has read S(n) out of TMEM, so
+      // a warpgroup finds its next tile ready when it finishes the current one.
+      bool ok = wait_or_abort(&bars->q_full, 0, ab);
+      for (int n = 0; ok && n < 2 && n < nitems; ++n) ok = qk(n);
+      for (int n = 0; ok && n < nitems; ++n) {
+        if (n + 2 < nitems && !qk(n + 2)) { ok = false; break; }
+        if (!pv(n)) { ok = false; break; }
       }
-      if (ok && nitems > 0) pv(nitems - 1);
       tc::mma_commit(&bars->drain);
       drain_wait(&bars->drain, 0);
     }
@@ -518,7 +529,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     const uint32_t o_col = tmem + lane_base + 128 + w * 32;
     uint8_t* p_buf = smem + OFF_P + w * P_BYTES;
     bool uni_q = false;                               // query-key mode: query j keeps no key
-    if (p.mask_mode == TRI_ATTN_MASK_QUERY_KEY && j < N) uni_q = !p.q_any[(long long)b * N + j];
+    if (p.mask_mode == TRI_ATTN_MASK_QUERY_KEY && j < N) uni_q = !p.row_any[(long long)b * N + j];
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     float oacc[2][DH];
 #pragma unroll
@@ -648,16 +659,23 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
   if (warp == 1) tc::tmem_dealloc(tmem, 256);
 }
 
-// Per (b, r): does row r of pair_mask[b] keep any key? (query-key mode)
-__global__ void mask_rows_any(const int32_t* __restrict__ mask, int N, long long rows,
-                              unsigned char* __restrict__ any) {
+// One warp per mask row (b, r): bit k of word k/32 is pair_mask[b, r, k] != 0
+// for k < N (0 beyond, up to `words` words), and any[row] says whether the row
+// keeps some key.
+__global__ void mask_summary(const int32_t* __restrict__ mask, int N, long long rows, int words,
+                             uint32_t* __restrict__ bits, unsigned char* __restrict__ any) {
   const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= rows) return;
   const int lane = threadIdx.x & 31;
-  int found = 0;
-  for (int k = lane; k < N; k += 32) found |= mask[row * N + k] != 0;
-  found = __any_sync(0xffffffffu, found);
-  if (lane == 0) any[row] = (unsigned char)found;
+  unsigned found = 0;
+  for (int wd = 0; wd < words; ++wd) {
+    const int k = wd * 32 + lane;
+    const bool keep = k < N && mask[row * N + k] != 0;
+    const unsigned w = __ballot_sync(0xffffffffu, keep);
+    found |= w;
+    if (lane == 0) bits[row * words + wd] = w;
+  }
+  if (lane == 0) any[row] = found != 0;
 }
 }  // namespace k2
 
@@ -888,7 +906,9 @@ bool map_heads(CUtensorMap* m, const void* base, int B, int N, int box_j) {
 
 struct TcState {
   CUtensorMap map_w, map_q, map_k, map_v, map_b, map_g, map_o, map_wo;
-  unsigned char* q_any;
+  unsigned char* row_any;    // (B*N) mask rows keeping some key
+  uint32_t* mbits;           // (B*N, words) mask bits
+  int words;
   int num_sms;
   int Nb;
 };
@@ -907,7 +927,8 @@ bool tri_tc_supported(int B, int N, int D, int h) {
 size_t tri_tc_extra_bytes(int B, int N, int, int h) {
   // bias-plane row padding and the per-row mask summary
   const size_t Nb = (size_t)round_up(N, 4);
-  return (size_t)B * h * N * (Nb - N) * sizeof(float) + (size_t)B * N + 256;
+  return (size_t)B * h * N * (Nb - N) * sizeof(float) + (size_t)B * N +
+         (size_t)B * N * 2 * ((N + 63) / 64) * 4 + 512;
 }
 
 cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const void* Wv,
@@ -924,7 +945,9 @@ cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const voi
     t->bias = nullptr;
     e = cudaMalloc((void**)&t->bias, (size_t)B * h * N * st->Nb * sizeof(float));
   }
-  if (e == cudaSuccess) e = cudaMalloc((void**)&st->q_any, (size_t)B * N);
+  st->words = 2 * ((N + k2::BK - 1) / k2::BK);
+  if (e == cudaSuccess) e = cudaMalloc((void**)&st->row_any, (size_t)B * N);
+  if (e == cudaSuccess) e = cudaMalloc((void**)&st->mbits, (size_t)B * N * st->words * 4);
   const size_t wbytes = (size_t)D * D * 2;
   const void* mats[4] = {Wq, Wk, Wv, Wg};
   for (int m = 0; m < 4 && e == cudaSuccess; ++m)
@@ -964,7 +987,8 @@ int tri_tc_bias_row_stride(const tri_attn_s* t) {
 void tri_tc_release(tri_attn_s* t) {
   TcState* st = (TcState*)t->tc;
   if (!st) return;
-  if (st->q_any) cudaFree(st->q_any);
+  if (st->row_any) cudaFree(st->row_any);
+  if (st->mbits) cudaFree(st->mbits);
   free(st);
   t->tc = nullptr;
 }
@@ -991,18 +1015,21 @@ cudaError_t tri_tc_forward(tri_attn_s* t, cudaStream_t s, const void* x, const i
   k1::ln_proj_tc<<<grid_rows, k1::kThreads, k1::SMEM, s>>>(map_x, st->map_w, p1);
   tri_mark(t, s, mark++, "ln_proj_tc");
 
-  if (t->mask_mode == TRI_ATTN_MASK_QUERY_KEY) {
+  {
     const long long rows = (long long)B * N;
-    k2::mask_rows_any<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(mask, N, rows, st->q_any);
-    tri_mark(t, s, mark++, "mask_rows_any");
+    k2::mask_summary<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(mask, N, rows, st->words,
+                                                              st->mbits, st->row_any);
+    tri_mark(t, s, mark++, "mask_summary");
   }
   k2::Params p2;
   p2.B = B; p2.N = N; p2.h = h; p2.mask_mode = t->mask_mode;
   p2.row_groups = (N + k2::R - 1) / k2::R;
-  p2.mask = mask; p2.q_any = st->q_any; p2.o = (__nv_bfloat16*)t->o; p2.dev_err = t->dev_err;
+  p2.jtiles = (N + k2::BQ - 1) / k2::BQ;
+  p2.words = st->words;
+  p2.mbits = st->mbits; p2.row_any = st->row_any; p2.o = (__nv_bfloat16*)t->o; p2.dev_err = t->dev_err;
   p2.polls = t->wait_limit;
   p2.scale_log2 = kLog2e / sqrtf((float)t->d);
-  dim3 g2((unsigned)(B * p2.row_groups), h, (N + k2::BQ - 1) / k2::BQ);
+  const unsigned g2 = (unsigned)((long long)B * p2.row_groups * h * p2.jtiles);
   k2::row_attn_tc<<<g2, k2::kThreads, k2::SMEM, s>>>(st->map_q, st->map_k, st->map_v, st->map_b, p2);
   tri_mark(t, s, mark++, "row_attn_tc");
 
