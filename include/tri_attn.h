@@ -138,9 +138,10 @@ int tri_attn_kernel_times(tri_attn_t t, float* ms, const char** names, int* n);
  *   "q", "k", "v", "g", "o"  (B*N*N, D) in the handle's dtype: per cell the
  *                           projections, the post-sigmoid gate and the
  *                           attention output before the gate;
- *   "bias"                  (B, h, N, row_stride) fp32 pair-bias plane; on the
- *                           bf16 path it holds log2(e) * bias, and -inf where
- *                           the query-key mask drops (j, k).
+ *   "bias"                  (B, h, N, row_stride) pair-bias plane: fp32 on the
+ *                           fp32 path; on the bf16 path fp16 holding
+ *                           log2(e) * bias, and -inf where the query-key mask
+ *                           drops (j, k).
  * Returns the device pointer, or NULL for an unknown name or handle;
  * *row_stride (may be NULL) receives the innermost row stride in elements. */
 void* tri_attn_debug_tensor(tri_attn_t t, const char* name, int64_t* row_stride);

@@ -240,14 +240,16 @@ class TriangularAttention:
     def intermediate(self, name: str) -> torch.Tensor:
         """Copy of an intermediate of the most recent forward (see
         tri_attn_debug_tensor): q, k, v, g, o as (B, N, N, D) in the handle's dtype
-        (bf16 is returned as its raw bits reinterpreted); bias as (B, h, N, N) fp32."""
+        (bf16 is returned as its raw bits reinterpreted); bias as (B, h, N, N) fp32
+        (stored in fp16 on the bf16 path)."""
         ptr, ld = tri_attn_debug_tensor(self.handle, name)
         if not ptr:
             raise KeyError(name)
         torch.cuda.synchronize()
         if name == "bias":
-            view = _DeviceView(ptr, (self.B, self.h, self.N, ld), "<f4")
-            return torch.as_tensor(view, device="cuda")[..., :self.N].clone()
+            ts = "<f4" if self.dtype == TRI_ATTN_F32 else "<f2"
+            view = _DeviceView(ptr, (self.B, self.h, self.N, ld), ts)
+            return torch.as_tensor(view, device="cuda")[..., :self.N].float()
         shape = (self.B, self.N, self.N, self.D)
         if self.torch_dtype == torch.float32:
             return torch.as_tensor(_DeviceView(ptr, shape, "<f4"), device="cuda").clone()

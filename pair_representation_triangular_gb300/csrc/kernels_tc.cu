@@ -8,14 +8,14 @@
 //                the epilogue writes q, k, v and sigmoid(g + bg) in bf16; the
 //                h pair-bias outputs (Wb x_hat) are computed on the CUDA cores
 //                from the same bf16 x_hat and written, scaled by log2(e), to
-//                the fp32 bias plane (B, h, N, Nb).
-//   row_attn_tc  flash-style row attention: a CTA owns (b, head t, 128 queries
-//                j, R rows i) and streams 64-key tiles; per tile S = Q K^T goes
-//                to TMEM, two softmax warpgroups add the shared pair bias
-//                (one smem tile serves all R rows), apply the key mask, run an
-//                online softmax in registers and write P (bf16) to smem;
-//                O_tile = P V goes to TMEM and is folded into a register
-//                accumulator. The (B, N, h, N, N) logits never exist.
+//                the fp16 bias plane (B, h, N, Nb).
+//   row_attn_tc  flash-style row attention, persistent: a work unit is
+//                (b, head t, R rows i, 256 queries j) streaming 64-key tiles;
+//                S = Q K^T goes to TMEM, two softmax warpgroups add the shared
+//                pair bias (held in registers across the R rows), apply the
+//                key mask and an online softmax with lazy rescaling, and write
+//                P (bf16) back into TMEM; O += P V accumulates in TMEM. The
+//                (B, N, h, N, N) logits never exist.
 //   gate_out_tc  g * o formed in shared memory as the A operand of the output
 //                projection GEMM; the epilogue adds bo and stores bf16.
 //
@@ -111,7 +111,7 @@ struct Params {
   const float* gamma; const float* beta; const float* bg; const float* wb;   // fp32
   const int32_t* mask;
   __nv_bfloat16 *q, *k, *v, *g;
-  float* bias;                 // (B, h, N, Nb), scaled by log2(e)
+  __half* bias;                // (B, h, N, Nb) fp16, scaled by log2(e)
   unsigned int* dev_err;
   long long polls;
 };
@@ -304,7 +304,8 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
         bool keep = true;
         if (p.mask_mode == TRI_ATTN_MASK_QUERY_KEY) keep = p.mask[cell] != 0;
         for (int t = 0; t < p.h; ++t)
-          p.bias[((bb * p.h + t) * p.N + rr) * p.Nb + cc] = keep ? bsum[t] * kLog2e : -INFINITY;
+          p.bias[((bb * p.h + t) * p.N + rr) * p.Nb + cc] =
+              __float2half_rn(keep ? bsum[t] * kLog2e : -INFINITY);
       }
       if (it >= 1 && !epilogue(it - 1)) { ok = false; break; }
     }
@@ -330,36 +331,40 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
 // K2: flash row attention
 // ---------------------------------------------------------------------------
 namespace k2 {
-constexpr int R = 4;                    // rows i per CTA (share each bias tile)
-constexpr int BQ = 128;                 // queries j per CTA
+constexpr int R = 4;                    // rows i per work unit (share each bias tile)
+constexpr int JW = 2;                   // 128-query tiles per unit, one per softmax warpgroup
+constexpr int BQ = 128;                 // queries per tile
 constexpr int BK = 64;                  // keys per tile
 constexpr int DH = 32;                  // head dim
 constexpr int STAGES = 2;
 constexpr int MAXW = 256;               // mask words per row (N <= 8192)
-constexpr int kThreads = 320;           // warp 0 TMA, 1 MMA, 2-5 softmax WG0, 6-9 WG1
-constexpr uint32_t Q_BYTES = BQ * DH * 2;          // 8 KB
-constexpr uint32_t KV_BYTES = BK * DH * 2;         // 4 KB each of K and V
-constexpr uint32_t BIAS_BYTES = BQ * BK * 4;       // 32 KB (two 16 KB boxes of 32 keys)
-constexpr uint32_t P_BYTES = BQ * BK * 2;          // 16 KB
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_KV = OFF_Q + R * Q_BYTES;                 // [stage][r] K then V
-constexpr uint32_t STAGE_KV = R * 2 * KV_BYTES;
-constexpr uint32_t OFF_BIAS = OFF_KV + STAGES * STAGE_KV;
-constexpr uint32_t OFF_P = OFF_BIAS + STAGES * BIAS_BYTES;
-constexpr uint32_t OFF_MASK = OFF_P + 2 * P_BYTES;
-constexpr uint32_t OFF_BAR = OFF_MASK + R * MAXW * 4 + 64;
+constexpr float kRescale = 8.0f;        // log2 growth of the running max that forces a rescale
+// Warpgroup 0: warp 0 TMA, warps 1 and 2 issue the MMAs of softmax warpgroup
+// 0 and 1 (two independent issue streams overlap the fixed per-instruction
+// latency of small-N tcgen05 MMAs), warp 3 idle; warpgroups 1 and 2 are the
+// softmax warpgroups for query tiles 0 and 1. Registers move from the
+// control warpgroup to the softmax ones: 384 x 168 = 128 x 56 + 256 x 224.
+constexpr int kThreads = 384;
+constexpr int kRegsCtl = 56, kRegsSoftmax = 224;
+constexpr uint32_t Q_BYTES = BQ * DH * 2;            // 8 KB per (row, query tile)
+constexpr uint32_t KV_BYTES = BK * DH * 2;           // 4 KB each of K and V
+constexpr uint32_t BIAS_BYTES = BQ * BK * 2;         // 16 KB fp16 bias tile per query tile
+constexpr uint32_t OFF_Q = 0;                        // [R][JW]
+constexpr uint32_t STAGE_KV = R * 2 * KV_BYTES;      // [R] K then V
+constexpr uint32_t STAGE_BYTES = STAGE_KV + JW * BIAS_BYTES;
+constexpr uint32_t OFF_STAGE = OFF_Q + R * JW * Q_BYTES;
+constexpr uint32_t OFF_BAR = OFF_STAGE + STAGES * STAGE_BYTES;
 constexpr uint32_t SMEM = OFF_BAR + 512 + 1024;
 
 struct Bars {
-  uint64_t q_full, kv_full[STAGES], kv_empty[STAGES];
-  uint64_t s_ready[2], s_free[2], p_full[2], p_free[2], o_ready[2], o_free[2], drain;
+  uint64_t q_full, q_empty, kv_full[STAGES], kv_empty[STAGES];
+  uint64_t s_ready[JW][2], s_free[JW][2], p_full[JW][2], o_free[JW], drain;
   uint32_t tmem_base;
   int abort;
-  int row_any[R];
 };
 
 struct Params {
-  int B, N, h, mask_mode, row_groups, jtiles, words;
+  int B, N, h, mask_mode, row_groups, jpairs, words, units;
   const uint32_t* mbits;          // (B*N rows, words): bit k = pair_mask[b, r, k] != 0, k < N
   const unsigned char* row_any;   // (B*N rows): the mask row keeps some key
   __nv_bfloat16* o;
@@ -368,6 +373,30 @@ struct Params {
   float scale_log2;               // log2(e) / sqrt(d)
 };
 
+struct Unit {
+  int b, t, rg, j0;               // j0: first query of the unit's 256-query pair
+};
+
+__device__ __forceinline__ Unit decode_unit(int u, const Params& p) {
+  Unit un;
+  const int jp = u % p.jpairs;
+  un.t = (u / p.jpairs) % p.h;
+  const int rgb = u / (p.jpairs * p.h);
+  un.rg = rgb % p.row_groups;
+  un.b = rgb / p.row_groups;
+  un.j0 = jp * BQ * JW;
+  return un;
+}
+
+// Persistent: CTA c serves work units c, c + G, c + 2G, ... A unit is (b, head t,
+// R rows i, 2 x 128 queries j); it streams 64-key tiles. Per tile the K and V
+// tiles of the R rows and one fp16 bias tile per query tile come in by TMA;
+// warpgroup w (queries j0 + 128w ...) reads its bias row once per key tile into
+// registers and uses it for all R rows. For each (key tile, row) item the MMA
+// thread computes S = Q K^T into one of the warpgroup's two TMEM S buffers; the
+// softmax writes P (bf16) back over S in TMEM, and O_r += P V accumulates in
+// TMEM. The running max is only moved (and O rescaled in TMEM) when it grows
+// by more than 2^8, so P stays <= 256.
 __global__ void __launch_bounds__(kThreads, 1)
 row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
             const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_b,
@@ -375,74 +404,44 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   Bars* bars = (Bars*)(smem + OFF_BAR);
-  uint32_t* mbits = (uint32_t*)(smem + OFF_MASK);       // [R][MAXW]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const Abort ab{&bars->abort, p.dev_err, p.polls};
-
   const int N = p.N;
-  // Block order: query tile fastest, then head, then row group, so the CTAs that
-  // share one row group's K/V tiles run side by side and hit them in L2.
-  const int jt = blockIdx.x % p.jtiles;
-  const int t = (blockIdx.x / p.jtiles) % p.h;
-  const int rgb = blockIdx.x / (p.jtiles * p.h);
-  const int rg = rgb % p.row_groups;
-  const int b = rgb / p.row_groups;
-  const int j0 = jt * BQ;
-  const int i0 = rg * R;
   const int KT = (N + BK - 1) / BK;
-  const int nitems = KT * R;
+  const int IPU = KT * R * JW;            // items per unit (both warpgroups)
+  int my_units = 0;
+  for (int u = blockIdx.x; u < p.units; u += gridDim.x) ++my_units;
 
   if (tid == 0) {
     tc::mbar_init(&bars->q_full, 1);
+    tc::mbar_init(&bars->q_empty, JW);           // one commit per MMA thread
     for (int s = 0; s < STAGES; ++s) {
       tc::mbar_init(&bars->kv_full[s], 1);
-      tc::mbar_init(&bars->kv_empty[s], 1);
+      tc::mbar_init(&bars->kv_empty[s], JW);
     }
-    for (int w = 0; w < 2; ++w) {
-      tc::mbar_init(&bars->s_ready[w], 1);
-      tc::mbar_init(&bars->s_free[w], 128);
-      tc::mbar_init(&bars->p_full[w], 128);
-      tc::mbar_init(&bars->p_free[w], 1);
-      tc::mbar_init(&bars->o_ready[w], 1);
+    for (int w = 0; w < JW; ++w) {
+      for (int b2 = 0; b2 < 2; ++b2) {
+        tc::mbar_init(&bars->s_ready[w][b2], 1);
+        tc::mbar_init(&bars->s_free[w][b2], 1);
+        tc::mbar_init(&bars->p_full[w][b2], 128);
+      }
       tc::mbar_init(&bars->o_free[w], 128);
     }
-    tc::mbar_init(&bars->drain, 1);
+    tc::mbar_init(&bars->drain, JW);
     bars->abort = 0;
     tc::fence_mbar_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(&bars->tmem_base, 256);
+    tc::tmem_alloc(&bars->tmem_base, 512);
     tc::tmem_relinquish();
-  }
-  // Key bits of the R rows for every 64-key tile. Row-key mode: the rows' own
-  // mask bits (precomputed by mask_summary); query-key mode: only keys k >= N
-  // drop here (the mask itself is folded into the bias plane).
-  {
-    const int W = 2 * KT;
-    for (int idx = tid; idx < R * W; idx += kThreads) {
-      const int r = idx / W, wd = idx % W;
-      const int i = i0 + r;
-      uint32_t bits;
-      if (p.mask_mode == TRI_ATTN_MASK_ROW_KEY) {
-        bits = i < N ? p.mbits[((long long)b * N + i) * p.words + wd] : 0u;
-      } else {
-        const int left = N - wd * 32;
-        bits = left >= 32 ? 0xffffffffu : left <= 0 ? 0u : ((1u << left) - 1u);
-      }
-      mbits[r * MAXW + wd] = bits;
-    }
-    if (tid < R) {
-      const int i = i0 + tid;
-      bars->row_any[tid] = p.mask_mode == TRI_ATTN_MASK_ROW_KEY
-                               ? (i < N && p.row_any[(long long)b * N + i] != 0) : 1;
-    }
   }
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  int issued_kt = 0;                        // producer: k-tiles whose loads were issued
+  int q_issued = 0, kg_issued = 0;          // producer: units / key tiles whose loads were issued
 
+  if (warp < 4) tc::regs_dec<kRegsCtl>();
   if (warp == 0) {
     // ---------------- TMA producer
     if (lane == 0) {
@@ -450,199 +449,288 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       tc::tma_prefetch_desc(&map_k);
       tc::tma_prefetch_desc(&map_v);
       tc::tma_prefetch_desc(&map_b);
-      const int row0 = b * N + i0;
-      tc::mbar_arrive_expect_tx(&bars->q_full, R * Q_BYTES);
-      for (int r = 0; r < R; ++r)
-        tc::tma_load_3d(smem + OFF_Q + r * Q_BYTES, &map_q, &bars->q_full, t * DH, j0, row0 + r);
-      for (int kt = 0; kt < KT; ++kt) {
-        const int s = kt % STAGES;
-        if (kt >= STAGES && !wait_or_abort(&bars->kv_empty[s], ((kt / STAGES) - 1) & 1, ab)) break;
-        uint8_t* kv = smem + OFF_KV + s * STAGE_KV;
-        uint8_t* bs = smem + OFF_BIAS + s * BIAS_BYTES;
-        tc::mbar_arrive_expect_tx(&bars->kv_full[s], STAGE_KV + BIAS_BYTES);
-        for (int r = 0; r < R; ++r) {
-          tc::tma_load_3d(kv + r * 2 * KV_BYTES, &map_k, &bars->kv_full[s], t * DH, kt * BK, row0 + r);
-          tc::tma_load_3d(kv + r * 2 * KV_BYTES + KV_BYTES, &map_v, &bars->kv_full[s], t * DH,
-                          kt * BK, row0 + r);
+      bool ok = true;
+      for (int ui = 0; ok && ui < my_units; ++ui) {
+        const Unit un = decode_unit(blockIdx.x + ui * gridDim.x, p);
+        const int row0 = un.b * N + un.rg * R;
+        if (ui >= 1 && !wait_or_abort(&bars->q_empty, (ui - 1) & 1, ab)) break;
+        tc::mbar_arrive_expect_tx(&bars->q_full, R * JW * Q_BYTES);
+        for (int r = 0; r < R; ++r)
+          for (int w = 0; w < JW; ++w)
+            tc::tma_load_3d(smem + OFF_Q + (r * JW + w) * Q_BYTES, &map_q, &bars->q_full,
+                            un.t * DH, un.j0 + w * BQ, row0 + r);
+        q_issued = ui + 1;
+        for (int kt = 0; kt < KT; ++kt) {
+          const int kg = kg_issued, s = kg % STAGES;
+          if (kg >= STAGES && !wait_or_abort(&bars->kv_empty[s], ((kg / STAGES) - 1) & 1, ab)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + OFF_STAGE + s * STAGE_BYTES;
+          tc::mbar_arrive_expect_tx(&bars->kv_full[s], STAGE_BYTES);
+          for (int r = 0; r < R; ++r) {
+            tc::tma_load_3d(st + r * 2 * KV_BYTES, &map_k, &bars->kv_full[s], un.t * DH, kt * BK,
+                            row0 + r);
+            tc::tma_load_3d(st + r * 2 * KV_BYTES + KV_BYTES, &map_v, &bars->kv_full[s],
+                            un.t * DH, kt * BK, row0 + r);
+          }
+          for (int w = 0; w < JW; ++w)
+            tc::tma_load_3d(st + STAGE_KV + w * BIAS_BYTES, &map_b, &bars->kv_full[s], kt * BK,
+                            un.j0 + w * BQ, un.b * p.h + un.t);
+          kg_issued = kg + 1;
         }
-        tc::tma_load_3d(bs, &map_b, &bars->kv_full[s], kt * BK, j0, b * p.h + t);
-        tc::tma_load_3d(bs + 16384, &map_b, &bars->kv_full[s], kt * BK + 32, j0, b * p.h + t);
-        issued_kt = kt + 1;
       }
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ---------------- MMA issuer of softmax warpgroup w (one thread)
     if (lane == 0) {
+      const int w = warp - 1;
       constexpr uint32_t id_qk = tc::idesc_bf16_f32(128, BK, 0, 0);
       constexpr uint32_t id_pv = tc::idesc_bf16_f32(128, DH, 0, 1);
       const uint32_t q0 = tc::smem_addr(smem + OFF_Q);
-      const uint32_t kv0 = tc::smem_addr(smem + OFF_KV);
-      const uint32_t p0 = tc::smem_addr(smem + OFF_P);
-      auto pv = [&](int m) -> bool {
-        const int km = m / R, rm = m % R, wm = m & 1, sm = km % STAGES, u = m >> 1;
-        if (!wait_or_abort(&bars->p_full[wm], u & 1, ab)) return false;
-        if (u >= 1 && !wait_or_abort(&bars->o_free[wm], (u - 1) & 1, ab)) return false;
-        tc::tc_fence_after();
-        const uint32_t vaddr = kv0 + sm * STAGE_KV + rm * 2 * KV_BYTES + KV_BYTES;
-        for (int ks = 0; ks < BK / 16; ++ks) {
-          const uint64_t ad = tc::smem_desc(p0 + wm * P_BYTES + ks * 32, 16, 1024, tc::SWZ_128B);
-          const uint64_t bd = tc::smem_desc(vaddr + ks * 1024, 16, 512, tc::SWZ_64B);
-          tc::mma_bf16_ss(tmem + 128 + wm * 32, ad, bd, id_pv, ks > 0);
+      const uint32_t st0 = tc::smem_addr(smem + OFF_STAGE);
+      // Event loop: issue S = Q K^T for the next item as soon as Q, the key
+      // tile and a free S buffer are there (at most two items ahead of P V),
+      // and P V as soon as the softmax has written P.
+      const int per_w = my_units * KT * R;
+      int nq = 0, np = 0;
+      uint64_t t_idle = 0;
+      long long idle_polls = 0;
+      bool ok = true;
+      while (ok && np < per_w) {
+        bool progress = false;
+        if (nq < per_w && nq - np < 2) {
+          const int a = nq;
+          const int ui = a / (KT * R), rem = a % (KT * R), kt = rem / R, r = rem % R;
+          const int kg = ui * KT + kt, s = kg % STAGES, sb = a & 1;
+          const bool ready = (!(kt == 0 && r == 0) || tc::mbar_test(&bars->q_full, ui & 1)) &&
+                             (r != 0 || tc::mbar_test(&bars->kv_full[s], (kg / STAGES) & 1)) &&
+                             (a < 2 || tc::mbar_test(&bars->s_free[w][sb], ((a >> 1) - 1) & 1));
+          if (ready) {
+            tc::tc_fence_after();
+            const uint32_t qa = q0 + (r * JW + w) * Q_BYTES;
+            const uint32_t ka = st0 + s * STAGE_BYTES + r * 2 * KV_BYTES;
+            for (int ks = 0; ks < DH / 16; ++ks)
+              tc::mma_bf16_ss(tmem + w * 256 + sb * BK,
+                              tc::smem_desc(qa + ks * 32, 16, 512, tc::SWZ_64B),
+                              tc::smem_desc(ka + ks * 32, 16, 512, tc::SWZ_64B), id_qk, ks > 0);
+            tc::mma_commit(&bars->s_ready[w][sb]);
+            if (kt == KT - 1 && r == R - 1) tc::mma_commit(&bars->q_empty);
+            nq = a + 1;
+            progress = true;
+          }
         }
-        tc::mma_commit(&bars->o_ready[wm]);
-        tc::mma_commit(&bars->p_free[wm]);
-        if (rm == R - 1) tc::mma_commit(&bars->kv_empty[sm]);
-        return true;
-      };
-      auto qk = [&](int n) -> bool {
-        const int kt = n / R, r = n % R, w = n & 1, s = kt % STAGES, u = n >> 1;
-        if (r == 0 && !wait_or_abort(&bars->kv_full[s], (kt / STAGES) & 1, ab)) return false;
-        if (u >= 1 && !wait_or_abort(&bars->s_free[w], (u - 1) & 1, ab)) return false;
-        tc::tc_fence_after();
-        const uint32_t kaddr = kv0 + s * STAGE_KV + r * 2 * KV_BYTES;
-        for (int ks = 0; ks < DH / 16; ++ks) {
-          const uint64_t ad = tc::smem_desc(q0 + r * Q_BYTES + ks * 32, 16, 512, tc::SWZ_64B);
-          const uint64_t bd = tc::smem_desc(kaddr + ks * 32, 16, 512, tc::SWZ_64B);
-          tc::mma_bf16_ss(tmem + w * BK, ad, bd, id_qk, ks > 0);
+        if (np < nq) {
+          const int c = np;
+          const int ui = c / (KT * R), rem = c % (KT * R), kt = rem / R, r = rem % R;
+          const int kg = ui * KT + kt, s = kg % STAGES, sb = c & 1;
+          const bool ready = tc::mbar_test(&bars->p_full[w][sb], (c >> 1) & 1) &&
+                             (!(kt == 0 && r == 0 && ui >= 1) ||
+                              tc::mbar_test(&bars->o_free[w], (ui - 1) & 1));
+          if (ready) {
+            tc::tc_fence_after();
+            const uint32_t va = st0 + s * STAGE_BYTES + r * 2 * KV_BYTES + KV_BYTES;
+            for (int ks = 0; ks < BK / 16; ++ks)
+              tc::mma_bf16_ts(tmem + w * 256 + 128 + r * DH, tmem + w * 256 + sb * BK + ks * 8,
+                              tc::smem_desc(va + ks * 1024, 16, 512, tc::SWZ_64B), id_pv,
+                              (kt > 0 || ks > 0) ? 1u : 0u);
+            tc::mma_commit(&bars->s_free[w][sb]);
+            if (r == R - 1) tc::mma_commit(&bars->kv_empty[s]);
+            np = c + 1;
+            progress = true;
+          }
         }
-        tc::mma_commit(&bars->s_ready[w]);
-        return true;
-      };
-      // S(n+2) is computed as soon as the softmax has read S(n) out of TMEM, so
-      // a warpgroup finds its next tile ready when it finishes the current one.
-      bool ok = wait_or_abort(&bars->q_full, 0, ab);
-      for (int n = 0; ok && n < 2 && n < nitems; ++n) ok = qk(n);
-      for (int n = 0; ok && n < nitems; ++n) {
-        if (n + 2 < nitems && !qk(n + 2)) { ok = false; break; }
-        if (!pv(n)) { ok = false; break; }
+        if (progress) {
+          idle_polls = 0;
+          t_idle = 0;
+        } else {
+          if (*(volatile int*)ab.flag) { ok = false; break; }
+          if (++idle_polls >= ab.polls) ok = false;
+          if ((idle_polls & 255) == 0) {
+            const uint64_t now = tc::global_timer_ns();
+            if (t_idle == 0) t_idle = now;
+            else if (now - t_idle > 2000000000ull) ok = false;
+          }
+          if (!ok) {
+            *(volatile int*)ab.flag = 1;
+            atomicOr(ab.dev_err, TRI_DEV_ERR_TIMEOUT);
+          }
+        }
       }
       tc::mma_commit(&bars->drain);
       drain_wait(&bars->drain, 0);
     }
-  } else {
-    // ---------------- softmax warpgroups: WG w handles rows r = w and w + 2
-    const int w = (warp - 2) >> 2;
-    const int jr = (warp & 3) * 32 + lane;          // query row in the tile = TMEM lane
-    const int j = j0 + jr;
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t s_col = tmem + lane_base + w * BK;
-    const uint32_t o_col = tmem + lane_base + 128 + w * 32;
-    uint8_t* p_buf = smem + OFF_P + w * P_BYTES;
-    bool uni_q = false;                               // query-key mode: query j keeps no key
-    if (p.mask_mode == TRI_ATTN_MASK_QUERY_KEY && j < N) uni_q = !p.row_any[(long long)b * N + j];
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-    float oacc[2][DH];
-#pragma unroll
-    for (int lr = 0; lr < 2; ++lr)
-#pragma unroll
-      for (int e = 0; e < DH; ++e) oacc[lr][e] = 0.f;
-    float pend_alpha = 0.f;
+  } else if (warp >= 4) {
+    // ---------------- softmax warpgroups
+    tc::regs_inc<kRegsSoftmax>();
+    const int w = (warp >> 2) - 1;
+    const int jr = (warp & 3) * 32 + lane;          // query row of the tile = TMEM lane
+    const uint32_t tb = tmem + ((uint32_t)((warp & 3) * 32) << 16) + w * 256;
+    const float sc = p.scale_log2;
     bool ok = true;
-    int step = 0;                                     // items done by this WG (= u)
-
-    auto fold_pending = [&](int lr_p) -> bool {       // O_tile of item step-1 into oacc[lr_p]
-      const int u = step - 1;
-      if (!warp_wait_or_abort(&bars->o_ready[w], u & 1, ab)) return false;
-      tc::tc_fence_after();
-      uint32_t ov[32];
-      tc::tmem_ld32(o_col, ov);
-      tc::tmem_ld_wait();
-      tc::tc_fence_before();
-      tc::mbar_arrive(&bars->o_free[w]);
+    for (int ui = 0; ok && ui < my_units; ++ui) {
+      const Unit un = decode_unit(blockIdx.x + ui * gridDim.x, p);
+      const int j = un.j0 + w * BQ + jr;
+      const bool valid_j = j < N;
+      bool uni[R];
+      float m_used[R], l_run[R];
+      bool uni_q = false;
+      if (p.mask_mode == TRI_ATTN_MASK_QUERY_KEY)
+        uni_q = !(valid_j && p.row_any[(long long)un.b * N + j]);
 #pragma unroll
-      for (int e = 0; e < DH; ++e)
-        oacc[lr_p][e] = fmaf(oacc[lr_p][e], pend_alpha, __uint_as_float(ov[e]));
-      return true;
-    };
-
-    for (int kt = 0; ok && kt < KT; ++kt) {
-      const int s = kt % STAGES;
+      for (int r = 0; r < R; ++r) {
+        const int i = un.rg * R + r;
+        uni[r] = uni_q || (p.mask_mode == TRI_ATTN_MASK_ROW_KEY &&
+                           !(i < N && p.row_any[(long long)un.b * N + i]));
+        m_used[r] = -INFINITY;
+        l_run[r] = 0.f;
+      }
+      // Row-key mask words of the R rows, fetched one key tile ahead.
+      uint32_t mw_next[R][2];
+      auto fetch_bits = [&](int kt) {
 #pragma unroll
-      for (int lr = 0; lr < 2; ++lr) {
-        if (!ok) break;
-        const int r = w + 2 * lr;
-        const int u = step;
-        // S tile of item (kt, r)
-        if (!warp_wait_or_abort(&bars->s_ready[w], u & 1, ab)) { ok = false; break; }
-        tc::tc_fence_after();
-        uint32_t sv[BK];
-        tc::tmem_ld32(s_col, *(uint32_t(*)[32])&sv[0]);
-        tc::tmem_ld32(s_col + 32, *(uint32_t(*)[32])&sv[32]);
-        tc::tmem_ld_wait();
-        tc::tc_fence_before();
-        tc::mbar_arrive(&bars->s_free[w]);
-        if (!warp_wait_or_abort(&bars->kv_full[s], (kt / STAGES) & 1, ab)) { ok = false; break; }
-        const uint32_t bw0 = mbits[r * MAXW + 2 * kt], bw1 = mbits[r * MAXW + 2 * kt + 1];
-        const bool uni = uni_q || !bars->row_any[r];
-        float x[BK];
-        if (uni) {
-#pragma unroll
-          for (int k = 0; k < BK; ++k) x[k] = (kt * BK + k < N) ? 0.f : -INFINITY;
-        } else {
-          const uint8_t* bsm = smem + OFF_BIAS + s * BIAS_BYTES;
-#pragma unroll
-          for (int c = 0; c < BK / 4; ++c) {
-            const float4 bv = *(const float4*)(bsm + (c >> 3) * 16384 + tc::swz_offset(jr, c & 7, 128));
-            x[4 * c + 0] = fmaf(__uint_as_float(sv[4 * c + 0]), p.scale_log2, bv.x);
-            x[4 * c + 1] = fmaf(__uint_as_float(sv[4 * c + 1]), p.scale_log2, bv.y);
-            x[4 * c + 2] = fmaf(__uint_as_float(sv[4 * c + 2]), p.scale_log2, bv.z);
-            x[4 * c + 3] = fmaf(__uint_as_float(sv[4 * c + 3]), p.scale_log2, bv.w);
+        for (int r = 0; r < R; ++r) {
+          const int i = un.rg * R + r;
+          mw_next[r][0] = mw_next[r][1] = 0xffffffffu;
+          if (p.mask_mode == TRI_ATTN_MASK_ROW_KEY && !uni[r] && kt < KT) {
+            const uint32_t* mw = p.mbits + ((long long)un.b * N + i) * p.words + 2 * kt;
+            mw_next[r][0] = __ldg(mw);
+            mw_next[r][1] = __ldg(mw + 1);
           }
-          if ((bw0 & bw1) != 0xffffffffu) {
+        }
+      };
+      fetch_bits(0);
+      for (int kt = 0; ok && kt < KT; ++kt) {
+        const int kg = ui * KT + kt, s = kg % STAGES;
+        uint32_t mw_cur[R][2];
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              if (!((bw0 >> k) & 1u)) x[k] = -INFINITY;
-              if (!((bw1 >> k) & 1u)) x[32 + k] = -INFINITY;
+        for (int r = 0; r < R; ++r) {
+          mw_cur[r][0] = mw_next[r][0];
+          mw_cur[r][1] = mw_next[r][1];
+        }
+        fetch_bits(kt + 1);
+        // Bias row of this query for the key tile, fp16 in smem -> fp32 registers.
+        if (!warp_wait_or_abort(&bars->kv_full[s], (kg / STAGES) & 1, ab)) { ok = false; break; }
+        float bf[BK];
+        {
+          const uint8_t* bs = smem + OFF_STAGE + s * STAGE_BYTES + STAGE_KV + w * BIAS_BYTES;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 u4 = *(const uint4*)(bs + tc::swz_offset(jr, c, 128));
+            const uint32_t hw[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __half22float2(*(const __half2*)&hw[e]);
+              bf[c * 8 + 2 * e] = f.x;
+              bf[c * 8 + 2 * e + 1] = f.y;
             }
           }
         }
-        float mt = x[0];
+        // Key bits of this tile: row-key mode per row, query-key mode only k < N.
+        const int left = N - kt * BK;
+        const uint32_t real0 = left >= 32 ? 0xffffffffu : (left <= 0 ? 0u : ((1u << left) - 1u));
+        const uint32_t real1 = left >= 64 ? 0xffffffffu
+                               : (left <= 32 ? 0u : ((1u << (left - 32)) - 1u));
 #pragma unroll
-        for (int k = 1; k < BK; ++k) mt = fmaxf(mt, x[k]);
-        const float m_new = fmaxf(m_run[lr], mt);
-        const float m_use = m_new == -INFINITY ? 0.f : m_new;
-        const float alpha = ex2_approx(m_run[lr] - m_use);
-        m_run[lr] = m_new;
-        float rs = 0.f;
-        uint32_t pk[BK / 2];
+        for (int r = 0; r < R; ++r) {
+          if (!ok) continue;
+          const int uw = ui * KT * R + kt * R + r, sb = uw & 1;
+          do {
+          const uint32_t bw0 = real0 & mw_cur[r][0], bw1 = real1 & mw_cur[r][1];
+          if (!warp_wait_or_abort(&bars->s_ready[w][sb], (uw >> 1) & 1, ab)) { ok = false; break; }
+          tc::tc_fence_after();
+          float x[BK];
+          tc::tmem_ld32(tb + sb * BK, *(uint32_t(*)[32])&x[0]);
+          tc::tmem_ld32(tb + sb * BK + 32, *(uint32_t(*)[32])&x[32]);
+          tc::tmem_ld_wait();
+          if (uni[r]) {
+            // A row (or query) that keeps no key weighs every real key equally.
 #pragma unroll
-        for (int k = 0; k < BK; k += 2) {
-          const float p0 = ex2_approx(x[k] - m_use), p1 = ex2_approx(x[k + 1] - m_use);
-          rs += p0 + p1;
-          pk[k / 2] = tc::pack_bf16x2(p0, p1);
+            for (int k = 0; k < 32; ++k) {
+              x[k] = ((real0 >> k) & 1u) ? 0.f : -INFINITY;
+              x[32 + k] = ((real1 >> k) & 1u) ? 0.f : -INFINITY;
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < BK; ++k) x[k] = fmaf(x[k], sc, bf[k]);
+            if ((bw0 & bw1) != 0xffffffffu) {
+#pragma unroll
+              for (int k = 0; k < 32; ++k) {
+                if (!((bw0 >> k) & 1u)) x[k] = -INFINITY;
+                if (!((bw1 >> k) & 1u)) x[32 + k] = -INFINITY;
+              }
+            }
+          }
+          float mx[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) mx[q] = x[q];
+#pragma unroll
+          for (int k = 8; k < BK; ++k) mx[k & 7] = fmaxf(mx[k & 7], x[k]);
+          const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+          const float m_new = fmaxf(m_used[r], mt);
+          bool need = false;
+          if (m_used[r] == -INFINITY) {
+            m_used[r] = m_new;                       // first live tile: O and l are still 0
+          } else if (m_new > m_used[r] + kRescale) {
+            need = true;
+          }
+          if (__any_sync(0xffffffffu, need)) {
+            // Warp-wide: rescale O_r in TMEM (lanes without a jump use 1).
+            const float alpha = need ? ex2_approx(m_used[r] - m_new) : 1.f;
+            if (need) m_used[r] = m_new;
+            l_run[r] *= alpha;
+            const int up = uw - 1;                   // PV(up) done => every PV on O_r done
+            if (!warp_wait_or_abort(&bars->s_free[w][up & 1], (up >> 1) & 1, ab)) { ok = false; break; }
+            tc::tc_fence_after();
+            uint32_t ov[32];
+            tc::tmem_ld32(tb + 128 + r * DH, ov);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tc::tmem_st32(tb + 128 + r * DH, ov);
+          }
+          const float mu = m_used[r] == -INFINITY ? 0.f : m_used[r];
+          float rs[4] = {0.f, 0.f, 0.f, 0.f};
+          uint32_t pk[32];
+#pragma unroll
+          for (int k = 0; k < BK; k += 2) {
+            const float p0 = ex2_approx(x[k] - mu), p1 = ex2_approx(x[k + 1] - mu);
+            rs[(k >> 1) & 3] += p0 + p1;
+            pk[k >> 1] = tc::pack_bf16x2(p0, p1);
+          }
+          l_run[r] += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+          tc::tmem_st32(tb + sb * BK, pk);            // P over the consumed S columns
+          tc::tmem_st_wait();
+          tc::tc_fence_before();
+          tc::mbar_arrive(&bars->p_full[w][sb]);
+          } while (0);
         }
-        l_run[lr] = fmaf(l_run[lr], alpha, rs);
-        // P (bf16) into smem buffer w once PV of this WG's previous item has read it.
-        if (u >= 1 && !warp_wait_or_abort(&bars->p_free[w], (u - 1) & 1, ab)) { ok = false; break; }
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *(uint4*)(p_buf + tc::swz_offset(jr, c, 128)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        tc::fence_proxy_async_smem();
-        tc::mbar_arrive(&bars->p_full[w]);
-        // Fold the previous item's O tile (the other local row) while this PV runs.
-        if (step >= 1 && !fold_pending(1 - lr)) { ok = false; break; }
-        pend_alpha = alpha;
-        ++step;
       }
-    }
-    if (ok && step >= 1) {
-      // The last item of this WG is local row 1 (R = 4 keeps the lr order 0,1,0,1,...).
-      ok = fold_pending(1);
-    }
-    if (ok && j < N) {
+      if (!ok) break;
+      // Unit epilogue: o = O / l for the R rows once the last PV has landed.
+      const int ulast = ui * KT * R + KT * R - 1;
+      if (!warp_wait_or_abort(&bars->s_free[w][ulast & 1], (ulast >> 1) & 1, ab)) { ok = false; break; }
+      tc::tc_fence_after();
 #pragma unroll
-      for (int lr = 0; lr < 2; ++lr) {
-        const int i = i0 + w + 2 * lr;
-        if (i >= N) continue;
-        const float inv = 1.0f / l_run[lr];
-        uint32_t pk[DH / 2];
+      for (int r = 0; r < R; ++r) {
+        uint32_t ov[32];
+        tc::tmem_ld32(tb + 128 + r * DH, ov);
+        tc::tmem_ld_wait();
+        const int i = un.rg * R + r;
+        if (valid_j && i < N) {
+          const float inv = 1.0f / l_run[r];
+          uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < DH; e += 2) pk[e / 2] = tc::pack_bf16x2(oacc[lr][e] * inv, oacc[lr][e + 1] * inv);
-        uint4* dst = (uint4*)(p.o + (((long long)b * N + i) * N + j) * (p.h * DH) + t * DH);
+          for (int e = 0; e < DH; e += 2)
+            pk[e / 2] = tc::pack_bf16x2(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
+          uint4* dst = (uint4*)(p.o + (((long long)un.b * N + i) * N + j) * (p.h * DH) + un.t * DH);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          for (int c = 0; c < 4; ++c) dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
       }
+      tc::tc_fence_before();
+      tc::mbar_arrive(&bars->o_free[w]);
     }
   }
 
@@ -650,13 +738,13 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0 && lane == 0) {
-    drain_wait(&bars->q_full, 0);
-    for (int kt = issued_kt - 1; kt >= 0 && kt >= issued_kt - STAGES; --kt)
-      drain_wait(&bars->kv_full[kt % STAGES], (kt / STAGES) & 1);
+    if (q_issued > 0) drain_wait(&bars->q_full, (q_issued - 1) & 1);
+    for (int kg = kg_issued - 1; kg >= 0 && kg >= kg_issued - STAGES; --kg)
+      drain_wait(&bars->kv_full[kg % STAGES], (kg / STAGES) & 1);
   }
   __syncthreads();
   tc::tc_fence_after();
-  if (warp == 1) tc::tmem_dealloc(tmem, 256);
+  if (warp == 1) tc::tmem_dealloc(tmem, 512);
 }
 
 // One warp per mask row (b, r): bit k of word k/32 is pair_mask[b, r, k] != 0
@@ -925,9 +1013,10 @@ bool tri_tc_supported(int B, int N, int D, int h) {
 }
 
 size_t tri_tc_extra_bytes(int B, int N, int, int h) {
-  // bias-plane row padding and the per-row mask summary
-  const size_t Nb = (size_t)round_up(N, 4);
-  return (size_t)B * h * N * (Nb - N) * sizeof(float) + (size_t)B * N +
+  // the fp16 bias plane (rows padded to Nb) replaces the fp32 one; plus the mask summary
+  const size_t Nb = (size_t)round_up(N, 8);
+  const size_t f16 = (size_t)B * h * N * Nb * 2, f32 = (size_t)B * h * N * N * 4;
+  return (f16 > f32 ? f16 - f32 : 0) + (size_t)B * N +
          (size_t)B * N * 2 * ((N + 63) / 64) * 4 + 512;
 }
 
@@ -937,13 +1026,14 @@ cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const voi
   if (!st) return cudaErrorMemoryAllocation;
   t->tc = st;
   const int B = t->B, N = t->N, D = t->D, h = t->h;
-  st->Nb = round_up(N, 4);
+  st->Nb = round_up(N, 8);
   cudaError_t e = cudaDeviceGetAttribute(&st->num_sms, cudaDevAttrMultiProcessorCount, t->device);
-  // The bias plane of the base workspace is (B, h, N, N); this path pads rows to Nb.
-  if (e == cudaSuccess && st->Nb != N) {
+  // This path keeps the bias plane in fp16 with rows padded to Nb (TMA strides
+  // are multiples of 16 bytes).
+  if (e == cudaSuccess) {
     cudaFree(t->bias);
     t->bias = nullptr;
-    e = cudaMalloc((void**)&t->bias, (size_t)B * h * N * st->Nb * sizeof(float));
+    e = cudaMalloc((void**)&t->bias, (size_t)B * h * N * st->Nb * 2);
   }
   st->words = 2 * ((N + k2::BK - 1) / k2::BK);
   if (e == cudaSuccess) e = cudaMalloc((void**)&st->row_any, (size_t)B * N);
@@ -962,9 +1052,9 @@ cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const voi
   ok = ok && map_heads(&st->map_v, t->v, B, N, k2::BK);
   {
     cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)N, (cuuint64_t)B * h};
-    cuuint64_t strides[2] = {(cuuint64_t)st->Nb * 4, (cuuint64_t)N * st->Nb * 4};
-    cuuint32_t box[3] = {32, (cuuint32_t)k2::BQ, 1};
-    ok = ok && make_map(&st->map_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, t->bias, dims, strides,
+    cuuint64_t strides[2] = {(cuuint64_t)st->Nb * 2, (cuuint64_t)N * st->Nb * 2};
+    cuuint32_t box[3] = {k2::BK, (cuuint32_t)k2::BQ, 1};
+    ok = ok && make_map(&st->map_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, t->bias, dims, strides,
                         box, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   ok = ok && map_rows_bf16(&st->map_g, t->g, cells, 128);
@@ -1008,7 +1098,7 @@ cudaError_t tri_tc_forward(tri_attn_s* t, cudaStream_t s, const void* x, const i
   p1.ntiles = ntiles;
   p1.gamma = t->gamma; p1.beta = t->beta; p1.bg = t->bg; p1.wb = t->wb_f32; p1.mask = mask;
   p1.q = (__nv_bfloat16*)t->q; p1.k = (__nv_bfloat16*)t->k; p1.v = (__nv_bfloat16*)t->v;
-  p1.g = (__nv_bfloat16*)t->g; p1.bias = t->bias; p1.dev_err = t->dev_err;
+  p1.g = (__nv_bfloat16*)t->g; p1.bias = (__half*)t->bias; p1.dev_err = t->dev_err;
   p1.polls = t->wait_limit;
   int mark = 0;
   tri_mark(t, s, mark++, nullptr);
@@ -1024,12 +1114,14 @@ cudaError_t tri_tc_forward(tri_attn_s* t, cudaStream_t s, const void* x, const i
   k2::Params p2;
   p2.B = B; p2.N = N; p2.h = h; p2.mask_mode = t->mask_mode;
   p2.row_groups = (N + k2::R - 1) / k2::R;
-  p2.jtiles = (N + k2::BQ - 1) / k2::BQ;
+  p2.jpairs = (N + k2::BQ * k2::JW - 1) / (k2::BQ * k2::JW);
+  p2.units = B * p2.row_groups * h * p2.jpairs;
   p2.words = st->words;
-  p2.mbits = st->mbits; p2.row_any = st->row_any; p2.o = (__nv_bfloat16*)t->o; p2.dev_err = t->dev_err;
+  p2.mbits = st->mbits; p2.row_any = st->row_any; p2.o = (__nv_bfloat16*)t->o;
+  p2.dev_err = t->dev_err;
   p2.polls = t->wait_limit;
   p2.scale_log2 = kLog2e / sqrtf((float)t->d);
-  const unsigned g2 = (unsigned)((long long)B * p2.row_groups * h * p2.jtiles);
+  const unsigned g2 = (unsigned)(p2.units < st->num_sms ? p2.units : st->num_sms);
   k2::row_attn_tc<<<g2, k2::kThreads, k2::SMEM, s>>>(st->map_q, st->map_k, st->map_v, st->map_b, p2);
   tri_mark(t, s, mark++, "row_attn_tc");
 
