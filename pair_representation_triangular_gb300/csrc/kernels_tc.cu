@@ -75,6 +75,12 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
@@ -343,9 +349,9 @@ constexpr float kRescale = 8.0f;        // log2 growth of the running max that f
 // 0 and 1 (two independent issue streams overlap the fixed per-instruction
 // latency of small-N tcgen05 MMAs), warp 3 idle; warpgroups 1 and 2 are the
 // softmax warpgroups for query tiles 0 and 1. Registers move from the
-// control warpgroup to the softmax ones: 384 x 168 = 128 x 56 + 256 x 224.
+// control warpgroup to the softmax ones: 384 x 168 = 128 x 40 + 256 x 232.
 constexpr int kThreads = 384;
-constexpr int kRegsCtl = 56, kRegsSoftmax = 224;
+constexpr int kRegsCtl = 40, kRegsSoftmax = 232;
 constexpr uint32_t Q_BYTES = BQ * DH * 2;            // 8 KB per (row, query tile)
 constexpr uint32_t KV_BYTES = BK * DH * 2;           // 4 KB each of K and V
 constexpr uint32_t BIAS_BYTES = BQ * BK * 2;         // 16 KB fp16 bias tile per query tile
@@ -611,7 +617,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         fetch_bits(kt + 1);
         // Bias row of this query for the key tile, fp16 in smem -> fp32 registers.
         if (!warp_wait_or_abort(&bars->kv_full[s], (kg / STAGES) & 1, ab)) { ok = false; break; }
-        float bf[BK];
+        float2 bf2[BK / 2];
         {
           const uint8_t* bs = smem + OFF_STAGE + s * STAGE_BYTES + STAGE_KV + w * BIAS_BYTES;
 #pragma unroll
@@ -619,11 +625,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
             const uint4 u4 = *(const uint4*)(bs + tc::swz_offset(jr, c, 128));
             const uint32_t hw[4] = {u4.x, u4.y, u4.z, u4.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __half22float2(*(const __half2*)&hw[e]);
-              bf[c * 8 + 2 * e] = f.x;
-              bf[c * 8 + 2 * e + 1] = f.y;
-            }
+            for (int e = 0; e < 4; ++e) bf2[c * 4 + e] = __half22float2(*(const __half2*)&hw[e]);
           }
         }
         // Key bits of this tile: row-key mode per row, query-key mode only k < N.
@@ -639,67 +641,83 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
           const uint32_t bw0 = real0 & mw_cur[r][0], bw1 = real1 & mw_cur[r][1];
           if (!warp_wait_or_abort(&bars->s_ready[w][sb], (uw >> 1) & 1, ab)) { ok = false; break; }
           tc::tc_fence_after();
-          float x[BK];
-          tc::tmem_ld32(tb + sb * BK, *(uint32_t(*)[32])&x[0]);
-          tc::tmem_ld32(tb + sb * BK + 32, *(uint32_t(*)[32])&x[32]);
-          tc::tmem_ld_wait();
-          if (uni[r]) {
-            // A row (or query) that keeps no key weighs every real key equally.
+          uint32_t pk[BK / 2];
+          // A tile whose keys are all dropped (on a row that keeps some key)
+          // contributes exactly 0; a row or query that keeps no key weighs
+          // every real key 1 (uniform softmax). Neither needs S or an exp.
+          const bool dead = (bw0 | bw1) == 0u;
+          const bool live = !uni[r] && !dead;
+          if (__any_sync(0xffffffffu, live)) {
+            float2 x2[BK / 2];
+            tc::tmem_ld32(tb + sb * BK, *(uint32_t(*)[32])&x2[0]);
+            tc::tmem_ld32(tb + sb * BK + 32, *(uint32_t(*)[32])&x2[16]);
+            tc::tmem_ld_wait();
+            const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              x[k] = ((real0 >> k) & 1u) ? 0.f : -INFINITY;
-              x[32 + k] = ((real1 >> k) & 1u) ? 0.f : -INFINITY;
-            }
-          } else {
-#pragma unroll
-            for (int k = 0; k < BK; ++k) x[k] = fmaf(x[k], sc, bf[k]);
+            for (int k = 0; k < BK / 2; ++k) x2[k] = __ffma2_rn(x2[k], sc2, bf2[k]);
             if ((bw0 & bw1) != 0xffffffffu) {
 #pragma unroll
-              for (int k = 0; k < 32; ++k) {
-                if (!((bw0 >> k) & 1u)) x[k] = -INFINITY;
-                if (!((bw1 >> k) & 1u)) x[32 + k] = -INFINITY;
+              for (int k = 0; k < 16; ++k) {
+                if (!((bw0 >> (2 * k)) & 1u)) x2[k].x = -INFINITY;
+                if (!((bw0 >> (2 * k + 1)) & 1u)) x2[k].y = -INFINITY;
+                if (!((bw1 >> (2 * k)) & 1u)) x2[16 + k].x = -INFINITY;
+                if (!((bw1 >> (2 * k + 1)) & 1u)) x2[16 + k].y = -INFINITY;
               }
             }
-          }
-          float mx[8];
+            float mx[4];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) mx[q] = x[q];
+            for (int q = 0; q < 4; ++q) mx[q] = fmaxf(x2[q].x, x2[q].y);
 #pragma unroll
-          for (int k = 8; k < BK; ++k) mx[k & 7] = fmaxf(mx[k & 7], x[k]);
-          const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-          const float m_new = fmaxf(m_used[r], mt);
-          bool need = false;
-          if (m_used[r] == -INFINITY) {
-            m_used[r] = m_new;                       // first live tile: O and l are still 0
-          } else if (m_new > m_used[r] + kRescale) {
-            need = true;
-          }
-          if (__any_sync(0xffffffffu, need)) {
-            // Warp-wide: rescale O_r in TMEM (lanes without a jump use 1).
-            const float alpha = need ? ex2_approx(m_used[r] - m_new) : 1.f;
-            if (need) m_used[r] = m_new;
-            l_run[r] *= alpha;
-            const int up = uw - 1;                   // PV(up) done => every PV on O_r done
-            if (!warp_wait_or_abort(&bars->s_free[w][up & 1], (up >> 1) & 1, ab)) { ok = false; break; }
-            tc::tc_fence_after();
-            uint32_t ov[32];
-            tc::tmem_ld32(tb + 128 + r * DH, ov);
-            tc::tmem_ld_wait();
+            for (int k = 4; k < BK / 2; ++k) mx[k & 3] = fmax3(mx[k & 3], x2[k].x, x2[k].y);
+            const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            const float m_new = fmaxf(m_used[r], mt);
+            bool need = false;
+            if (live) {
+              if (m_used[r] == -INFINITY) m_used[r] = m_new;   // first live tile: O, l still 0
+              else if (m_new > m_used[r] + kRescale) need = true;
+            }
+            if (__any_sync(0xffffffffu, need)) {
+              // Warp-wide: rescale O_r in TMEM (lanes without a jump use 1).
+              const float alpha = need ? ex2_approx(m_used[r] - m_new) : 1.f;
+              if (need) m_used[r] = m_new;
+              l_run[r] *= alpha;
+              const int up = uw - 1;                   // PV(up) done => every PV on O_r done
+              if (!warp_wait_or_abort(&bars->s_free[w][up & 1], (up >> 1) & 1, ab)) { ok = false; break; }
+              tc::tc_fence_after();
+              uint32_t ov[32];
+              tc::tmem_ld32(tb + 128 + r * DH, ov);
+              tc::tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tc::tmem_st32(tb + 128 + r * DH, ov);
-          }
-          const float mu = m_used[r] == -INFINITY ? 0.f : m_used[r];
-          float rs[4] = {0.f, 0.f, 0.f, 0.f};
-          uint32_t pk[32];
+              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+              tc::tmem_st32(tb + 128 + r * DH, ov);
+            }
+            const float mu = m_used[r] == -INFINITY ? 0.f : m_used[r];
+            const float2 nmu2 = make_float2(-mu, -mu);
+            float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
 #pragma unroll
-          for (int k = 0; k < BK; k += 2) {
-            const float p0 = ex2_approx(x[k] - mu), p1 = ex2_approx(x[k + 1] - mu);
-            rs[(k >> 1) & 3] += p0 + p1;
-            pk[k >> 1] = tc::pack_bf16x2(p0, p1);
+            for (int k = 0; k < BK / 2; ++k) {
+              const float2 e2 = __fadd2_rn(x2[k], nmu2);
+              const float2 p2 = make_float2(ex2_approx(e2.x), ex2_approx(e2.y));
+              rs2[k & 3] = __fadd2_rn(rs2[k & 3], p2);
+              pk[k] = tc::pack_bf16x2(p2.x, p2.y);
+            }
+            const float2 t2 = __fadd2_rn(__fadd2_rn(rs2[0], rs2[1]), __fadd2_rn(rs2[2], rs2[3]));
+            if (live) l_run[r] += t2.x + t2.y;
           }
-          l_run[r] += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+          if (!live) {
+            // real-key weights 1 (uniform row) or all 0 (dead tile), in bf16 pairs
+            const uint32_t w0 = uni[r] ? real0 : 0u, w1 = uni[r] ? real1 : 0u;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              pk[k] = (((w0 >> (2 * k)) & 1u) ? 0x3F80u : 0u) | (((w0 >> (2 * k + 1)) & 1u) ? 0x3F800000u : 0u);
+              pk[16 + k] = (((w1 >> (2 * k)) & 1u) ? 0x3F80u : 0u) | (((w1 >> (2 * k + 1)) & 1u) ? 0x3F800000u : 0u);
+            }
+            if (uni[r]) {
+              m_used[r] = 0.f;
+              l_run[r] += (float)(__popc(w0) + __popc(w1));
+            }
+          }
           tc::tmem_st32(tb + sb * BK, pk);            // P over the consumed S columns
           tc::tmem_st_wait();
           tc::tc_fence_before();
