@@ -495,73 +495,48 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       constexpr uint32_t id_pv = tc::idesc_bf16_f32(128, DH, 0, 1);
       const uint32_t q0 = tc::smem_addr(smem + OFF_Q);
       const uint32_t st0 = tc::smem_addr(smem + OFF_STAGE);
-      // Event loop: issue S = Q K^T for the next item as soon as Q, the key
-      // tile and a free S buffer are there (at most two items ahead of P V),
-      // and P V as soon as the softmax has written P.
+      // Per warpgroup the order of events is fixed, so blocking waits (which
+      // suspend the thread in hardware) lose nothing: S for items 0 and 1, then
+      // P V(c) once P(c) is written and S(c + 2) once P V(c) has released the
+      // S buffer.
       const int per_w = my_units * KT * R;
-      int nq = 0, np = 0;
-      uint64_t t_idle = 0;
-      long long idle_polls = 0;
+      auto qk = [&](int a) -> bool {
+        const int ui = a / (KT * R), rem = a % (KT * R), kt = rem / R, r = rem % R;
+        const int kg = ui * KT + kt, s = kg % STAGES, sb = a & 1;
+        if (kt == 0 && r == 0 && !wait_or_abort(&bars->q_full, ui & 1, ab)) return false;
+        if (r == 0 && !wait_or_abort(&bars->kv_full[s], (kg / STAGES) & 1, ab)) return false;
+        if (a >= 2 && !wait_or_abort(&bars->s_free[w][sb], ((a >> 1) - 1) & 1, ab)) return false;
+        tc::tc_fence_after();
+        const uint32_t qa = q0 + (r * JW + w) * Q_BYTES;
+        const uint32_t ka = st0 + s * STAGE_BYTES + r * 2 * KV_BYTES;
+        for (int ks = 0; ks < DH / 16; ++ks)
+          tc::mma_bf16_ss(tmem + w * 256 + sb * BK, tc::smem_desc(qa + ks * 32, 16, 512, tc::SWZ_64B),
+                          tc::smem_desc(ka + ks * 32, 16, 512, tc::SWZ_64B), id_qk, ks > 0);
+        tc::mma_commit(&bars->s_ready[w][sb]);
+        if (kt == KT - 1 && r == R - 1) tc::mma_commit(&bars->q_empty);
+        return true;
+      };
+      auto pv = [&](int c) -> bool {
+        const int ui = c / (KT * R), rem = c % (KT * R), kt = rem / R, r = rem % R;
+        const int kg = ui * KT + kt, s = kg % STAGES, sb = c & 1;
+        if (!wait_or_abort(&bars->p_full[w][sb], (c >> 1) & 1, ab)) return false;
+        if (kt == 0 && r == 0 && ui >= 1 && !wait_or_abort(&bars->o_free[w], (ui - 1) & 1, ab))
+          return false;
+        tc::tc_fence_after();
+        const uint32_t va = st0 + s * STAGE_BYTES + r * 2 * KV_BYTES + KV_BYTES;
+        for (int ks = 0; ks < BK / 16; ++ks)
+          tc::mma_bf16_ts(tmem + w * 256 + 128 + r * DH, tmem + w * 256 + sb * BK + ks * 8,
+                          tc::smem_desc(va + ks * 1024, 16, 512, tc::SWZ_64B), id_pv,
+                          (kt > 0 || ks > 0) ? 1u : 0u);
+        tc::mma_commit(&bars->s_free[w][sb]);
+        if (r == R - 1) tc::mma_commit(&bars->kv_empty[s]);
+        return true;
+      };
       bool ok = true;
-      while (ok && np < per_w) {
-        bool progress = false;
-        if (nq < per_w && nq - np < 2) {
-          const int a = nq;
-          const int ui = a / (KT * R), rem = a % (KT * R), kt = rem / R, r = rem % R;
-          const int kg = ui * KT + kt, s = kg % STAGES, sb = a & 1;
-          const bool ready = (!(kt == 0 && r == 0) || tc::mbar_test(&bars->q_full, ui & 1)) &&
-                             (r != 0 || tc::mbar_test(&bars->kv_full[s], (kg / STAGES) & 1)) &&
-                             (a < 2 || tc::mbar_test(&bars->s_free[w][sb], ((a >> 1) - 1) & 1));
-          if (ready) {
-            tc::tc_fence_after();
-            const uint32_t qa = q0 + (r * JW + w) * Q_BYTES;
-            const uint32_t ka = st0 + s * STAGE_BYTES + r * 2 * KV_BYTES;
-            for (int ks = 0; ks < DH / 16; ++ks)
-              tc::mma_bf16_ss(tmem + w * 256 + sb * BK,
-                              tc::smem_desc(qa + ks * 32, 16, 512, tc::SWZ_64B),
-                              tc::smem_desc(ka + ks * 32, 16, 512, tc::SWZ_64B), id_qk, ks > 0);
-            tc::mma_commit(&bars->s_ready[w][sb]);
-            if (kt == KT - 1 && r == R - 1) tc::mma_commit(&bars->q_empty);
-            nq = a + 1;
-            progress = true;
-          }
-        }
-        if (np < nq) {
-          const int c = np;
-          const int ui = c / (KT * R), rem = c % (KT * R), kt = rem / R, r = rem % R;
-          const int kg = ui * KT + kt, s = kg % STAGES, sb = c & 1;
-          const bool ready = tc::mbar_test(&bars->p_full[w][sb], (c >> 1) & 1) &&
-                             (!(kt == 0 && r == 0 && ui >= 1) ||
-                              tc::mbar_test(&bars->o_free[w], (ui - 1) & 1));
-          if (ready) {
-            tc::tc_fence_after();
-            const uint32_t va = st0 + s * STAGE_BYTES + r * 2 * KV_BYTES + KV_BYTES;
-            for (int ks = 0; ks < BK / 16; ++ks)
-              tc::mma_bf16_ts(tmem + w * 256 + 128 + r * DH, tmem + w * 256 + sb * BK + ks * 8,
-                              tc::smem_desc(va + ks * 1024, 16, 512, tc::SWZ_64B), id_pv,
-                              (kt > 0 || ks > 0) ? 1u : 0u);
-            tc::mma_commit(&bars->s_free[w][sb]);
-            if (r == R - 1) tc::mma_commit(&bars->kv_empty[s]);
-            np = c + 1;
-            progress = true;
-          }
-        }
-        if (progress) {
-          idle_polls = 0;
-          t_idle = 0;
-        } else {
-          if (*(volatile int*)ab.flag) { ok = false; break; }
-          if (++idle_polls >= ab.polls) ok = false;
-          if ((idle_polls & 255) == 0) {
-            const uint64_t now = tc::global_timer_ns();
-            if (t_idle == 0) t_idle = now;
-            else if (now - t_idle > 2000000000ull) ok = false;
-          }
-          if (!ok) {
-            *(volatile int*)ab.flag = 1;
-            atomicOr(ab.dev_err, TRI_DEV_ERR_TIMEOUT);
-          }
-        }
+      for (int a = 0; ok && a < 2 && a < per_w; ++a) ok = qk(a);
+      for (int c = 0; ok && c < per_w; ++c) {
+        ok = pv(c);
+        if (ok && c + 2 < per_w) ok = qk(c + 2);
       }
       tc::mma_commit(&bars->drain);
       drain_wait(&bars->drain, 0);
