@@ -75,6 +75,18 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Logistic function for the gate; its result is rounded to bf16, so the
+// hardware exp2 and reciprocal approximations are accurate enough.
+__device__ __forceinline__ float sigmoid_approx(float z) {
+  return rcp_approx(1.0f + ex2_approx(-z * kLog2e));
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -95,18 +107,24 @@ namespace k1 {
 constexpr int BM = 128;                 // cells per tile
 constexpr int KD = 128;                 // channels (GEMM K)
 constexpr int NQ = 512;                 // q|k|v|g columns
-constexpr int kThreads = 192;           // warps 0-3 LN + epilogue, 4 TMA, 5 MMA
+// Warps 0-7 LayerNorm + epilogue (two per TMEM lane quarter: warp q handles the
+// channel half / column half 0, warp q + 4 half 1), warp 8 TMA, warp 9 MMA.
+constexpr int kWorkers = 256;
+constexpr int kThreads = kWorkers + 64;
 constexpr uint32_t W_BYTES = NQ * KD * 2;           // 128 KB, two K-halves of 64 KB
 constexpr uint32_t X_BYTES = BM * KD * 2;           // 32 KB, two K-halves of 16 KB
 constexpr uint32_t OFF_W = 0;
 constexpr uint32_t OFF_X = OFF_W + W_BYTES;
 constexpr uint32_t OFF_PAR = OFF_X + 2 * X_BYTES;   // gamma, beta, bg [128] + Wb [4][128] fp32
 constexpr uint32_t PAR_BYTES = (3 * KD + 4 * KD) * 4;
-constexpr uint32_t OFF_BAR = OFF_PAR + PAR_BYTES;
+constexpr uint32_t OFF_STG = OFF_PAR + PAR_BYTES;   // per worker warp: 32 rows x 64 B staging
+constexpr uint32_t STG_BYTES = 32 * 64;
+constexpr uint32_t OFF_BAR = OFF_STG + 8 * STG_BYTES;
 constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;     // + alignment slack
 
 struct Bars {
-  uint64_t w_full, x_full[2], x_empty[2], a_ready[2], tmem_full, tmem_empty, drain;
+  uint64_t w_full, x_full[2], x_empty[2], a_ready[2], acc_full[2], acc_empty[2], drain;
+  uint64_t ln_read[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -122,8 +140,18 @@ struct Params {
   long long polls;
 };
 
+// Persistent: CTA c serves 128-cell tiles c, c + G, ... [Wq;Wk;Wv;Wg] (bf16,
+// K-major, 128 KB) stays in shared memory. Per tile the x tile arrives by TMA;
+// the 256 workers normalise it in place (the two threads of a cell each own
+// one 64-channel half and compute the row statistics from the whole row) and
+// compute two of the h = 4 bias outputs each from the bf16 x_hat; the MMA warp
+// issues the two N = 256 halves (q|k, v|g) into TMEM columns 0-255 / 256-511,
+// each with its own full/empty barriers, so the next tile's first half can
+// start while the epilogue still reads the second.
 __global__ void __launch_bounds__(kThreads, 1)
 ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+           const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+           const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_g,
            const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -140,10 +168,11 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&bars->x_full[b], 1);
       tc::mbar_init(&bars->x_empty[b], 1);
-      tc::mbar_init(&bars->a_ready[b], 128);
+      tc::mbar_init(&bars->a_ready[b], kWorkers);
+      tc::mbar_init(&bars->acc_full[b], 1);
+      tc::mbar_init(&bars->acc_empty[b], 128);
+      tc::mbar_init(&bars->ln_read[b], kWorkers);
     }
-    tc::mbar_init(&bars->tmem_full, 1);
-    tc::mbar_init(&bars->tmem_empty, 128);
     tc::mbar_init(&bars->drain, 1);
     bars->abort = 0;
     tc::fence_mbar_init();
@@ -154,7 +183,7 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
     s_bg[i] = p.bg[i];
   }
   for (int i = tid; i < 4 * KD; i += kThreads) s_wb[i] = i < p.h * KD ? p.wb[i] : 0.f;
-  if (warp == 5) {
+  if (warp == 9) {
     tc::tmem_alloc(&bars->tmem_base, 512);
     tc::tmem_relinquish();
   }
@@ -162,12 +191,11 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const int ntiles = p.ntiles;
   int my_tiles = 0;
-  for (int t = blockIdx.x; t < ntiles; t += gridDim.x) ++my_tiles;
+  for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) ++my_tiles;
   int issued = 0;                          // tile loads issued (producer thread)
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---------------- TMA producer
     if (lane == 0) {
       tc::tma_prefetch_desc(&map_x);
@@ -188,7 +216,7 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
         issued = it + 1;
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 256, 0, 0);
@@ -197,63 +225,78 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
       for (int it = 0; ok && it < my_tiles; ++it) {
         const int b = it & 1;
         if (!wait_or_abort(&bars->a_ready[b], (it >> 1) & 1, ab)) break;
-        if (it >= 1 && !wait_or_abort(&bars->tmem_empty, (it - 1) & 1, ab)) break;
-        tc::tc_fence_after();
         const uint32_t a0 = tc::smem_addr(smem + OFF_X + b * X_BYTES);
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
-          const uint64_t ad = tc::smem_desc(a0 + ko, 16, 1024, tc::SWZ_128B);
-          for (int nh = 0; nh < 2; ++nh) {
+        for (int nh = 0; nh < 2 && ok; ++nh) {
+          if (it >= 1 && !wait_or_abort(&bars->acc_empty[nh], (it - 1) & 1, ab)) { ok = false; break; }
+          tc::tc_fence_after();
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
+            const uint64_t ad = tc::smem_desc(a0 + ko, 16, 1024, tc::SWZ_128B);
             const uint64_t bd = tc::smem_desc(w0 + (ks >> 2) * 65536 + nh * 32768 + (ks & 3) * 32,
                                               16, 1024, tc::SWZ_128B);
             tc::mma_bf16_ss(tmem + nh * 256, ad, bd, idesc, ks > 0);
           }
+          tc::mma_commit(&bars->acc_full[nh]);
         }
-        tc::mma_commit(&bars->tmem_full);
+        if (!ok) break;
         tc::mma_commit(&bars->x_empty[b]);
       }
       tc::mma_commit(&bars->drain);
       drain_wait(&bars->drain, 0);
     }
   } else {
-    // ---------------- LayerNorm + bias (prologue) and epilogue: thread = cell row
-    const int r = tid;                      // 0..127, TMEM lane r
+    // ---------------- workers: cell row r = TMEM lane, channel / column half hh
+    const int q4 = warp & 3, hh = warp >> 2;
+    const int r = q4 * 32 + lane;
     const long long NN = (long long)p.N * p.N;
+    // Epilogue: each 32-row x 32-column chunk goes TMEM -> registers -> bf16 in a
+    // swizzled smem staging tile -> one TMA store (full 64-byte row segments;
+    // rows past the last cell are clipped by the tensor bounds).
+    uint8_t* stg = smem + OFF_STG + warp * STG_BYTES;
     auto epilogue = [&](int it) -> bool {
-      if (!warp_wait_or_abort(&bars->tmem_full, it & 1, ab)) return false;
+      if (!warp_wait_or_abort(&bars->acc_full[hh], it & 1, ab)) return false;
       tc::tc_fence_after();
       const int tile = blockIdx.x + it * gridDim.x;
-      const long long cell = (long long)tile * BM + r;
-      const bool valid = cell < p.cells;
+      const int row0 = tile * BM + q4 * 32;
 #pragma unroll 1
-      for (int ch = 0; ch < 16; ++ch) {
+      for (int ch = 0; ch < 8; ++ch) {
         uint32_t acc[32];
-        tc::tmem_ld32(tc::tmem_addr(tmem, (warp & 3) * 32, ch * 32), acc);
+        tc::tmem_ld32(tc::tmem_addr(tmem, q4 * 32, hh * 256 + ch * 32), acc);
         tc::tmem_ld_wait();
-        const int sect = ch >> 2, col0 = (ch & 3) * 32;
+        const int sect = hh * 2 + (ch >> 2), col0 = (ch & 3) * 32;
         uint32_t packed[16];
         if (sect == 3) {
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const float z0 = __uint_as_float(acc[2 * e]) + s_bg[col0 + 2 * e];
             const float z1 = __uint_as_float(acc[2 * e + 1]) + s_bg[col0 + 2 * e + 1];
-            packed[e] = tc::pack_bf16x2(1.0f / (1.0f + __expf(-z0)), 1.0f / (1.0f + __expf(-z1)));
+            packed[e] = tc::pack_bf16x2(sigmoid_approx(z0), sigmoid_approx(z1));
           }
         } else {
 #pragma unroll
           for (int e = 0; e < 16; ++e)
             packed[e] = tc::pack_bf16x2(__uint_as_float(acc[2 * e]), __uint_as_float(acc[2 * e + 1]));
         }
-        if (valid) {
-          __nv_bfloat16* base = sect == 0 ? p.q : sect == 1 ? p.k : sect == 2 ? p.v : p.g;
-          uint4* dst = (uint4*)(base + cell * KD + col0);
+        if (ch > 0) {                      // the previous chunk's store has read the staging tile
+          if (lane == 0) tc::tma_store_wait_read<0>();
+          __syncwarp();
+        }
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
+        for (int c = 0; c < 4; ++c)
+          *(uint4*)(stg + tc::swz_offset(lane, c, 64)) =
+              make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const CUtensorMap* m = sect == 0 ? &map_q : sect == 1 ? &map_k : sect == 2 ? &map_v : &map_g;
+          tc::tma_store_2d(m, stg, col0, row0);
+          tc::tma_store_commit();
         }
       }
       tc::tc_fence_before();
-      tc::mbar_arrive(&bars->tmem_empty);
+      tc::mbar_arrive(&bars->acc_empty[hh]);
+      if (lane == 0) tc::tma_store_wait_read<0>();
+      __syncwarp();
       return true;
     };
     bool ok = true;
@@ -263,44 +306,64 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
       const int tile = blockIdx.x + it * gridDim.x;
       const long long cell = (long long)tile * BM + r;
       uint8_t* xs = smem + OFF_X + b * X_BYTES;
-      // Row r of the tile: 16 chunks of 8 bf16, chunk c in K-half c/8 at a swizzled slot.
-      float xv[KD];
+      // Row statistics from the whole row (both halves), two passes over smem.
+      auto chunk = [&](int c) -> uint4 {
+        return *(const uint4*)(xs + (c >> 3) * 16384 + tc::swz_offset(r, c & 7, 128));
+      };
+      float s0 = 0.f, s1 = 0.f;
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
-        const uint4 u = *(const uint4*)(xs + (c >> 3) * 16384 + tc::swz_offset(r, c & 7, 128));
+        const uint4 u = chunk(c);
+        s0 += (bf16_lo(u.x) + bf16_hi(u.x)) + (bf16_lo(u.y) + bf16_hi(u.y));
+        s1 += (bf16_lo(u.z) + bf16_hi(u.z)) + (bf16_lo(u.w) + bf16_hi(u.w));
+      }
+      const float mean = (s0 + s1) * (1.0f / KD);
+      float ss0 = 0.f, ss1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint4 u = chunk(c);
         const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          xv[c * 8 + 2 * e] = bf16_lo(w4[e]);
-          xv[c * 8 + 2 * e + 1] = bf16_hi(w4[e]);
+          const float d0 = bf16_lo(w4[e]) - mean, d1 = bf16_hi(w4[e]) - mean;
+          ss0 = fmaf(d0, d0, ss0);
+          ss1 = fmaf(d1, d1, ss1);
         }
       }
-      float s = 0.f;
+      const float rstd = rsqrtf((ss0 + ss1) * (1.0f / KD) + 1e-5f);
+      // Normalise (rounded to bf16 as the MMA sees it): keep this thread's half,
+      // and dot the whole row into bias heads 2*hh and 2*hh+1.
+      float bsum[2] = {0.f, 0.f};
+      uint32_t mine[32];
 #pragma unroll
-      for (int e = 0; e < KD; ++e) s += xv[e];
-      const float mean = s * (1.0f / KD);
-      float ss = 0.f;
+      for (int pass = 0; pass < 2; ++pass) {            // the other half, then this half
+        const int hf = pass == 0 ? 1 - hh : hh;
 #pragma unroll
-      for (int e = 0; e < KD; ++e) { const float d = xv[e] - mean; ss = fmaf(d, d, ss); }
-      const float rstd = rsqrtf(ss * (1.0f / KD) + 1e-5f);
-      float bsum[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int c = 0; c < 8; ++c) {
+          const uint4 u = chunk(hf * 8 + c);
+          const uint32_t in4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        uint32_t w4[4];
+          for (int e = 0; e < 4; ++e) {
+            const int i0 = hf * 64 + c * 8 + 2 * e;
+            const uint32_t pw = tc::pack_bf16x2((bf16_lo(in4[e]) - mean) * rstd * s_gamma[i0] + s_beta[i0],
+                                                (bf16_hi(in4[e]) - mean) * rstd * s_gamma[i0 + 1] + s_beta[i0 + 1]);
+            const float r0 = bf16_lo(pw), r1 = bf16_hi(pw);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i0 = c * 8 + 2 * e;
-          const float y0 = (xv[i0] - mean) * rstd * s_gamma[i0] + s_beta[i0];
-          const float y1 = (xv[i0 + 1] - mean) * rstd * s_gamma[i0 + 1] + s_beta[i0 + 1];
-          w4[e] = tc::pack_bf16x2(y0, y1);
-          const float r0 = bf16_lo(w4[e]), r1 = bf16_hi(w4[e]);
-#pragma unroll
-          for (int t = 0; t < 4; ++t)
-            bsum[t] = fmaf(r1, s_wb[t * KD + i0 + 1], fmaf(r0, s_wb[t * KD + i0], bsum[t]));
+            for (int t = 0; t < 2; ++t)
+              bsum[t] = fmaf(r1, s_wb[(2 * hh + t) * KD + i0 + 1],
+                             fmaf(r0, s_wb[(2 * hh + t) * KD + i0], bsum[t]));
+            if (pass == 1) mine[c * 4 + e] = pw;
+          }
         }
-        *(uint4*)(xs + (c >> 3) * 16384 + tc::swz_offset(r, c & 7, 128)) =
-            make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
+      // The other thread of this row reads both halves: write this half back
+      // only once every worker has finished reading the tile.
+      tc::mbar_arrive(&bars->ln_read[b]);
+      if (!warp_wait_or_abort(&bars->ln_read[b], (it >> 1) & 1, ab)) { ok = false; break; }
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *(uint4*)(xs + hh * 16384 + tc::swz_offset(r, c, 128)) =
+            make_uint4(mine[4 * c], mine[4 * c + 1], mine[4 * c + 2], mine[4 * c + 3]);
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(&bars->a_ready[b]);
       if (cell < p.cells) {
@@ -309,9 +372,13 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
         const long long rr = rc / p.N, cc = rc - rr * p.N;
         bool keep = true;
         if (p.mask_mode == TRI_ATTN_MASK_QUERY_KEY) keep = p.mask[cell] != 0;
-        for (int t = 0; t < p.h; ++t)
-          p.bias[((bb * p.h + t) * p.N + rr) * p.Nb + cc] =
-              __float2half_rn(keep ? bsum[t] * kLog2e : -INFINITY);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int head = 2 * hh + t;
+          if (head < p.h)
+            p.bias[((bb * p.h + head) * p.N + rr) * p.Nb + cc] =
+                __float2half_rn(keep ? bsum[t] * kLog2e : -INFINITY);
+        }
       }
       if (it >= 1 && !epilogue(it - 1)) { ok = false; break; }
     }
@@ -319,16 +386,17 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
   }
 
   // ---------------- teardown: every issued copy lands, every MMA completes
+  if (warp < 8 && lane == 0) tc::tma_store_wait_all<0>();
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     drain_wait(&bars->w_full, 0);
     for (int it = issued - 1; it >= 0 && it >= issued - 2; --it)
       drain_wait(&bars->x_full[it & 1], (it >> 1) & 1);
   }
   __syncthreads();
   tc::tc_fence_after();
-  if (warp == 5) tc::tmem_dealloc(tmem, 512);
+  if (warp == 9) tc::tmem_dealloc(tmem, 512);
 }
 }  // namespace k1
 
@@ -987,6 +1055,7 @@ bool map_heads(CUtensorMap* m, const void* base, int B, int N, int box_j) {
 
 struct TcState {
   CUtensorMap map_w, map_q, map_k, map_v, map_b, map_g, map_o, map_wo;
+  CUtensorMap st_q, st_k, st_v, st_g;      // K1 output stores: (cells, 128) bf16, 32 x 32 boxes
   unsigned char* row_any;    // (B*N) mask rows keeping some key
   uint32_t* mbits;           // (B*N, words) mask bits
   int words;
@@ -1051,6 +1120,17 @@ cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const voi
                         box, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   ok = ok && map_rows_bf16(&st->map_g, t->g, cells, 128);
+  {
+    void* outs[4] = {t->q, t->k, t->v, t->g};
+    CUtensorMap* maps[4] = {&st->st_q, &st->st_k, &st->st_v, &st->st_g};
+    for (int m = 0; m < 4 && ok; ++m) {
+      cuuint64_t dims[2] = {128, (cuuint64_t)cells};
+      cuuint64_t strides[1] = {256};
+      cuuint32_t box[2] = {32, 32};
+      ok = make_map(maps[m], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, outs[m], dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_64B);
+    }
+  }
   ok = ok && map_rows_bf16(&st->map_o, t->o, cells, 128);
   ok = ok && map_rows_bf16(&st->map_wo, t->w_out, 128, 128);
   if (!ok) return cudaErrorInvalidValue;
@@ -1095,7 +1175,8 @@ cudaError_t tri_tc_forward(tri_attn_s* t, cudaStream_t s, const void* x, const i
   p1.polls = t->wait_limit;
   int mark = 0;
   tri_mark(t, s, mark++, nullptr);
-  k1::ln_proj_tc<<<grid_rows, k1::kThreads, k1::SMEM, s>>>(map_x, st->map_w, p1);
+  k1::ln_proj_tc<<<grid_rows, k1::kThreads, k1::SMEM, s>>>(map_x, st->map_w, st->st_q, st->st_k,
+                                                           st->st_v, st->st_g, p1);
   tri_mark(t, s, mark++, "ln_proj_tc");
 
   {
