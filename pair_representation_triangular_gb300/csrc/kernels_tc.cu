@@ -23,6 +23,7 @@
 // 1-18 and layer definitions; "FW-GLM-5-1 l2_p6", quoted Model.forward.
 #include <math.h>
 #include <stdio.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -115,11 +116,9 @@ constexpr uint32_t W_BYTES = NQ * KD * 2;           // 128 KB, two K-halves of 6
 constexpr uint32_t X_BYTES = BM * KD * 2;           // 32 KB, two K-halves of 16 KB
 constexpr uint32_t OFF_W = 0;
 constexpr uint32_t OFF_X = OFF_W + W_BYTES;
-constexpr uint32_t OFF_PAR = OFF_X + 2 * X_BYTES;   // gamma, beta, bg [128] + Wb [4][128] fp32
-constexpr uint32_t PAR_BYTES = (3 * KD + 4 * KD) * 4;
-constexpr uint32_t OFF_STG = OFF_PAR + PAR_BYTES;   // per worker warp: 32 rows x 64 B staging
+constexpr uint32_t OFF_STG = OFF_X + 2 * X_BYTES;   // per worker warp: 2 x (32 rows x 64 B)
 constexpr uint32_t STG_BYTES = 32 * 64;
-constexpr uint32_t OFF_BAR = OFF_STG + 8 * STG_BYTES;
+constexpr uint32_t OFF_BAR = OFF_STG + 8 * 2 * STG_BYTES;
 constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;     // + alignment slack
 
 struct Bars {
@@ -129,10 +128,15 @@ struct Bars {
   int abort;
 };
 
+// LayerNorm and bias parameters travel by value in the kernel parameter block
+// (constant bank): every read index is known at compile time.
+struct Consts {
+  float gamma[KD], beta[KD], bg[KD], wb[4][KD];
+};
+
 struct Params {
   long long cells;
   int N, Nb, h, mask_mode, ntiles;
-  const float* gamma; const float* beta; const float* bg; const float* wb;   // fp32
   const int32_t* mask;
   __nv_bfloat16 *q, *k, *v, *g;
   __half* bias;                // (B, h, N, Nb) fp16, scaled by log2(e)
@@ -152,14 +156,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
            const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
            const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_g,
-           const Params p) {
+           const Params p, const __grid_constant__ Consts cst) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   Bars* bars = (Bars*)(smem + OFF_BAR);
-  float* s_gamma = (float*)(smem + OFF_PAR);
-  float* s_beta = s_gamma + KD;
-  float* s_bg = s_beta + KD;
-  float* s_wb = s_bg + KD;                 // [4][128]
+  const float* s_gamma = cst.gamma;
+  const float* s_beta = cst.beta;
+  const float* s_bg = cst.bg;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const Abort ab{&bars->abort, p.dev_err, p.polls};
 
@@ -170,19 +173,13 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
       tc::mbar_init(&bars->x_empty[b], 1);
       tc::mbar_init(&bars->a_ready[b], kWorkers);
       tc::mbar_init(&bars->acc_full[b], 1);
-      tc::mbar_init(&bars->acc_empty[b], 128);
+      tc::mbar_init(&bars->acc_empty[b], kWorkers);
       tc::mbar_init(&bars->ln_read[b], kWorkers);
     }
     tc::mbar_init(&bars->drain, 1);
     bars->abort = 0;
     tc::fence_mbar_init();
   }
-  for (int i = tid; i < KD; i += kThreads) {
-    s_gamma[i] = p.gamma[i];
-    s_beta[i] = p.beta[i];
-    s_bg[i] = p.bg[i];
-  }
-  for (int i = tid; i < 4 * KD; i += kThreads) s_wb[i] = i < p.h * KD ? p.wb[i] : 0.f;
   if (warp == 9) {
     tc::tmem_alloc(&bars->tmem_base, 512);
     tc::tmem_relinquish();
@@ -252,51 +249,59 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
     // Epilogue: each 32-row x 32-column chunk goes TMEM -> registers -> bf16 in a
     // swizzled smem staging tile -> one TMA store (full 64-byte row segments;
     // rows past the last cell are clipped by the tensor bounds).
-    uint8_t* stg = smem + OFF_STG + warp * STG_BYTES;
+    // The two warps of a lane quarter split every 128-column section (q, k, v,
+    // g) in halves, so both carry the same sigmoid load; accumulator half nh
+    // (q|k or v|g) is released as soon as both warps have read it.
+    uint8_t* stg0 = smem + OFF_STG + warp * 2 * STG_BYTES;
+    int nst = 0;                                  // TMA stores issued by this warp
     auto epilogue = [&](int it) -> bool {
-      if (!warp_wait_or_abort(&bars->acc_full[hh], it & 1, ab)) return false;
-      tc::tc_fence_after();
       const int tile = blockIdx.x + it * gridDim.x;
       const int row0 = tile * BM + q4 * 32;
 #pragma unroll 1
-      for (int ch = 0; ch < 8; ++ch) {
-        uint32_t acc[32];
-        tc::tmem_ld32(tc::tmem_addr(tmem, q4 * 32, hh * 256 + ch * 32), acc);
-        tc::tmem_ld_wait();
-        const int sect = hh * 2 + (ch >> 2), col0 = (ch & 3) * 32;
-        uint32_t packed[16];
-        if (sect == 3) {
+      for (int nh = 0; nh < 2; ++nh) {
+        if (!warp_wait_or_abort(&bars->acc_full[nh], it & 1, ab)) return false;
+        tc::tc_fence_after();
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          const int sect = nh * 2 + (cc >> 1);
+          const int col0 = hh * 64 + (cc & 1) * 32;          // within the section
+          uint32_t acc[32];
+          tc::tmem_ld32(tc::tmem_addr(tmem, q4 * 32, sect * 128 + col0), acc);
+          tc::tmem_ld_wait();
+          uint32_t packed[16];
+          if (sect == 3) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float z0 = __uint_as_float(acc[2 * e]) + s_bg[col0 + 2 * e];
-            const float z1 = __uint_as_float(acc[2 * e + 1]) + s_bg[col0 + 2 * e + 1];
-            packed[e] = tc::pack_bf16x2(sigmoid_approx(z0), sigmoid_approx(z1));
+            for (int e = 0; e < 16; ++e) {
+              const float z0 = __uint_as_float(acc[2 * e]) + s_bg[col0 + 2 * e];
+              const float z1 = __uint_as_float(acc[2 * e + 1]) + s_bg[col0 + 2 * e + 1];
+              packed[e] = tc::pack_bf16x2(sigmoid_approx(z0), sigmoid_approx(z1));
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              packed[e] = tc::pack_bf16x2(__uint_as_float(acc[2 * e]), __uint_as_float(acc[2 * e + 1]));
           }
-        } else {
+          uint8_t* stg = stg0 + (nst & 1) * STG_BYTES;
+          if (nst >= 2) {                    // the store two back has read this staging tile
+            if (lane == 0) tc::tma_store_wait_read<1>();
+            __syncwarp();
+          }
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            packed[e] = tc::pack_bf16x2(__uint_as_float(acc[2 * e]), __uint_as_float(acc[2 * e + 1]));
-        }
-        if (ch > 0) {                      // the previous chunk's store has read the staging tile
-          if (lane == 0) tc::tma_store_wait_read<0>();
+          for (int c = 0; c < 4; ++c)
+            *(uint4*)(stg + tc::swz_offset(lane, c, 64)) =
+                make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+          tc::fence_proxy_async_smem();
           __syncwarp();
+          if (lane == 0) {
+            const CUtensorMap* m = sect == 0 ? &map_q : sect == 1 ? &map_k : sect == 2 ? &map_v : &map_g;
+            tc::tma_store_2d(m, stg, col0, row0);
+            tc::tma_store_commit();
+          }
+          ++nst;
         }
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          *(uint4*)(stg + tc::swz_offset(lane, c, 64)) =
-              make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          const CUtensorMap* m = sect == 0 ? &map_q : sect == 1 ? &map_k : sect == 2 ? &map_v : &map_g;
-          tc::tma_store_2d(m, stg, col0, row0);
-          tc::tma_store_commit();
-        }
+        tc::tc_fence_before();
+        tc::mbar_arrive(&bars->acc_empty[nh]);
       }
-      tc::tc_fence_before();
-      tc::mbar_arrive(&bars->acc_empty[hh]);
-      if (lane == 0) tc::tma_store_wait_read<0>();
-      __syncwarp();
       return true;
     };
     bool ok = true;
@@ -350,8 +355,7 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
             const float r0 = bf16_lo(pw), r1 = bf16_hi(pw);
 #pragma unroll
             for (int t = 0; t < 2; ++t)
-              bsum[t] = fmaf(r1, s_wb[(2 * hh + t) * KD + i0 + 1],
-                             fmaf(r0, s_wb[(2 * hh + t) * KD + i0], bsum[t]));
+              bsum[t] = fmaf(r1, cst.wb[2 * hh + t][i0 + 1], fmaf(r0, cst.wb[2 * hh + t][i0], bsum[t]));
             if (pass == 1) mine[c * 4 + e] = pw;
           }
         }
@@ -1054,6 +1058,7 @@ bool map_heads(CUtensorMap* m, const void* base, int B, int N, int box_j) {
 }
 
 struct TcState {
+  k1::Consts consts;                        // LayerNorm / gate-bias / pair-bias weights (fp32)
   CUtensorMap map_w, map_q, map_k, map_v, map_b, map_g, map_o, map_wo;
   CUtensorMap st_q, st_k, st_v, st_g;      // K1 output stores: (cells, 128) bf16, 32 x 32 boxes
   unsigned char* row_any;    // (B*N) mask rows keeping some key
@@ -1105,6 +1110,14 @@ cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const voi
   for (int m = 0; m < 4 && e == cudaSuccess; ++m)
     e = cudaMemcpyAsync((char*)t->w_proj + m * wbytes, mats[m], wbytes, cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(t->w_out, Wo, wbytes, cudaMemcpyDeviceToDevice, s);
+  if (e != cudaSuccess) return e;
+  // fp32 copies of the small parameters, made by tri_attn_create, go by value.
+  memset(&st->consts, 0, sizeof(st->consts));
+  if (e == cudaSuccess) e = cudaMemcpyAsync(st->consts.gamma, t->gamma, D * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(st->consts.beta, t->beta, D * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(st->consts.bg, t->bg, D * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(st->consts.wb, t->wb_f32, (size_t)h * D * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return e;
 
   const long long cells = t->cells;
@@ -1169,14 +1182,14 @@ cudaError_t tri_tc_forward(tri_attn_s* t, cudaStream_t s, const void* x, const i
   k1::Params p1;
   p1.cells = cells; p1.N = N; p1.Nb = st->Nb; p1.h = h; p1.mask_mode = t->mask_mode;
   p1.ntiles = ntiles;
-  p1.gamma = t->gamma; p1.beta = t->beta; p1.bg = t->bg; p1.wb = t->wb_f32; p1.mask = mask;
+  p1.mask = mask;
   p1.q = (__nv_bfloat16*)t->q; p1.k = (__nv_bfloat16*)t->k; p1.v = (__nv_bfloat16*)t->v;
   p1.g = (__nv_bfloat16*)t->g; p1.bias = (__half*)t->bias; p1.dev_err = t->dev_err;
   p1.polls = t->wait_limit;
   int mark = 0;
   tri_mark(t, s, mark++, nullptr);
   k1::ln_proj_tc<<<grid_rows, k1::kThreads, k1::SMEM, s>>>(map_x, st->map_w, st->st_q, st->st_k,
-                                                           st->st_v, st->st_g, p1);
+                                                           st->st_v, st->st_g, p1, st->consts);
   tri_mark(t, s, mark++, "ln_proj_tc");
 
   {
