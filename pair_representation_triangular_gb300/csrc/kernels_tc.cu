@@ -409,40 +409,38 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
 // K2: flash row attention
 // ---------------------------------------------------------------------------
 namespace k2 {
-constexpr int R = 4;                    // rows i per work unit (share each bias tile)
-constexpr int JW = 2;                   // 128-query tiles per unit, one per softmax warpgroup
-constexpr int BQ = 128;                 // queries per tile
+constexpr int R = 3;                    // rows i per work unit = softmax warpgroups
+constexpr int BQ = 128;                 // queries j per unit
 constexpr int BK = 64;                  // keys per tile
 constexpr int DH = 32;                  // head dim
-constexpr int STAGES = 2;
+constexpr int STAGES = 3;
 constexpr int MAXW = 256;               // mask words per row (N <= 8192)
 constexpr float kRescale = 8.0f;        // log2 growth of the running max that forces a rescale
-// Warpgroup 0: warp 0 TMA, warps 1 and 2 issue the MMAs of softmax warpgroup
-// 0 and 1 (two independent issue streams overlap the fixed per-instruction
-// latency of small-N tcgen05 MMAs), warp 3 idle; warpgroups 1 and 2 are the
-// softmax warpgroups for query tiles 0 and 1. Registers move from the
-// control warpgroup to the softmax ones: 384 x 168 = 128 x 40 + 256 x 232.
-constexpr int kThreads = 384;
-constexpr int kRegsCtl = 40, kRegsSoftmax = 232;
-constexpr uint32_t Q_BYTES = BQ * DH * 2;            // 8 KB per (row, query tile)
+// Warpgroup 0: warp 0 TMA, warps 1-3 issue the MMAs of softmax warpgroups 1-3;
+// warpgroup w = 1..3 runs the softmax of row w - 1 of the unit. Registers move
+// from the control warpgroup to the softmax ones: 512 x 128 >= 128 x 48 + 384 x 152.
+constexpr int kThreads = 512;
+constexpr int kRegsCtl = 48, kRegsSoftmax = 152;
+constexpr int kTmemPerRow = 160;        // S0 (64) | S1 (64) | O (32) columns per softmax warpgroup
+constexpr uint32_t Q_BYTES = BQ * DH * 2;            // 8 KB per row
 constexpr uint32_t KV_BYTES = BK * DH * 2;           // 4 KB each of K and V
-constexpr uint32_t BIAS_BYTES = BQ * BK * 2;         // 16 KB fp16 bias tile per query tile
-constexpr uint32_t OFF_Q = 0;                        // [R][JW]
+constexpr uint32_t BIAS_BYTES = BQ * BK * 2;         // 16 KB fp16 bias tile
+constexpr uint32_t OFF_Q = 0;                        // [2][R] Q tiles
 constexpr uint32_t STAGE_KV = R * 2 * KV_BYTES;      // [R] K then V
-constexpr uint32_t STAGE_BYTES = STAGE_KV + JW * BIAS_BYTES;
-constexpr uint32_t OFF_STAGE = OFF_Q + R * JW * Q_BYTES;
+constexpr uint32_t STAGE_BYTES = STAGE_KV + BIAS_BYTES;
+constexpr uint32_t OFF_STAGE = OFF_Q + 2 * R * Q_BYTES;
 constexpr uint32_t OFF_BAR = OFF_STAGE + STAGES * STAGE_BYTES;
 constexpr uint32_t SMEM = OFF_BAR + 512 + 1024;
 
 struct Bars {
-  uint64_t q_full, q_empty, kv_full[STAGES], kv_empty[STAGES];
-  uint64_t s_ready[JW][2], s_free[JW][2], p_full[JW][2], o_free[JW], drain;
+  uint64_t q_full[2], q_empty[2], kv_full[STAGES], kv_empty[STAGES];
+  uint64_t s_ready[R][2], s_free[R][2], p_full[R][2], o_free[R], drain;
   uint32_t tmem_base;
   int abort;
 };
 
 struct Params {
-  int B, N, h, mask_mode, row_groups, jpairs, words, units;
+  int B, N, h, mask_mode, row_groups, jtiles, words, units;
   const uint32_t* mbits;          // (B*N rows, words): bit k = pair_mask[b, r, k] != 0, k < N
   const unsigned char* row_any;   // (B*N rows): the mask row keeps some key
   __nv_bfloat16* o;
@@ -452,29 +450,29 @@ struct Params {
 };
 
 struct Unit {
-  int b, t, rg, j0;               // j0: first query of the unit's 256-query pair
+  int b, t, rg, j0;
 };
 
 __device__ __forceinline__ Unit decode_unit(int u, const Params& p) {
   Unit un;
-  const int jp = u % p.jpairs;
-  un.t = (u / p.jpairs) % p.h;
-  const int rgb = u / (p.jpairs * p.h);
+  const int jt = u % p.jtiles;
+  un.t = (u / p.jtiles) % p.h;
+  const int rgb = u / (p.jtiles * p.h);
   un.rg = rgb % p.row_groups;
   un.b = rgb / p.row_groups;
-  un.j0 = jp * BQ * JW;
+  un.j0 = jt * BQ;
   return un;
 }
 
-// Persistent: CTA c serves work units c, c + G, c + 2G, ... A unit is (b, head t,
-// R rows i, 2 x 128 queries j); it streams 64-key tiles. Per tile the K and V
-// tiles of the R rows and one fp16 bias tile per query tile come in by TMA;
-// warpgroup w (queries j0 + 128w ...) reads its bias row once per key tile into
-// registers and uses it for all R rows. For each (key tile, row) item the MMA
-// thread computes S = Q K^T into one of the warpgroup's two TMEM S buffers; the
-// softmax writes P (bf16) back over S in TMEM, and O_r += P V accumulates in
-// TMEM. The running max is only moved (and O rescaled in TMEM) when it grows
-// by more than 2^8, so P stays <= 256.
+// Persistent: CTA c serves work units c, c + G, ... A unit is (b, head t, R = 3
+// rows i, 128 queries j); it streams 64-key tiles, each stage holding the K and
+// V tiles of the R rows and the one fp16 bias tile they share. Softmax
+// warpgroup r owns row r: per key tile its MMA thread computes S = Q K^T into
+// one of the warpgroup's two TMEM S buffers (the next tile's S while the
+// softmax works on the current one); the softmax adds the bias, applies the key
+// mask and the online softmax, and writes P (bf16) back over S in TMEM; O +=
+// P V accumulates in TMEM. The running max only moves (and O is rescaled in
+// TMEM) when it grows by more than 2^8, so P stays <= 256.
 __global__ void __launch_bounds__(kThreads, 1)
 row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
             const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_b,
@@ -486,26 +484,27 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
   const Abort ab{&bars->abort, p.dev_err, p.polls};
   const int N = p.N;
   const int KT = (N + BK - 1) / BK;
-  const int IPU = KT * R * JW;            // items per unit (both warpgroups)
   int my_units = 0;
   for (int u = blockIdx.x; u < p.units; u += gridDim.x) ++my_units;
 
   if (tid == 0) {
-    tc::mbar_init(&bars->q_full, 1);
-    tc::mbar_init(&bars->q_empty, JW);           // one commit per MMA thread
+    for (int q = 0; q < 2; ++q) {
+      tc::mbar_init(&bars->q_full[q], 1);
+      tc::mbar_init(&bars->q_empty[q], R);           // one commit per MMA thread
+    }
     for (int s = 0; s < STAGES; ++s) {
       tc::mbar_init(&bars->kv_full[s], 1);
-      tc::mbar_init(&bars->kv_empty[s], JW);
+      tc::mbar_init(&bars->kv_empty[s], R);
     }
-    for (int w = 0; w < JW; ++w) {
+    for (int r = 0; r < R; ++r) {
       for (int b2 = 0; b2 < 2; ++b2) {
-        tc::mbar_init(&bars->s_ready[w][b2], 1);
-        tc::mbar_init(&bars->s_free[w][b2], 1);
-        tc::mbar_init(&bars->p_full[w][b2], 128);
+        tc::mbar_init(&bars->s_ready[r][b2], 1);
+        tc::mbar_init(&bars->s_free[r][b2], 1);
+        tc::mbar_init(&bars->p_full[r][b2], 128);
       }
-      tc::mbar_init(&bars->o_free[w], 128);
+      tc::mbar_init(&bars->o_free[r], 128);
     }
-    tc::mbar_init(&bars->drain, JW);
+    tc::mbar_init(&bars->drain, R);
     bars->abort = 0;
     tc::fence_mbar_init();
   }
@@ -519,10 +518,10 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
   const uint32_t tmem = bars->tmem_base;
   int q_issued = 0, kg_issued = 0;          // producer: units / key tiles whose loads were issued
 
-  if (warp < 4) tc::regs_dec<kRegsCtl>();
-  if (warp == 0) {
-    // ---------------- TMA producer
-    if (lane == 0) {
+  if (warp < 4) {
+    tc::regs_dec<kRegsCtl>();
+    if (warp == 0 && lane == 0) {
+      // ---------------- TMA producer
       tc::tma_prefetch_desc(&map_q);
       tc::tma_prefetch_desc(&map_k);
       tc::tma_prefetch_desc(&map_v);
@@ -531,12 +530,12 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       for (int ui = 0; ok && ui < my_units; ++ui) {
         const Unit un = decode_unit(blockIdx.x + ui * gridDim.x, p);
         const int row0 = un.b * N + un.rg * R;
-        if (ui >= 1 && !wait_or_abort(&bars->q_empty, (ui - 1) & 1, ab)) break;
-        tc::mbar_arrive_expect_tx(&bars->q_full, R * JW * Q_BYTES);
+        const int qb = ui & 1;
+        if (ui >= 2 && !wait_or_abort(&bars->q_empty[qb], ((ui >> 1) - 1) & 1, ab)) break;
+        tc::mbar_arrive_expect_tx(&bars->q_full[qb], R * Q_BYTES);
         for (int r = 0; r < R; ++r)
-          for (int w = 0; w < JW; ++w)
-            tc::tma_load_3d(smem + OFF_Q + (r * JW + w) * Q_BYTES, &map_q, &bars->q_full,
-                            un.t * DH, un.j0 + w * BQ, row0 + r);
+          tc::tma_load_3d(smem + OFF_Q + (qb * R + r) * Q_BYTES, &map_q, &bars->q_full[qb],
+                          un.t * DH, un.j0, row0 + r);
         q_issued = ui + 1;
         for (int kt = 0; kt < KT; ++kt) {
           const int kg = kg_issued, s = kg % STAGES;
@@ -552,250 +551,210 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
             tc::tma_load_3d(st + r * 2 * KV_BYTES + KV_BYTES, &map_v, &bars->kv_full[s],
                             un.t * DH, kt * BK, row0 + r);
           }
-          for (int w = 0; w < JW; ++w)
-            tc::tma_load_3d(st + STAGE_KV + w * BIAS_BYTES, &map_b, &bars->kv_full[s], kt * BK,
-                            un.j0 + w * BQ, un.b * p.h + un.t);
+          tc::tma_load_3d(st + STAGE_KV, &map_b, &bars->kv_full[s], kt * BK, un.j0,
+                          un.b * p.h + un.t);
           kg_issued = kg + 1;
         }
       }
-    }
-  } else if (warp == 1 || warp == 2) {
-    // ---------------- MMA issuer of softmax warpgroup w (one thread)
-    if (lane == 0) {
-      const int w = warp - 1;
+    } else if (warp >= 1 && lane == 0) {
+      // ---------------- MMA issuer of softmax warpgroup r = warp - 1
+      const int r = warp - 1;
       constexpr uint32_t id_qk = tc::idesc_bf16_f32(128, BK, 0, 0);
       constexpr uint32_t id_pv = tc::idesc_bf16_f32(128, DH, 0, 1);
       const uint32_t q0 = tc::smem_addr(smem + OFF_Q);
       const uint32_t st0 = tc::smem_addr(smem + OFF_STAGE);
-      // Per warpgroup the order of events is fixed, so blocking waits (which
-      // suspend the thread in hardware) lose nothing: S for items 0 and 1, then
-      // P V(c) once P(c) is written and S(c + 2) once P V(c) has released the
-      // S buffer.
-      const int per_w = my_units * KT * R;
-      auto qk = [&](int a) -> bool {
-        const int ui = a / (KT * R), rem = a % (KT * R), kt = rem / R, r = rem % R;
-        const int kg = ui * KT + kt, s = kg % STAGES, sb = a & 1;
-        if (kt == 0 && r == 0 && !wait_or_abort(&bars->q_full, ui & 1, ab)) return false;
-        if (r == 0 && !wait_or_abort(&bars->kv_full[s], (kg / STAGES) & 1, ab)) return false;
-        if (a >= 2 && !wait_or_abort(&bars->s_free[w][sb], ((a >> 1) - 1) & 1, ab)) return false;
+      const uint32_t tr = tmem + r * kTmemPerRow;
+      const int total = my_units * KT;     // one item per key tile
+      // S for items 0 and 1, then P V(c) once P(c) is written and S(c + 2) once
+      // P V(c) has released the S buffer.
+      auto qk = [&](int c) -> bool {
+        const int ui = c / KT, kt = c % KT, s = c % STAGES, sb = c & 1;
+        if (kt == 0 && !wait_or_abort(&bars->q_full[ui & 1], (ui >> 1) & 1, ab)) return false;
+        if (!wait_or_abort(&bars->kv_full[s], (c / STAGES) & 1, ab)) return false;
+        if (c >= 2 && !wait_or_abort(&bars->s_free[r][sb], ((c >> 1) - 1) & 1, ab)) return false;
         tc::tc_fence_after();
-        const uint32_t qa = q0 + (r * JW + w) * Q_BYTES;
+        const uint32_t qa = q0 + ((ui & 1) * R + r) * Q_BYTES;
         const uint32_t ka = st0 + s * STAGE_BYTES + r * 2 * KV_BYTES;
         for (int ks = 0; ks < DH / 16; ++ks)
-          tc::mma_bf16_ss(tmem + w * 256 + sb * BK, tc::smem_desc(qa + ks * 32, 16, 512, tc::SWZ_64B),
+          tc::mma_bf16_ss(tr + sb * BK, tc::smem_desc(qa + ks * 32, 16, 512, tc::SWZ_64B),
                           tc::smem_desc(ka + ks * 32, 16, 512, tc::SWZ_64B), id_qk, ks > 0);
-        tc::mma_commit(&bars->s_ready[w][sb]);
-        if (kt == KT - 1 && r == R - 1) tc::mma_commit(&bars->q_empty);
+        tc::mma_commit(&bars->s_ready[r][sb]);
+        if (kt == KT - 1) tc::mma_commit(&bars->q_empty[ui & 1]);
         return true;
       };
       auto pv = [&](int c) -> bool {
-        const int ui = c / (KT * R), rem = c % (KT * R), kt = rem / R, r = rem % R;
-        const int kg = ui * KT + kt, s = kg % STAGES, sb = c & 1;
-        if (!wait_or_abort(&bars->p_full[w][sb], (c >> 1) & 1, ab)) return false;
-        if (kt == 0 && r == 0 && ui >= 1 && !wait_or_abort(&bars->o_free[w], (ui - 1) & 1, ab))
-          return false;
+        const int ui = c / KT, kt = c % KT, s = c % STAGES, sb = c & 1;
+        if (!wait_or_abort(&bars->p_full[r][sb], (c >> 1) & 1, ab)) return false;
+        if (kt == 0 && ui >= 1 && !wait_or_abort(&bars->o_free[r], (ui - 1) & 1, ab)) return false;
         tc::tc_fence_after();
         const uint32_t va = st0 + s * STAGE_BYTES + r * 2 * KV_BYTES + KV_BYTES;
         for (int ks = 0; ks < BK / 16; ++ks)
-          tc::mma_bf16_ts(tmem + w * 256 + 128 + r * DH, tmem + w * 256 + sb * BK + ks * 8,
+          tc::mma_bf16_ts(tr + 128, tr + sb * BK + ks * 8,
                           tc::smem_desc(va + ks * 1024, 16, 512, tc::SWZ_64B), id_pv,
                           (kt > 0 || ks > 0) ? 1u : 0u);
-        tc::mma_commit(&bars->s_free[w][sb]);
-        if (r == R - 1) tc::mma_commit(&bars->kv_empty[s]);
+        tc::mma_commit(&bars->s_free[r][sb]);
+        tc::mma_commit(&bars->kv_empty[s]);
         return true;
       };
       bool ok = true;
-      for (int a = 0; ok && a < 2 && a < per_w; ++a) ok = qk(a);
-      for (int c = 0; ok && c < per_w; ++c) {
+      for (int c = 0; ok && c < 2 && c < total; ++c) ok = qk(c);
+      for (int c = 0; ok && c < total; ++c) {
         ok = pv(c);
-        if (ok && c + 2 < per_w) ok = qk(c + 2);
+        if (ok && c + 2 < total) ok = qk(c + 2);
       }
       tc::mma_commit(&bars->drain);
       drain_wait(&bars->drain, 0);
     }
-  } else if (warp >= 4) {
-    // ---------------- softmax warpgroups
+  } else {
+    // ---------------- softmax warpgroups: row r of each unit, thread = query row
     tc::regs_inc<kRegsSoftmax>();
-    const int w = (warp >> 2) - 1;
+    const int r = (warp >> 2) - 1;
     const int jr = (warp & 3) * 32 + lane;          // query row of the tile = TMEM lane
-    const uint32_t tb = tmem + ((uint32_t)((warp & 3) * 32) << 16) + w * 256;
+    const uint32_t tb = tmem + ((uint32_t)((warp & 3) * 32) << 16) + r * kTmemPerRow;
     const float sc = p.scale_log2;
+    const float2 sc2 = make_float2(sc, sc);
     bool ok = true;
     for (int ui = 0; ok && ui < my_units; ++ui) {
       const Unit un = decode_unit(blockIdx.x + ui * gridDim.x, p);
-      const int j = un.j0 + w * BQ + jr;
-      const bool valid_j = j < N;
-      bool uni[R];
-      float m_used[R], l_run[R];
-      bool uni_q = false;
+      const int j = un.j0 + jr;
+      const int i = un.rg * R + r;
+      const bool valid = j < N && i < N;
+      bool uni;
       if (p.mask_mode == TRI_ATTN_MASK_QUERY_KEY)
-        uni_q = !(valid_j && p.row_any[(long long)un.b * N + j]);
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int i = un.rg * R + r;
-        uni[r] = uni_q || (p.mask_mode == TRI_ATTN_MASK_ROW_KEY &&
-                           !(i < N && p.row_any[(long long)un.b * N + i]));
-        m_used[r] = -INFINITY;
-        l_run[r] = 0.f;
-      }
-      // Row-key mask words of the R rows, fetched one key tile ahead.
-      uint32_t mw_next[R][2];
-      auto fetch_bits = [&](int kt) {
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const int i = un.rg * R + r;
-          mw_next[r][0] = mw_next[r][1] = 0xffffffffu;
-          if (p.mask_mode == TRI_ATTN_MASK_ROW_KEY && !uni[r] && kt < KT) {
-            const uint32_t* mw = p.mbits + ((long long)un.b * N + i) * p.words + 2 * kt;
-            mw_next[r][0] = __ldg(mw);
-            mw_next[r][1] = __ldg(mw + 1);
-          }
-        }
-      };
-      fetch_bits(0);
+        uni = !(j < N && p.row_any[(long long)un.b * N + j]);
+      else
+        uni = !(i < N && p.row_any[(long long)un.b * N + i]);
+      float m_used = -INFINITY, l_run = 0.f;
+      const uint32_t* mrow = p.mbits + ((long long)un.b * N + (i < N ? i : 0)) * p.words;
+      const bool use_bits = p.mask_mode == TRI_ATTN_MASK_ROW_KEY && !uni;
+      uint32_t nb0 = use_bits ? __ldg(mrow) : 0xffffffffu;
+      uint32_t nb1 = use_bits ? __ldg(mrow + 1) : 0xffffffffu;
       for (int kt = 0; ok && kt < KT; ++kt) {
-        const int kg = ui * KT + kt, s = kg % STAGES;
-        uint32_t mw_cur[R][2];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          mw_cur[r][0] = mw_next[r][0];
-          mw_cur[r][1] = mw_next[r][1];
+        const int c = ui * KT + kt, s = c % STAGES, sb = c & 1;
+        const uint32_t mb0 = nb0, mb1 = nb1;
+        if (use_bits && kt + 1 < KT) {                 // next tile's mask words, one ahead
+          nb0 = __ldg(mrow + 2 * kt + 2);
+          nb1 = __ldg(mrow + 2 * kt + 3);
         }
-        fetch_bits(kt + 1);
-        // Bias row of this query for the key tile, fp16 in smem -> fp32 registers.
-        if (!warp_wait_or_abort(&bars->kv_full[s], (kg / STAGES) & 1, ab)) { ok = false; break; }
-        float2 bf2[BK / 2];
-        {
-          const uint8_t* bs = smem + OFF_STAGE + s * STAGE_BYTES + STAGE_KV + w * BIAS_BYTES;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 u4 = *(const uint4*)(bs + tc::swz_offset(jr, c, 128));
-            const uint32_t hw[4] = {u4.x, u4.y, u4.z, u4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) bf2[c * 4 + e] = __half22float2(*(const __half2*)&hw[e]);
-          }
-        }
-        // Key bits of this tile: row-key mode per row, query-key mode only k < N.
         const int left = N - kt * BK;
         const uint32_t real0 = left >= 32 ? 0xffffffffu : (left <= 0 ? 0u : ((1u << left) - 1u));
         const uint32_t real1 = left >= 64 ? 0xffffffffu
                                : (left <= 32 ? 0u : ((1u << (left - 32)) - 1u));
+        const uint32_t bw0 = real0 & mb0, bw1 = real1 & mb1;
+        if (!warp_wait_or_abort(&bars->s_ready[r][sb], (c >> 1) & 1, ab)) { ok = false; break; }
+        tc::tc_fence_after();
+        uint32_t pk[BK / 2];
+        // A tile whose keys are all dropped (on a row that keeps some key)
+        // contributes exactly 0; a row or query that keeps no key weighs every
+        // real key 1 (uniform softmax). Neither needs S or an exp.
+        const bool live = !uni && (bw0 | bw1) != 0u;
+        if (__any_sync(0xffffffffu, live)) {
+          float2 x2[BK / 2];
+          tc::tmem_ld32(tb + sb * BK, *(uint32_t(*)[32])&x2[0]);
+          tc::tmem_ld32(tb + sb * BK + 32, *(uint32_t(*)[32])&x2[16]);
+          // The bias tile of this stage (the S MMA already waited for it).
+          if (!warp_wait_or_abort(&bars->kv_full[s], (c / STAGES) & 1, ab)) { ok = false; break; }
+          const uint8_t* bs = smem + OFF_STAGE + s * STAGE_BYTES + STAGE_KV;
+          uint4 bq[8];
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          if (!ok) continue;
-          const int uw = ui * KT * R + kt * R + r, sb = uw & 1;
-          do {
-          const uint32_t bw0 = real0 & mw_cur[r][0], bw1 = real1 & mw_cur[r][1];
-          if (!warp_wait_or_abort(&bars->s_ready[w][sb], (uw >> 1) & 1, ab)) { ok = false; break; }
-          tc::tc_fence_after();
-          uint32_t pk[BK / 2];
-          // A tile whose keys are all dropped (on a row that keeps some key)
-          // contributes exactly 0; a row or query that keeps no key weighs
-          // every real key 1 (uniform softmax). Neither needs S or an exp.
-          const bool dead = (bw0 | bw1) == 0u;
-          const bool live = !uni[r] && !dead;
-          if (__any_sync(0xffffffffu, live)) {
-            float2 x2[BK / 2];
-            tc::tmem_ld32(tb + sb * BK, *(uint32_t(*)[32])&x2[0]);
-            tc::tmem_ld32(tb + sb * BK + 32, *(uint32_t(*)[32])&x2[16]);
-            tc::tmem_ld_wait();
-            const float2 sc2 = make_float2(sc, sc);
+          for (int q = 0; q < 8; ++q) bq[q] = *(const uint4*)(bs + tc::swz_offset(jr, q, 128));
+          tc::tmem_ld_wait();
 #pragma unroll
-            for (int k = 0; k < BK / 2; ++k) x2[k] = __ffma2_rn(x2[k], sc2, bf2[k]);
-            if ((bw0 & bw1) != 0xffffffffu) {
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t hw[4] = {bq[q].x, bq[q].y, bq[q].z, bq[q].w};
 #pragma unroll
-              for (int k = 0; k < 16; ++k) {
-                if (!((bw0 >> (2 * k)) & 1u)) x2[k].x = -INFINITY;
-                if (!((bw0 >> (2 * k + 1)) & 1u)) x2[k].y = -INFINITY;
-                if (!((bw1 >> (2 * k)) & 1u)) x2[16 + k].x = -INFINITY;
-                if (!((bw1 >> (2 * k + 1)) & 1u)) x2[16 + k].y = -INFINITY;
-              }
-            }
-            float mx[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) mx[q] = fmaxf(x2[q].x, x2[q].y);
-#pragma unroll
-            for (int k = 4; k < BK / 2; ++k) mx[k & 3] = fmax3(mx[k & 3], x2[k].x, x2[k].y);
-            const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-            const float m_new = fmaxf(m_used[r], mt);
-            bool need = false;
-            if (live) {
-              if (m_used[r] == -INFINITY) m_used[r] = m_new;   // first live tile: O, l still 0
-              else if (m_new > m_used[r] + kRescale) need = true;
-            }
-            if (__any_sync(0xffffffffu, need)) {
-              // Warp-wide: rescale O_r in TMEM (lanes without a jump use 1).
-              const float alpha = need ? ex2_approx(m_used[r] - m_new) : 1.f;
-              if (need) m_used[r] = m_new;
-              l_run[r] *= alpha;
-              const int up = uw - 1;                   // PV(up) done => every PV on O_r done
-              if (!warp_wait_or_abort(&bars->s_free[w][up & 1], (up >> 1) & 1, ab)) { ok = false; break; }
-              tc::tc_fence_after();
-              uint32_t ov[32];
-              tc::tmem_ld32(tb + 128 + r * DH, ov);
-              tc::tmem_ld_wait();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-              tc::tmem_st32(tb + 128 + r * DH, ov);
-            }
-            const float mu = m_used[r] == -INFINITY ? 0.f : m_used[r];
-            const float2 nmu2 = make_float2(-mu, -mu);
-            float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                             make_float2(0.f, 0.f)};
-#pragma unroll
-            for (int k = 0; k < BK / 2; ++k) {
-              const float2 e2 = __fadd2_rn(x2[k], nmu2);
-              const float2 p2 = make_float2(ex2_approx(e2.x), ex2_approx(e2.y));
-              rs2[k & 3] = __fadd2_rn(rs2[k & 3], p2);
-              pk[k] = tc::pack_bf16x2(p2.x, p2.y);
-            }
-            const float2 t2 = __fadd2_rn(__fadd2_rn(rs2[0], rs2[1]), __fadd2_rn(rs2[2], rs2[3]));
-            if (live) l_run[r] += t2.x + t2.y;
+            for (int e = 0; e < 4; ++e)
+              x2[q * 4 + e] = __ffma2_rn(x2[q * 4 + e], sc2, __half22float2(*(const __half2*)&hw[e]));
           }
-          if (!live) {
-            // real-key weights 1 (uniform row) or all 0 (dead tile), in bf16 pairs
-            const uint32_t w0 = uni[r] ? real0 : 0u, w1 = uni[r] ? real1 : 0u;
+          if ((bw0 & bw1) != 0xffffffffu) {
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-              pk[k] = (((w0 >> (2 * k)) & 1u) ? 0x3F80u : 0u) | (((w0 >> (2 * k + 1)) & 1u) ? 0x3F800000u : 0u);
-              pk[16 + k] = (((w1 >> (2 * k)) & 1u) ? 0x3F80u : 0u) | (((w1 >> (2 * k + 1)) & 1u) ? 0x3F800000u : 0u);
-            }
-            if (uni[r]) {
-              m_used[r] = 0.f;
-              l_run[r] += (float)(__popc(w0) + __popc(w1));
+              if (!((bw0 >> (2 * k)) & 1u)) x2[k].x = -INFINITY;
+              if (!((bw0 >> (2 * k + 1)) & 1u)) x2[k].y = -INFINITY;
+              if (!((bw1 >> (2 * k)) & 1u)) x2[16 + k].x = -INFINITY;
+              if (!((bw1 >> (2 * k + 1)) & 1u)) x2[16 + k].y = -INFINITY;
             }
           }
-          tc::tmem_st32(tb + sb * BK, pk);            // P over the consumed S columns
-          tc::tmem_st_wait();
-          tc::tc_fence_before();
-          tc::mbar_arrive(&bars->p_full[w][sb]);
-          } while (0);
+          float mx[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) mx[q] = fmaxf(x2[q].x, x2[q].y);
+#pragma unroll
+          for (int k = 4; k < BK / 2; ++k) mx[k & 3] = fmax3(mx[k & 3], x2[k].x, x2[k].y);
+          const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+          const float m_new = fmaxf(m_used, mt);
+          bool need = false;
+          if (live) {
+            if (m_used == -INFINITY) m_used = m_new;      // first live tile: O, l still 0
+            else if (m_new > m_used + kRescale) need = true;
+          }
+          if (__any_sync(0xffffffffu, need)) {
+            // Warp-wide: rescale O in TMEM (lanes without a jump use 1) once
+            // the previous P V, the last one on O, has landed.
+            const float alpha = need ? ex2_approx(m_used - m_new) : 1.f;
+            if (need) m_used = m_new;
+            l_run *= alpha;
+            const int up = c - 1;
+            if (!warp_wait_or_abort(&bars->s_free[r][up & 1], (up >> 1) & 1, ab)) { ok = false; break; }
+            tc::tc_fence_after();
+            uint32_t ov[32];
+            tc::tmem_ld32(tb + 128, ov);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tc::tmem_st32(tb + 128, ov);
+          }
+          const float mu = m_used == -INFINITY ? 0.f : m_used;
+          const float2 nmu2 = make_float2(-mu, -mu);
+          float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                           make_float2(0.f, 0.f)};
+#pragma unroll
+          for (int k = 0; k < BK / 2; ++k) {
+            const float2 e2 = __fadd2_rn(x2[k], nmu2);
+            const float2 p2 = make_float2(ex2_approx(e2.x), ex2_approx(e2.y));
+            rs2[k & 3] = __fadd2_rn(rs2[k & 3], p2);
+            pk[k] = tc::pack_bf16x2(p2.x, p2.y);
+          }
+          const float2 t2 = __fadd2_rn(__fadd2_rn(rs2[0], rs2[1]), __fadd2_rn(rs2[2], rs2[3]));
+          if (live) l_run += t2.x + t2.y;
         }
+        if (!live) {
+          // real-key weights 1 (uniform row) or all 0 (dead tile), in bf16 pairs
+          const uint32_t w0 = uni ? real0 : 0u, w1 = uni ? real1 : 0u;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            pk[k] = (((w0 >> (2 * k)) & 1u) ? 0x3F80u : 0u) | (((w0 >> (2 * k + 1)) & 1u) ? 0x3F800000u : 0u);
+            pk[16 + k] = (((w1 >> (2 * k)) & 1u) ? 0x3F80u : 0u) | (((w1 >> (2 * k + 1)) & 1u) ? 0x3F800000u : 0u);
+          }
+          if (uni) {
+            m_used = 0.f;
+            l_run += (float)(__popc(w0) + __popc(w1));
+          }
+        }
+        tc::tmem_st32(tb + sb * BK, pk);              // P over the consumed S columns
+        tc::tmem_st_wait();
+        tc::tc_fence_before();
+        tc::mbar_arrive(&bars->p_full[r][sb]);
       }
       if (!ok) break;
-      // Unit epilogue: o = O / l for the R rows once the last PV has landed.
-      const int ulast = ui * KT * R + KT * R - 1;
-      if (!warp_wait_or_abort(&bars->s_free[w][ulast & 1], (ulast >> 1) & 1, ab)) { ok = false; break; }
+      // Unit epilogue: o = O / l once the last P V has landed.
+      const int clast = ui * KT + KT - 1;
+      if (!warp_wait_or_abort(&bars->s_free[r][clast & 1], (clast >> 1) & 1, ab)) { ok = false; break; }
       tc::tc_fence_after();
+      uint32_t ov[32];
+      tc::tmem_ld32(tb + 128, ov);
+      tc::tmem_ld_wait();
+      if (valid) {
+        const float inv = 1.0f / l_run;
+        uint32_t po[16];
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        uint32_t ov[32];
-        tc::tmem_ld32(tb + 128 + r * DH, ov);
-        tc::tmem_ld_wait();
-        const int i = un.rg * R + r;
-        if (valid_j && i < N) {
-          const float inv = 1.0f / l_run[r];
-          uint32_t pk[16];
+        for (int e = 0; e < DH; e += 2)
+          po[e / 2] = tc::pack_bf16x2(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
+        uint4* dst = (uint4*)(p.o + (((long long)un.b * N + i) * N + j) * (p.h * DH) + un.t * DH);
 #pragma unroll
-          for (int e = 0; e < DH; e += 2)
-            pk[e / 2] = tc::pack_bf16x2(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
-          uint4* dst = (uint4*)(p.o + (((long long)un.b * N + i) * N + j) * (p.h * DH) + un.t * DH);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        }
+        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(po[4 * q], po[4 * q + 1], po[4 * q + 2], po[4 * q + 3]);
       }
       tc::tc_fence_before();
-      tc::mbar_arrive(&bars->o_free[w]);
+      tc::mbar_arrive(&bars->o_free[r]);
     }
   }
 
@@ -803,7 +762,8 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0 && lane == 0) {
-    if (q_issued > 0) drain_wait(&bars->q_full, (q_issued - 1) & 1);
+    for (int ui = q_issued - 1; ui >= 0 && ui >= q_issued - 2; --ui)
+      drain_wait(&bars->q_full[ui & 1], (ui >> 1) & 1);
     for (int kg = kg_issued - 1; kg >= 0 && kg >= kg_issued - STAGES; --kg)
       drain_wait(&bars->kv_full[kg % STAGES], (kg / STAGES) & 1);
   }
@@ -1201,8 +1161,8 @@ cudaError_t tri_tc_forward(tri_attn_s* t, cudaStream_t s, const void* x, const i
   k2::Params p2;
   p2.B = B; p2.N = N; p2.h = h; p2.mask_mode = t->mask_mode;
   p2.row_groups = (N + k2::R - 1) / k2::R;
-  p2.jpairs = (N + k2::BQ * k2::JW - 1) / (k2::BQ * k2::JW);
-  p2.units = B * p2.row_groups * h * p2.jpairs;
+  p2.jtiles = (N + k2::BQ - 1) / k2::BQ;
+  p2.units = B * p2.row_groups * h * p2.jtiles;
   p2.words = st->words;
   p2.mbits = st->mbits; p2.row_any = st->row_any; p2.o = (__nv_bfloat16*)t->o;
   p2.dev_err = t->dev_err;
