@@ -48,9 +48,10 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
   if (tc::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = tc::global_timer_ns();
   for (long long n = 1; n < a.polls; ++n) {
-    if (tc::mbar_try_wait(bar, parity)) return true;
-    if (*(volatile int*)a.flag) return false;
-    if ((n & 255) == 0 && tc::global_timer_ns() - t0 > 2000000000ull) break;
+    // Sleeps up to 20 us per poll instead of spinning; the phase wakes it.
+    if (tc::mbar_try_wait_hint(bar, parity, 20000u)) return true;
+    if (tc::lds_volatile(a.flag)) return false;
+    if ((n & 15) == 0 && tc::global_timer_ns() - t0 > 2000000000ull) break;
   }
   *(volatile int*)a.flag = 1;
   atomicOr(a.dev_err, TRI_DEV_ERR_TIMEOUT);
@@ -91,6 +92,20 @@ __device__ __forceinline__ float sigmoid_approx(float z) {
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// fp16 half of a packed pair plus an fp32 value, rounded once in fp32.
+__device__ __forceinline__ float add_f16lo_f32(uint32_t h2, float c) {
+  float d;
+  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, lo, %2;\n\t}"
+      : "=f"(d) : "r"(h2), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float add_f16hi_f32(uint32_t h2, float c) {
+  float d;
+  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, hi, %2;\n\t}"
+      : "=f"(d) : "r"(h2), "f"(c));
   return d;
 }
 
@@ -414,14 +429,17 @@ constexpr int BQ = 128;                 // queries j per unit
 constexpr int BK = 64;                  // keys per tile
 constexpr int DH = 32;                  // head dim
 constexpr int STAGES = 3;
-constexpr int MAXW = 256;               // mask words per row (N <= 8192)
-constexpr float kRescale = 8.0f;        // log2 growth of the running max that forces a rescale
-// Warpgroup 0: warp 0 TMA, warps 1-3 issue the MMAs of softmax warpgroups 1-3;
-// warpgroup w = 1..3 runs the softmax of row w - 1 of the unit. Registers move
-// from the control warpgroup to the softmax ones: 512 x 128 >= 128 x 48 + 384 x 152.
+constexpr int kIssuers = R;             // MMA issuer warps, one row each
+// Warpgroup 0: warp 0 TMA, warp 1 + r issues the MMAs of row r; warpgroup
+// w = 1..3 runs the softmax of row w - 1 of the unit. Registers move from the
+// control warpgroup to the softmax ones: 512 x 128 >= 128 x 48 + 384 x 152.
 constexpr int kThreads = 512;
 constexpr int kRegsCtl = 48, kRegsSoftmax = 152;
-constexpr int kTmemPerRow = 160;        // S0 (64) | S1 (64) | O (32) columns per softmax warpgroup
+// TMEM per row: S (64 fp32 columns) | P (32 columns of bf16 pairs) | O (32).
+// S is free again as soon as the softmax has loaded it, so the next tile's
+// S = Q K^T runs during the current softmax.
+constexpr int kTmemPerRow = 128;
+constexpr int TM_P = 64, TM_O = 96;
 constexpr uint32_t Q_BYTES = BQ * DH * 2;            // 8 KB per row
 constexpr uint32_t KV_BYTES = BK * DH * 2;           // 4 KB each of K and V
 constexpr uint32_t BIAS_BYTES = BQ * BK * 2;         // 16 KB fp16 bias tile
@@ -434,7 +452,7 @@ constexpr uint32_t SMEM = OFF_BAR + 512 + 1024;
 
 struct Bars {
   uint64_t q_full[2], q_empty[2], kv_full[STAGES], kv_empty[STAGES];
-  uint64_t s_ready[R][2], s_free[R][2], p_full[R][2], o_free[R], drain;
+  uint64_t s_ready[R], s_free[R], p_full[R], p_free[R], o_free[R], drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -464,15 +482,22 @@ __device__ __forceinline__ Unit decode_unit(int u, const Params& p) {
   return un;
 }
 
+// Real-key bits of word w (keys 32w..32w+31 of a tile with `left` keys left).
+__device__ __forceinline__ uint32_t real_bits(int left, int w) {
+  const int n = left - 32 * w;
+  return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
+}
+
 // Persistent: CTA c serves work units c, c + G, ... A unit is (b, head t, R = 3
-// rows i, 128 queries j); it streams 64-key tiles, each stage holding the K and
-// V tiles of the R rows and the one fp16 bias tile they share. Softmax
-// warpgroup r owns row r: per key tile its MMA thread computes S = Q K^T into
-// one of the warpgroup's two TMEM S buffers (the next tile's S while the
-// softmax works on the current one); the softmax adds the bias, applies the key
-// mask and the online softmax, and writes P (bf16) back over S in TMEM; O +=
-// P V accumulates in TMEM. The running max only moves (and O is rescaled in
-// TMEM) when it grows by more than 2^8, so P stays <= 256.
+// rows i, 128 queries j); it streams 64-key tiles, each stage holding the K
+// and V tiles of the three rows and the fp16 bias tile they share. Softmax
+// warpgroup r owns row r; S = Q K^T of the next tile is computed into the
+// row's S columns as soon as the softmax has loaded the current one. The
+// softmax adds the bias, drops masked keys and writes P = 2^(x - mu) (bf16)
+// to the row's P columns in one pass; O += P V accumulates in TMEM. The
+// reference mu of a query row is the max of its first live tile and moves
+// (rescaling O in TMEM) only when a tile's sum of P reaches 2^32, so no
+// per-tile max is taken in the common case.
 __global__ void __launch_bounds__(kThreads, 1)
 row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
             const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_b,
@@ -490,21 +515,20 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
   if (tid == 0) {
     for (int q = 0; q < 2; ++q) {
       tc::mbar_init(&bars->q_full[q], 1);
-      tc::mbar_init(&bars->q_empty[q], R);           // one commit per MMA thread
+      tc::mbar_init(&bars->q_empty[q], kIssuers);    // one commit per issuer
     }
     for (int s = 0; s < STAGES; ++s) {
       tc::mbar_init(&bars->kv_full[s], 1);
-      tc::mbar_init(&bars->kv_empty[s], R);
+      tc::mbar_init(&bars->kv_empty[s], kIssuers);
     }
     for (int r = 0; r < R; ++r) {
-      for (int b2 = 0; b2 < 2; ++b2) {
-        tc::mbar_init(&bars->s_ready[r][b2], 1);
-        tc::mbar_init(&bars->s_free[r][b2], 1);
-        tc::mbar_init(&bars->p_full[r][b2], 128);
-      }
+      tc::mbar_init(&bars->s_ready[r], 1);
+      tc::mbar_init(&bars->s_free[r], 128);
+      tc::mbar_init(&bars->p_full[r], 128);
+      tc::mbar_init(&bars->p_free[r], 1);
       tc::mbar_init(&bars->o_free[r], 128);
     }
-    tc::mbar_init(&bars->drain, R);
+    tc::mbar_init(&bars->drain, kIssuers);
     bars->abort = 0;
     tc::fence_mbar_init();
   }
@@ -556,51 +580,51 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
           kg_issued = kg + 1;
         }
       }
-    } else if (warp >= 1 && lane == 0) {
-      // ---------------- MMA issuer of softmax warpgroup r = warp - 1
-      const int r = warp - 1;
+    } else if (warp >= 1 && warp <= R && lane == 0) {
+      // ---------------- MMA issuer of row r = warp - 1
+      const int ra = warp - 1;
       constexpr uint32_t id_qk = tc::idesc_bf16_f32(128, BK, 0, 0);
       constexpr uint32_t id_pv = tc::idesc_bf16_f32(128, DH, 0, 1);
       const uint32_t q0 = tc::smem_addr(smem + OFF_Q);
       const uint32_t st0 = tc::smem_addr(smem + OFF_STAGE);
-      const uint32_t tr = tmem + r * kTmemPerRow;
       const int total = my_units * KT;     // one item per key tile
-      // S for items 0 and 1, then P V(c) once P(c) is written and S(c + 2) once
-      // P V(c) has released the S buffer.
-      auto qk = [&](int c) -> bool {
-        const int ui = c / KT, kt = c % KT, s = c % STAGES, sb = c & 1;
+      // S(c + 1) as soon as the softmax has loaded S(c); P V(c) once P(c) is
+      // written.
+      auto qk = [&](int r, int c) -> bool {
+        const int ui = c / KT, kt = c % KT, s = c % STAGES;
         if (kt == 0 && !wait_or_abort(&bars->q_full[ui & 1], (ui >> 1) & 1, ab)) return false;
         if (!wait_or_abort(&bars->kv_full[s], (c / STAGES) & 1, ab)) return false;
-        if (c >= 2 && !wait_or_abort(&bars->s_free[r][sb], ((c >> 1) - 1) & 1, ab)) return false;
+        if (c >= 1 && !wait_or_abort(&bars->s_free[r], (c - 1) & 1, ab)) return false;
         tc::tc_fence_after();
         const uint32_t qa = q0 + ((ui & 1) * R + r) * Q_BYTES;
         const uint32_t ka = st0 + s * STAGE_BYTES + r * 2 * KV_BYTES;
+        const uint32_t tr = tmem + r * kTmemPerRow;
         for (int ks = 0; ks < DH / 16; ++ks)
-          tc::mma_bf16_ss(tr + sb * BK, tc::smem_desc(qa + ks * 32, 16, 512, tc::SWZ_64B),
+          tc::mma_bf16_ss(tr, tc::smem_desc(qa + ks * 32, 16, 512, tc::SWZ_64B),
                           tc::smem_desc(ka + ks * 32, 16, 512, tc::SWZ_64B), id_qk, ks > 0);
-        tc::mma_commit(&bars->s_ready[r][sb]);
+        tc::mma_commit(&bars->s_ready[r]);
         if (kt == KT - 1) tc::mma_commit(&bars->q_empty[ui & 1]);
         return true;
       };
-      auto pv = [&](int c) -> bool {
-        const int ui = c / KT, kt = c % KT, s = c % STAGES, sb = c & 1;
-        if (!wait_or_abort(&bars->p_full[r][sb], (c >> 1) & 1, ab)) return false;
+      auto pv = [&](int r, int c) -> bool {
+        const int ui = c / KT, kt = c % KT, s = c % STAGES;
+        if (!wait_or_abort(&bars->p_full[r], c & 1, ab)) return false;
         if (kt == 0 && ui >= 1 && !wait_or_abort(&bars->o_free[r], (ui - 1) & 1, ab)) return false;
         tc::tc_fence_after();
         const uint32_t va = st0 + s * STAGE_BYTES + r * 2 * KV_BYTES + KV_BYTES;
+        const uint32_t tr = tmem + r * kTmemPerRow;
         for (int ks = 0; ks < BK / 16; ++ks)
-          tc::mma_bf16_ts(tr + 128, tr + sb * BK + ks * 8,
+          tc::mma_bf16_ts(tr + TM_O, tr + TM_P + ks * 8,
                           tc::smem_desc(va + ks * 1024, 16, 512, tc::SWZ_64B), id_pv,
                           (kt > 0 || ks > 0) ? 1u : 0u);
-        tc::mma_commit(&bars->s_free[r][sb]);
+        tc::mma_commit(&bars->p_free[r]);
         tc::mma_commit(&bars->kv_empty[s]);
         return true;
       };
-      bool ok = true;
-      for (int c = 0; ok && c < 2 && c < total; ++c) ok = qk(c);
+      bool ok = total > 0 ? qk(ra, 0) : true;
       for (int c = 0; ok && c < total; ++c) {
-        ok = pv(c);
-        if (ok && c + 2 < total) ok = qk(c + 2);
+        if (c + 1 < total) ok = qk(ra, c + 1);
+        if (ok) ok = pv(ra, c);
       }
       tc::mma_commit(&bars->drain);
       drain_wait(&bars->drain, 0);
@@ -611,8 +635,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     const int r = (warp >> 2) - 1;
     const int jr = (warp & 3) * 32 + lane;          // query row of the tile = TMEM lane
     const uint32_t tb = tmem + ((uint32_t)((warp & 3) * 32) << 16) + r * kTmemPerRow;
-    const float sc = p.scale_log2;
-    const float2 sc2 = make_float2(sc, sc);
+    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
     bool ok = true;
     for (int ui = 0; ok && ui < my_units; ++ui) {
       const Unit un = decode_unit(blockIdx.x + ui * gridDim.x, p);
@@ -627,121 +650,161 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       float m_used = -INFINITY, l_run = 0.f;
       const uint32_t* mrow = p.mbits + ((long long)un.b * N + (i < N ? i : 0)) * p.words;
       const bool use_bits = p.mask_mode == TRI_ATTN_MASK_ROW_KEY && !uni;
-      uint32_t nb0 = use_bits ? __ldg(mrow) : 0xffffffffu;
-      uint32_t nb1 = use_bits ? __ldg(mrow + 1) : 0xffffffffu;
+      uint2 nbits = use_bits ? __ldg((const uint2*)mrow) : make_uint2(0xffffffffu, 0xffffffffu);
       for (int kt = 0; ok && kt < KT; ++kt) {
-        const int c = ui * KT + kt, s = c % STAGES, sb = c & 1;
-        const uint32_t mb0 = nb0, mb1 = nb1;
-        if (use_bits && kt + 1 < KT) {                 // next tile's mask words, one ahead
-          nb0 = __ldg(mrow + 2 * kt + 2);
-          nb1 = __ldg(mrow + 2 * kt + 3);
-        }
+        const int c = ui * KT + kt, s = c % STAGES;
+        const uint2 mb = nbits;
+        if (use_bits && kt + 1 < KT) nbits = __ldg((const uint2*)(mrow + 2 * (kt + 1)));
         const int left = N - kt * BK;
-        const uint32_t real0 = left >= 32 ? 0xffffffffu : (left <= 0 ? 0u : ((1u << left) - 1u));
-        const uint32_t real1 = left >= 64 ? 0xffffffffu
-                               : (left <= 32 ? 0u : ((1u << (left - 32)) - 1u));
-        const uint32_t bw0 = real0 & mb0, bw1 = real1 & mb1;
-        if (!warp_wait_or_abort(&bars->s_ready[r][sb], (c >> 1) & 1, ab)) { ok = false; break; }
-        tc::tc_fence_after();
-        uint32_t pk[BK / 2];
-        // A tile whose keys are all dropped (on a row that keeps some key)
-        // contributes exactly 0; a row or query that keeps no key weighs every
-        // real key 1 (uniform softmax). Neither needs S or an exp.
+        const uint32_t rl0 = real_bits(left, 0), rl1 = real_bits(left, 1);
+        const uint32_t bw0 = rl0 & mb.x, bw1 = rl1 & mb.y;
+        const bool all_kept = (bw0 & bw1) == 0xffffffffu;
         const bool live = !uni && (bw0 | bw1) != 0u;
-        if (__any_sync(0xffffffffu, live)) {
-          float2 x2[BK / 2];
-          tc::tmem_ld32(tb + sb * BK, *(uint32_t(*)[32])&x2[0]);
-          tc::tmem_ld32(tb + sb * BK + 32, *(uint32_t(*)[32])&x2[16]);
-          // The bias tile of this stage (the S MMA already waited for it).
-          if (!warp_wait_or_abort(&bars->kv_full[s], (c / STAGES) & 1, ab)) { ok = false; break; }
-          const uint8_t* bs = smem + OFF_STAGE + s * STAGE_BYTES + STAGE_KV;
-          uint4 bq[8];
+        // Bias row jr of the stage (128-byte swizzle: 16-byte chunk q of the row
+        // sits at chunk q ^ (jr & 7)); the row base is 128-byte aligned.
+        const uint32_t brow = tc::smem_addr(smem + OFF_STAGE + s * STAGE_BYTES + STAGE_KV) +
+                              jr * 128u + ((jr & 7u) << 4);
+        const bool any_live = __any_sync(0xffffffffu, live);
+        if (any_live && !warp_wait_or_abort(&bars->kv_full[s], (c / STAGES) & 1, ab)) { ok = false; break; }
+        if (!warp_wait_or_abort(&bars->s_ready[r], c & 1, ab)) { ok = false; break; }
+        tc::tc_fence_after();
+        float2 x2[BK / 2];
+        uint4 bq[8];                                   // the row's 64 fp16 biases
+        if (any_live) {
+          tc::tmem_ld32(tb, *(uint32_t(*)[32])&x2[0]);
+          tc::tmem_ld32(tb + 32, *(uint32_t(*)[32])&x2[16]);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) bq[q] = *(const uint4*)(bs + tc::swz_offset(jr, q, 128));
+          for (int q = 0; q < 8; ++q) bq[q] = tc::lds128(brow ^ (q << 4));
           tc::tmem_ld_wait();
+        }
+        tc::tc_fence_before();
+        tc::mbar_arrive(&bars->s_free[r]);            // S columns may take the next tile
+        if (any_live && !all_kept) {
+          // Dropped keys: S = -inf, which the bias add keeps at -inf (P = 0).
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            if (!((bw0 >> (2 * k)) & 1u)) x2[k].x = -INFINITY;
+            if (!((bw0 >> (2 * k + 1)) & 1u)) x2[k].y = -INFINITY;
+            if (!((bw1 >> (2 * k)) & 1u)) x2[16 + k].x = -INFINITY;
+            if (!((bw1 >> (2 * k + 1)) & 1u)) x2[16 + k].y = -INFINITY;
+          }
+        }
+        // Largest logit x = S * sc + bias of the tile, in log2 units.
+        auto tile_max = [&]() -> float {
+          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          const float2 z2 = make_float2(0.f, 0.f);
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             const uint32_t hw[4] = {bq[q].x, bq[q].y, bq[q].z, bq[q].w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              x2[q * 4 + e] = __ffma2_rn(x2[q * 4 + e], sc2, __half22float2(*(const __half2*)&hw[e]));
-          }
-          if ((bw0 & bw1) != 0xffffffffu) {
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              if (!((bw0 >> (2 * k)) & 1u)) x2[k].x = -INFINITY;
-              if (!((bw0 >> (2 * k + 1)) & 1u)) x2[k].y = -INFINITY;
-              if (!((bw1 >> (2 * k)) & 1u)) x2[16 + k].x = -INFINITY;
-              if (!((bw1 >> (2 * k + 1)) & 1u)) x2[16 + k].y = -INFINITY;
+            for (int e = 0; e < 4; ++e) {
+              const float2 y = __ffma2_rn(x2[q * 4 + e], sc2, z2);
+              mx[e] = fmax3(mx[e], add_f16lo_f32(hw[e], y.x), add_f16hi_f32(hw[e], y.y));
             }
           }
-          float mx[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) mx[q] = fmaxf(x2[q].x, x2[q].y);
-#pragma unroll
-          for (int k = 4; k < BK / 2; ++k) mx[k & 3] = fmax3(mx[k & 3], x2[k].x, x2[k].y);
-          const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-          const float m_new = fmaxf(m_used, mt);
-          bool need = false;
+          return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        };
+        // P = 2^(x - mu) for one 32-key quarter, packed in bf16 pairs, and its
+        // sum. A lane that is not live writes 1 on every real key of a uniform
+        // row or query, else 0.
+        auto p_part = [&](int hf, float mu, uint32_t (&pk)[16]) -> float2 {
+          float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
           if (live) {
-            if (m_used == -INFINITY) m_used = m_new;      // first live tile: O, l still 0
-            else if (m_new > m_used + kRescale) need = true;
-          }
-          if (__any_sync(0xffffffffu, need)) {
-            // Warp-wide: rescale O in TMEM (lanes without a jump use 1) once
-            // the previous P V, the last one on O, has landed.
-            const float alpha = need ? ex2_approx(m_used - m_new) : 1.f;
-            if (need) m_used = m_new;
-            l_run *= alpha;
-            const int up = c - 1;
-            if (!warp_wait_or_abort(&bars->s_free[r][up & 1], (up >> 1) & 1, ab)) { ok = false; break; }
-            tc::tc_fence_after();
-            uint32_t ov[32];
-            tc::tmem_ld32(tb + 128, ov);
-            tc::tmem_ld_wait();
+            const float2 nmu2 = make_float2(-mu, -mu);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tc::tmem_st32(tb + 128, ov);
-          }
-          const float mu = m_used == -INFINITY ? 0.f : m_used;
-          const float2 nmu2 = make_float2(-mu, -mu);
-          float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                           make_float2(0.f, 0.f)};
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const int q = hf * 4 + q4;
+              const uint32_t hw[4] = {bq[q].x, bq[q].y, bq[q].z, bq[q].w};
 #pragma unroll
-          for (int k = 0; k < BK / 2; ++k) {
-            const float2 e2 = __fadd2_rn(x2[k], nmu2);
-            const float2 p2 = make_float2(ex2_approx(e2.x), ex2_approx(e2.y));
-            rs2[k & 3] = __fadd2_rn(rs2[k & 3], p2);
-            pk[k] = tc::pack_bf16x2(p2.x, p2.y);
-          }
-          const float2 t2 = __fadd2_rn(__fadd2_rn(rs2[0], rs2[1]), __fadd2_rn(rs2[2], rs2[3]));
-          if (live) l_run += t2.x + t2.y;
-        }
-        if (!live) {
-          // real-key weights 1 (uniform row) or all 0 (dead tile), in bf16 pairs
-          const uint32_t w0 = uni ? real0 : 0u, w1 = uni ? real1 : 0u;
+              for (int e = 0; e < 4; ++e) {
+                const float2 y = __ffma2_rn(x2[q * 4 + e], sc2, nmu2);
+                const float2 p2 = make_float2(ex2_approx(add_f16lo_f32(hw[e], y.x)),
+                                              ex2_approx(add_f16hi_f32(hw[e], y.y)));
+                if (e & 1) sb = __fadd2_rn(sb, p2);
+                else sa = __fadd2_rn(sa, p2);
+                pk[q4 * 4 + e] = tc::pack_bf16x2(p2.x, p2.y);
+              }
+            }
+          } else {
+            const uint32_t w = uni ? (hf ? rl1 : rl0) : 0u;
+            if (w == 0u || w == 0xffffffffu) {
+              const uint32_t v = w ? 0x3F803F80u : 0u;
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            pk[k] = (((w0 >> (2 * k)) & 1u) ? 0x3F80u : 0u) | (((w0 >> (2 * k + 1)) & 1u) ? 0x3F800000u : 0u);
-            pk[16 + k] = (((w1 >> (2 * k)) & 1u) ? 0x3F80u : 0u) | (((w1 >> (2 * k + 1)) & 1u) ? 0x3F800000u : 0u);
+              for (int k = 0; k < 16; ++k) pk[k] = v;
+            } else {
+#pragma unroll
+              for (int k = 0; k < 16; ++k)
+                pk[k] = (((w >> (2 * k)) & 1u) ? 0x3F80u : 0u) | (((w >> (2 * k + 1)) & 1u) ? 0x3F800000u : 0u);
+            }
           }
-          if (uni) {
-            m_used = 0.f;
-            l_run += (float)(__popc(w0) + __popc(w1));
+          return __fadd2_rn(sa, sb);
+        };
+        // A lane's reference max mu is set on its first live tile and moves only
+        // when a tile's sum of P reaches 2^32 (its logits rose by more than
+        // about 26), so P stays finite and O, l never overflow in fp32.
+        if (any_live) {
+          const bool need_max = live && m_used == -INFINITY;
+          if (__any_sync(0xffffffffu, need_max)) {
+            const float mt = tile_max();
+            if (need_max) m_used = mt;
           }
         }
-        tc::tmem_st32(tb + sb * BK, pk);              // P over the consumed S columns
+        float mu = m_used == -INFINITY ? 0.f : m_used;
+        uint32_t pk[16];
+        float2 ts2 = p_part(0, mu, pk);
+        // P V(c - 1) still reads the P columns and is the last MMA on O.
+        if (c >= 1 && !warp_wait_or_abort(&bars->p_free[r], (c - 1) & 1, ab)) { ok = false; break; }
+        tc::tc_fence_after();
+        tc::tmem_st16(tb + TM_P, pk);
+        ts2 = __fadd2_rn(ts2, p_part(1, mu, pk));
+        tc::tmem_st16(tb + TM_P + 16, pk);
+        float tsum = ts2.x + ts2.y;
+        if (any_live) {
+          const bool ovf = live && !(tsum < 4294967296.f);
+          if (__any_sync(0xffffffffu, ovf)) {
+            // Rare: raise mu to the tile max, rescale O and l, redo P.
+            const float mt = tile_max();
+            float alpha = 1.f;
+            if (ovf) {
+              alpha = ex2_approx(m_used - mt);
+              m_used = mt;
+              mu = mt;
+              l_run *= alpha;
+            }
+            tc::tmem_st_wait();
+#pragma unroll 1
+            for (int oh = 0; oh < 2; ++oh) {
+              uint32_t ov[16];
+              tc::tmem_ld16(tb + TM_O + 16 * oh, ov);
+              tc::tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+              tc::tmem_st16(tb + TM_O + 16 * oh, ov);
+            }
+            ts2 = p_part(0, mu, pk);
+            tc::tmem_st16(tb + TM_P, pk);
+            ts2 = __fadd2_rn(ts2, p_part(1, mu, pk));
+            tc::tmem_st16(tb + TM_P + 16, pk);
+            tsum = ts2.x + ts2.y;
+          }
+        }
+        if (live) {
+          l_run += tsum;
+        } else if (uni) {
+          m_used = 0.f;
+          l_run += (float)(__popc(rl0) + __popc(rl1));
+        }
         tc::tmem_st_wait();
         tc::tc_fence_before();
-        tc::mbar_arrive(&bars->p_full[r][sb]);
+        tc::mbar_arrive(&bars->p_full[r]);
       }
       if (!ok) break;
       // Unit epilogue: o = O / l once the last P V has landed.
       const int clast = ui * KT + KT - 1;
-      if (!warp_wait_or_abort(&bars->s_free[r][clast & 1], (clast >> 1) & 1, ab)) { ok = false; break; }
+      if (!warp_wait_or_abort(&bars->p_free[r], clast & 1, ab)) { ok = false; break; }
       tc::tc_fence_after();
       uint32_t ov[32];
-      tc::tmem_ld32(tb + 128, ov);
+      tc::tmem_ld32(tb + TM_O, ov);
       tc::tmem_ld_wait();
       if (valid) {
         const float inv = 1.0f / l_run;
@@ -1035,7 +1098,7 @@ int round_up(int a, int b) { return (a + b - 1) / b * b; }
 
 bool tri_tc_supported(int B, int N, int D, int h) {
   const long long cells = (long long)B * N * N;
-  return D == 128 && h == 4 && N >= 1 && N <= k2::MAXW * 32 && cells < (1ll << 31) &&
+  return D == 128 && h == 4 && N >= 1 && N <= 8192 && cells < (1ll << 31) &&
          (long long)B * N < (1ll << 31) / 8;
 }
 
@@ -1062,7 +1125,7 @@ cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const voi
     t->bias = nullptr;
     e = cudaMalloc((void**)&t->bias, (size_t)B * h * N * st->Nb * 2);
   }
-  st->words = 2 * ((N + k2::BK - 1) / k2::BK);
+  st->words = 2 * ((N + k2::BK - 1) / k2::BK);   // two 32-key words per 64-key tile
   if (e == cudaSuccess) e = cudaMalloc((void**)&st->row_any, (size_t)B * N);
   if (e == cudaSuccess) e = cudaMalloc((void**)&st->mbits, (size_t)B * N * st->words * 4);
   const size_t wbytes = (size_t)D * D * 2;
@@ -1088,7 +1151,7 @@ cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const voi
   {
     cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)N, (cuuint64_t)B * h};
     cuuint64_t strides[2] = {(cuuint64_t)st->Nb * 2, (cuuint64_t)N * st->Nb * 2};
-    cuuint32_t box[3] = {k2::BK, (cuuint32_t)k2::BQ, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)k2::BQ, 1};   // 128-byte rows for SWIZZLE_128B
     ok = ok && make_map(&st->map_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, t->bias, dims, strides,
                         box, CU_TENSOR_MAP_SWIZZLE_128B);
   }
