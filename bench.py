@@ -59,19 +59,22 @@ def parse_args():
 
 # ------------------------------------------------------------------ workload math
 def algorithmic_work(w):
-    """Per-kernel algorithmic FLOPs and HBM bytes of one forward (bf16 path):
-    K1 reads x and writes q, k, v, g (bf16) and the fp32 bias plane; K2 reads
-    q, k, v, the bias plane and the mask, writes o; K3 reads g and o, writes out."""
+    """Per-kernel algorithmic FLOPs and HBM bytes of one forward, each tensor
+    read or written once: K1 reads x and writes q, k, v, g and the bias plane
+    (fp16 on the bf16 path, fp32 on the fp32 path); the mask summary reads the
+    int32 mask and writes its bit rows and row flags; K2 reads q, k, v, the bias
+    plane and the bit rows, writes o; K3 reads g and o, writes out."""
     P, D, h, N, B = w.cells, w.D, w.h, w.N, w.B
     s = 2 if w.dtype == "bf16" else 4
+    bias = (2 if w.dtype == "bf16" else 4) * P * h
+    bits = B * N * (1 + 8 * ((N + 63) // 64))
     return {
         "ln_proj": {"flops": 2.0 * P * D * (4 * D + h),
-                    "bytes": P * D * s + 4 * P * D * s + 4 * P * h},
+                    "bytes": P * D * s + 4 * P * D * s + bias},
         "row_attn": {"flops": 4.0 * B * N ** 3 * D,
-                     "bytes": 3 * P * D * s + 4 * P * h + 4 * P + P * D * s},
+                     "bytes": 3 * P * D * s + bias + bits + P * D * s},
         "gate_out": {"flops": 2.0 * P * D * D, "bytes": 3 * P * D * s},
-        "mask_summary": {"flops": 0.0,
-                         "bytes": 4 * P + B * N * (1 + 8 * ((N + 63) // 64))},
+        "mask_summary": {"flops": 0.0, "bytes": 4 * P + bits},
     }
 
 

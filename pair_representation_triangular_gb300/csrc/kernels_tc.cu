@@ -123,10 +123,13 @@ namespace k1 {
 constexpr int BM = 128;                 // cells per tile
 constexpr int KD = 128;                 // channels (GEMM K)
 constexpr int NQ = 512;                 // q|k|v|g columns
-// Warps 0-7 LayerNorm + epilogue (two per TMEM lane quarter: warp q handles the
-// channel half / column half 0, warp q + 4 half 1), warp 8 TMA, warp 9 MMA.
-constexpr int kWorkers = 256;
-constexpr int kThreads = kWorkers + 64;
+// Warps 0-7 LayerNorm (two per row: warp q handles channel half 0 of rows
+// 32q..32q+31, warp q + 4 half 1), warps 8-15 epilogue (two per TMEM lane
+// quarter, one per column half), warp 16 TMA, warp 17 MMA. The LayerNorm of
+// the next tile runs while the epilogue drains the current one.
+constexpr int kWorkers = 256;           // LayerNorm threads (and epilogue threads)
+constexpr int kThreads = 2 * kWorkers + 64;
+constexpr int kTmaWarp = 16, kMmaWarp = 17;
 constexpr uint32_t W_BYTES = NQ * KD * 2;           // 128 KB, two K-halves of 64 KB
 constexpr uint32_t X_BYTES = BM * KD * 2;           // 32 KB, two K-halves of 16 KB
 constexpr uint32_t OFF_W = 0;
@@ -136,9 +139,14 @@ constexpr uint32_t STG_BYTES = 32 * 64;
 constexpr uint32_t OFF_BAR = OFF_STG + 8 * 2 * STG_BYTES;
 constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;     // + alignment slack
 
+// The two worker warps of lane quarter q (q and q + 4), which share the tile's
+// rows, meet at named barrier 1 + q.
+__device__ __forceinline__ void pair_sync(int q) {
+  asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory");
+}
+
 struct Bars {
   uint64_t w_full, x_full[2], x_empty[2], a_ready[2], acc_full[2], acc_empty[2], drain;
-  uint64_t ln_read[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -162,8 +170,9 @@ struct Params {
 // Persistent: CTA c serves 128-cell tiles c, c + G, ... [Wq;Wk;Wv;Wg] (bf16,
 // K-major, 128 KB) stays in shared memory. Per tile the x tile arrives by TMA;
 // the 256 workers normalise it in place (the two threads of a cell each own
-// one 64-channel half and compute the row statistics from the whole row) and
-// compute two of the h = 4 bias outputs each from the bf16 x_hat; the MMA warp
+// one 64-channel half; each takes the row statistics from the whole row in one
+// shifted pass) and compute two of the h = 4 bias outputs each from the bf16
+// x_hat; the MMA warp
 // issues the two N = 256 halves (q|k, v|g) into TMEM columns 0-255 / 256-511,
 // each with its own full/empty barriers, so the next tile's first half can
 // start while the epilogue still reads the second.
@@ -189,13 +198,12 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
       tc::mbar_init(&bars->a_ready[b], kWorkers);
       tc::mbar_init(&bars->acc_full[b], 1);
       tc::mbar_init(&bars->acc_empty[b], kWorkers);
-      tc::mbar_init(&bars->ln_read[b], kWorkers);
     }
     tc::mbar_init(&bars->drain, 1);
     bars->abort = 0;
     tc::fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tc::tmem_alloc(&bars->tmem_base, 512);
     tc::tmem_relinquish();
   }
@@ -207,7 +215,7 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
   for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) ++my_tiles;
   int issued = 0;                          // tile loads issued (producer thread)
 
-  if (warp == 8) {
+  if (warp == kTmaWarp) {
     // ---------------- TMA producer
     if (lane == 0) {
       tc::tma_prefetch_desc(&map_x);
@@ -228,7 +236,7 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
         issued = it + 1;
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 256, 0, 0);
@@ -256,18 +264,104 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
       tc::mma_commit(&bars->drain);
       drain_wait(&bars->drain, 0);
     }
-  } else {
-    // ---------------- workers: cell row r = TMEM lane, channel / column half hh
+  } else if (warp < kWorkers / 32) {
+    // ---------------- LayerNorm: cell row r, channel half hh
     const int q4 = warp & 3, hh = warp >> 2;
     const int r = q4 * 32 + lane;
     const long long NN = (long long)p.N * p.N;
+    bool ok = true;
+    for (int it = 0; ok && it < my_tiles; ++it) {
+      const int b = it & 1;
+      if (!warp_wait_or_abort(&bars->x_full[b], (it >> 1) & 1, ab)) { ok = false; break; }
+      const int tile = blockIdx.x + it * gridDim.x;
+      const long long cell = (long long)tile * BM + r;
+      uint8_t* xs = smem + OFF_X + b * X_BYTES;
+      auto chunk = [&](int c) -> uint4 {
+        return *(const uint4*)(xs + (c >> 3) * 16384 + tc::swz_offset(r, c & 7, 128));
+      };
+      // Row statistics in one pass over the whole row, shifted by its first
+      // channel K so that the sum of squares does not cancel.
+      const float K0 = bf16_lo(chunk(0).x);
+      const float2 nk2 = make_float2(-K0, -K0);
+      float2 s2 = make_float2(0.f, 0.f), q2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint4 u = chunk(c);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 d = __fadd2_rn(make_float2(bf16_lo(w4[e]), bf16_hi(w4[e])), nk2);
+          s2 = __fadd2_rn(s2, d);
+          q2 = __ffma2_rn(d, d, q2);
+        }
+      }
+      const float S1 = (s2.x + s2.y) * (1.0f / KD);             // mean of x - K
+      const float var = fmaxf((q2.x + q2.y) * (1.0f / KD) - S1 * S1, 0.f);
+      const float mean = K0 + S1;
+      const float rstd = rsqrtf(var + 1e-5f);
+      // Normalise (rounded to bf16 as the MMA sees it): keep this thread's half,
+      // and dot the whole row into bias heads 2*hh and 2*hh+1.
+      const float2 rs2 = make_float2(rstd, rstd), nm2 = make_float2(-mean * rstd, -mean * rstd);
+      float2 bp[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      uint32_t mine[32];
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass) {            // the other half, then this half
+        const int hf = pass == 0 ? 1 - hh : hh;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 u = chunk(hf * 8 + c);
+          const uint32_t in4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i0 = hf * 64 + c * 8 + 2 * e;
+            const float2 t = __ffma2_rn(make_float2(bf16_lo(in4[e]), bf16_hi(in4[e])), rs2, nm2);
+            const float2 y = __ffma2_rn(t, make_float2(s_gamma[i0], s_gamma[i0 + 1]),
+                                        make_float2(s_beta[i0], s_beta[i0 + 1]));
+            const uint32_t pw = tc::pack_bf16x2(y.x, y.y);
+            const float2 rr = make_float2(bf16_lo(pw), bf16_hi(pw));
+#pragma unroll
+            for (int t2 = 0; t2 < 2; ++t2)
+              bp[t2] = __ffma2_rn(rr, make_float2(cst.wb[2 * hh + t2][i0], cst.wb[2 * hh + t2][i0 + 1]), bp[t2]);
+            if (pass == 1) mine[c * 4 + e] = pw;
+          }
+        }
+      }
+      // The other thread of this row has read both halves once it reaches the
+      // pair barrier; then each thread writes its own half back.
+      pair_sync(q4);
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *(uint4*)(xs + hh * 16384 + tc::swz_offset(r, c, 128)) =
+            make_uint4(mine[4 * c], mine[4 * c + 1], mine[4 * c + 2], mine[4 * c + 3]);
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&bars->a_ready[b]);
+      const float bsum[2] = {bp[0].x + bp[0].y, bp[1].x + bp[1].y};
+      if (cell < p.cells) {
+        const long long bb = cell / NN;
+        const long long rc = cell - bb * NN;
+        const long long rr = rc / p.N, cc = rc - rr * p.N;
+        bool keep = true;
+        if (p.mask_mode == TRI_ATTN_MASK_QUERY_KEY) keep = p.mask[cell] != 0;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int head = 2 * hh + t;
+          if (head < p.h)
+            p.bias[((bb * p.h + head) * p.N + rr) * p.Nb + cc] =
+                __float2half_rn(keep ? bsum[t] * kLog2e : -INFINITY);
+        }
+      }
+    }
+  } else if (warp < 2 * kWorkers / 32) {
+    // ---------------- epilogue: cell row r = TMEM lane, column half hh
+    const int ew = warp - kWorkers / 32;
+    const int q4 = ew & 3, hh = ew >> 2;
     // Epilogue: each 32-row x 32-column chunk goes TMEM -> registers -> bf16 in a
     // swizzled smem staging tile -> one TMA store (full 64-byte row segments;
     // rows past the last cell are clipped by the tensor bounds).
     // The two warps of a lane quarter split every 128-column section (q, k, v,
     // g) in halves, so both carry the same sigmoid load; accumulator half nh
     // (q|k or v|g) is released as soon as both warps have read it.
-    uint8_t* stg0 = smem + OFF_STG + warp * 2 * STG_BYTES;
+    uint8_t* stg0 = smem + OFF_STG + ew * 2 * STG_BYTES;
     int nst = 0;                                  // TMA stores issued by this warp
     auto epilogue = [&](int it) -> bool {
       const int tile = blockIdx.x + it * gridDim.x;
@@ -319,103 +413,22 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
       }
       return true;
     };
-    bool ok = true;
-    for (int it = 0; ok && it < my_tiles; ++it) {
-      const int b = it & 1;
-      if (!warp_wait_or_abort(&bars->x_full[b], (it >> 1) & 1, ab)) { ok = false; break; }
-      const int tile = blockIdx.x + it * gridDim.x;
-      const long long cell = (long long)tile * BM + r;
-      uint8_t* xs = smem + OFF_X + b * X_BYTES;
-      // Row statistics from the whole row (both halves), two passes over smem.
-      auto chunk = [&](int c) -> uint4 {
-        return *(const uint4*)(xs + (c >> 3) * 16384 + tc::swz_offset(r, c & 7, 128));
-      };
-      float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint4 u = chunk(c);
-        s0 += (bf16_lo(u.x) + bf16_hi(u.x)) + (bf16_lo(u.y) + bf16_hi(u.y));
-        s1 += (bf16_lo(u.z) + bf16_hi(u.z)) + (bf16_lo(u.w) + bf16_hi(u.w));
-      }
-      const float mean = (s0 + s1) * (1.0f / KD);
-      float ss0 = 0.f, ss1 = 0.f;
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint4 u = chunk(c);
-        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float d0 = bf16_lo(w4[e]) - mean, d1 = bf16_hi(w4[e]) - mean;
-          ss0 = fmaf(d0, d0, ss0);
-          ss1 = fmaf(d1, d1, ss1);
-        }
-      }
-      const float rstd = rsqrtf((ss0 + ss1) * (1.0f / KD) + 1e-5f);
-      // Normalise (rounded to bf16 as the MMA sees it): keep this thread's half,
-      // and dot the whole row into bias heads 2*hh and 2*hh+1.
-      float bsum[2] = {0.f, 0.f};
-      uint32_t mine[32];
-#pragma unroll
-      for (int pass = 0; pass < 2; ++pass) {            // the other half, then this half
-        const int hf = pass == 0 ? 1 - hh : hh;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 u = chunk(hf * 8 + c);
-          const uint32_t in4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i0 = hf * 64 + c * 8 + 2 * e;
-            const uint32_t pw = tc::pack_bf16x2((bf16_lo(in4[e]) - mean) * rstd * s_gamma[i0] + s_beta[i0],
-                                                (bf16_hi(in4[e]) - mean) * rstd * s_gamma[i0 + 1] + s_beta[i0 + 1]);
-            const float r0 = bf16_lo(pw), r1 = bf16_hi(pw);
-#pragma unroll
-            for (int t = 0; t < 2; ++t)
-              bsum[t] = fmaf(r1, cst.wb[2 * hh + t][i0 + 1], fmaf(r0, cst.wb[2 * hh + t][i0], bsum[t]));
-            if (pass == 1) mine[c * 4 + e] = pw;
-          }
-        }
-      }
-      // The other thread of this row reads both halves: write this half back
-      // only once every worker has finished reading the tile.
-      tc::mbar_arrive(&bars->ln_read[b]);
-      if (!warp_wait_or_abort(&bars->ln_read[b], (it >> 1) & 1, ab)) { ok = false; break; }
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *(uint4*)(xs + hh * 16384 + tc::swz_offset(r, c, 128)) =
-            make_uint4(mine[4 * c], mine[4 * c + 1], mine[4 * c + 2], mine[4 * c + 3]);
-      tc::fence_proxy_async_smem();
-      tc::mbar_arrive(&bars->a_ready[b]);
-      if (cell < p.cells) {
-        const long long bb = cell / NN;
-        const long long rc = cell - bb * NN;
-        const long long rr = rc / p.N, cc = rc - rr * p.N;
-        bool keep = true;
-        if (p.mask_mode == TRI_ATTN_MASK_QUERY_KEY) keep = p.mask[cell] != 0;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int head = 2 * hh + t;
-          if (head < p.h)
-            p.bias[((bb * p.h + head) * p.N + rr) * p.Nb + cc] =
-                __float2half_rn(keep ? bsum[t] * kLog2e : -INFINITY);
-        }
-      }
-      if (it >= 1 && !epilogue(it - 1)) { ok = false; break; }
-    }
-    if (ok && my_tiles > 0) epilogue(my_tiles - 1);
+    for (int it = 0; it < my_tiles; ++it)
+      if (!epilogue(it)) break;
   }
 
   // ---------------- teardown: every issued copy lands, every MMA completes
-  if (warp < 8 && lane == 0) tc::tma_store_wait_all<0>();
+  if (warp >= kWorkers / 32 && warp < 2 * kWorkers / 32 && lane == 0) tc::tma_store_wait_all<0>();
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 8 && lane == 0) {
+  if (warp == kTmaWarp && lane == 0) {
     drain_wait(&bars->w_full, 0);
     for (int it = issued - 1; it >= 0 && it >= issued - 2; --it)
       drain_wait(&bars->x_full[it & 1], (it >> 1) & 1);
   }
   __syncthreads();
   tc::tc_fence_after();
-  if (warp == 9) tc::tmem_dealloc(tmem, 512);
+  if (warp == kMmaWarp) tc::tmem_dealloc(tmem, 512);
 }
 }  // namespace k1
 
