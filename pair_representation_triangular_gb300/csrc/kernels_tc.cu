@@ -649,21 +649,33 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     const int jr = (warp & 3) * 32 + lane;          // query row of the tile = TMEM lane
     const uint32_t tb = tmem + ((uint32_t)((warp & 3) * 32) << 16) + r * kTmemPerRow;
     const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+    // A unit's mask summary (its query row's or key row's "keeps some key"
+    // flag, and the row's first mask word) is loaded one unit ahead.
+    auto unit_loads = [&](int u, unsigned& any, uint2& bits0) {
+      const Unit nu = decode_unit(u, p);
+      const int nj = nu.j0 + jr, ni = nu.rg * R + r;
+      if (p.mask_mode == TRI_ATTN_MASK_QUERY_KEY)
+        any = nj < N ? __ldg(p.row_any + (long long)nu.b * N + nj) : 0u;
+      else
+        any = ni < N ? __ldg(p.row_any + (long long)nu.b * N + ni) : 0u;
+      bits0 = __ldg((const uint2*)(p.mbits + ((long long)nu.b * N + (ni < N ? ni : 0)) * p.words));
+    };
+    unsigned nx_any = 0u;
+    uint2 nx_bits = make_uint2(0u, 0u);
+    if (my_units > 0) unit_loads(blockIdx.x, nx_any, nx_bits);
     bool ok = true;
     for (int ui = 0; ok && ui < my_units; ++ui) {
       const Unit un = decode_unit(blockIdx.x + ui * gridDim.x, p);
       const int j = un.j0 + jr;
       const int i = un.rg * R + r;
       const bool valid = j < N && i < N;
-      bool uni;
-      if (p.mask_mode == TRI_ATTN_MASK_QUERY_KEY)
-        uni = !(j < N && p.row_any[(long long)un.b * N + j]);
-      else
-        uni = !(i < N && p.row_any[(long long)un.b * N + i]);
+      const bool uni = nx_any == 0u;
+      const uint2 bits0 = nx_bits;
+      if (ui + 1 < my_units) unit_loads(blockIdx.x + (ui + 1) * gridDim.x, nx_any, nx_bits);
       float m_used = -INFINITY, l_run = 0.f;
       const uint32_t* mrow = p.mbits + ((long long)un.b * N + (i < N ? i : 0)) * p.words;
       const bool use_bits = p.mask_mode == TRI_ATTN_MASK_ROW_KEY && !uni;
-      uint2 nbits = use_bits ? __ldg((const uint2*)mrow) : make_uint2(0xffffffffu, 0xffffffffu);
+      uint2 nbits = use_bits ? bits0 : make_uint2(0xffffffffu, 0xffffffffu);
       for (int kt = 0; ok && kt < KT; ++kt) {
         const int c = ui * KT + kt, s = c % STAGES;
         const uint2 mb = nbits;
@@ -819,6 +831,10 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       uint32_t ov[32];
       tc::tmem_ld32(tb + TM_O, ov);
       tc::tmem_ld_wait();
+      // O is in registers: its columns may take the next unit before the
+      // global stores below are issued.
+      tc::tc_fence_before();
+      tc::mbar_arrive(&bars->o_free[r]);
       if (valid) {
         const float inv = 1.0f / l_run;
         uint32_t po[16];
@@ -829,8 +845,6 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
 #pragma unroll
         for (int q = 0; q < 4; ++q) dst[q] = make_uint4(po[4 * q], po[4 * q + 1], po[4 * q + 2], po[4 * q + 3]);
       }
-      tc::tc_fence_before();
-      tc::mbar_arrive(&bars->o_free[r]);
     }
   }
 
