@@ -78,6 +78,58 @@ def algorithmic_work(w):
     }
 
 
+# DRAM traffic per pair cell (dram__bytes_read.sum + dram__bytes_write.sum of
+# one launch, divided by its B*N^2 cells) from the ncu capture of the B=1,
+# N=384 bf16 workload summarised in profiles/kernels_b1-n384-d128-h4-bf16-pad320.md.
+# It holds for the tensor-core kernel sources whose SHA-256 prefix is recorded
+# here; for any other source the bench reports traffic as null.
+TRAFFIC_SOURCES = ("kernels_tc.cu", "tc_ptx.cuh", "common.cuh")
+TRAFFIC_PER_CELL = {
+    "source_sha256": "913ed778902d1e06",
+    "capture": "b1-n384-d128-h4-bf16-pad320",
+    "ln_proj_tc": (37.936128e6 + 96.833024e6) / 147456,
+    "row_attn_tc": (114.522624e6 + 15.438592e6) / 147456,
+    "gate_out_tc": (75.560704e6 + 3.693568e6) / 147456,
+}
+
+
+def kernel_source_sha() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, "pair_representation_triangular_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, cells: int):
+    """Bytes one launch of `kernel` moves to and from DRAM, scaled by cells from
+    the recorded capture, or None if the kernel sources changed since."""
+    per_cell = TRAFFIC_PER_CELL.get(kernel)
+    if per_cell is None or kernel_source_sha() != TRAFFIC_PER_CELL["source_sha256"]:
+        return None
+    return per_cell * cells
+
+
+def max_over_ranks(x: float, device) -> float:
+    """Largest value of x over all ranks of the default process group (x itself
+    when no group is initialised or it has one rank)."""
+    import torch
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return x
+    if torch.distributed.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(cells_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Pair-cells per second over all ranks: every rank runs its own forward of
+    `cells_per_rank` cells per step, and the slowest rank's step time counts."""
+    return world * cells_per_rank / (ms_per_step / 1e3)
+
+
 def kernel_key(name: str) -> str:
     for k in ("ln_proj", "row_attn", "gate_out", "mask_summary"):
         if name.startswith(k):
@@ -275,13 +327,9 @@ def run_native(args, rank, world):
     if st != tb.TRI_ATTN_OK:
         raise RuntimeError(f"timed forward failed: {tb.tri_attn_status_string(st)}")
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms_total = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(sum(step_ms), dev)
     ms_per_step = ms_total / args.steps
-    value = world * w.cells / (ms_per_step / 1e3)
+    value = whole_job_rate(w.cells, world, ms_per_step)
 
     # e2e: host buffers through the C ABI (copies inside the timed region)
     tb.tri_attn_enable_kernel_timing(mod.handle, False)
@@ -293,11 +341,7 @@ def run_native(args, rank, world):
     t0 = time.perf_counter()
     for _ in range(args.e2e_steps):
         mod.forward_host(xh, mh, oh)
-    e2e_s = (time.perf_counter() - t0) / args.e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / args.e2e_steps, dev)
     h2d = xh.numel() * xh.element_size() + mh.numel() * mh.element_size()
     d2h = oh.numel() * oh.element_size()
 
@@ -327,7 +371,10 @@ def run_native(args, rank, world):
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["kernel"] = top
     roof["peak_source"] = peak_src + " (burst)"
-    roof["traffic"] = None
+    roof["traffic"] = measured_traffic(top, w.cells) if w.dtype == "bf16" else None
+    if roof["traffic"] is not None:
+        roof["traffic_note"] = ("dram read+write bytes per launch, scaled by cells from the ncu "
+                                "capture of " + TRAFFIC_PER_CELL["capture"])
     roof["kernel_ms"] = {k: round(v, 5) for k, v in avg.items()}
     roof["kernel_share"] = {k: round(v / total, 4) for k, v in avg.items()}
     roof["kernel_roofline_frac"] = {}
