@@ -44,8 +44,12 @@ struct Abort {
 
 // Bounded wait; on time-out or when another role has already aborted, raises
 // the abort flag (and records a time-out) and returns false.
+__device__ __forceinline__ bool wait_or_abort_slow(uint64_t* bar, uint32_t parity, const Abort a);
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const Abort& a) {
   if (tc::mbar_try_wait(bar, parity)) return true;
+  return wait_or_abort_slow(bar, parity, a);
+}
+__device__ __forceinline__ bool wait_or_abort_slow(uint64_t* bar, uint32_t parity, const Abort a) {
   const uint64_t t0 = tc::global_timer_ns();
   for (long long n = 1; n < a.polls; ++n) {
     // Sleeps up to 20 us per poll instead of spinning; the phase wakes it.
@@ -501,6 +505,89 @@ __device__ __forceinline__ uint32_t real_bits(int left, int w) {
   return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
 }
 
+// P = 2^(S sc + bias - mu) of one 32-key half (keys 32 hf ..), packed in bf16
+// pairs, and its sum; a lane that is not live writes 1 on every real key of a
+// uniform row or query (`w` = that half's real-key bits), else 0.
+__device__ __forceinline__ float2 p_half(const float2 (&x2)[BK / 2], const uint4 (&bq)[8], int hf,
+                                         float2 sc2, float mu, bool live, uint32_t w,
+                                         uint32_t (&pk)[16]) {
+  float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
+  if (live) {
+    const float2 nmu2 = make_float2(-mu, -mu);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const int q = hf * 4 + q4;
+      const uint32_t hw[4] = {bq[q].x, bq[q].y, bq[q].z, bq[q].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 y = __ffma2_rn(x2[q * 4 + e], sc2, nmu2);
+        const float2 p2 = make_float2(ex2_approx(add_f16lo_f32(hw[e], y.x)),
+                                      ex2_approx(add_f16hi_f32(hw[e], y.y)));
+        if (e & 1) sb = __fadd2_rn(sb, p2);
+        else sa = __fadd2_rn(sa, p2);
+        pk[q4 * 4 + e] = tc::pack_bf16x2(p2.x, p2.y);
+      }
+    }
+  } else if (w == 0u || w == 0xffffffffu) {
+    const uint32_t v = w ? 0x3F803F80u : 0u;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) pk[k] = v;
+  } else {
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+      pk[k] = (((w >> (2 * k)) & 1u) ? 0x3F80u : 0u) | (((w >> (2 * k + 1)) & 1u) ? 0x3F800000u : 0u);
+  }
+  return __fadd2_rn(sa, sb);
+}
+
+// Largest logit x = S sc + bias of a 64-key tile, in log2 units.
+__device__ __forceinline__ float tile_max(const float2 (&x2)[BK / 2], const uint4 (&bq)[8], float2 sc2) {
+  float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  const float2 z2 = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint32_t hw[4] = {bq[q].x, bq[q].y, bq[q].z, bq[q].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 y = __ffma2_rn(x2[q * 4 + e], sc2, z2);
+      mx[e] = fmax3(mx[e], add_f16lo_f32(hw[e], y.x), add_f16hi_f32(hw[e], y.y));
+    }
+  }
+  return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+}
+
+// Rare path: some lane's sum of P over the tile reached 2^32. Those lanes raise mu to
+// the tile max; O (in TMEM) and l are rescaled, and the tile's P is recomputed
+// and stored again. Called by whole warps once the P V that last read P and O
+// has completed. Returns the new sum of P of the tile.
+__device__ __forceinline__ float redo_tile(const float2 (&x2)[BK / 2], const uint4 (&bq)[8], uint32_t tb,
+                                        float2 sc2, bool live, bool ovf, uint32_t w0, uint32_t w1,
+                                        float& m_used, float& l_run) {
+  const float mt = tile_max(x2, bq, sc2);
+  float alpha = 1.f;
+  if (ovf) {
+    alpha = ex2_approx(m_used - mt);
+    m_used = mt;
+    l_run *= alpha;
+  }
+  tc::tmem_st_wait();
+#pragma unroll 1
+  for (int oh = 0; oh < 2; ++oh) {
+    uint32_t ov[16];
+    tc::tmem_ld16(tb + TM_O + 16 * oh, ov);
+    tc::tmem_ld_wait();
+#pragma unroll
+    for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+    tc::tmem_st16(tb + TM_O + 16 * oh, ov);
+  }
+  uint32_t pk[16];
+  float2 ts2 = p_half(x2, bq, 0, sc2, m_used, live, w0, pk);
+  tc::tmem_st16(tb + TM_P, pk);
+  ts2 = __fadd2_rn(ts2, p_half(x2, bq, 1, sc2, m_used, live, w1, pk));
+  tc::tmem_st16(tb + TM_P + 16, pk);
+  return ts2.x + ts2.y;
+}
+
 // Persistent: CTA c serves work units c, c + G, ... A unit is (b, head t, R = 3
 // rows i, 128 queries j); it streams 64-key tiles, each stage holding the K
 // and V tiles of the three rows and the fp16 bias tile they share. Softmax
@@ -714,104 +801,30 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
             if (!((bw1 >> (2 * k + 1)) & 1u)) x2[16 + k].y = -INFINITY;
           }
         }
-        // Largest logit x = S * sc + bias of the tile, in log2 units.
-        auto tile_max = [&]() -> float {
-          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-          const float2 z2 = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint32_t hw[4] = {bq[q].x, bq[q].y, bq[q].z, bq[q].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 y = __ffma2_rn(x2[q * 4 + e], sc2, z2);
-              mx[e] = fmax3(mx[e], add_f16lo_f32(hw[e], y.x), add_f16hi_f32(hw[e], y.y));
-            }
-          }
-          return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        };
-        // P = 2^(x - mu) for one 32-key quarter, packed in bf16 pairs, and its
-        // sum. A lane that is not live writes 1 on every real key of a uniform
-        // row or query, else 0.
-        auto p_part = [&](int hf, float mu, uint32_t (&pk)[16]) -> float2 {
-          float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
-          if (live) {
-            const float2 nmu2 = make_float2(-mu, -mu);
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              const int q = hf * 4 + q4;
-              const uint32_t hw[4] = {bq[q].x, bq[q].y, bq[q].z, bq[q].w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 y = __ffma2_rn(x2[q * 4 + e], sc2, nmu2);
-                const float2 p2 = make_float2(ex2_approx(add_f16lo_f32(hw[e], y.x)),
-                                              ex2_approx(add_f16hi_f32(hw[e], y.y)));
-                if (e & 1) sb = __fadd2_rn(sb, p2);
-                else sa = __fadd2_rn(sa, p2);
-                pk[q4 * 4 + e] = tc::pack_bf16x2(p2.x, p2.y);
-              }
-            }
-          } else {
-            const uint32_t w = uni ? (hf ? rl1 : rl0) : 0u;
-            if (w == 0u || w == 0xffffffffu) {
-              const uint32_t v = w ? 0x3F803F80u : 0u;
-#pragma unroll
-              for (int k = 0; k < 16; ++k) pk[k] = v;
-            } else {
-#pragma unroll
-              for (int k = 0; k < 16; ++k)
-                pk[k] = (((w >> (2 * k)) & 1u) ? 0x3F80u : 0u) | (((w >> (2 * k + 1)) & 1u) ? 0x3F800000u : 0u);
-            }
-          }
-          return __fadd2_rn(sa, sb);
-        };
         // A lane's reference max mu is set on its first live tile and moves only
         // when a tile's sum of P reaches 2^32 (its logits rose by more than
         // about 26), so P stays finite and O, l never overflow in fp32.
         if (any_live) {
           const bool need_max = live && m_used == -INFINITY;
           if (__any_sync(0xffffffffu, need_max)) {
-            const float mt = tile_max();
+            const float mt = tile_max(x2, bq, sc2);
             if (need_max) m_used = mt;
           }
         }
-        float mu = m_used == -INFINITY ? 0.f : m_used;
+        const float mu = m_used == -INFINITY ? 0.f : m_used;
+        const uint32_t w0 = uni ? rl0 : 0u, w1 = uni ? rl1 : 0u;
         uint32_t pk[16];
-        float2 ts2 = p_part(0, mu, pk);
+        float2 ts2 = p_half(x2, bq, 0, sc2, mu, live, w0, pk);
         // P V(c - 1) still reads the P columns and is the last MMA on O.
         if (c >= 1 && !warp_wait_or_abort(&bars->p_free[r], (c - 1) & 1, ab)) { ok = false; break; }
         tc::tc_fence_after();
         tc::tmem_st16(tb + TM_P, pk);
-        ts2 = __fadd2_rn(ts2, p_part(1, mu, pk));
+        ts2 = __fadd2_rn(ts2, p_half(x2, bq, 1, sc2, mu, live, w1, pk));
         tc::tmem_st16(tb + TM_P + 16, pk);
         float tsum = ts2.x + ts2.y;
         if (any_live) {
           const bool ovf = live && !(tsum < 4294967296.f);
-          if (__any_sync(0xffffffffu, ovf)) {
-            // Rare: raise mu to the tile max, rescale O and l, redo P.
-            const float mt = tile_max();
-            float alpha = 1.f;
-            if (ovf) {
-              alpha = ex2_approx(m_used - mt);
-              m_used = mt;
-              mu = mt;
-              l_run *= alpha;
-            }
-            tc::tmem_st_wait();
-#pragma unroll 1
-            for (int oh = 0; oh < 2; ++oh) {
-              uint32_t ov[16];
-              tc::tmem_ld16(tb + TM_O + 16 * oh, ov);
-              tc::tmem_ld_wait();
-#pragma unroll
-              for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-              tc::tmem_st16(tb + TM_O + 16 * oh, ov);
-            }
-            ts2 = p_part(0, mu, pk);
-            tc::tmem_st16(tb + TM_P, pk);
-            ts2 = __fadd2_rn(ts2, p_part(1, mu, pk));
-            tc::tmem_st16(tb + TM_P + 16, pk);
-            tsum = ts2.x + ts2.y;
-          }
+          if (__any_sync(0xffffffffu, ovf)) tsum = redo_tile(x2, bq, tb, sc2, live, ovf, w0, w1, m_used, l_run);
         }
         if (live) {
           l_run += tsum;
