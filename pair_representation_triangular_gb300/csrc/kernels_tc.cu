@@ -452,11 +452,13 @@ constexpr int kIssuers = R;             // MMA issuer warps, one row each
 // control warpgroup to the softmax ones: 512 x 128 >= 128 x 48 + 384 x 152.
 constexpr int kThreads = 512;
 constexpr int kRegsCtl = 48, kRegsSoftmax = 152;
-// TMEM per row: S (64 fp32 columns) | P (32 columns of bf16 pairs) | O (32).
-// S is free again as soon as the softmax has loaded it, so the next tile's
-// S = Q K^T runs during the current softmax.
-constexpr int kTmemPerRow = 128;
-constexpr int TM_P = 64, TM_O = 96;
+// TMEM per row: S0 | S1 (64 fp32 columns each) | O (32). Tile c's S lands in
+// buffer c & 1 and its P (bf16 pairs, 32 columns) is written over it; the MMA
+// thread issues P V(c) and then S(c + 2) into the same buffer, so the tensor
+// pipe's issue order keeps them apart and S(c + 1) is already waiting in the
+// other buffer while tile c's softmax runs.
+constexpr int kTmemPerRow = 160;
+constexpr int TM_S1 = 64, TM_O = 128;
 constexpr uint32_t Q_BYTES = BQ * DH * 2;            // 8 KB per row
 constexpr uint32_t KV_BYTES = BK * DH * 2;           // 4 KB each of K and V
 constexpr uint32_t BIAS_BYTES = BQ * BK * 2;         // 16 KB fp16 bias tile
@@ -469,7 +471,10 @@ constexpr uint32_t SMEM = OFF_BAR + 512 + 1024;
 
 struct Bars {
   uint64_t q_full[2], q_empty[2], kv_full[STAGES], kv_empty[STAGES];
-  uint64_t s_ready[R], s_free[R], p_full[R], p_free[R], o_free[R], drain;
+  // s_ready and p_full follow the S/P buffer (tile parity): a warp with no live
+  // lanes runs ahead, and its arrivals for tile c + 1 must not complete the
+  // phase of tile c.
+  uint64_t s_ready[R][2], p_full[R][2], p_free[R][2], o_free[R], drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -557,12 +562,12 @@ __device__ __forceinline__ float tile_max(const float2 (&x2)[BK / 2], const uint
 }
 
 // Rare path: some lane's sum of P over the tile reached 2^32. Those lanes raise mu to
-// the tile max; O (in TMEM) and l are rescaled, and the tile's P is recomputed
-// and stored again. Called by whole warps once the P V that last read P and O
+// the tile max; O (in TMEM, at tb + TM_O) and l are rescaled, and the tile's P
+// is recomputed and stored again at tp. Called by whole warps once the P V that last read P and O
 // has completed. Returns the new sum of P of the tile.
 __device__ __forceinline__ float redo_tile(const float2 (&x2)[BK / 2], const uint4 (&bq)[8], uint32_t tb,
-                                        float2 sc2, bool live, bool ovf, uint32_t w0, uint32_t w1,
-                                        float& m_used, float& l_run) {
+                                        uint32_t tp, float2 sc2, bool live, bool ovf, uint32_t w0,
+                                        uint32_t w1, float& m_used, float& l_run) {
   const float mt = tile_max(x2, bq, sc2);
   float alpha = 1.f;
   if (ovf) {
@@ -582,9 +587,9 @@ __device__ __forceinline__ float redo_tile(const float2 (&x2)[BK / 2], const uin
   }
   uint32_t pk[16];
   float2 ts2 = p_half(x2, bq, 0, sc2, m_used, live, w0, pk);
-  tc::tmem_st16(tb + TM_P, pk);
+  tc::tmem_st16(tp, pk);
   ts2 = __fadd2_rn(ts2, p_half(x2, bq, 1, sc2, m_used, live, w1, pk));
-  tc::tmem_st16(tb + TM_P + 16, pk);
+  tc::tmem_st16(tp + 16, pk);
   return ts2.x + ts2.y;
 }
 
@@ -622,10 +627,12 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       tc::mbar_init(&bars->kv_empty[s], kIssuers);
     }
     for (int r = 0; r < R; ++r) {
-      tc::mbar_init(&bars->s_ready[r], 1);
-      tc::mbar_init(&bars->s_free[r], 128);
-      tc::mbar_init(&bars->p_full[r], 128);
-      tc::mbar_init(&bars->p_free[r], 1);
+      for (int b = 0; b < 2; ++b) {
+        tc::mbar_init(&bars->s_ready[r][b], 1);
+        tc::mbar_init(&bars->p_full[r][b], 128);
+      }
+      tc::mbar_init(&bars->p_free[r][0], 1);
+      tc::mbar_init(&bars->p_free[r][1], 1);
       tc::mbar_init(&bars->o_free[r], 128);
     }
     tc::mbar_init(&bars->drain, kIssuers);
@@ -682,49 +689,48 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       }
     } else if (warp >= 1 && warp <= R && lane == 0) {
       // ---------------- MMA issuer of row r = warp - 1
-      const int ra = warp - 1;
+      const int r = warp - 1;
+      const uint32_t tr = tmem + r * kTmemPerRow;
       constexpr uint32_t id_qk = tc::idesc_bf16_f32(128, BK, 0, 0);
       constexpr uint32_t id_pv = tc::idesc_bf16_f32(128, DH, 0, 1);
       const uint32_t q0 = tc::smem_addr(smem + OFF_Q);
       const uint32_t st0 = tc::smem_addr(smem + OFF_STAGE);
       const int total = my_units * KT;     // one item per key tile
-      // S(c + 1) as soon as the softmax has loaded S(c); P V(c) once P(c) is
-      // written.
-      auto qk = [&](int r, int c) -> bool {
+      // S(0), S(1); then per tile c, once P(c) is written: P V(c) from buffer
+      // c & 1, then S(c + 2) into the same buffer.
+      auto qk = [&](int c) -> bool {
         const int ui = c / KT, kt = c % KT, s = c % STAGES;
         if (kt == 0 && !wait_or_abort(&bars->q_full[ui & 1], (ui >> 1) & 1, ab)) return false;
         if (!wait_or_abort(&bars->kv_full[s], (c / STAGES) & 1, ab)) return false;
-        if (c >= 1 && !wait_or_abort(&bars->s_free[r], (c - 1) & 1, ab)) return false;
         tc::tc_fence_after();
         const uint32_t qa = q0 + ((ui & 1) * R + r) * Q_BYTES;
         const uint32_t ka = st0 + s * STAGE_BYTES + r * 2 * KV_BYTES;
-        const uint32_t tr = tmem + r * kTmemPerRow;
         for (int ks = 0; ks < DH / 16; ++ks)
-          tc::mma_bf16_ss(tr, tc::smem_desc(qa + ks * 32, 16, 512, tc::SWZ_64B),
+          tc::mma_bf16_ss(tr + (c & 1) * TM_S1, tc::smem_desc(qa + ks * 32, 16, 512, tc::SWZ_64B),
                           tc::smem_desc(ka + ks * 32, 16, 512, tc::SWZ_64B), id_qk, ks > 0);
-        tc::mma_commit(&bars->s_ready[r]);
+        tc::mma_commit(&bars->s_ready[r][c & 1]);
         if (kt == KT - 1) tc::mma_commit(&bars->q_empty[ui & 1]);
         return true;
       };
-      auto pv = [&](int r, int c) -> bool {
+      auto pv = [&](int c) -> bool {
         const int ui = c / KT, kt = c % KT, s = c % STAGES;
-        if (!wait_or_abort(&bars->p_full[r], c & 1, ab)) return false;
+        if (!wait_or_abort(&bars->p_full[r][c & 1], (c >> 1) & 1, ab)) return false;
         if (kt == 0 && ui >= 1 && !wait_or_abort(&bars->o_free[r], (ui - 1) & 1, ab)) return false;
         tc::tc_fence_after();
         const uint32_t va = st0 + s * STAGE_BYTES + r * 2 * KV_BYTES + KV_BYTES;
-        const uint32_t tr = tmem + r * kTmemPerRow;
         for (int ks = 0; ks < BK / 16; ++ks)
-          tc::mma_bf16_ts(tr + TM_O, tr + TM_P + ks * 8,
+          tc::mma_bf16_ts(tr + TM_O, tr + (c & 1) * TM_S1 + ks * 8,
                           tc::smem_desc(va + ks * 1024, 16, 512, tc::SWZ_64B), id_pv,
                           (kt > 0 || ks > 0) ? 1u : 0u);
-        tc::mma_commit(&bars->p_free[r]);
+        tc::mma_commit(&bars->p_free[r][c & 1]);
         tc::mma_commit(&bars->kv_empty[s]);
         return true;
       };
-      bool ok = total > 0 ? qk(ra, 0) : true;
+      bool ok = true;
+      for (int c = 0; ok && c < 2 && c < total; ++c) ok = qk(c);
       for (int c = 0; ok && c < total; ++c) {
-        if (c + 1 < total) ok = qk(ra, c + 1);
-        if (ok) ok = pv(ra, c);
+        ok = pv(c);
+        if (ok && c + 2 < total) ok = qk(c + 2);
       }
       tc::mma_commit(&bars->drain);
       drain_wait(&bars->drain, 0);
@@ -778,19 +784,18 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
                               jr * 128u + ((jr & 7u) << 4);
         const bool any_live = __any_sync(0xffffffffu, live);
         if (any_live && !warp_wait_or_abort(&bars->kv_full[s], (c / STAGES) & 1, ab)) { ok = false; break; }
-        if (!warp_wait_or_abort(&bars->s_ready[r], c & 1, ab)) { ok = false; break; }
+        if (!warp_wait_or_abort(&bars->s_ready[r][c & 1], (c >> 1) & 1, ab)) { ok = false; break; }
         tc::tc_fence_after();
+        const uint32_t tsb = tb + (c & 1) * TM_S1;     // S(c), then P(c) over it
         float2 x2[BK / 2];
         uint4 bq[8];                                   // the row's 64 fp16 biases
         if (any_live) {
-          tc::tmem_ld32(tb, *(uint32_t(*)[32])&x2[0]);
-          tc::tmem_ld32(tb + 32, *(uint32_t(*)[32])&x2[16]);
+          tc::tmem_ld32(tsb, *(uint32_t(*)[32])&x2[0]);
+          tc::tmem_ld32(tsb + 32, *(uint32_t(*)[32])&x2[16]);
 #pragma unroll
           for (int q = 0; q < 8; ++q) bq[q] = tc::lds128(brow ^ (q << 4));
           tc::tmem_ld_wait();
         }
-        tc::tc_fence_before();
-        tc::mbar_arrive(&bars->s_free[r]);            // S columns may take the next tile
         if (any_live && !all_kept) {
           // Dropped keys: S = -inf, which the bias add keeps at -inf (P = 0).
 #pragma unroll
@@ -815,16 +820,19 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         const uint32_t w0 = uni ? rl0 : 0u, w1 = uni ? rl1 : 0u;
         uint32_t pk[16];
         float2 ts2 = p_half(x2, bq, 0, sc2, mu, live, w0, pk);
-        // P V(c - 1) still reads the P columns and is the last MMA on O.
-        if (c >= 1 && !warp_wait_or_abort(&bars->p_free[r], (c - 1) & 1, ab)) { ok = false; break; }
-        tc::tc_fence_after();
-        tc::tmem_st16(tb + TM_P, pk);
+        tc::tmem_st16(tsb, pk);
         ts2 = __fadd2_rn(ts2, p_half(x2, bq, 1, sc2, mu, live, w1, pk));
-        tc::tmem_st16(tb + TM_P + 16, pk);
+        tc::tmem_st16(tsb + 16, pk);
         float tsum = ts2.x + ts2.y;
         if (any_live) {
           const bool ovf = live && !(tsum < 4294967296.f);
-          if (__any_sync(0xffffffffu, ovf)) tsum = redo_tile(x2, bq, tb, sc2, live, ovf, w0, w1, m_used, l_run);
+          if (__any_sync(0xffffffffu, ovf)) {
+            // O is stable once P V(c - 1), the last MMA on it, has landed
+            // (S(c) landing implied P V(c - 2)).
+            if (c >= 1 && !warp_wait_or_abort(&bars->p_free[r][(c - 1) & 1], ((c - 1) >> 1) & 1, ab)) { ok = false; break; }
+            tc::tc_fence_after();
+            tsum = redo_tile(x2, bq, tb, tsb, sc2, live, ovf, w0, w1, m_used, l_run);
+          }
         }
         if (live) {
           l_run += tsum;
@@ -834,12 +842,12 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         }
         tc::tmem_st_wait();
         tc::tc_fence_before();
-        tc::mbar_arrive(&bars->p_full[r]);
+        tc::mbar_arrive(&bars->p_full[r][c & 1]);
       }
       if (!ok) break;
       // Unit epilogue: o = O / l once the last P V has landed.
       const int clast = ui * KT + KT - 1;
-      if (!warp_wait_or_abort(&bars->p_free[r], clast & 1, ab)) { ok = false; break; }
+      if (!warp_wait_or_abort(&bars->p_free[r][clast & 1], (clast >> 1) & 1, ab)) { ok = false; break; }
       tc::tc_fence_after();
       uint32_t ov[32];
       tc::tmem_ld32(tb + TM_O, ov);
