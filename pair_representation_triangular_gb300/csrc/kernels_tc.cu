@@ -157,8 +157,11 @@ struct Bars {
 
 // LayerNorm and bias parameters travel by value in the kernel parameter block
 // (constant bank): every read index is known at compile time.
+// gw[t][c] = gamma[c] Wb[t][c], gws[t] = sum_c gw[t][c], bw[t] = sum_c beta[c] Wb[t][c]:
+// with t_c = (x_c - mean) rstd, bias[t] = sum_c x_hat_c Wb[t][c]
+// = rstd (sum_c (x_c - K) gw[t][c] - (mean - K) gws[t]) + bw[t] for any shift K.
 struct Consts {
-  float gamma[KD], beta[KD], bg[KD], wb[4][KD];
+  float gamma[KD], beta[KD], bg[KD], gw[4][KD], gws[4], bw[4];
 };
 
 struct Params {
@@ -174,9 +177,9 @@ struct Params {
 // Persistent: CTA c serves 128-cell tiles c, c + G, ... [Wq;Wk;Wv;Wg] (bf16,
 // K-major, 128 KB) stays in shared memory. Per tile the x tile arrives by TMA;
 // the 256 workers normalise it in place (the two threads of a cell each own
-// one 64-channel half; each takes the row statistics from the whole row in one
-// shifted pass) and compute two of the h = 4 bias outputs each from the bf16
-// x_hat; the MMA warp
+// one 64-channel half; each takes the row statistics and two of the h = 4
+// bias outputs from the whole row in one shifted pass, the bias through gamma
+// and beta folded into Wb); the MMA warp
 // issues the two N = 256 halves (q|k, v|g) into TMEM columns 0-255 / 256-511,
 // each with its own full/empty barriers, so the next tile's first half can
 // start while the epilogue still reads the second.
@@ -283,51 +286,50 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
       auto chunk = [&](int c) -> uint4 {
         return *(const uint4*)(xs + (c >> 3) * 16384 + tc::swz_offset(r, c & 7, 128));
       };
-      // Row statistics in one pass over the whole row, shifted by its first
-      // channel K so that the sum of squares does not cancel.
+      // One pass over the whole row, shifted by its first channel K so that the
+      // sums do not cancel: the row statistics and this thread's two bias heads
+      // (2 hh, 2 hh + 1) through the folded constants of k1::Consts.
       const float K0 = bf16_lo(chunk(0).x);
       const float2 nk2 = make_float2(-K0, -K0);
       float2 s2 = make_float2(0.f, 0.f), q2 = make_float2(0.f, 0.f);
+      float2 bp[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         const uint4 u = chunk(c);
         const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
+          const int i0 = c * 8 + 2 * e;
           const float2 d = __fadd2_rn(make_float2(bf16_lo(w4[e]), bf16_hi(w4[e])), nk2);
           s2 = __fadd2_rn(s2, d);
           q2 = __ffma2_rn(d, d, q2);
+#pragma unroll
+          for (int t2 = 0; t2 < 2; ++t2)
+            bp[t2] = __ffma2_rn(d, make_float2(cst.gw[2 * hh + t2][i0], cst.gw[2 * hh + t2][i0 + 1]), bp[t2]);
         }
       }
       const float S1 = (s2.x + s2.y) * (1.0f / KD);             // mean of x - K
       const float var = fmaxf((q2.x + q2.y) * (1.0f / KD) - S1 * S1, 0.f);
       const float mean = K0 + S1;
       const float rstd = rsqrtf(var + 1e-5f);
-      // Normalise (rounded to bf16 as the MMA sees it): keep this thread's half,
-      // and dot the whole row into bias heads 2*hh and 2*hh+1.
+      float bsum[2];
+#pragma unroll
+      for (int t2 = 0; t2 < 2; ++t2)
+        bsum[t2] = rstd * ((bp[t2].x + bp[t2].y) - S1 * cst.gws[2 * hh + t2]) + cst.bw[2 * hh + t2];
+      // Normalise this thread's half, rounded to bf16 as the MMA sees it.
       const float2 rs2 = make_float2(rstd, rstd), nm2 = make_float2(-mean * rstd, -mean * rstd);
-      float2 bp[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       uint32_t mine[32];
 #pragma unroll
-      for (int pass = 0; pass < 2; ++pass) {            // the other half, then this half
-        const int hf = pass == 0 ? 1 - hh : hh;
+      for (int c = 0; c < 8; ++c) {
+        const uint4 u = chunk(hh * 8 + c);
+        const uint32_t in4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 u = chunk(hf * 8 + c);
-          const uint32_t in4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i0 = hf * 64 + c * 8 + 2 * e;
-            const float2 t = __ffma2_rn(make_float2(bf16_lo(in4[e]), bf16_hi(in4[e])), rs2, nm2);
-            const float2 y = __ffma2_rn(t, make_float2(s_gamma[i0], s_gamma[i0 + 1]),
-                                        make_float2(s_beta[i0], s_beta[i0 + 1]));
-            const uint32_t pw = tc::pack_bf16x2(y.x, y.y);
-            const float2 rr = make_float2(bf16_lo(pw), bf16_hi(pw));
-#pragma unroll
-            for (int t2 = 0; t2 < 2; ++t2)
-              bp[t2] = __ffma2_rn(rr, make_float2(cst.wb[2 * hh + t2][i0], cst.wb[2 * hh + t2][i0 + 1]), bp[t2]);
-            if (pass == 1) mine[c * 4 + e] = pw;
-          }
+        for (int e = 0; e < 4; ++e) {
+          const int i0 = hh * 64 + c * 8 + 2 * e;
+          const float2 t = __ffma2_rn(make_float2(bf16_lo(in4[e]), bf16_hi(in4[e])), rs2, nm2);
+          const float2 y = __ffma2_rn(t, make_float2(s_gamma[i0], s_gamma[i0 + 1]),
+                                      make_float2(s_beta[i0], s_beta[i0 + 1]));
+          mine[c * 4 + e] = tc::pack_bf16x2(y.x, y.y);
         }
       }
       // The other thread of this row has read both halves once it reaches the
@@ -339,7 +341,6 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
             make_uint4(mine[4 * c], mine[4 * c + 1], mine[4 * c + 2], mine[4 * c + 3]);
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(&bars->a_ready[b]);
-      const float bsum[2] = {bp[0].x + bp[0].y, bp[1].x + bp[1].y};
       if (cell < p.cells) {
         const long long bb = cell / NN;
         const long long rc = cell - bb * NN;
@@ -1187,9 +1188,21 @@ cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const voi
   if (e == cudaSuccess) e = cudaMemcpyAsync(st->consts.gamma, t->gamma, D * 4, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(st->consts.beta, t->beta, D * 4, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(st->consts.bg, t->bg, D * 4, cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(st->consts.wb, t->wb_f32, (size_t)h * D * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(st->consts.gw, t->wb_f32, (size_t)h * D * 4, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return e;
+  // Fold gamma and beta into the bias projection (see k1::Consts).
+  for (int hd = 0; hd < h; ++hd) {
+    double gs = 0.0, bs = 0.0;
+    for (int c = 0; c < D; ++c) {
+      const double wbv = st->consts.gw[hd][c];
+      bs += (double)st->consts.beta[c] * wbv;
+      st->consts.gw[hd][c] = (float)((double)st->consts.gamma[c] * wbv);
+      gs += st->consts.gw[hd][c];
+    }
+    st->consts.gws[hd] = (float)gs;
+    st->consts.bw[hd] = (float)bs;
+  }
 
   const long long cells = t->cells;
   bool ok = map_rows_bf16(&st->map_w, t->w_proj, 512, 256);
