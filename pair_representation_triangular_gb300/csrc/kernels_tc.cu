@@ -81,16 +81,16 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-__device__ __forceinline__ float rcp_approx(float x) {
+// Logistic function for the gate, 1/(1 + e^-z) = (1 + tanh(z/2)) / 2, with the
+// hardware tanh approximation (one special-function operation; its error is
+// well below the bf16 rounding the gate gets).
+__device__ __forceinline__ float tanh_approx(float x) {
   float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-
-// Logistic function for the gate; its result is rounded to bf16, so the
-// hardware exp2 and reciprocal approximations are accurate enough.
 __device__ __forceinline__ float sigmoid_approx(float z) {
-  return rcp_approx(1.0f + ex2_approx(-z * kLog2e));
+  return fmaf(0.5f, tanh_approx(0.5f * z), 0.5f);
 }
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
