@@ -375,43 +375,56 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
       for (int nh = 0; nh < 2; ++nh) {
         if (!warp_wait_or_abort(&bars->acc_full[nh], it & 1, ab)) return false;
         tc::tc_fence_after();
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
+        // Half-chunk k (16 columns) of the 8 this warp drains from accumulator
+        // half nh: chunk k / 2 = 32 columns of section nh * 2 + k / 4. The load
+        // of half-chunk k + 1 is in flight while half-chunk k is converted.
+        auto hc_addr = [&](int k) {
+          const int cc = k >> 1, sect = nh * 2 + (cc >> 1);
+          return tc::tmem_addr(tmem, q4 * 32, sect * 128 + hh * 64 + (cc & 1) * 32 + (k & 1) * 16);
+        };
+        uint32_t accb[2][16];
+        tc::tmem_ld16(hc_addr(0), accb[0]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int cc = k >> 1;
           const int sect = nh * 2 + (cc >> 1);
           const int col0 = hh * 64 + (cc & 1) * 32;          // within the section
-          uint32_t acc[32];
-          tc::tmem_ld32(tc::tmem_addr(tmem, q4 * 32, sect * 128 + col0), acc);
           tc::tmem_ld_wait();
-          uint32_t packed[16];
+          if (k + 1 < 8) tc::tmem_ld16(hc_addr(k + 1), accb[(k + 1) & 1]);
+          const uint32_t (&acc)[16] = accb[k & 1];
+          uint32_t packed[8];
           if (sect == 3) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float z0 = __uint_as_float(acc[2 * e]) + s_bg[col0 + 2 * e];
-              const float z1 = __uint_as_float(acc[2 * e + 1]) + s_bg[col0 + 2 * e + 1];
+            for (int e = 0; e < 8; ++e) {
+              const int cg = col0 + (k & 1) * 16 + 2 * e;
+              const float z0 = __uint_as_float(acc[2 * e]) + s_bg[cg];
+              const float z1 = __uint_as_float(acc[2 * e + 1]) + s_bg[cg + 1];
               packed[e] = tc::pack_bf16x2(sigmoid_approx(z0), sigmoid_approx(z1));
             }
           } else {
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
+            for (int e = 0; e < 8; ++e)
               packed[e] = tc::pack_bf16x2(__uint_as_float(acc[2 * e]), __uint_as_float(acc[2 * e + 1]));
           }
           uint8_t* stg = stg0 + (nst & 1) * STG_BYTES;
-          if (nst >= 2) {                    // the store two back has read this staging tile
+          if ((k & 1) == 0 && nst >= 2) {    // the store two back has read this staging tile
             if (lane == 0) tc::tma_store_wait_read<1>();
             __syncwarp();
           }
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            *(uint4*)(stg + tc::swz_offset(lane, c, 64)) =
+          for (int c = 0; c < 2; ++c)
+            *(uint4*)(stg + tc::swz_offset(lane, (k & 1) * 2 + c, 64)) =
                 make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
-          tc::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            const CUtensorMap* m = sect == 0 ? &map_q : sect == 1 ? &map_k : sect == 2 ? &map_v : &map_g;
-            tc::tma_store_2d(m, stg, col0, row0);
-            tc::tma_store_commit();
+          if (k & 1) {
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const CUtensorMap* m = sect == 0 ? &map_q : sect == 1 ? &map_k : sect == 2 ? &map_v : &map_g;
+              tc::tma_store_2d(m, stg, col0, row0);
+              tc::tma_store_commit();
+            }
+            ++nst;
           }
-          ++nst;
         }
         tc::tc_fence_before();
         tc::mbar_arrive(&bars->acc_empty[nh]);
