@@ -924,7 +924,11 @@ __global__ void mask_summary(const int32_t* __restrict__ mask, int N, long long 
 namespace k3 {
 constexpr int BM = 128;
 constexpr int KD = 128;
-constexpr int kThreads = 192;           // warps 0-3 gate + epilogue, 4 TMA, 5 MMA
+// Warps 0-3 form g * o (one cell row per thread), warps 4-7 drain the
+// accumulator (TMEM lane quarter = warp % 4), warp 8 TMA, warp 9 MMA: the gate
+// product of tile t + 1 is formed while the epilogue drains tile t.
+constexpr int kThreads = 320;
+constexpr int kTmaWarp = 8, kMmaWarp = 9;
 constexpr uint32_t T_BYTES = BM * KD * 2;           // 32 KB tile (two K-halves)
 constexpr uint32_t OFF_W = 0;                       // Wo, 32 KB
 constexpr uint32_t OFF_G = OFF_W + T_BYTES;         // g tiles [2]; become the A operand
@@ -971,7 +975,7 @@ gate_out_tc(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ C
     tc::fence_mbar_init();
   }
   for (int i = tid; i < KD; i += kThreads) s_bo[i] = p.bo[i];
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc::tmem_alloc(&bars->tmem_base, 256);
     tc::tmem_relinquish();
   }
@@ -983,7 +987,7 @@ gate_out_tc(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ C
   for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) ++my_tiles;
   int issued = 0;
 
-  if (warp == 4) {
+  if (warp == kTmaWarp) {
     if (lane == 0) {
       tc::tma_prefetch_desc(&map_g);
       tc::tma_prefetch_desc(&map_o);
@@ -1005,7 +1009,7 @@ gate_out_tc(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ C
         issued = it + 1;
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 128, 0, 0);
       const uint32_t w0 = tc::smem_addr(smem + OFF_W);
@@ -1027,18 +1031,48 @@ gate_out_tc(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ C
       tc::mma_commit(&bars->drain);
       drain_wait(&bars->drain, 0);
     }
-  } else {
+  } else if (warp < 4) {
+    // ---------------- gate: a = g * o in place (one cell row per thread)
     const int r = tid;
-    auto epilogue = [&](int it) -> bool {
+    for (int it = 0; it < my_tiles; ++it) {
       const int b = it & 1;
-      if (!warp_wait_or_abort(&bars->acc_full[b], (it >> 1) & 1, ab)) return false;
+      if (!warp_wait_or_abort(&bars->in_full[b], (it >> 1) & 1, ab)) break;
+      uint8_t* gs = smem + OFF_G + b * T_BYTES;
+      const uint8_t* os = smem + OFF_O + b * T_BYTES;
+#pragma unroll 4
+      for (int c = 0; c < 16; ++c) {
+        const uint32_t off = (c >> 3) * 16384 + tc::swz_offset(r, c & 7, 128);
+        const uint4 gu = *(const uint4*)(gs + off);
+        const uint4 ou = *(const uint4*)(os + off);
+        // bf16 x bf16 is exact in fp32, so the packed bf16 product rounds it once.
+        const uint32_t ga[4] = {gu.x, gu.y, gu.z, gu.w}, oa[4] = {ou.x, ou.y, ou.z, ou.w};
+        uint32_t res[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __nv_bfloat162 pr = __hmul2(*(const __nv_bfloat162*)&ga[e], *(const __nv_bfloat162*)&oa[e]);
+          res[e] = *(const uint32_t*)&pr;
+        }
+        *(uint4*)(gs + off) = make_uint4(res[0], res[1], res[2], res[3]);
+      }
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&bars->a_ready[b]);
+    }
+  } else if (warp < 8) {
+    // ---------------- epilogue: cell row = TMEM lane of this warp's quarter
+    const int q4 = warp & 3;
+    for (int it = 0; it < my_tiles; ++it) {
+      const int b = it & 1;
+      if (!warp_wait_or_abort(&bars->acc_full[b], (it >> 1) & 1, ab)) break;
       tc::tc_fence_after();
-      const long long cell = (long long)(blockIdx.x + it * gridDim.x) * BM + r;
-#pragma unroll 1
+      const long long cell = (long long)(blockIdx.x + it * gridDim.x) * BM + q4 * 32 + lane;
+      // Chunk ch + 1 is loaded from TMEM while chunk ch is converted and stored.
+      uint32_t accb[2][32];
+      tc::tmem_ld32(tc::tmem_addr(tmem, q4 * 32, b * 128), accb[0]);
+#pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
-        uint32_t acc[32];
-        tc::tmem_ld32(tc::tmem_addr(tmem, (warp & 3) * 32, b * 128 + ch * 32), acc);
         tc::tmem_ld_wait();
+        if (ch + 1 < 4) tc::tmem_ld32(tc::tmem_addr(tmem, q4 * 32, b * 128 + (ch + 1) * 32), accb[(ch + 1) & 1]);
+        const uint32_t (&acc)[32] = accb[ch & 1];
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
@@ -1052,43 +1086,18 @@ gate_out_tc(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ C
       }
       tc::tc_fence_before();
       tc::mbar_arrive(&bars->acc_empty[b]);
-      return true;
-    };
-    bool ok = true;
-    for (int it = 0; ok && it < my_tiles; ++it) {
-      const int b = it & 1;
-      if (!warp_wait_or_abort(&bars->in_full[b], (it >> 1) & 1, ab)) { ok = false; break; }
-      uint8_t* gs = smem + OFF_G + b * T_BYTES;
-      const uint8_t* os = smem + OFF_O + b * T_BYTES;
-#pragma unroll 4
-      for (int c = 0; c < 16; ++c) {
-        const uint32_t off = (c >> 3) * 16384 + tc::swz_offset(r, c & 7, 128);
-        const uint4 gu = *(const uint4*)(gs + off);
-        const uint4 ou = *(const uint4*)(os + off);
-        const uint32_t ga[4] = {gu.x, gu.y, gu.z, gu.w}, oa[4] = {ou.x, ou.y, ou.z, ou.w};
-        uint32_t res[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          res[e] = tc::pack_bf16x2(bf16_lo(ga[e]) * bf16_lo(oa[e]), bf16_hi(ga[e]) * bf16_hi(oa[e]));
-        *(uint4*)(gs + off) = make_uint4(res[0], res[1], res[2], res[3]);
-      }
-      tc::fence_proxy_async_smem();
-      tc::mbar_arrive(&bars->a_ready[b]);
-      if (it >= 1 && !epilogue(it - 1)) { ok = false; break; }
     }
-    if (ok && my_tiles > 0) epilogue(my_tiles - 1);
   }
-
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 4 && lane == 0) {
+  if (warp == kTmaWarp && lane == 0) {
     drain_wait(&bars->w_full, 0);
     for (int it = issued - 1; it >= 0 && it >= issued - 2; --it)
       drain_wait(&bars->in_full[it & 1], (it >> 1) & 1);
   }
   __syncthreads();
   tc::tc_fence_after();
-  if (warp == 5) tc::tmem_dealloc(tmem, 256);
+  if (warp == kMmaWarp) tc::tmem_dealloc(tmem, 256);
 }
 }  // namespace k3
 
