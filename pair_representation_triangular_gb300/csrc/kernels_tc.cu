@@ -524,10 +524,11 @@ __device__ __forceinline__ uint32_t real_bits(int left, int w) {
   return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
 }
 
-// P = 2^(S sc + bias - mu) of one 32-key half (keys 32 hf ..), packed in bf16
-// pairs, and its sum; a lane that is not live writes 1 on every real key of a
-// uniform row or query (`w` = that half's real-key bits), else 0.
-__device__ __forceinline__ float2 p_half(const float2 (&x2)[BK / 2], const uint4 (&bq)[8], int hf,
+// P = 2^(S sc + bias - mu) of one 32-key half (keys 32 hf ..; bh = its 32 fp16
+// biases), packed in bf16 pairs, and its sum; a lane that is not live writes 1
+// on every real key of a uniform row or query (`w` = that half's real-key
+// bits), else 0.
+__device__ __forceinline__ float2 p_half(const float2 (&x2)[BK / 2], const uint4 (&bh)[4], int hf,
                                          float2 sc2, float mu, bool live, uint32_t w,
                                          uint32_t (&pk)[16]) {
   float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
@@ -536,7 +537,7 @@ __device__ __forceinline__ float2 p_half(const float2 (&x2)[BK / 2], const uint4
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4) {
       const int q = hf * 4 + q4;
-      const uint32_t hw[4] = {bq[q].x, bq[q].y, bq[q].z, bq[q].w};
+      const uint32_t hw[4] = {bh[q4].x, bh[q4].y, bh[q4].z, bh[q4].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 y = __ffma2_rn(x2[q * 4 + e], sc2, nmu2);
@@ -559,17 +560,29 @@ __device__ __forceinline__ float2 p_half(const float2 (&x2)[BK / 2], const uint4
   return __fadd2_rn(sa, sb);
 }
 
+// The 32 fp16 biases of half hf of a tile row (brow: the row's swizzled base,
+// 16-byte chunk q at brow ^ (q << 4)).
+__device__ __forceinline__ void load_bias_half(uint32_t brow, int hf, uint4 (&bh)[4]) {
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) bh[q4] = tc::lds128(brow ^ ((hf * 4 + q4) << 4));
+}
+
 // Largest logit x = S sc + bias of a 64-key tile, in log2 units.
-__device__ __forceinline__ float tile_max(const float2 (&x2)[BK / 2], const uint4 (&bq)[8], float2 sc2) {
+__device__ __forceinline__ float tile_max(const float2 (&x2)[BK / 2], uint32_t brow, float2 sc2) {
   float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
   const float2 z2 = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const uint32_t hw[4] = {bq[q].x, bq[q].y, bq[q].z, bq[q].w};
+  for (int hf = 0; hf < 2; ++hf) {
+    uint4 bh[4];
+    load_bias_half(brow, hf, bh);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 y = __ffma2_rn(x2[q * 4 + e], sc2, z2);
-      mx[e] = fmax3(mx[e], add_f16lo_f32(hw[e], y.x), add_f16hi_f32(hw[e], y.y));
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const uint32_t hw[4] = {bh[q4].x, bh[q4].y, bh[q4].z, bh[q4].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 y = __ffma2_rn(x2[(hf * 4 + q4) * 4 + e], sc2, z2);
+        mx[e] = fmax3(mx[e], add_f16lo_f32(hw[e], y.x), add_f16hi_f32(hw[e], y.y));
+      }
     }
   }
   return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
@@ -579,10 +592,10 @@ __device__ __forceinline__ float tile_max(const float2 (&x2)[BK / 2], const uint
 // the tile max; O (in TMEM, at tb + TM_O) and l are rescaled, and the tile's P
 // is recomputed and stored again at tp. Called by whole warps once the P V that last read P and O
 // has completed. Returns the new sum of P of the tile.
-__device__ __forceinline__ float redo_tile(const float2 (&x2)[BK / 2], const uint4 (&bq)[8], uint32_t tb,
+__device__ __forceinline__ float redo_tile(const float2 (&x2)[BK / 2], uint32_t brow, uint32_t tb,
                                         uint32_t tp, float2 sc2, bool live, bool ovf, uint32_t w0,
                                         uint32_t w1, float& m_used, float& l_run) {
-  const float mt = tile_max(x2, bq, sc2);
+  const float mt = tile_max(x2, brow, sc2);
   float alpha = 1.f;
   if (ovf) {
     alpha = ex2_approx(m_used - mt);
@@ -600,9 +613,12 @@ __device__ __forceinline__ float redo_tile(const float2 (&x2)[BK / 2], const uin
     tc::tmem_st16(tb + TM_O + 16 * oh, ov);
   }
   uint32_t pk[16];
-  float2 ts2 = p_half(x2, bq, 0, sc2, m_used, live, w0, pk);
+  uint4 bh[4];
+  load_bias_half(brow, 0, bh);
+  float2 ts2 = p_half(x2, bh, 0, sc2, m_used, live, w0, pk);
   tc::tmem_st16(tp, pk);
-  ts2 = __fadd2_rn(ts2, p_half(x2, bq, 1, sc2, m_used, live, w1, pk));
+  load_bias_half(brow, 1, bh);
+  ts2 = __fadd2_rn(ts2, p_half(x2, bh, 1, sc2, m_used, live, w1, pk));
   tc::tmem_st16(tp + 16, pk);
   return ts2.x + ts2.y;
 }
@@ -802,12 +818,11 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         tc::tc_fence_after();
         const uint32_t tsb = tb + (c & 1) * TM_S1;     // S(c), then P(c) over it
         float2 x2[BK / 2];
-        uint4 bq[8];                                   // the row's 64 fp16 biases
+        uint4 bh[4];                                   // 32 fp16 biases of one half
         if (any_live) {
           tc::tmem_ld32(tsb, *(uint32_t(*)[32])&x2[0]);
           tc::tmem_ld32(tsb + 32, *(uint32_t(*)[32])&x2[16]);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) bq[q] = tc::lds128(brow ^ (q << 4));
+          load_bias_half(brow, 0, bh);
           tc::tmem_ld_wait();
         }
         if (any_live && !all_kept) {
@@ -825,27 +840,28 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         // about 26), so P stays finite and O, l never overflow in fp32.
         if (any_live) {
           const bool need_max = live && m_used == -INFINITY;
-          if (__any_sync(0xffffffffu, need_max)) {
-            const float mt = tile_max(x2, bq, sc2);
+          if (__builtin_expect(__any_sync(0xffffffffu, need_max), 0)) {
+            const float mt = tile_max(x2, brow, sc2);
             if (need_max) m_used = mt;
           }
         }
         const float mu = m_used == -INFINITY ? 0.f : m_used;
         const uint32_t w0 = uni ? rl0 : 0u, w1 = uni ? rl1 : 0u;
         uint32_t pk[16];
-        float2 ts2 = p_half(x2, bq, 0, sc2, mu, live, w0, pk);
+        float2 ts2 = p_half(x2, bh, 0, sc2, mu, live, w0, pk);
         tc::tmem_st16(tsb, pk);
-        ts2 = __fadd2_rn(ts2, p_half(x2, bq, 1, sc2, mu, live, w1, pk));
+        if (any_live) load_bias_half(brow, 1, bh);
+        ts2 = __fadd2_rn(ts2, p_half(x2, bh, 1, sc2, mu, live, w1, pk));
         tc::tmem_st16(tsb + 16, pk);
         float tsum = ts2.x + ts2.y;
         if (any_live) {
           const bool ovf = live && !(tsum < 4294967296.f);
-          if (__any_sync(0xffffffffu, ovf)) {
+          if (__builtin_expect(__any_sync(0xffffffffu, ovf), 0)) {
             // O is stable once P V(c - 1), the last MMA on it, has landed
             // (S(c) landing implied P V(c - 2)).
             if (c >= 1 && !warp_wait_or_abort(&bars->p_free[r][(c - 1) & 1], ((c - 1) >> 1) & 1, ab)) { ok = false; break; }
             tc::tc_fence_after();
-            tsum = redo_tile(x2, bq, tb, tsb, sc2, live, ovf, w0, w1, m_used, l_run);
+            tsum = redo_tile(x2, brow, tb, tsb, sc2, live, ovf, w0, w1, m_used, l_run);
           }
         }
         if (live) {
