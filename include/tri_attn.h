@@ -64,7 +64,7 @@ enum {
 /* Build a handle for one problem shape and one set of weights.
  *
  * B, N, D, h: batch, pair-grid side, channels, heads; D % h == 0. Supported:
- *   TRI_ATTN_F32  any B, N >= 1, D <= 256 with d = D/h <= 128;
+ *   TRI_ATTN_F32  any B, N >= 1, even D <= 256 with d = D/h <= 128;
  *   TRI_ATTN_BF16 the tensor-core path: D == 128, h == 4 (d == 32), any B,
  *                 1 <= N <= 8192, B*N*N < 2^31.
  *   Other shapes return TRI_ATTN_ERR_UNSUPPORTED (there is no fallback path).

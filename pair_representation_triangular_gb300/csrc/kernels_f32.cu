@@ -29,70 +29,100 @@ __global__ void pack_transpose_f32(const float* __restrict__ W, int rows, int D,
   dst[(size_t)e * ld + col0 + r] = W[idx];
 }
 
+// Shared-memory operand of the two projection kernels: the block's 32 cells
+// stored channel-major, xt[e * kXtLd + c], rows padded to 36 floats so that
+// four consecutive cells load as one aligned 16-byte vector.
+constexpr int kXtLd = kCellsPerBlock + 4;
+
+// Row stride of the packed projection weights [D][4D + h], rounded up to an
+// even count so that every output pair loads as one aligned float2.
+inline int proj_ld(int D, int h) { return (4 * D + h + 1) & ~1; }
+
+// acc[i][c] += sum_e xt[e][c0 + c] * Wt[e][o0 + i] for i < 2, c < CT: one
+// thread's 2-output x CT-cell tile of a skinny GEMM over D channels.
+template <int CT>
+__device__ __forceinline__ void tile_gemm(const float* __restrict__ xt, int c0, int D,
+                                          const float* __restrict__ Wt, int ld, int o0,
+                                          float (&acc)[2][CT]) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int c = 0; c < CT; ++c) acc[i][c] = 0.f;
+#pragma unroll 2
+  for (int e = 0; e < D; ++e) {
+    const float2 w = *(const float2*)(Wt + (size_t)e * ld + o0);
+    float xv[CT];
+#pragma unroll
+    for (int c = 0; c < CT; c += 4) *(float4*)&xv[c] = *(const float4*)(xt + e * kXtLd + c0 + c);
+#pragma unroll
+    for (int c = 0; c < CT; ++c) {
+      acc[0][c] = fmaf(xv[c], w.x, acc[0][c]);
+      acc[1][c] = fmaf(xv[c], w.y, acc[1][c]);
+    }
+  }
+}
+
 // LayerNorm ("FW-GLM-5-1 l2_p6", self.layer_norm) and the concatenated
 // projection [Wq|Wk|Wv|Wg|Wb] ("Kimi-K2.6 l2_p6", op list steps 1-3 and 5-7).
+// A block takes 32 cells: one warp per cell normalises it into the
+// channel-major operand; then 2-output x 16-cell thread tiles cover the 4D
+// main outputs and a last pass the h bias outputs.
 __global__ void __launch_bounds__(kProjThreads)
 ln_proj_f32(const float* __restrict__ x, long long cells, int N, int D, int h,
             const float* __restrict__ gamma, const float* __restrict__ beta,
-            const float* __restrict__ Wt,      // [D][4D + h]
+            const float* __restrict__ Wt, int ldw,   // [D][ldw], 4D + h columns used
             const float* __restrict__ bg,
             float* __restrict__ q, float* __restrict__ k, float* __restrict__ v,
             float* __restrict__ g, float* __restrict__ bias) {
-  extern __shared__ float xs[];            // [kCellsPerBlock][D]
+  extern __shared__ float xt[];            // [D][kXtLd]
   const long long cell0 = (long long)blockIdx.x * kCellsPerBlock;
   const int ncell = (int)min((long long)kCellsPerBlock, cells - cell0);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  for (int idx = tid; idx < kCellsPerBlock * D; idx += kProjThreads) {
-    int c = idx / D;
-    xs[idx] = (c < ncell) ? x[(cell0 + c) * D + (idx % D)] : 0.f;
-  }
-  __syncthreads();
-
   // Mean and biased variance over D, eps 1e-5 inside the square root.
   for (int c = warp; c < kCellsPerBlock; c += kProjThreads / 32) {
-    float* row = xs + c * D;
+    const float* row = x + (cell0 + c) * D;
+    const bool real = c < ncell;
     float s = 0.f;
-    for (int e = lane; e < D; e += 32) s += row[e];
+    for (int e = lane; e < D; e += 32) s += real ? row[e] : 0.f;
     for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     const float mean = s / D;
     float ss = 0.f;
-    for (int e = lane; e < D; e += 32) { float t = row[e] - mean; ss += t * t; }
+    for (int e = lane; e < D; e += 32) { const float t = real ? row[e] - mean : 0.f; ss += t * t; }
     for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
     const float rstd = 1.0f / sqrtf(ss / D + 1e-5f);
-    for (int e = lane; e < D; e += 32) row[e] = (row[e] - mean) * rstd * gamma[e] + beta[e];
+    for (int e = lane; e < D; e += 32)
+      xt[e * kXtLd + c] = real ? (row[e] - mean) * rstd * gamma[e] + beta[e] : 0.f;
   }
   __syncthreads();
 
-  const int nout = 4 * D + h;
   const long long NN = (long long)N * N;
-  for (int o = tid; o < nout; o += kProjThreads) {
-    float acc[kCellsPerBlock];
+  constexpr int CT = 16;
+  const int tiles = (4 * D / 2) * (kCellsPerBlock / CT);
+  for (int t = tid; t < tiles; t += kProjThreads) {
+    const int o0 = (t / (kCellsPerBlock / CT)) * 2, c0 = (t % (kCellsPerBlock / CT)) * CT;
+    float acc[2][CT];
+    tile_gemm<CT>(xt, c0, D, Wt, ldw, o0, acc);
 #pragma unroll
-    for (int c = 0; c < kCellsPerBlock; ++c) acc[c] = 0.f;
-    for (int e = 0; e < D; ++e) {
-      const float w = Wt[(size_t)e * nout + o];
-#pragma unroll
-      for (int c = 0; c < kCellsPerBlock; ++c) acc[c] = fmaf(xs[c * D + e], w, acc[c]);
-    }
-    const int sect = o / D, col = o % D;
-    if (sect < 4) {
+    for (int i = 0; i < 2; ++i) {
+      const int o = o0 + i, sect = o / D, col = o % D;
       float* dst = sect == 0 ? q : sect == 1 ? k : sect == 2 ? v : g;
-      const float add = sect == 3 ? bg[col] : 0.f;
 #pragma unroll
-      for (int c = 0; c < kCellsPerBlock; ++c) {
-        float val = acc[c];
-        if (sect == 3) val = 1.0f / (1.0f + expf(-(val + add)));
-        if (c < ncell) dst[(cell0 + c) * D + col] = val;
+      for (int c = 0; c < CT; ++c) {
+        float val = acc[i][c];
+        if (sect == 3) val = 1.0f / (1.0f + expf(-(val + bg[col])));
+        if (c0 + c < ncell) dst[(cell0 + c0 + c) * D + col] = val;
       }
-    } else {
-      const int t = o - 4 * D;
-#pragma unroll
-      for (int c = 0; c < kCellsPerBlock; ++c) {
-        const long long cell = cell0 + c;
-        const long long b = cell / NN;
-        if (c < ncell) bias[(b * h + t) * NN + (cell - b * NN)] = acc[c];   // bias[b, t, r, c]
-      }
+    }
+  }
+  // The h bias outputs, bias[b, t, r, c] of each cell.
+  for (int i = tid; i < h * kCellsPerBlock; i += kProjThreads) {
+    const int t = i / kCellsPerBlock, c = i % kCellsPerBlock;
+    float acc = 0.f;
+    for (int e = 0; e < D; ++e) acc = fmaf(xt[e * kXtLd + c], Wt[(size_t)e * ldw + 4 * D + t], acc);
+    if (c < ncell) {
+      const long long cell = cell0 + c, b = cell / NN;
+      bias[(b * h + t) * NN + (cell - b * NN)] = acc;
     }
   }
 }
@@ -179,33 +209,33 @@ row_attn_f32(const float* __restrict__ q, const float* __restrict__ k,
   }
 }
 
-// Gate and output projection ("Kimi-K2.6 l2_p6", op list steps 17-18).
+// Gate and output projection ("Kimi-K2.6 l2_p6", op list steps 17-18): the
+// block's 32 cells of g * o go channel-major into shared memory, then
+// 2-output x 8-cell thread tiles of the output projection.
 __global__ void __launch_bounds__(kProjThreads)
 gate_out_f32(const float* __restrict__ g, const float* __restrict__ o, long long cells, int D,
              const float* __restrict__ Wot,     // [D][D] (in, out)
              const float* __restrict__ bo, float* __restrict__ out) {
-  extern __shared__ float as[];               // [kCellsPerBlock][D]
+  extern __shared__ float xt[];               // [D][kXtLd]
   const long long cell0 = (long long)blockIdx.x * kCellsPerBlock;
   const int ncell = (int)min((long long)kCellsPerBlock, cells - cell0);
   for (int idx = threadIdx.x; idx < kCellsPerBlock * D; idx += kProjThreads) {
-    const int c = idx / D;
-    const long long src = (cell0 + c) * D + (idx % D);
-    as[idx] = (c < ncell) ? g[src] * o[src] : 0.f;
+    const int c = idx / D, e = idx % D;
+    const long long src = (cell0 + c) * D + e;
+    xt[e * kXtLd + c] = (c < ncell) ? g[src] * o[src] : 0.f;
   }
   __syncthreads();
-  for (int col = threadIdx.x; col < D; col += kProjThreads) {
-    float acc[kCellsPerBlock];
+  constexpr int CT = 8;
+  const int tiles = (D / 2) * (kCellsPerBlock / CT);
+  for (int t = threadIdx.x; t < tiles; t += kProjThreads) {
+    const int o0 = (t / (kCellsPerBlock / CT)) * 2, c0 = (t % (kCellsPerBlock / CT)) * CT;
+    float acc[2][CT];
+    tile_gemm<CT>(xt, c0, D, Wot, D, o0, acc);
 #pragma unroll
-    for (int c = 0; c < kCellsPerBlock; ++c) acc[c] = 0.f;
-    for (int e = 0; e < D; ++e) {
-      const float w = Wot[(size_t)e * D + col];
+    for (int i = 0; i < 2; ++i)
 #pragma unroll
-      for (int c = 0; c < kCellsPerBlock; ++c) acc[c] = fmaf(as[c * D + e], w, acc[c]);
-    }
-    const float add = bo[col];
-#pragma unroll
-    for (int c = 0; c < kCellsPerBlock; ++c)
-      if (c < ncell) out[(cell0 + c) * D + col] = acc[c] + add;
+      for (int c = 0; c < CT; ++c)
+        if (c0 + c < ncell) out[(cell0 + c0 + c) * D + o0 + i] = acc[i][c] + bo[o0 + i];
   }
 }
 
@@ -214,7 +244,7 @@ gate_out_f32(const float* __restrict__ g, const float* __restrict__ o, long long
 cudaError_t tri_f32_pack_weights(tri_attn_s* t, const void* Wq, const void* Wk, const void* Wv,
                                  const void* Wg, const void* Wb, const void* Wo,
                                  cudaStream_t s) {
-  const int D = t->D, h = t->h, nout = 4 * D + h;
+  const int D = t->D, h = t->h, nout = proj_ld(D, h);
   float* wp = (float*)t->w_proj;
   const void* mats[5] = {Wq, Wk, Wv, Wg, Wb};
   for (int m = 0; m < 5; ++m) {
@@ -233,13 +263,13 @@ cudaError_t tri_f32_forward(tri_attn_s* t, cudaStream_t s, const float* x,
   const long long cells = t->cells;
   const int D = t->D, h = t->h, d = t->d, N = t->N;
   const unsigned nblk = (unsigned)((cells + kCellsPerBlock - 1) / kCellsPerBlock);
-  const size_t smem = (size_t)kCellsPerBlock * D * sizeof(float);
+  const size_t smem = (size_t)kXtLd * D * sizeof(float);
   float *q = (float*)t->q, *k = (float*)t->k, *v = (float*)t->v, *g = (float*)t->g,
         *o = (float*)t->o;
   tri_mark(t, s, 0, nullptr);
   ln_proj_f32<<<nblk, kProjThreads, smem, s>>>(x, cells, N, D, h, t->gamma, t->beta,
-                                               (const float*)t->w_proj, t->bg, q, k, v, g,
-                                               t->bias);
+                                               (const float*)t->w_proj, proj_ld(D, h), t->bg,
+                                               q, k, v, g, t->bias);
   tri_mark(t, s, 1, "ln_proj_f32");
   dim3 grid((unsigned)(t->B * (long long)N), h, (N + kQueriesPerBlock - 1) / kQueriesPerBlock);
 #define TRI_ATTN_F32_CASE(MD)                                                              \
@@ -265,7 +295,7 @@ cudaError_t tri_f32_forward(tri_attn_s* t, cudaStream_t s, const float* x,
 
 cudaError_t tri_f32_forward_raw(const TriF32Raw& a, cudaStream_t s) {
   const long long cells = (long long)a.B * a.N * a.N;
-  const int D = a.D, h = a.h, d = a.D / a.h, N = a.N, nout = 4 * D + h;
+  const int D = a.D, h = a.h, d = a.D / a.h, N = a.N, nout = proj_ld(D, h);
   const void* mats[5] = {a.Wq, a.Wk, a.Wv, a.Wg, a.Wb};
   for (int m = 0; m < 5; ++m) {
     const int rows = m < 4 ? D : h;
@@ -275,9 +305,9 @@ cudaError_t tri_f32_forward_raw(const TriF32Raw& a, cudaStream_t s) {
   }
   pack_transpose_f32<<<(D * D + 255) / 256, 256, 0, s>>>(a.Wo, D, D, a.w_out, D, 0);
   const unsigned nblk = (unsigned)((cells + kCellsPerBlock - 1) / kCellsPerBlock);
-  const size_t smem = (size_t)kCellsPerBlock * D * sizeof(float);
+  const size_t smem = (size_t)kXtLd * D * sizeof(float);
   ln_proj_f32<<<nblk, kProjThreads, smem, s>>>(a.x, cells, N, D, h, a.gamma, a.beta, a.w_proj,
-                                               a.bg, a.q, a.k, a.v, a.g, a.bias);
+                                               nout, a.bg, a.q, a.k, a.v, a.g, a.bias);
   dim3 grid((unsigned)(a.B * (long long)N), h, (N + kQueriesPerBlock - 1) / kQueriesPerBlock);
   const int md = d <= 8 ? 8 : d <= 16 ? 16 : d <= 32 ? 32 : d <= 64 ? 64 : 128;
   switch (md) {

@@ -46,11 +46,12 @@ cudaError_t scratch_address(unsigned char** out) {
 
 size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
 
-// Scratch bytes one call needs: packed weights, five (cells x D) intermediates
-// and the bias plane, each 256-byte aligned.
+// Scratch bytes one call needs: packed weights (projection rows padded to an
+// even count), five (cells x D) intermediates and the bias plane, each
+// 256-byte aligned.
 size_t scratch_bytes(int B, int N, int D, int h) {
   const size_t cells = (size_t)B * N * N;
-  return round256((size_t)(4 * D + h) * D * 4) + round256((size_t)D * D * 4) +
+  return round256((size_t)((4 * D + h + 1) & ~1) * D * 4) + round256((size_t)D * D * 4) +
          5 * round256(cells * D * 4) + round256((size_t)B * h * N * N * 4);
 }
 
@@ -70,7 +71,7 @@ extern "C" int tri_attn_forward_noalloc(int B, int N, int D, int h, int mask_mod
   for (const void* p : ptrs)
     if (!p || ((uintptr_t)p & 15u)) return TRI_ATTN_ERR_INVALID_ARG;
   if (!pair_mask || ((uintptr_t)pair_mask & 3u)) return TRI_ATTN_ERR_INVALID_ARG;
-  if (D > 256 || D / h > 128) return TRI_ATTN_ERR_UNSUPPORTED;
+  if (D > 256 || D / h > 128 || (D & 1)) return TRI_ATTN_ERR_UNSUPPORTED;
   if ((long long)B * N * N * D > (1ll << 40)) return TRI_ATTN_ERR_UNSUPPORTED;
   if (scratch_bytes(B, N, D, h) > kNoAllocScratchBytes)
     return TRI_ATTN_ERR_UNSUPPORTED;      // the problem does not fit the fixed scratch
@@ -88,7 +89,7 @@ extern "C" int tri_attn_forward_noalloc(int B, int N, int D, int h, int mask_mod
   // call (weights packed first, then each intermediate in full), so nothing
   // needs clearing between calls.
   unsigned char* p = base;
-  a.w_proj = (float*)p; p += round256((size_t)(4 * D + h) * D * 4);
+  a.w_proj = (float*)p; p += round256((size_t)((4 * D + h + 1) & ~1) * D * 4);
   a.w_out = (float*)p;  p += round256((size_t)D * D * 4);
   float** acts[5] = {&a.q, &a.k, &a.v, &a.g, &a.o};
   for (float** ap : acts) { *ap = (float*)p; p += round256(cells * D * 4); }

@@ -47,7 +47,7 @@ int check_shape(int B, int N, int D, int h, int dtype) {
   const long long cells = (long long)B * N * N;
   if (cells * (long long)D > (1ll << 40)) return TRI_ATTN_ERR_INVALID_ARG;
   if (dtype == TRI_ATTN_F32) {
-    if (D > 256 || D / h > 128) return TRI_ATTN_ERR_UNSUPPORTED;
+    if (D > 256 || D / h > 128 || (D & 1)) return TRI_ATTN_ERR_UNSUPPORTED;
   } else if (!tri_tc_supported(B, N, D, h)) {
     return TRI_ATTN_ERR_UNSUPPORTED;
   }
