@@ -480,7 +480,11 @@ constexpr uint32_t OFF_Q = 0;                        // [2][R] Q tiles
 constexpr uint32_t STAGE_KV = R * 2 * KV_BYTES;      // [R] K then V
 constexpr uint32_t STAGE_BYTES = STAGE_KV + BIAS_BYTES;
 constexpr uint32_t OFF_STAGE = OFF_Q + 2 * R * Q_BYTES;
-constexpr uint32_t OFF_BAR = OFF_STAGE + STAGES * STAGE_BYTES;
+// o of a unit leaves through one TMA store per softmax warp: 32 queries x one
+// head (64 bytes), staged with the 64-byte swizzle.
+constexpr uint32_t OST_BYTES = 32 * DH * 2;
+constexpr uint32_t OFF_OST = OFF_STAGE + STAGES * STAGE_BYTES;
+constexpr uint32_t OFF_BAR = OFF_OST + 3 * 4 * OST_BYTES;
 constexpr uint32_t SMEM = OFF_BAR + 512 + 1024;
 
 struct Bars {
@@ -497,7 +501,6 @@ struct Params {
   int B, N, h, mask_mode, row_groups, jtiles, words, units;
   const uint32_t* mbits;          // (B*N rows, words): bit k = pair_mask[b, r, k] != 0, k < N
   const unsigned char* row_any;   // (B*N rows): the mask row keeps some key
-  __nv_bfloat16* o;
   unsigned int* dev_err;
   long long polls;
   float scale_log2;               // log2(e) / sqrt(d)
@@ -589,12 +592,13 @@ __device__ __forceinline__ float tile_max(const float2 (&x2)[BK / 2], uint32_t b
 }
 
 // Rare path: some lane's sum of P over the tile reached 2^32. Those lanes raise mu to
-// the tile max; O (in TMEM, at tb + TM_O) and l are rescaled, and the tile's P
-// is recomputed and stored again at tp. Called by whole warps once the P V that last read P and O
-// has completed. Returns the new sum of P of the tile.
+// the tile max; O (in TMEM, at tb + TM_O, when it holds this unit's sum: o_live) and
+// l are rescaled, and the tile's P is recomputed and stored again at tp. Called by
+// whole warps once the P V that last read P and O has completed. Returns the new
+// sum of P of the tile.
 __device__ __forceinline__ float redo_tile(const float2 (&x2)[BK / 2], uint32_t brow, uint32_t tb,
-                                        uint32_t tp, float2 sc2, bool live, bool ovf, uint32_t w0,
-                                        uint32_t w1, float& m_used, float& l_run) {
+                                        uint32_t tp, float2 sc2, bool live, bool ovf, bool o_live,
+                                        uint32_t w0, uint32_t w1, float& m_used, float& l_run) {
   const float mt = tile_max(x2, brow, sc2);
   float alpha = 1.f;
   if (ovf) {
@@ -604,7 +608,7 @@ __device__ __forceinline__ float redo_tile(const float2 (&x2)[BK / 2], uint32_t 
   }
   tc::tmem_st_wait();
 #pragma unroll 1
-  for (int oh = 0; oh < 2; ++oh) {
+  for (int oh = 0; o_live && oh < 2; ++oh) {
     uint32_t ov[16];
     tc::tmem_ld16(tb + TM_O + 16 * oh, ov);
     tc::tmem_ld_wait();
@@ -636,7 +640,7 @@ __device__ __forceinline__ float redo_tile(const float2 (&x2)[BK / 2], uint32_t 
 __global__ void __launch_bounds__(kThreads, 1)
 row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
             const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_b,
-            const Params p) {
+            const __grid_constant__ CUtensorMap map_o, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   Bars* bars = (Bars*)(smem + OFF_BAR);
@@ -786,12 +790,51 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     unsigned nx_any = 0u;
     uint2 nx_bits = make_uint2(0u, 0u);
     if (my_units > 0) unit_loads(blockIdx.x, nx_any, nx_bits);
+    // Unit epilogue: o = O / l once the unit's last P V has landed, staged in
+    // shared memory and written by one TMA store per warp (queries past N are
+    // clipped by the store; rows past N and warps whose 32 queries all lie
+    // past N skip it). One 16-byte shared store per lane and chunk replaces
+    // 32 scattered 16-byte global stores per warp instruction.
+    uint8_t* const ostg = smem + OFF_OST + (warp - 4) * OST_BYTES;
+    bool ost_pending = false;
+    auto finish_unit = [&](const Unit& fu, int clast, float l) -> bool {
+      if (!warp_wait_or_abort(&bars->p_free[r][clast & 1], (clast >> 1) & 1, ab)) return false;
+      tc::tc_fence_after();
+      uint32_t ov[32];
+      tc::tmem_ld32(tb + TM_O, ov);
+      tc::tmem_ld_wait();
+      // O is in registers: its columns may take the next unit.
+      tc::tc_fence_before();
+      tc::mbar_arrive(&bars->o_free[r]);
+      const int fi = fu.rg * R + r, fj = fu.j0 + (warp & 3) * 32;
+      if (fi < N && fj < N) {
+        const float inv = 1.0f / l;
+        uint32_t po[16];
+#pragma unroll
+        for (int e = 0; e < DH; e += 2)
+          po[e / 2] = tc::pack_bf16x2(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
+        if (ost_pending) {                 // the previous store has read the staging tile
+          if (lane == 0) tc::tma_store_wait_read<0>();
+          __syncwarp();
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *(uint4*)(ostg + tc::swz_offset(lane, q, 64)) =
+              make_uint4(po[4 * q], po[4 * q + 1], po[4 * q + 2], po[4 * q + 3]);
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tc::tma_store_3d(&map_o, ostg, fu.t * DH, fj, fu.b * N + fi);
+          tc::tma_store_commit();
+        }
+        ost_pending = true;
+      }
+      return true;
+    };
     bool ok = true;
     for (int ui = 0; ok && ui < my_units; ++ui) {
       const Unit un = decode_unit(blockIdx.x + ui * gridDim.x, p);
-      const int j = un.j0 + jr;
       const int i = un.rg * R + r;
-      const bool valid = j < N && i < N;
       const bool uni = nx_any == 0u;
       const uint2 bits0 = nx_bits;
       if (ui + 1 < my_units) unit_loads(blockIdx.x + (ui + 1) * gridDim.x, nx_any, nx_bits);
@@ -859,9 +902,10 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
           if (__builtin_expect(__any_sync(0xffffffffu, ovf), 0)) {
             // O is stable once P V(c - 1), the last MMA on it, has landed
             // (S(c) landing implied P V(c - 2)).
-            if (c >= 1 && !warp_wait_or_abort(&bars->p_free[r][(c - 1) & 1], ((c - 1) >> 1) & 1, ab)) { ok = false; break; }
+            // On a unit's first tile O holds no sum of this unit yet.
+            if (kt >= 1 && !warp_wait_or_abort(&bars->p_free[r][(c - 1) & 1], ((c - 1) >> 1) & 1, ab)) { ok = false; break; }
             tc::tc_fence_after();
-            tsum = redo_tile(x2, brow, tb, tsb, sc2, live, ovf, w0, w1, m_used, l_run);
+            tsum = redo_tile(x2, brow, tb, tsb, sc2, live, ovf, kt >= 1, w0, w1, m_used, l_run);
           }
         }
         if (live) {
@@ -875,29 +919,11 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         tc::mbar_arrive(&bars->p_full[r][c & 1]);
       }
       if (!ok) break;
-      // Unit epilogue: o = O / l once the last P V has landed.
-      const int clast = ui * KT + KT - 1;
-      if (!warp_wait_or_abort(&bars->p_free[r][clast & 1], (clast >> 1) & 1, ab)) { ok = false; break; }
-      tc::tc_fence_after();
-      uint32_t ov[32];
-      tc::tmem_ld32(tb + TM_O, ov);
-      tc::tmem_ld_wait();
-      // O is in registers: its columns may take the next unit before the
-      // global stores below are issued.
-      tc::tc_fence_before();
-      tc::mbar_arrive(&bars->o_free[r]);
-      if (valid) {
-        const float inv = 1.0f / l_run;
-        uint32_t po[16];
-#pragma unroll
-        for (int e = 0; e < DH; e += 2)
-          po[e / 2] = tc::pack_bf16x2(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
-        uint4* dst = (uint4*)(p.o + (((long long)un.b * N + i) * N + j) * (p.h * DH) + un.t * DH);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(po[4 * q], po[4 * q + 1], po[4 * q + 2], po[4 * q + 3]);
-      }
+      if (!finish_unit(un, ui * KT + KT - 1, l_run)) { ok = false; break; }
     }
+    if (lane == 0) tc::tma_store_wait_all<0>();
   }
+
 
   // ---------------- teardown
   tc::tc_fence_before();
@@ -1171,6 +1197,7 @@ struct TcState {
   k1::Consts consts;                        // LayerNorm / gate-bias / pair-bias weights (fp32)
   CUtensorMap map_w, map_q, map_k, map_v, map_b, map_g, map_o, map_wo;
   CUtensorMap st_q, st_k, st_v, st_g;      // K1 output stores: (cells, 128) bf16, 32 x 32 boxes
+  CUtensorMap map_os;                      // K2 output stores: one head x 32 queries of a row
   unsigned char* row_any;    // (B*N) mask rows keeping some key
   uint32_t* mbits;           // (B*N, words) mask bits
   int words;
@@ -1247,6 +1274,7 @@ cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const voi
   ok = ok && map_heads(&st->map_q, t->q, B, N, k2::BQ);
   ok = ok && map_heads(&st->map_k, t->k, B, N, k2::BK);
   ok = ok && map_heads(&st->map_v, t->v, B, N, k2::BK);
+  ok = ok && map_heads(&st->map_os, t->o, B, N, 32);
   {
     cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)N, (cuuint64_t)B * h};
     cuuint64_t strides[2] = {(cuuint64_t)st->Nb * 2, (cuuint64_t)N * st->Nb * 2};
@@ -1326,12 +1354,13 @@ cudaError_t tri_tc_forward(tri_attn_s* t, cudaStream_t s, const void* x, const i
   p2.jtiles = (N + k2::BQ - 1) / k2::BQ;
   p2.units = B * p2.row_groups * h * p2.jtiles;
   p2.words = st->words;
-  p2.mbits = st->mbits; p2.row_any = st->row_any; p2.o = (__nv_bfloat16*)t->o;
+  p2.mbits = st->mbits; p2.row_any = st->row_any;
   p2.dev_err = t->dev_err;
   p2.polls = t->wait_limit;
   p2.scale_log2 = kLog2e / sqrtf((float)t->d);
   const unsigned g2 = (unsigned)(p2.units < st->num_sms ? p2.units : st->num_sms);
-  k2::row_attn_tc<<<g2, k2::kThreads, k2::SMEM, s>>>(st->map_q, st->map_k, st->map_v, st->map_b, p2);
+  k2::row_attn_tc<<<g2, k2::kThreads, k2::SMEM, s>>>(st->map_q, st->map_k, st->map_v, st->map_b,
+                                                      st->map_os, p2);
   tri_mark(t, s, mark++, "row_attn_tc");
 
   k3::Params p3;
