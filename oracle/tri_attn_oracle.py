@@ -40,6 +40,16 @@ Readings where the pages are silent or disagree:
     uniform weight 1/N instead of NaN.
   * Dropout is the identity (eval mode, [P2] discussion of ``nn.Dropout``).
   * Any nonzero mask entry keeps the key.
+  * Ending-node variant. The pages name only the starting-node module. Its
+    counterpart is read as the same module applied to the grid with its two
+    node axes exchanged: out_end = T(out_start(T(x), T(pair_mask))), T swapping
+    the two N axes. Written out per output cell (b, i, j), the softmax then
+    runs along column j:
+        l_k = q[b,i,j,t] . k[b,k,j,t] / sqrt(d) + bias[b,t,k,i]
+        o[b,i,j,t] = sum_k p_k v[b,k,j,t]
+    and key k is dropped when pair_mask[b,k,j] == 0 (MASK_ROW_KEY) or
+    pair_mask[b,k,i] == 0 (MASK_QUERY_KEY). ``forward_ending`` computes this
+    per column from the formula, not through the transposes.
 """
 from __future__ import annotations
 
@@ -181,3 +191,52 @@ def forward(x, pair_mask, params, h, mask_mode=MASK_ROW_KEY):
     B, N = x.shape[0], x.shape[1]
     rows = [(b, i) for b in range(B) for i in range(N)]
     return forward_rows(x, pair_mask, params, h, rows, mask_mode).reshape(x.shape)
+
+
+# ---------------------------------------------------------------- ending node
+def column_keep(pair_mask, b, j, mask_mode):
+    """Boolean keep[i, k] for the ending-node softmax of column (b, j).
+
+    MASK_ROW_KEY:   keep[i, k] = pair_mask[b, k, j] != 0 (same for every query i).
+    MASK_QUERY_KEY: keep[i, k] = pair_mask[b, k, i] != 0.
+    ``pair_mask=None`` keeps every key."""
+    if pair_mask is None:
+        return None
+    N = pair_mask.shape[-1]
+    if mask_mode == MASK_ROW_KEY:
+        return np.broadcast_to(pair_mask[b, :, j] != 0, (N, N))
+    if mask_mode == MASK_QUERY_KEY:
+        return (pair_mask[b] != 0).T
+    raise ValueError(f"unknown mask mode {mask_mode}")
+
+
+def column_bias(bias_b):
+    """Pair bias of the ending-node softmax: entry [t, i, k] (query i, key k)
+    is bias[b, t, k, i]."""
+    return np.transpose(bias_b, (0, 2, 1))
+
+
+def forward_ending_columns(x, pair_mask, params, h, cols, mask_mode=MASK_ROW_KEY):
+    """Ending node: ``out[b, :, j, :]`` for each (b, j) in ``cols``, array
+    (len(cols), N, D). Column (b, j) holds the queries i (cells (b, i, j)) and
+    the keys k (cells (b, k, j)) of its softmax."""
+    x = _f64(x)
+    P = {k: _f64(v) for k, v in params.items()}
+    B, N, _, D = x.shape
+    x_hat_all = layer_norm(x, P["gamma"], P["beta"])
+    bias = bias_plane(linear(x_hat_all, P["Wb"]))
+    out = np.empty((len(cols), N, D))
+    for n, (b, j) in enumerate(cols):
+        q_j, k_j, v_j, g_j, _ = project(x_hat_all[b, :, j], P)
+        keep = column_keep(pair_mask, b, j, mask_mode)
+        o_j = row_attention(q_j, k_j, v_j, column_bias(bias[b]), keep, h)
+        out[n] = output_projection(g_j, o_j, P)
+    return out
+
+
+def forward_ending(x, pair_mask, params, h, mask_mode=MASK_ROW_KEY):
+    """Ending-node forward: out (B, N, N, D) in float64."""
+    B, N, D = x.shape[0], x.shape[1], x.shape[3]
+    cols = [(b, j) for b in range(B) for j in range(N)]
+    res = forward_ending_columns(x, pair_mask, params, h, cols, mask_mode)
+    return res.reshape(B, N, N, D).transpose(0, 2, 1, 3)

@@ -191,11 +191,93 @@ def pin_hand_worked_example():
             np.testing.assert_allclose(out[0, i, j], [0.5 * o0, -0.5 * o0], rtol=0, atol=1e-14)
 
 
+# --------------------------------------------------------- ending-node pins
+
+def _swap(a):
+    """Exchange the two node axes of a (B, N, N, ...) array."""
+    return np.swapaxes(a, 1, 2)
+
+
+def pin_ending_is_module_on_swapped_grid():
+    """The ending node is the starting-node module on the grid with its node
+    axes exchanged: forward_ending(x, m) = T(module(T(x), T(m))), the module
+    here being the torch-library statement of the op list (tiny shapes; the
+    diagonal of the mask is kept so that every row and column keeps a key)."""
+    for N in (1, 2, 3, 5):
+        for h in (1, 2, 4):
+            x, mask, P = _inputs(2, N, 8, h, seed=300 + 10 * N + h)
+            mask = mask.copy()
+            for r in range(N):
+                mask[:, r, r] = 1
+            for mode in (O.MASK_ROW_KEY, O.MASK_QUERY_KEY):
+                want = _swap(TLM.forward(_swap(x), _swap(mask), P, h, mode))
+                np.testing.assert_allclose(O.forward_ending(x, mask, P, h, mode), want,
+                                           rtol=0, atol=1e-12)
+
+
+def pin_ending_n1_closed_form():
+    """N = 1: the ending node has the same closed form as the starting node."""
+    for mode in (O.MASK_ROW_KEY, O.MASK_QUERY_KEY):
+        x, _, P = _inputs(2, 1, 8, 2, seed=31)
+        mask = np.zeros((2, 1, 1), np.int32)
+        xn = _lib_ln(x, P)
+        g = torch.sigmoid(F.linear(xn, _t(P["Wg"]), _t(P["bg"])))
+        ref = F.linear(g * F.linear(xn, _t(P["Wv"])), _t(P["Wo"]), _t(P["bo"])).numpy()
+        np.testing.assert_allclose(O.forward_ending(x, mask, P, 2, mode), ref, rtol=0, atol=1e-12)
+
+
+def pin_ending_single_kept_key():
+    """Row-key reading: a column j0 whose mask column pair_mask[b, :, j0] keeps
+    only k* gives o[b, i, j0] = v[b, k*, j0] for every query i. Query-key
+    reading: a query i0 whose column pair_mask[b, :, i0] keeps only k* gives
+    o[b, i0, j] = v[b, k*, j] in every column j."""
+    B, N, D, h = 1, 6, 8, 2
+    x, _, P = _inputs(B, N, D, h, seed=32)
+    xn = _lib_ln(x, P)
+    g = torch.sigmoid(F.linear(xn, _t(P["Wg"]), _t(P["bg"])))
+    v = F.linear(xn, _t(P["Wv"]))
+    j0, k_star = 1, 4
+    mask = np.ones((B, N, N), np.int32)
+    mask[0, :, j0] = 0
+    mask[0, k_star, j0] = 1
+    out = O.forward_ending(x, mask, P, h, O.MASK_ROW_KEY)
+    for i in range(N):
+        ref = F.linear(g[0, i, j0] * v[0, k_star, j0], _t(P["Wo"]), _t(P["bo"])).numpy()
+        np.testing.assert_allclose(out[0, i, j0], ref, rtol=0, atol=1e-12)
+    out = O.forward_ending(x, mask, P, h, O.MASK_QUERY_KEY)
+    for j in range(N):     # query i = j0 keeps only k_star in every column j
+        ref = F.linear(g[0, j0, j] * v[0, k_star, j], _t(P["Wo"]), _t(P["bo"])).numpy()
+        np.testing.assert_allclose(out[0, j0, j], ref, rtol=0, atol=1e-12)
+
+
+def pin_ending_zero_query_weights():
+    """Wq = 0, nothing masked: the ending-node weights of query i are
+    softmax_k(bias[b, t, k, i]) in every column j (bias from torch's linear),
+    so out[b, i, j] = Wo (g * sum_k p[t, i, k] v[b, k, j]) + bo."""
+    B, N, D, h = 1, 5, 8, 4
+    x, _, P = _inputs(B, N, D, h, seed=33)
+    P["Wq"] = np.zeros_like(P["Wq"])
+    xn = _lib_ln(x, P)
+    bias = F.linear(xn, _t(P["Wb"])).permute(0, 3, 1, 2)          # (B, h, r, c)
+    p = torch.softmax(bias[0].transpose(1, 2), dim=-1)             # [t, i, k] over k
+    g = torch.sigmoid(F.linear(xn, _t(P["Wg"]), _t(P["bg"])))
+    v = F.linear(xn, _t(P["Wv"]))
+    d = D // h
+    ones = np.ones((B, N, N), np.int32)
+    for mode in (O.MASK_ROW_KEY, O.MASK_QUERY_KEY):
+        out = O.forward_ending(x, ones, P, h, mode)
+        for j in range(N):
+            o = torch.cat([p[t] @ v[0, :, j, t * d:(t + 1) * d] for t in range(h)], dim=1)
+            want = F.linear(g[0, :, j] * o, _t(P["Wo"]), _t(P["bo"])).numpy()
+            np.testing.assert_allclose(out[0, :, j], want, rtol=0, atol=1e-12)
+
+
 PINS = {f.__name__: f for f in (
     pin_n1_closed_form, pin_rows_sum_to_one, pin_all_ones_mask_is_no_mask,
     pin_relabelling_equivariance, pin_single_kept_key, pin_zero_query_weights,
     pin_mean_of_kept_values, pin_zero_value_weights, pin_torch_library_module,
-    pin_hand_worked_example)}
+    pin_hand_worked_example, pin_ending_is_module_on_swapped_grid,
+    pin_ending_n1_closed_form, pin_ending_single_kept_key, pin_ending_zero_query_weights)}
 
 
 @pytest.mark.parametrize("name", list(PINS))
@@ -283,7 +365,30 @@ def _forward_rows_bias_of_row_i(x, pair_mask, params, h, rows, mask_mode=O.MASK_
     return out
 
 
-_REAL = {n: getattr(O, n) for n in ("project", "row_attention")}
+def _column_bias_untransposed(bias_b):
+    return bias_b
+
+
+def _column_keep_of_row(pair_mask, b, j, mode):
+    return _REAL["keep_matrix"](pair_mask, b, j, mode)
+
+
+def _forward_ending_row_cells(x, pair_mask, params, h, cols, mask_mode=O.MASK_ROW_KEY):
+    x = np.asarray(x, np.float64)
+    P = {k: np.asarray(v, np.float64) for k, v in params.items()}
+    B, N, _, D = x.shape
+    xa = O.layer_norm(x, P["gamma"], P["beta"])
+    bias = O.bias_plane(O.linear(xa, P["Wb"]))
+    out = np.empty((len(cols), N, D))
+    for n, (b, j) in enumerate(cols):
+        q_j, k_j, v_j, g_j, _ = O.project(xa[b, j, :], P)          # row j, not column j
+        o_j = O.row_attention(q_j, k_j, v_j, O.column_bias(bias[b]),
+                              O.column_keep(pair_mask, b, j, mask_mode), h)
+        out[n] = O.output_projection(g_j, o_j, P)
+    return out
+
+
+_REAL = {n: getattr(O, n) for n in ("project", "row_attention", "keep_matrix")}
 
 MISTAKES = [
     # (oracle attribute, wrong stand-in, the pin that must catch it)
@@ -301,6 +406,11 @@ MISTAKES = [
     ("output_projection", _outproj_one_value, "pin_n1_closed_form"),
     ("project", _project_gate_no_bias, "pin_n1_closed_form"),
     ("row_attention", _row_attention_value_head_shift, "pin_single_kept_key"),
+    ("column_bias", _column_bias_untransposed, "pin_ending_zero_query_weights"),
+    ("column_bias", _column_bias_untransposed, "pin_ending_is_module_on_swapped_grid"),
+    ("column_keep", _column_keep_of_row, "pin_ending_single_kept_key"),
+    ("forward_ending_columns", _forward_ending_row_cells, "pin_ending_is_module_on_swapped_grid"),
+    ("forward_ending_columns", _forward_ending_row_cells, "pin_ending_single_kept_key"),
 ]
 
 
