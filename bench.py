@@ -51,6 +51,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--mask-mode", type=int, default=0)
+    ap.add_argument("--node", default="starting", choices=["starting", "ending"])
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
@@ -192,17 +193,22 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU oracle baseline
 def _oracle_rows_worker(args):
-    """Rows of the oracle forward in a spawned worker (single-threaded BLAS)."""
-    x_rows, mask, params, h, rows, mode, bias_b = args
+    """Softmax lines of the oracle forward in a spawned worker (single-threaded
+    BLAS): rows i of the grid for the starting node, columns for the ending
+    node."""
+    x_lines, mask, params, h, lines, mode, bias_b, ending = args
     import numpy as np
     import oracle.tri_attn_oracle as O
     P = {k: np.asarray(v, np.float64) for k, v in params.items()}
     out = []
-    for n, (b, i) in enumerate(rows):
-        x_hat = O.layer_norm(np.asarray(x_rows[n], np.float64), P["gamma"], P["beta"])
+    for n, (b, a) in enumerate(lines):
+        x_hat = O.layer_norm(np.asarray(x_lines[n], np.float64), P["gamma"], P["beta"])
         q, k, v, g, _ = O.project(x_hat, P)
-        keep = O.keep_matrix(mask, b, i, mode)
-        o = O.row_attention(q, k, v, bias_b, keep, h)
+        if ending:
+            keep, bias_l = O.column_keep(mask, b, a, mode), O.column_bias(bias_b)
+        else:
+            keep, bias_l = O.keep_matrix(mask, b, a, mode), bias_b
+        o = O.row_attention(q, k, v, bias_l, keep, h)
         out.append(O.output_projection(g, o, P))
     return len(out)
 
@@ -216,11 +222,12 @@ def _oracle_bias_worker(args):
     return O.linear(x_hat, P["Wb"])
 
 
-def cpu_oracle_sample(w, inp, mode, budget_s=20.0, cores=None):
+def cpu_oracle_sample(w, inp, mode, budget_s=20.0, cores=None, ending=False):
     """Time the oracle on this host: the full bias plane (every cell) plus as many
-    rows as fit in about `budget_s`, spread over `cores` spawned processes; the
-    full-forward time is extrapolated from the per-row time. Returns the JSON
-    object of the baseline."""
+    softmax lines (rows, or columns for the ending node) as fit in about
+    `budget_s`, spread over `cores` spawned processes; the full-forward time is
+    extrapolated from the per-line time. Returns the JSON object of the
+    baseline."""
     import numpy as np
     cores = cores or os.cpu_count() or 1
     env_keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
@@ -244,9 +251,8 @@ def cpu_oracle_sample(w, inp, mode, budget_s=20.0, cores=None):
             batch = cores
             while done < len(rows_all):
                 chunk = rows_all[done:done + batch]
-                jobs = [((inp["x"][b, i],), inp["pair_mask"], inp["params"], w.h, [(b, i)], mode,
-                         bias[b]) for b, i in chunk]
-                jobs = [(j[0], j[1], j[2], j[3], j[4], j[5], j[6]) for j in jobs]
+                jobs = [(((inp["x"][b, :, i] if ending else inp["x"][b, i]),), inp["pair_mask"],
+                         inp["params"], w.h, [(b, i)], mode, bias[b], ending) for b, i in chunk]
                 t1 = time.perf_counter()
                 pool.map(_oracle_rows_worker, jobs, chunksize=1)
                 t_rows += time.perf_counter() - t1
@@ -271,6 +277,16 @@ def cpu_oracle_sample(w, inp, mode, budget_s=20.0, cores=None):
                        f"in rows: {t_full:.1f} s")}
 
 
+def bench_config(w, args, world):
+    """The `config` object of both arms' JSON lines."""
+    return {"workload": w.name, "B": w.B, "N": w.N, "D": w.D, "h": w.h,
+            "node": args.node,
+            "mask_mode": "row-key" if args.mask_mode == 0 else "query-key",
+            "l2": f"flushed (256 MB write) before each timed step; x is "
+                  f"{w.cells * w.D * (2 if w.dtype == 'bf16' else 4) / 1e6:.0f} MB",
+            "parallelism": f"{world} independent problems, one per GPU"}
+
+
 # ------------------------------------------------------------------ native arm
 def run_native(args, rank, world):
     import numpy as np
@@ -291,7 +307,8 @@ def run_native(args, rank, world):
     x = torch.from_numpy(inp["x"]).to(dev, td)
     m = torch.from_numpy(inp["pair_mask"]).to(dev)
     out = torch.empty_like(x)
-    mod = tb.TriangularAttention(w.B, w.N, w.D, w.h, dt, args.mask_mode, params)
+    node = tb.TRI_ATTN_ENDING_NODE if args.node == "ending" else tb.TRI_ATTN_STARTING_NODE
+    mod = tb.TriangularAttention(w.B, w.N, w.D, w.h, dt, args.mask_mode | node, params)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     tb.tri_attn_enable_kernel_timing(mod.handle, True)
@@ -388,10 +405,7 @@ def run_native(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic (seeded)",
-        "config": {"workload": w.name, "B": w.B, "N": w.N, "D": w.D, "h": w.h,
-                   "mask_mode": "row-key" if args.mask_mode == 0 else "query-key",
-                   "l2": "flushed (256 MB write) before each timed step; x is 151 MB",
-                   "parallelism": f"{world} independent problems, one per GPU"},
+        "config": bench_config(w, args, world),
         "e2e": {"value": world * w.cells / e2e_s, "unit": "pair-cells/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
@@ -416,7 +430,8 @@ def main():
         base = None
         for s in range(args.warmup + args.steps):
             budget = 2.0 if s < args.warmup else max(2.0, 150.0 / max(args.steps, 1))
-            r = cpu_oracle_sample(w, inp, args.mask_mode, budget_s=budget)
+            r = cpu_oracle_sample(w, inp, args.mask_mode, budget_s=budget,
+                                  ending=args.node == "ending")
             if s >= args.warmup:
                 vals.append(r["value"])
                 base = r
@@ -427,7 +442,7 @@ def main():
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": w.cells / value * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-            "config": {"workload": w.name, "B": w.B, "N": w.N, "D": w.D, "h": w.h},
+            "config": bench_config(w, args, world),
             "cpu_baseline": base,
             "e2e": {"value": value, "unit": "pair-cells/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
@@ -439,7 +454,8 @@ def main():
     result, w, inp = run_native(args, rank, world)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
-            result["cpu_baseline"] = cpu_oracle_sample(w, inp, args.mask_mode, budget_s=20.0)
+            result["cpu_baseline"] = cpu_oracle_sample(w, inp, args.mask_mode, budget_s=20.0,
+                                                       ending=args.node == "ending")
         print(json.dumps(result))
     if world > 1:
         import torch

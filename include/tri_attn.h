@@ -22,6 +22,18 @@
  *                           (the quoted code's broadcast of pair_mask over rows i)
  * A softmax row whose keys are all dropped gets the uniform weight 1/N.
  *
+ * Node variants (OR-ed into the mask reading to form the `mode` argument):
+ *   TRI_ATTN_STARTING_NODE  the operation above: attention along rows i.
+ *   TRI_ATTN_ENDING_NODE    the same module on the grid with its two node axes
+ *                           exchanged, out = T(f(T(pair_repr), T(pair_mask)))
+ *                           where T swaps the two N axes; per output cell
+ *                           (b, i, j) the softmax runs along column j:
+ *       l_k = q[b,i,j,t].k[b,k,j,t] / sqrt(d) + bias[b,t,k,i]
+ *       o[b,i,j,t] = sum_k softmax_k(l) v[b,k,j,t]
+ *     with key k dropped when pair_mask[b,k,j] == 0 (row-key reading) or
+ *     pair_mask[b,k,i] == 0 (query-key reading). The pages name only the
+ *     starting-node module; this reading of its counterpart is the plainest one.
+ *
  * Conventions for every entry point:
  *   - Tensors are dense, row-major (C order), of the element type given by
  *     `dtype` (float for TRI_ATTN_F32, bfloat16 for TRI_ATTN_BF16); pair_mask is
@@ -50,6 +62,7 @@ typedef struct tri_attn_s* tri_attn_t;
 
 enum { TRI_ATTN_F32 = 0, TRI_ATTN_BF16 = 1 };
 enum { TRI_ATTN_MASK_ROW_KEY = 0, TRI_ATTN_MASK_QUERY_KEY = 1 };
+enum { TRI_ATTN_STARTING_NODE = 0, TRI_ATTN_ENDING_NODE = 2 };
 
 enum {
   TRI_ATTN_OK = 0,
@@ -68,7 +81,9 @@ enum {
  *   TRI_ATTN_BF16 the tensor-core path: D == 128, h == 4 (d == 32), any B,
  *                 1 <= N <= 8192, B*N*N < 2^31.
  *   Other shapes return TRI_ATTN_ERR_UNSUPPORTED (there is no fallback path).
- * mask_mode: TRI_ATTN_MASK_ROW_KEY or TRI_ATTN_MASK_QUERY_KEY (see above).
+ * mode: a mask reading (TRI_ATTN_MASK_ROW_KEY or TRI_ATTN_MASK_QUERY_KEY),
+ *   OR-ed with TRI_ATTN_ENDING_NODE for the ending-node variant (see above);
+ *   any other bit gives TRI_ATTN_ERR_INVALID_ARG.
  * Weights (device pointers, element type `dtype`), nn.Linear layout:
  *   ln_gamma, ln_beta [D]; Wq, Wk, Wv, Wg [D][D]; bg [D]; Wb [h][D]; Wo [D][D]; bo [D].
  *   Which Linear carries a bias follows the layer definitions on
@@ -80,7 +95,7 @@ enum {
  * intermediates (q, k, v, g, the bias plane and the attention output).
  * On success *out receives the handle; on failure *out is NULL and nothing
  * is leaked. */
-int tri_attn_create(tri_attn_t* out, int B, int N, int D, int h, int dtype, int mask_mode,
+int tri_attn_create(tri_attn_t* out, int B, int N, int D, int h, int dtype, int mode,
                     const void* ln_gamma, const void* ln_beta,
                     const void* Wq, const void* Wk, const void* Wv,
                     const void* Wg, const void* bg, const void* Wb,
@@ -138,10 +153,12 @@ int tri_attn_kernel_times(tri_attn_t t, float* ms, const char** names, int* n);
  *   "q", "k", "v", "g", "o"  (B*N*N, D) in the handle's dtype: per cell the
  *                           projections, the post-sigmoid gate and the
  *                           attention output before the gate;
- *   "bias"                  (B, h, N, row_stride) pair-bias plane: fp32 on the
- *                           fp32 path; on the bf16 path fp16 holding
- *                           log2(e) * bias, and -inf where the query-key mask
- *                           drops (j, k).
+ *   "bias"                  (B, h, N, row_stride) pair-bias plane indexed
+ *                           [b, t, query, key]: bias[b,t,j,k] for the starting
+ *                           node, bias[b,t,k,i] at [b,t,i,k] for the ending
+ *                           node; fp32 on the fp32 path; on the bf16 path fp16
+ *                           holding log2(e) * bias, and -inf where the
+ *                           query-key mask drops the key.
  * Returns the device pointer, or NULL for an unknown name or handle;
  * *row_stride (may be NULL) receives the innermost row stride in elements. */
 void* tri_attn_debug_tensor(tri_attn_t t, const char* name, int64_t* row_stride);
@@ -165,10 +182,11 @@ int tri_attn_set_wait_limit(tri_attn_t t, long long spins);
  * (B, N, N, D), pair_mask (B, N, N) and out (B, N, N, D). The intermediates live
  * in one fixed 16 MiB device array inside the library, which every GPU that
  * loads the library holds until the process exits. A problem needs
- *   4 * ((4D + h) * D + D * D + 5 * B * N * N * D + B * h * N * N) bytes
- * (each of those seven regions rounded up to 256); larger problems return
- * TRI_ATTN_ERR_UNSUPPORTED without launching anything. Other shape rules are
- * those of TRI_ATTN_F32 in tri_attn_create; the mask mode is as there.
+ *   4 * (P * D + D * D + 5 * B * N * N * D + B * h * N * N) bytes, P = 4D + h
+ * rounded up to an even count (each of those seven regions rounded up to 256);
+ * larger problems return TRI_ATTN_ERR_UNSUPPORTED without launching anything.
+ * Other shape rules are those of TRI_ATTN_F32 in tri_attn_create; `mode` is as
+ * there.
  *
  * The call is asynchronous on `stream`. The first call on each device looks up
  * the array's device address (cudaGetSymbolAddress, with that device current),
@@ -177,7 +195,7 @@ int tri_attn_set_wait_limit(tri_attn_t t, long long spins);
  * written earlier in the same call, so nothing is cleared): calls that can
  * overlap on the GPU, on different streams or from different threads, race on
  * it and must be serialised by the caller. */
-int tri_attn_forward_noalloc(int B, int N, int D, int h, int mask_mode,
+int tri_attn_forward_noalloc(int B, int N, int D, int h, int mode,
                              const float* ln_gamma, const float* ln_beta,
                              const float* Wq, const float* Wk, const float* Wv,
                              const float* Wg, const float* bg, const float* Wb,

@@ -20,6 +20,8 @@ TRI_ATTN_F32 = 0
 TRI_ATTN_BF16 = 1
 TRI_ATTN_MASK_ROW_KEY = 0
 TRI_ATTN_MASK_QUERY_KEY = 1
+TRI_ATTN_STARTING_NODE = 0
+TRI_ATTN_ENDING_NODE = 2        # OR-ed into the mode: attention along columns
 
 TRI_ATTN_OK = 0
 TRI_ATTN_ERR_INVALID_ARG = 1
@@ -111,7 +113,7 @@ def tri_attn_workspace_bytes(B, N, D, h, dtype) -> int:
     return n.value
 
 
-def tri_attn_create(B, N, D, h, dtype, mask_mode, params: dict, stream=None) -> ctypes.c_void_p:
+def tri_attn_create(B, N, D, h, dtype, mode, params: dict, stream=None) -> ctypes.c_void_p:
     """``params``: device tensors gamma, beta, Wq, Wk, Wv, Wg, bg, Wb, Wo, bo of the
     handle's dtype (nn.Linear layout). Returns the opaque handle."""
     want = _DTYPES.get(dtype)
@@ -122,7 +124,7 @@ def tri_attn_create(B, N, D, h, dtype, mask_mode, params: dict, stream=None) -> 
             raise ValueError(f"{name} must be a contiguous {want} CUDA tensor")
         ptrs.append(t.data_ptr())
     handle = ctypes.c_void_p()
-    _check(load_library().tri_attn_create(ctypes.byref(handle), B, N, D, h, dtype, mask_mode,
+    _check(load_library().tri_attn_create(ctypes.byref(handle), B, N, D, h, dtype, mode,
                                           *ptrs, _stream_ptr(stream)), "tri_attn_create")
     return handle
 
@@ -171,14 +173,14 @@ def tri_attn_kernel_times(handle) -> list:
     return [(names[i].decode(), float(ms[i])) for i in range(n.value)]
 
 
-def tri_attn_forward_noalloc(B, N, D, h, mask_mode, params: dict, stream,
+def tri_attn_forward_noalloc(B, N, D, h, mode, params: dict, stream,
                              pair_repr: torch.Tensor, pair_mask: torch.Tensor,
                              out: torch.Tensor) -> None:
     """fp32 forward that allocates nothing on the device (see include/tri_attn.h):
     for callers that may not allocate; intermediates use the library's fixed
     16 MiB scratch, so problems beyond it raise TriAttnError (UNSUPPORTED)."""
     ptrs = [params[name].data_ptr() for name in PARAM_ORDER]
-    _check(load_library().tri_attn_forward_noalloc(B, N, D, h, mask_mode, *ptrs,
+    _check(load_library().tri_attn_forward_noalloc(B, N, D, h, mode, *ptrs,
                                                    _stream_ptr(stream), pair_repr.data_ptr(),
                                                    pair_mask.data_ptr(), out.data_ptr()),
            "tri_attn_forward_noalloc")
@@ -201,14 +203,14 @@ class _DeviceView:
 
 
 class TriangularAttention:
-    """Owns one handle: ``TriangularAttention(B, N, D, h, dtype, mask_mode, params)``,
+    """Owns one handle: ``TriangularAttention(B, N, D, h, dtype, mode, params)``,
     then ``forward(pair_repr, pair_mask)`` returns a new output tensor."""
 
-    def __init__(self, B, N, D, h, dtype, mask_mode, params, stream=None):
+    def __init__(self, B, N, D, h, dtype, mode, params, stream=None):
         self.B, self.N, self.D, self.h = B, N, D, h
-        self.dtype, self.mask_mode = dtype, mask_mode
+        self.dtype, self.mode = dtype, mode
         self.torch_dtype = _DTYPES[dtype]
-        self.handle = tri_attn_create(B, N, D, h, dtype, mask_mode, params, stream)
+        self.handle = tri_attn_create(B, N, D, h, dtype, mode, params, stream)
 
     def _check_inputs(self, x, mask, out, device_side=True):
         shape = (self.B, self.N, self.N, self.D)

@@ -17,8 +17,16 @@
 // hardware suspend hint, so this is on the order of a second).
 #define TRI_DEFAULT_WAIT_LIMIT (1ll << 24)
 
+// Split of the `mode` argument: the mask reading and the node variant.
+inline bool tri_mode_valid(int mode) {
+  return (mode & ~(TRI_ATTN_MASK_QUERY_KEY | TRI_ATTN_ENDING_NODE)) == 0;
+}
+inline int tri_mask_mode(int mode) { return mode & TRI_ATTN_MASK_QUERY_KEY; }
+inline bool tri_ending(int mode) { return (mode & TRI_ATTN_ENDING_NODE) != 0; }
+
 struct tri_attn_s {
   int B, N, D, h, d, dtype, mask_mode;
+  bool ending;                     // ending-node variant (attention along columns)
   long long cells;                 // B * N * N
   int device;
   // Packed weights (owned).
@@ -65,6 +73,7 @@ cudaError_t tri_f32_forward(tri_attn_s* t, cudaStream_t s, const float* x,
 // layout are packed into w_proj / w_out, intermediates go to q..o and bias.
 struct TriF32Raw {
   int B, N, D, h, mask_mode;
+  bool ending;
   const float *gamma, *beta, *Wq, *Wk, *Wv, *Wg, *bg, *Wb, *Wo, *bo;
   const float* x;
   const int32_t* mask;

@@ -1,13 +1,15 @@
-// fp32 SIMT path of starting-node triangular self-attention.
+// fp32 SIMT path of triangular self-attention (starting and ending node).
 //
 // Three kernels, in the split of the "Kimi-K2.6 l2_p6" POPCORNBENCH page
 // (preprocess / attention / finalize), written for fp32 accuracy rather than
 // tensor-core throughput:
 //   ln_proj_f32    LayerNorm + the five projections of every cell, gate sigmoid,
 //                  pair bias scattered to its (B, h, N, N) plane;
-//   row_attn_f32   per (row i, head, 128 queries): logits with the shared pair
+//   row_attn_f32   per (line, head, 128 queries): logits with the shared pair
 //                  bias, mask replacement by -1e9, online softmax over keys
-//                  staged 32 at a time, P.V;
+//                  staged 32 at a time, P.V. A line is a row i of the grid
+//                  (starting node) or a column j (ending node): its cell x
+//                  sits at b N^2 + a sa + x sx with (sa, sx) = (N, 1) or (1, N);
 //   gate_out_f32   g * o followed by the output projection and its bias.
 #include <math.h>
 
@@ -66,9 +68,11 @@ __device__ __forceinline__ void tile_gemm(const float* __restrict__ xt, int c0, 
 // projection [Wq|Wk|Wv|Wg|Wb] ("Kimi-K2.6 l2_p6", op list steps 1-3 and 5-7).
 // A block takes 32 cells: one warp per cell normalises it into the
 // channel-major operand; then 2-output x 16-cell thread tiles cover the 4D
-// main outputs and a last pass the h bias outputs.
+// main outputs and a last pass the h bias outputs. The bias of cell (b, r, c)
+// goes to [b, t, r, c] of the plane, or to [b, t, c, r] for the ending node
+// (the plane is indexed [query, key] along the attended line).
 __global__ void __launch_bounds__(kProjThreads)
-ln_proj_f32(const float* __restrict__ x, long long cells, int N, int D, int h,
+ln_proj_f32(const float* __restrict__ x, long long cells, int N, int D, int h, int ending,
             const float* __restrict__ gamma, const float* __restrict__ beta,
             const float* __restrict__ Wt, int ldw,   // [D][ldw], 4D + h columns used
             const float* __restrict__ bg,
@@ -121,20 +125,25 @@ ln_proj_f32(const float* __restrict__ x, long long cells, int N, int D, int h,
     float acc = 0.f;
     for (int e = 0; e < D; ++e) acc = fmaf(xt[e * kXtLd + c], Wt[(size_t)e * ldw + 4 * D + t], acc);
     if (c < ncell) {
-      const long long cell = cell0 + c, b = cell / NN;
-      bias[(b * h + t) * NN + (cell - b * NN)] = acc;
+      const long long cell = cell0 + c, b = cell / NN, rc = cell - b * NN;
+      const long long pos = ending ? (rc % N) * N + rc / N : rc;
+      bias[(b * h + t) * NN + pos] = acc;
     }
   }
 }
 
 // Row attention ("Kimi-K2.6 l2_p6", op list steps 8-16): block = (128 queries
-// j, head t, row (b, i)); one thread per query, keys in chunks of KC.
-template <int MAXD, int KC>
+// j, head t, line (b, a)); one thread per query, keys in chunks of KC. Cell x
+// of the line is b N^2 + a sa + x sx, (sa, sx) = (N, 1) for the starting node
+// and (1, N) for the ending node (END); the pair bias is read at [b, t, query,
+// key], and the query-key mask at b N^2 + query sa + key sx.
+template <int MAXD, int KC, bool END>
 __global__ void __launch_bounds__(kQueriesPerBlock)
 row_attn_f32(const float* __restrict__ q, const float* __restrict__ k,
              const float* __restrict__ v, const float* __restrict__ bias,
              const int32_t* __restrict__ mask, int mask_mode,
              int N, int D, int h, int d, float* __restrict__ o) {
+  const int sa = END ? 1 : N, sx = END ? N : 1;
   __shared__ float Ks[KC][MAXD];
   __shared__ float Vs[KC][MAXD];
   __shared__ float Bs[kQueriesPerBlock][KC + 1];
@@ -142,9 +151,10 @@ row_attn_f32(const float* __restrict__ q, const float* __restrict__ k,
   __shared__ int Mrow[KC];
 
   const int tid = threadIdx.x;
-  const long long row = blockIdx.x;              // b * N + i
+  const long long row = blockIdx.x;              // b * N + a
   const int t = blockIdx.y;
   const long long b = row / N;
+  const long long line0 = b * (long long)N * N + (row - b * N) * sa;   // cell 0 of the line
   const int j0 = blockIdx.z * kQueriesPerBlock;
   const int j = j0 + tid;
   const bool active = j < N;
@@ -154,7 +164,7 @@ row_attn_f32(const float* __restrict__ q, const float* __restrict__ k,
   float qv[MAXD], acc[MAXD];
 #pragma unroll
   for (int e = 0; e < MAXD; ++e) {
-    qv[e] = (active && e < d) ? q[(row * N + j) * D + t * d + e] : 0.f;
+    qv[e] = (active && e < d) ? q[(line0 + (long long)j * sx) * D + t * d + e] : 0.f;
     acc[e] = 0.f;
   }
   float m = -INFINITY, l = 0.f;
@@ -165,7 +175,7 @@ row_attn_f32(const float* __restrict__ q, const float* __restrict__ k,
     for (int idx = tid; idx < KC * MAXD; idx += kQueriesPerBlock) {
       const int kk = idx / MAXD, e = idx % MAXD;
       const bool in = kk < nk && e < d;
-      const long long src = (row * N + k0 + kk) * D + t * d + e;
+      const long long src = (line0 + (long long)(k0 + kk) * sx) * D + t * d + e;
       Ks[kk][e] = in ? k[src] : 0.f;
       Vs[kk][e] = in ? v[src] : 0.f;
     }
@@ -174,10 +184,11 @@ row_attn_f32(const float* __restrict__ q, const float* __restrict__ k,
       const bool in = (j0 + jj) < N && kk < nk;
       Bs[jj][kk] = in ? bias[(b * h + t) * NN + (long long)(j0 + jj) * N + k0 + kk] : 0.f;
       if (mask_mode == TRI_ATTN_MASK_QUERY_KEY)
-        Ms[jj][kk] = (in && mask[b * NN + (long long)(j0 + jj) * N + k0 + kk] != 0) ? 1 : 0;
+        Ms[jj][kk] =
+            (in && mask[b * NN + (long long)(j0 + jj) * sa + (long long)(k0 + kk) * sx] != 0) ? 1 : 0;
     }
     if (mask_mode == TRI_ATTN_MASK_ROW_KEY && tid < KC)
-      Mrow[tid] = tid < nk ? mask[row * N + k0 + tid] : 0;
+      Mrow[tid] = tid < nk ? mask[line0 + (long long)(k0 + tid) * sx] : 0;
     __syncthreads();
 
 #pragma unroll 1
@@ -205,7 +216,7 @@ row_attn_f32(const float* __restrict__ q, const float* __restrict__ k,
     const float inv = 1.0f / l;
 #pragma unroll
     for (int e = 0; e < MAXD; ++e)
-      if (e < d) o[(row * N + j) * D + t * d + e] = acc[e] * inv;
+      if (e < d) o[(line0 + (long long)j * sx) * D + t * d + e] = acc[e] * inv;
   }
 }
 
@@ -239,6 +250,50 @@ gate_out_f32(const float* __restrict__ g, const float* __restrict__ o, long long
   }
 }
 
+// The three kernels of one forward on packed weights and the given buffers.
+struct F32Launch {
+  long long cells;
+  int B, N, D, h, mask_mode;
+  bool ending;
+  const float *x, *gamma, *beta, *w_proj, *bg, *w_out, *bo;
+  const int32_t* mask;
+  float *q, *k, *v, *g, *o, *bias, *out;
+};
+
+cudaError_t launch_f32(const F32Launch& a, cudaStream_t s, tri_attn_s* timing) {
+  const int D = a.D, h = a.h, d = a.D / a.h, N = a.N;
+  const unsigned nblk = (unsigned)((a.cells + kCellsPerBlock - 1) / kCellsPerBlock);
+  const size_t smem = (size_t)kXtLd * D * sizeof(float);
+  if (timing) tri_mark(timing, s, 0, nullptr);
+  ln_proj_f32<<<nblk, kProjThreads, smem, s>>>(a.x, a.cells, N, D, h, a.ending ? 1 : 0, a.gamma,
+                                               a.beta, a.w_proj, proj_ld(D, h), a.bg, a.q, a.k,
+                                               a.v, a.g, a.bias);
+  if (timing) tri_mark(timing, s, 1, "ln_proj_f32");
+  dim3 grid((unsigned)(a.B * (long long)N), h, (N + kQueriesPerBlock - 1) / kQueriesPerBlock);
+#define TRI_ATTN_F32_CASE(MD)                                                              \
+  case MD:                                                                                 \
+    if (a.ending)                                                                          \
+      row_attn_f32<MD, (MD >= 128 ? 16 : kKeyChunk), true><<<grid, kQueriesPerBlock, 0, s>>>( \
+          a.q, a.k, a.v, a.bias, a.mask, a.mask_mode, N, D, h, d, a.o);                    \
+    else                                                                                   \
+      row_attn_f32<MD, (MD >= 128 ? 16 : kKeyChunk), false><<<grid, kQueriesPerBlock, 0, s>>>( \
+          a.q, a.k, a.v, a.bias, a.mask, a.mask_mode, N, D, h, d, a.o);                    \
+    break;
+  const int md = d <= 8 ? 8 : d <= 16 ? 16 : d <= 32 ? 32 : d <= 64 ? 64 : 128;
+  switch (md) {
+    TRI_ATTN_F32_CASE(8)
+    TRI_ATTN_F32_CASE(16)
+    TRI_ATTN_F32_CASE(32)
+    TRI_ATTN_F32_CASE(64)
+    TRI_ATTN_F32_CASE(128)
+  }
+#undef TRI_ATTN_F32_CASE
+  if (timing) tri_mark(timing, s, 2, "row_attn_f32");
+  gate_out_f32<<<nblk, kProjThreads, smem, s>>>(a.g, a.o, a.cells, D, a.w_out, a.bo, a.out);
+  if (timing) tri_mark(timing, s, 3, "gate_out_f32");
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t tri_f32_pack_weights(tri_attn_s* t, const void* Wq, const void* Wk, const void* Wv,
@@ -260,68 +315,31 @@ cudaError_t tri_f32_pack_weights(tri_attn_s* t, const void* Wq, const void* Wk, 
 
 cudaError_t tri_f32_forward(tri_attn_s* t, cudaStream_t s, const float* x,
                             const int32_t* mask, float* out) {
-  const long long cells = t->cells;
-  const int D = t->D, h = t->h, d = t->d, N = t->N;
-  const unsigned nblk = (unsigned)((cells + kCellsPerBlock - 1) / kCellsPerBlock);
-  const size_t smem = (size_t)kXtLd * D * sizeof(float);
-  float *q = (float*)t->q, *k = (float*)t->k, *v = (float*)t->v, *g = (float*)t->g,
-        *o = (float*)t->o;
-  tri_mark(t, s, 0, nullptr);
-  ln_proj_f32<<<nblk, kProjThreads, smem, s>>>(x, cells, N, D, h, t->gamma, t->beta,
-                                               (const float*)t->w_proj, proj_ld(D, h), t->bg,
-                                               q, k, v, g, t->bias);
-  tri_mark(t, s, 1, "ln_proj_f32");
-  dim3 grid((unsigned)(t->B * (long long)N), h, (N + kQueriesPerBlock - 1) / kQueriesPerBlock);
-#define TRI_ATTN_F32_CASE(MD)                                                              \
-  case MD:                                                                                 \
-    row_attn_f32<MD, (MD >= 128 ? 16 : kKeyChunk)><<<grid, kQueriesPerBlock, 0, s>>>(q, k, v, t->bias, mask, t->mask_mode, \
-                                                       N, D, h, d, o);                     \
-    break;
-  const int md = d <= 8 ? 8 : d <= 16 ? 16 : d <= 32 ? 32 : d <= 64 ? 64 : 128;
-  switch (md) {
-    TRI_ATTN_F32_CASE(8)
-    TRI_ATTN_F32_CASE(16)
-    TRI_ATTN_F32_CASE(32)
-    TRI_ATTN_F32_CASE(64)
-    TRI_ATTN_F32_CASE(128)
-  }
-#undef TRI_ATTN_F32_CASE
-  tri_mark(t, s, 2, "row_attn_f32");
-  gate_out_f32<<<nblk, kProjThreads, smem, s>>>(g, o, cells, D, (const float*)t->w_out, t->bo,
-                                                out);
-  tri_mark(t, s, 3, "gate_out_f32");
-  return cudaGetLastError();
+  F32Launch a;
+  a.cells = t->cells; a.B = t->B; a.N = t->N; a.D = t->D; a.h = t->h;
+  a.mask_mode = t->mask_mode; a.ending = t->ending;
+  a.x = x; a.gamma = t->gamma; a.beta = t->beta; a.w_proj = (const float*)t->w_proj;
+  a.bg = t->bg; a.w_out = (const float*)t->w_out; a.bo = t->bo; a.mask = mask;
+  a.q = (float*)t->q; a.k = (float*)t->k; a.v = (float*)t->v; a.g = (float*)t->g;
+  a.o = (float*)t->o; a.bias = t->bias; a.out = out;
+  return launch_f32(a, s, t);
 }
 
-cudaError_t tri_f32_forward_raw(const TriF32Raw& a, cudaStream_t s) {
-  const long long cells = (long long)a.B * a.N * a.N;
-  const int D = a.D, h = a.h, d = a.D / a.h, N = a.N, nout = proj_ld(D, h);
-  const void* mats[5] = {a.Wq, a.Wk, a.Wv, a.Wg, a.Wb};
+cudaError_t tri_f32_forward_raw(const TriF32Raw& r, cudaStream_t s) {
+  const int D = r.D, h = r.h, nout = proj_ld(D, h);
+  const void* mats[5] = {r.Wq, r.Wk, r.Wv, r.Wg, r.Wb};
   for (int m = 0; m < 5; ++m) {
     const int rows = m < 4 ? D : h;
     const int n = rows * D;
-    pack_transpose_f32<<<(n + 255) / 256, 256, 0, s>>>((const float*)mats[m], rows, D, a.w_proj,
+    pack_transpose_f32<<<(n + 255) / 256, 256, 0, s>>>((const float*)mats[m], rows, D, r.w_proj,
                                                        nout, m * D);
   }
-  pack_transpose_f32<<<(D * D + 255) / 256, 256, 0, s>>>(a.Wo, D, D, a.w_out, D, 0);
-  const unsigned nblk = (unsigned)((cells + kCellsPerBlock - 1) / kCellsPerBlock);
-  const size_t smem = (size_t)kXtLd * D * sizeof(float);
-  ln_proj_f32<<<nblk, kProjThreads, smem, s>>>(a.x, cells, N, D, h, a.gamma, a.beta, a.w_proj,
-                                               nout, a.bg, a.q, a.k, a.v, a.g, a.bias);
-  dim3 grid((unsigned)(a.B * (long long)N), h, (N + kQueriesPerBlock - 1) / kQueriesPerBlock);
-  const int md = d <= 8 ? 8 : d <= 16 ? 16 : d <= 32 ? 32 : d <= 64 ? 64 : 128;
-  switch (md) {
-    case 8: row_attn_f32<8, kKeyChunk><<<grid, kQueriesPerBlock, 0, s>>>(
-        a.q, a.k, a.v, a.bias, a.mask, a.mask_mode, N, D, h, d, a.o); break;
-    case 16: row_attn_f32<16, kKeyChunk><<<grid, kQueriesPerBlock, 0, s>>>(
-        a.q, a.k, a.v, a.bias, a.mask, a.mask_mode, N, D, h, d, a.o); break;
-    case 32: row_attn_f32<32, kKeyChunk><<<grid, kQueriesPerBlock, 0, s>>>(
-        a.q, a.k, a.v, a.bias, a.mask, a.mask_mode, N, D, h, d, a.o); break;
-    case 64: row_attn_f32<64, kKeyChunk><<<grid, kQueriesPerBlock, 0, s>>>(
-        a.q, a.k, a.v, a.bias, a.mask, a.mask_mode, N, D, h, d, a.o); break;
-    default: row_attn_f32<128, 16><<<grid, kQueriesPerBlock, 0, s>>>(
-        a.q, a.k, a.v, a.bias, a.mask, a.mask_mode, N, D, h, d, a.o); break;
-  }
-  gate_out_f32<<<nblk, kProjThreads, smem, s>>>(a.g, a.o, cells, D, a.w_out, a.bo, a.out);
-  return cudaGetLastError();
+  pack_transpose_f32<<<(D * D + 255) / 256, 256, 0, s>>>(r.Wo, D, D, r.w_out, D, 0);
+  F32Launch a;
+  a.cells = (long long)r.B * r.N * r.N; a.B = r.B; a.N = r.N; a.D = D; a.h = h;
+  a.mask_mode = r.mask_mode; a.ending = r.ending;
+  a.x = r.x; a.gamma = r.gamma; a.beta = r.beta; a.w_proj = r.w_proj; a.bg = r.bg;
+  a.w_out = r.w_out; a.bo = r.bo; a.mask = r.mask;
+  a.q = r.q; a.k = r.k; a.v = r.v; a.g = r.g; a.o = r.o; a.bias = r.bias; a.out = r.out;
+  return launch_f32(a, s, nullptr);
 }

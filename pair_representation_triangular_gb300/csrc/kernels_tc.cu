@@ -167,6 +167,7 @@ struct Consts {
 struct Params {
   long long cells;
   int N, Nb, h, mask_mode, ntiles;
+  int ending;                  // bias of cell (r, c) goes to plane row c, column r
   const int32_t* mask;
   __nv_bfloat16 *q, *k, *v, *g;
   __half* bias;                // (B, h, N, Nb) fp16, scaled by log2(e)
@@ -348,10 +349,12 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
         bool keep = true;
         if (p.mask_mode == TRI_ATTN_MASK_QUERY_KEY) keep = p.mask[cell] != 0;
 #pragma unroll
+        const long long pr = p.ending ? cc : rr, pc = p.ending ? rr : cc;
+#pragma unroll
         for (int t = 0; t < 2; ++t) {
           const int head = 2 * hh + t;
           if (head < p.h)
-            p.bias[((bb * p.h + head) * p.N + rr) * p.Nb + cc] =
+            p.bias[((bb * p.h + head) * p.N + pr) * p.Nb + pc] =
                 __float2half_rn(keep ? bsum[t] * kLog2e : -INFINITY);
         }
       }
@@ -694,13 +697,13 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       bool ok = true;
       for (int ui = 0; ok && ui < my_units; ++ui) {
         const Unit un = decode_unit(blockIdx.x + ui * gridDim.x, p);
-        const int row0 = un.b * N + un.rg * R;
+        const int a0 = un.rg * R;
         const int qb = ui & 1;
         if (ui >= 2 && !wait_or_abort(&bars->q_empty[qb], ((ui >> 1) - 1) & 1, ab)) break;
         tc::mbar_arrive_expect_tx(&bars->q_full[qb], R * Q_BYTES);
         for (int r = 0; r < R; ++r)
-          tc::tma_load_3d(smem + OFF_Q + (qb * R + r) * Q_BYTES, &map_q, &bars->q_full[qb],
-                          un.t * DH, un.j0, row0 + r);
+          tc::tma_load_4d(smem + OFF_Q + (qb * R + r) * Q_BYTES, &map_q, &bars->q_full[qb],
+                          un.t * DH, un.j0, a0 + r, un.b);
         q_issued = ui + 1;
         for (int kt = 0; kt < KT; ++kt) {
           const int kg = kg_issued, s = kg % STAGES;
@@ -711,10 +714,10 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
           uint8_t* st = smem + OFF_STAGE + s * STAGE_BYTES;
           tc::mbar_arrive_expect_tx(&bars->kv_full[s], STAGE_BYTES);
           for (int r = 0; r < R; ++r) {
-            tc::tma_load_3d(st + r * 2 * KV_BYTES, &map_k, &bars->kv_full[s], un.t * DH, kt * BK,
-                            row0 + r);
-            tc::tma_load_3d(st + r * 2 * KV_BYTES + KV_BYTES, &map_v, &bars->kv_full[s],
-                            un.t * DH, kt * BK, row0 + r);
+            tc::tma_load_4d(st + r * 2 * KV_BYTES, &map_k, &bars->kv_full[s], un.t * DH, kt * BK,
+                            a0 + r, un.b);
+            tc::tma_load_4d(st + r * 2 * KV_BYTES + KV_BYTES, &map_v, &bars->kv_full[s],
+                            un.t * DH, kt * BK, a0 + r, un.b);
           }
           tc::tma_load_3d(st + STAGE_KV, &map_b, &bars->kv_full[s], kt * BK, un.j0,
                           un.b * p.h + un.t);
@@ -824,7 +827,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tc::tma_store_3d(&map_o, ostg, fu.t * DH, fj, fu.b * N + fi);
+          tc::tma_store_4d(&map_o, ostg, fu.t * DH, fj, fi, fu.b);
           tc::tma_store_commit();
         }
         ost_pending = true;
@@ -956,6 +959,42 @@ __global__ void mask_summary(const int32_t* __restrict__ mask, int N, long long 
     if (lane == 0) bits[row * words + wd] = w;
   }
   if (lane == 0) any[row] = found != 0;
+}
+
+// Ending node: line (b, a) is column a of the mask (key k = grid row k). A
+// block takes 32 columns of one batch, lane = column a; warp wp forms the
+// words w = wp, wp + 8, ... (bit kk of word w: pair_mask[b, 32 w + kk, a] != 0,
+// each of its 32 loads one coalesced 128-byte row segment across the warp),
+// and the block ORs them into the column's "keeps some key" flag.
+__global__ void __launch_bounds__(256)
+mask_summary_cols(const int32_t* __restrict__ mask, int N, int words, uint32_t* __restrict__ bits,
+                  unsigned char* __restrict__ any) {
+  __shared__ uint32_t found[8][32];
+  const int cblocks = (N + 31) >> 5;
+  const long long b = blockIdx.x / cblocks;
+  const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
+  const int a = (int)(blockIdx.x % cblocks) * 32 + lane;
+  uint32_t acc = 0;
+  if (a < N) {
+    const int32_t* col = mask + b * N * N + a;
+    for (int w = wp; w < words; w += 8) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int kk = 0; kk < 32; ++kk) {
+        const int k = 32 * w + kk;
+        if (k < N && col[(long long)k * N] != 0) word |= 1u << kk;
+      }
+      bits[(b * N + a) * words + w] = word;
+      acc |= word;
+    }
+  }
+  found[wp][lane] = acc;
+  __syncthreads();
+  if (wp == 0 && a < N) {
+#pragma unroll
+    for (int i = 1; i < 8; ++i) acc |= found[i][lane];
+    any[b * N + a] = acc != 0;
+  }
 }
 }  // namespace k2
 
@@ -1170,7 +1209,7 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base
               CUtensorMapSwizzle swz) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  cuuint32_t es[3] = {1, 1, 1};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
   return enc(m, dt, rank, const_cast<void*>(base), dims, strides_bytes, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -1184,12 +1223,16 @@ bool map_rows_bf16(CUtensorMap* m, const void* base, long long rows, int box_row
                   CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// (B*N rows, N cells, 128 channels) bf16, box of one head (32 ch) x box_j cells.
-bool map_heads(CUtensorMap* m, const void* base, int B, int N, int box_j) {
-  cuuint64_t dims[3] = {128, (cuuint64_t)N, (cuuint64_t)B * N};
-  cuuint64_t strides[2] = {256, (cuuint64_t)N * 256};
-  cuuint32_t box[3] = {32, (cuuint32_t)box_j, 1};
-  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box,
+// A (B, N, N, 128) bf16 activation seen as (channel, position x along a line,
+// line a, batch b): lines are the grid's rows (starting node: cell (a, x)) or
+// its columns (ending node: cell (x, a)). Box: one head (32 channels) x box_x
+// positions of one line.
+bool map_lines(CUtensorMap* m, const void* base, int B, int N, int box_x, bool ending) {
+  const cuuint64_t cell = 256, row = (cuuint64_t)N * 256;
+  cuuint64_t dims[4] = {128, (cuuint64_t)N, (cuuint64_t)N, (cuuint64_t)B};
+  cuuint64_t strides[3] = {ending ? row : cell, ending ? cell : row, (cuuint64_t)N * row};
+  cuuint32_t box[4] = {32, (cuuint32_t)box_x, 1, 1};
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box,
                   CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
@@ -1271,10 +1314,10 @@ cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const voi
 
   const long long cells = t->cells;
   bool ok = map_rows_bf16(&st->map_w, t->w_proj, 512, 256);
-  ok = ok && map_heads(&st->map_q, t->q, B, N, k2::BQ);
-  ok = ok && map_heads(&st->map_k, t->k, B, N, k2::BK);
-  ok = ok && map_heads(&st->map_v, t->v, B, N, k2::BK);
-  ok = ok && map_heads(&st->map_os, t->o, B, N, 32);
+  ok = ok && map_lines(&st->map_q, t->q, B, N, k2::BQ, t->ending);
+  ok = ok && map_lines(&st->map_k, t->k, B, N, k2::BK, t->ending);
+  ok = ok && map_lines(&st->map_v, t->v, B, N, k2::BK, t->ending);
+  ok = ok && map_lines(&st->map_os, t->o, B, N, 32, t->ending);
   {
     cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)N, (cuuint64_t)B * h};
     cuuint64_t strides[2] = {(cuuint64_t)st->Nb * 2, (cuuint64_t)N * st->Nb * 2};
@@ -1331,6 +1374,7 @@ cudaError_t tri_tc_forward(tri_attn_s* t, cudaStream_t s, const void* x, const i
 
   k1::Params p1;
   p1.cells = cells; p1.N = N; p1.Nb = st->Nb; p1.h = h; p1.mask_mode = t->mask_mode;
+  p1.ending = t->ending ? 1 : 0;
   p1.ntiles = ntiles;
   p1.mask = mask;
   p1.q = (__nv_bfloat16*)t->q; p1.k = (__nv_bfloat16*)t->k; p1.v = (__nv_bfloat16*)t->v;
@@ -1344,9 +1388,15 @@ cudaError_t tri_tc_forward(tri_attn_s* t, cudaStream_t s, const void* x, const i
 
   {
     const long long rows = (long long)B * N;
-    k2::mask_summary<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(mask, N, rows, st->words,
-                                                              st->mbits, st->row_any);
-    tri_mark(t, s, mark++, "mask_summary");
+    if (!t->ending) {
+      k2::mask_summary<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(mask, N, rows, st->words,
+                                                                st->mbits, st->row_any);
+      tri_mark(t, s, mark++, "mask_summary");
+    } else {
+      const unsigned blocks = (unsigned)(B * (long long)((N + 31) / 32));
+      k2::mask_summary_cols<<<blocks, 256, 0, s>>>(mask, N, st->words, st->mbits, st->row_any);
+      tri_mark(t, s, mark++, "mask_summary_cols");
+    }
   }
   k2::Params p2;
   p2.B = B; p2.N = N; p2.h = h; p2.mask_mode = t->mask_mode;

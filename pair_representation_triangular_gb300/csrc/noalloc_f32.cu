@@ -57,7 +57,7 @@ size_t scratch_bytes(int B, int N, int D, int h) {
 
 }  // namespace
 
-extern "C" int tri_attn_forward_noalloc(int B, int N, int D, int h, int mask_mode,
+extern "C" int tri_attn_forward_noalloc(int B, int N, int D, int h, int mode,
                                         const float* ln_gamma, const float* ln_beta,
                                         const float* Wq, const float* Wk, const float* Wv,
                                         const float* Wg, const float* bg, const float* Wb,
@@ -65,8 +65,7 @@ extern "C" int tri_attn_forward_noalloc(int B, int N, int D, int h, int mask_mod
                                         const float* pair_repr, const int32_t* pair_mask,
                                         float* out) {
   if (B < 1 || N < 1 || D < 1 || h < 1 || D % h) return TRI_ATTN_ERR_INVALID_ARG;
-  if (mask_mode != TRI_ATTN_MASK_ROW_KEY && mask_mode != TRI_ATTN_MASK_QUERY_KEY)
-    return TRI_ATTN_ERR_INVALID_ARG;
+  if (!tri_mode_valid(mode)) return TRI_ATTN_ERR_INVALID_ARG;
   const void* ptrs[] = {ln_gamma, ln_beta, Wq, Wk, Wv, Wg, bg, Wb, Wo, bo, pair_repr, out};
   for (const void* p : ptrs)
     if (!p || ((uintptr_t)p & 15u)) return TRI_ATTN_ERR_INVALID_ARG;
@@ -81,7 +80,8 @@ extern "C" int tri_attn_forward_noalloc(int B, int N, int D, int h, int mask_mod
   if (e != cudaSuccess) return TRI_ATTN_ERR_CUDA;
   const size_t cells = (size_t)B * N * N;
   TriF32Raw a;
-  a.B = B; a.N = N; a.D = D; a.h = h; a.mask_mode = mask_mode;
+  a.B = B; a.N = N; a.D = D; a.h = h;
+  a.mask_mode = tri_mask_mode(mode); a.ending = tri_ending(mode);
   a.gamma = ln_gamma; a.beta = ln_beta; a.Wq = Wq; a.Wk = Wk; a.Wv = Wv; a.Wg = Wg;
   a.bg = bg; a.Wb = Wb; a.Wo = Wo; a.bo = bo;
   a.x = pair_repr; a.mask = pair_mask; a.out = out;

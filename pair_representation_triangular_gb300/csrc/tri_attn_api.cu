@@ -93,7 +93,7 @@ int tri_attn_workspace_bytes(int B, int N, int D, int h, int dtype, size_t* byte
   return TRI_ATTN_OK;
 }
 
-int tri_attn_create(tri_attn_t* out, int B, int N, int D, int h, int dtype, int mask_mode,
+int tri_attn_create(tri_attn_t* out, int B, int N, int D, int h, int dtype, int mode,
                     const void* ln_gamma, const void* ln_beta, const void* Wq, const void* Wk,
                     const void* Wv, const void* Wg, const void* bg, const void* Wb,
                     const void* Wo, const void* bo, void* stream) {
@@ -101,8 +101,7 @@ int tri_attn_create(tri_attn_t* out, int B, int N, int D, int h, int dtype, int 
   *out = nullptr;
   int st = check_shape(B, N, D, h, dtype);
   if (st) return st;
-  if (mask_mode != TRI_ATTN_MASK_ROW_KEY && mask_mode != TRI_ATTN_MASK_QUERY_KEY)
-    return TRI_ATTN_ERR_INVALID_ARG;
+  if (!tri_mode_valid(mode)) return TRI_ATTN_ERR_INVALID_ARG;
   const void* ptrs[] = {ln_gamma, ln_beta, Wq, Wk, Wv, Wg, bg, Wb, Wo, bo};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return TRI_ATTN_ERR_INVALID_ARG;
@@ -111,7 +110,7 @@ int tri_attn_create(tri_attn_t* out, int B, int N, int D, int h, int dtype, int 
   tri_attn_s* t = (tri_attn_s*)calloc(1, sizeof(tri_attn_s));
   if (!t) return TRI_ATTN_ERR_OOM;
   t->B = B; t->N = N; t->D = D; t->h = h; t->d = D / h;
-  t->dtype = dtype; t->mask_mode = mask_mode;
+  t->dtype = dtype; t->mask_mode = tri_mask_mode(mode); t->ending = tri_ending(mode);
   t->cells = (long long)B * N * N;
   t->wait_limit = TRI_DEFAULT_WAIT_LIMIT;
   cudaError_t e = cudaGetDevice(&t->device);

@@ -44,7 +44,8 @@ def test_create_rejects_bad_arguments_before_cuda(lib):
     assert _create(lib, 0, 8, 64, 4, 0) == tb.TRI_ATTN_ERR_INVALID_ARG      # B < 1
     assert _create(lib, 1, 0, 64, 4, 0) == tb.TRI_ATTN_ERR_INVALID_ARG      # N < 1
     assert _create(lib, 1, 8, 64, 4, 7) == tb.TRI_ATTN_ERR_INVALID_ARG      # dtype
-    assert _create(lib, 1, 8, 64, 4, 0, mode=3) == tb.TRI_ATTN_ERR_INVALID_ARG
+    assert _create(lib, 1, 8, 64, 4, 0, mode=4) == tb.TRI_ATTN_ERR_INVALID_ARG   # unknown bit
+    assert _create(lib, 1, 8, 64, 4, 0, mode=-1) == tb.TRI_ATTN_ERR_INVALID_ARG
     assert _create(lib, 1, 8, 64, 4, 0, ptr=0) == tb.TRI_ATTN_ERR_INVALID_ARG  # NULL weights
     assert _create(lib, 1, 8, 64, 4, 0, ptr=24) == tb.TRI_ATTN_ERR_INVALID_ARG  # misaligned
     assert _create(lib, 1, 8, 512, 4, 0) == tb.TRI_ATTN_ERR_UNSUPPORTED     # f32 D > 256

@@ -24,7 +24,7 @@ def _lib():
     tb.load_library()
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])      # mask reading | ending-node flag
 def test_noalloc_matches_forward_on_two_calls(mode):
     for seed in (11, 12):                      # two calls in a row, different inputs
         w = W.custom(2, 32, 64, 4, "f32", "bernoulli", seed=seed)
