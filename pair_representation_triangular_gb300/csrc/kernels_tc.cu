@@ -1,21 +1,27 @@
-// bf16 tensor-core path of starting-node triangular self-attention (sm_103a).
+// bf16 tensor-core path of triangular self-attention, starting and ending node
+// (sm_103a).
 //
-// Three kernels, each built on tcgen05 MMAs with operands staged by TMA in
-// swizzled shared memory and accumulators in tensor memory (TMEM):
+// Four kernels; the three GEMM-shaped ones are built on tcgen05 MMAs with
+// operands staged by TMA in swizzled shared memory and accumulators in tensor
+// memory (TMEM):
 //
 //   ln_proj_tc   LayerNorm as the prologue of one concatenated projection GEMM
 //                x_hat [128 cells x 128] . [Wq|Wk|Wv|Wg]^T -> 512 TMEM columns;
-//                the epilogue writes q, k, v and sigmoid(g + bg) in bf16; the
-//                h pair-bias outputs (Wb x_hat) are computed on the CUDA cores
-//                from the same bf16 x_hat and written, scaled by log2(e), to
-//                the fp16 bias plane (B, h, N, Nb).
-//   row_attn_tc  flash-style row attention, persistent: a work unit is
-//                (b, head t, R rows i, 256 queries j) streaming 64-key tiles;
-//                S = Q K^T goes to TMEM, two softmax warpgroups add the shared
-//                pair bias (held in registers across the R rows), apply the
-//                key mask and an online softmax with lazy rescaling, and write
-//                P (bf16) back into TMEM; O += P V accumulates in TMEM. The
-//                (B, N, h, N, N) logits never exist.
+//                the epilogue writes q, k, v and sigmoid(g + bg) in bf16. The
+//                h pair-bias outputs (Wb x_hat, with gamma and beta folded into
+//                Wb) come out of the LayerNorm's statistics pass on the CUDA
+//                cores and go, scaled by log2(e), to the fp16 bias plane
+//                (B, h, N, Nb), indexed [query, key] along the attended line.
+//   mask_summary / mask_summary_cols
+//                keep bits and a "keeps some key" flag of every line.
+//   row_attn_tc  flash-style line attention, persistent: a work unit is
+//                (b, head t, R = 3 lines, 128 queries) streaming 64-key tiles.
+//                Lines are grid rows (starting node) or columns (ending node);
+//                only the tensor maps tell them apart. S = Q K^T goes to TMEM;
+//                one softmax warpgroup per line adds the shared fp16 bias
+//                tile, drops masked keys and writes P = 2^(x - mu) in bf16
+//                over S (mu: a lazily moved reference max); O += P V
+//                accumulates in TMEM. The (B, N, h, N, N) logits never exist.
 //   gate_out_tc  g * o formed in shared memory as the A operand of the output
 //                projection GEMM; the epilogue adds bo and stores bf16.
 //
