@@ -354,7 +354,6 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
         const long long rr = rc / p.N, cc = rc - rr * p.N;
         bool keep = true;
         if (p.mask_mode == TRI_ATTN_MASK_QUERY_KEY) keep = p.mask[cell] != 0;
-#pragma unroll
         const long long pr = p.ending ? cc : rr, pc = p.ending ? rr : cc;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -506,8 +505,15 @@ struct Bars {
   int abort;
 };
 
+// A step of gridDim.x units written in the units' mixed radix (query tile,
+// head, row group, batch; query tile fastest).
+struct UnitStep {
+  int jt, t, rg, b;
+};
+
 struct Params {
   int B, N, h, mask_mode, row_groups, jtiles, words, units;
+  UnitStep step;                  // gridDim.x in unit digits
   const uint32_t* mbits;          // (B*N rows, words): bit k = pair_mask[b, r, k] != 0, k < N
   const unsigned char* row_any;   // (B*N rows): the mask row keeps some key
   unsigned int* dev_err;
@@ -516,18 +522,45 @@ struct Params {
 };
 
 struct Unit {
-  int b, t, rg, j0;
+  int b, t, rg, jt, j0;
 };
 
 __device__ __forceinline__ Unit decode_unit(int u, const Params& p) {
   Unit un;
-  const int jt = u % p.jtiles;
+  un.jt = u % p.jtiles;
   un.t = (u / p.jtiles) % p.h;
   const int rgb = u / (p.jtiles * p.h);
   un.rg = rgb % p.row_groups;
   un.b = rgb / p.row_groups;
-  un.j0 = jt * BQ;
+  un.j0 = un.jt * BQ;
   return un;
+}
+
+// The unit gridDim.x further on: digit-wise addition with carries (each digit
+// of the step is below its radix, so one subtraction per digit suffices).
+__device__ __forceinline__ void step_unit(Unit& u, const Params& p) {
+  int v = u.jt + p.step.jt;
+  int c = v >= p.jtiles;
+  u.jt = c ? v - p.jtiles : v;
+  v = u.t + p.step.t + c;
+  c = v >= p.h;
+  u.t = c ? v - p.h : v;
+  v = u.rg + p.step.rg + c;
+  c = v >= p.row_groups;
+  u.rg = c ? v - p.row_groups : v;
+  u.b += p.step.b + c;
+  u.j0 = u.jt * BQ;
+}
+
+// Position of the tile stream of one MMA thread: global tile c, its unit ui,
+// key tile kt, stage s and the stage ring's phase, advanced without dividing.
+struct TileIt {
+  int c, ui, kt, s, sph;
+};
+__device__ __forceinline__ void advance(TileIt& it, int KT) {
+  ++it.c;
+  if (++it.kt == KT) { it.kt = 0; ++it.ui; }
+  if (++it.s == STAGES) { it.s = 0; it.sph ^= 1; }
 }
 
 // Real-key bits of word w (keys 32w..32w+31 of a tile with `left` keys left).
@@ -701,8 +734,8 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       tc::tma_prefetch_desc(&map_v);
       tc::tma_prefetch_desc(&map_b);
       bool ok = true;
-      for (int ui = 0; ok && ui < my_units; ++ui) {
-        const Unit un = decode_unit(blockIdx.x + ui * gridDim.x, p);
+      Unit un = decode_unit(blockIdx.x, p);
+      for (int ui = 0; ok && ui < my_units; ++ui, step_unit(un, p)) {
         const int a0 = un.rg * R;
         const int qb = ui & 1;
         if (ui >= 2 && !wait_or_abort(&bars->q_empty[qb], ((ui >> 1) - 1) & 1, ab)) break;
@@ -741,39 +774,44 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       const int total = my_units * KT;     // one item per key tile
       // S(0), S(1); then per tile c, once P(c) is written: P V(c) from buffer
       // c & 1, then S(c + 2) into the same buffer.
-      auto qk = [&](int c) -> bool {
-        const int ui = c / KT, kt = c % KT, s = c % STAGES;
-        if (kt == 0 && !wait_or_abort(&bars->q_full[ui & 1], (ui >> 1) & 1, ab)) return false;
-        if (!wait_or_abort(&bars->kv_full[s], (c / STAGES) & 1, ab)) return false;
+      auto qk = [&](const TileIt& it) -> bool {
+        const int c = it.c;
+        if (it.kt == 0 && !wait_or_abort(&bars->q_full[it.ui & 1], (it.ui >> 1) & 1, ab)) return false;
+        if (!wait_or_abort(&bars->kv_full[it.s], it.sph, ab)) return false;
         tc::tc_fence_after();
-        const uint32_t qa = q0 + ((ui & 1) * R + r) * Q_BYTES;
-        const uint32_t ka = st0 + s * STAGE_BYTES + r * 2 * KV_BYTES;
+        const uint32_t qa = q0 + ((it.ui & 1) * R + r) * Q_BYTES;
+        const uint32_t ka = st0 + it.s * STAGE_BYTES + r * 2 * KV_BYTES;
         for (int ks = 0; ks < DH / 16; ++ks)
           tc::mma_bf16_ss(tr + (c & 1) * TM_S1, tc::smem_desc(qa + ks * 32, 16, 512, tc::SWZ_64B),
                           tc::smem_desc(ka + ks * 32, 16, 512, tc::SWZ_64B), id_qk, ks > 0);
         tc::mma_commit(&bars->s_ready[r][c & 1]);
-        if (kt == KT - 1) tc::mma_commit(&bars->q_empty[ui & 1]);
+        if (it.kt == KT - 1) tc::mma_commit(&bars->q_empty[it.ui & 1]);
         return true;
       };
-      auto pv = [&](int c) -> bool {
-        const int ui = c / KT, kt = c % KT, s = c % STAGES;
+      auto pv = [&](const TileIt& it) -> bool {
+        const int c = it.c;
         if (!wait_or_abort(&bars->p_full[r][c & 1], (c >> 1) & 1, ab)) return false;
-        if (kt == 0 && ui >= 1 && !wait_or_abort(&bars->o_free[r], (ui - 1) & 1, ab)) return false;
+        if (it.kt == 0 && it.ui >= 1 && !wait_or_abort(&bars->o_free[r], (it.ui - 1) & 1, ab))
+          return false;
         tc::tc_fence_after();
-        const uint32_t va = st0 + s * STAGE_BYTES + r * 2 * KV_BYTES + KV_BYTES;
+        const uint32_t va = st0 + it.s * STAGE_BYTES + r * 2 * KV_BYTES + KV_BYTES;
         for (int ks = 0; ks < BK / 16; ++ks)
           tc::mma_bf16_ts(tr + TM_O, tr + (c & 1) * TM_S1 + ks * 8,
                           tc::smem_desc(va + ks * 1024, 16, 512, tc::SWZ_64B), id_pv,
-                          (kt > 0 || ks > 0) ? 1u : 0u);
+                          (it.kt > 0 || ks > 0) ? 1u : 0u);
         tc::mma_commit(&bars->p_free[r][c & 1]);
-        tc::mma_commit(&bars->kv_empty[s]);
+        tc::mma_commit(&bars->kv_empty[it.s]);
         return true;
       };
       bool ok = true;
-      for (int c = 0; ok && c < 2 && c < total; ++c) ok = qk(c);
-      for (int c = 0; ok && c < total; ++c) {
-        ok = pv(c);
-        if (ok && c + 2 < total) ok = qk(c + 2);
+      TileIt itq{0, 0, 0, 0, 0}, itp{0, 0, 0, 0, 0};
+      for (; ok && itq.c < 2 && itq.c < total; advance(itq, KT)) ok = qk(itq);
+      for (; ok && itp.c < total; advance(itp, KT)) {
+        ok = pv(itp);
+        if (ok && itq.c < total) {
+          ok = qk(itq);
+          advance(itq, KT);
+        }
       }
       tc::mma_commit(&bars->drain);
       drain_wait(&bars->drain, 0);
@@ -787,8 +825,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
     // A unit's mask summary (its query row's or key row's "keeps some key"
     // flag, and the row's first mask word) is loaded one unit ahead.
-    auto unit_loads = [&](int u, unsigned& any, uint2& bits0) {
-      const Unit nu = decode_unit(u, p);
+    auto unit_loads = [&](const Unit& nu, unsigned& any, uint2& bits0) {
       const int nj = nu.j0 + jr, ni = nu.rg * R + r;
       if (p.mask_mode == TRI_ATTN_MASK_QUERY_KEY)
         any = nj < N ? __ldg(p.row_any + (long long)nu.b * N + nj) : 0u;
@@ -798,7 +835,8 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     };
     unsigned nx_any = 0u;
     uint2 nx_bits = make_uint2(0u, 0u);
-    if (my_units > 0) unit_loads(blockIdx.x, nx_any, nx_bits);
+    Unit nxu = decode_unit(blockIdx.x, p);          // the unit after the current one
+    if (my_units > 0) unit_loads(nxu, nx_any, nx_bits);
     // Unit epilogue: o = O / l once the unit's last P V has landed, staged in
     // shared memory and written by one TMA store per warp (queries past N are
     // clipped by the store; rows past N and warps whose 32 queries all lie
@@ -817,7 +855,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       tc::mbar_arrive(&bars->o_free[r]);
       const int fi = fu.rg * R + r, fj = fu.j0 + (warp & 3) * 32;
       if (fi < N && fj < N) {
-        const float inv = 1.0f / l;
+        const float inv = __frcp_rn(l);
         uint32_t po[16];
 #pragma unroll
         for (int e = 0; e < DH; e += 2)
@@ -842,11 +880,12 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     };
     bool ok = true;
     for (int ui = 0; ok && ui < my_units; ++ui) {
-      const Unit un = decode_unit(blockIdx.x + ui * gridDim.x, p);
+      const Unit un = nxu;
+      step_unit(nxu, p);
       const int i = un.rg * R + r;
       const bool uni = nx_any == 0u;
       const uint2 bits0 = nx_bits;
-      if (ui + 1 < my_units) unit_loads(blockIdx.x + (ui + 1) * gridDim.x, nx_any, nx_bits);
+      if (ui + 1 < my_units) unit_loads(nxu, nx_any, nx_bits);
       float m_used = -INFINITY, l_run = 0.f;
       const uint32_t* mrow = p.mbits + ((long long)un.b * N + (i < N ? i : 0)) * p.words;
       const bool use_bits = p.mask_mode == TRI_ATTN_MASK_ROW_KEY && !uni;
@@ -1415,6 +1454,13 @@ cudaError_t tri_tc_forward(tri_attn_s* t, cudaStream_t s, const void* x, const i
   p2.polls = t->wait_limit;
   p2.scale_log2 = kLog2e / sqrtf((float)t->d);
   const unsigned g2 = (unsigned)(p2.units < st->num_sms ? p2.units : st->num_sms);
+  {
+    const int g1 = (int)g2 / p2.jtiles, g0 = g1 / h;
+    p2.step.jt = (int)g2 % p2.jtiles;
+    p2.step.t = g1 % h;
+    p2.step.rg = g0 % p2.row_groups;
+    p2.step.b = g0 / p2.row_groups;
+  }
   k2::row_attn_tc<<<g2, k2::kThreads, k2::SMEM, s>>>(st->map_q, st->map_k, st->map_v, st->map_b,
                                                       st->map_os, p2);
   tri_mark(t, s, mark++, "row_attn_tc");
