@@ -75,7 +75,7 @@ def _rank_main(rank, world, port, mode, ending, out):
 
 def _run(mode, ending):
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_rank_main, args=(world, _free_port(), mode, ending, out), nprocs=world, join=True)
         return out["result"]
