@@ -879,6 +879,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       return true;
     };
     bool ok = true;
+    TileIt its{0, 0, 0, 0, 0};                      // this warp's tile stream
     for (int ui = 0; ok && ui < my_units; ++ui) {
       const Unit un = nxu;
       step_unit(nxu, p);
@@ -890,8 +891,8 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       const uint32_t* mrow = p.mbits + ((long long)un.b * N + (i < N ? i : 0)) * p.words;
       const bool use_bits = p.mask_mode == TRI_ATTN_MASK_ROW_KEY && !uni;
       uint2 nbits = use_bits ? bits0 : make_uint2(0xffffffffu, 0xffffffffu);
-      for (int kt = 0; ok && kt < KT; ++kt) {
-        const int c = ui * KT + kt, s = c % STAGES;
+      for (int kt = 0; ok && kt < KT; ++kt, advance(its, KT)) {
+        const int c = its.c, s = its.s;
         const uint2 mb = nbits;
         if (use_bits && kt + 1 < KT) nbits = __ldg((const uint2*)(mrow + 2 * (kt + 1)));
         const int left = N - kt * BK;
@@ -903,9 +904,14 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         // sits at chunk q ^ (jr & 7)); the row base is 128-byte aligned.
         const uint32_t brow = tc::smem_addr(smem + OFF_STAGE + s * STAGE_BYTES + STAGE_KV) +
                               jr * 128u + ((jr & 7u) << 4);
+        // The stage (its bias tile) and S(c): both barriers are polled back to
+        // back so that their latencies overlap, then one vote settles them.
+        bool okk = tc::mbar_try_wait(&bars->kv_full[s], its.sph);
+        bool oks = tc::mbar_try_wait(&bars->s_ready[r][c & 1], (c >> 1) & 1);
+        if (!okk) okk = wait_or_abort_slow(&bars->kv_full[s], its.sph, ab);
+        if (okk && !oks) oks = wait_or_abort_slow(&bars->s_ready[r][c & 1], (c >> 1) & 1, ab);
+        if (!__all_sync(0xffffffffu, okk && oks)) { ok = false; break; }
         const bool any_live = __any_sync(0xffffffffu, live);
-        if (any_live && !warp_wait_or_abort(&bars->kv_full[s], (c / STAGES) & 1, ab)) { ok = false; break; }
-        if (!warp_wait_or_abort(&bars->s_ready[r][c & 1], (c >> 1) & 1, ab)) { ok = false; break; }
         tc::tc_fence_after();
         const uint32_t tsb = tb + (c & 1) * TM_S1;     // S(c), then P(c) over it
         float2 x2[BK / 2];
