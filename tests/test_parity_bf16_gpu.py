@@ -98,3 +98,33 @@ def test_bf16_forward_host_matches_device():
         assert torch.equal(oh, od.cpu())
     finally:
         mod.close()
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_bf16_logits_rising_past_the_reference_max(mode):
+    """The kernel's reference max comes from a query row's first live tile and
+    moves only when a later tile's sum of P reaches 2^32. Here the pair bias of
+    keys 64..127 sits 56..80 log2 units and that of keys >= 128 at ~115, against
+    at most ~42 in the first tile, so query rows take the rescaling path, most
+    of them twice (mode 2: the ending node, where the same construction on the
+    grid's rows feeds the bias of the column lines). x and Wb are bf16-exact:
+    channel 0 carries a spike of 8 (keys 64..127) or 64 (keys >= 128), and Wb
+    reads channel 0 alone (8.0 per head)."""
+    w = W.custom(1, 200, 128, 4, "bf16", "bernoulli", seed=61)
+    inp = W.make_inputs(w)
+    x = inp["x"]
+    if mode & tb.TRI_ATTN_ENDING_NODE:
+        x[0, 64:128, :, 0] = 8.0
+        x[0, 128:, :, 0] = 64.0
+    else:
+        x[0, :, 64:128, 0] = 8.0
+        x[0, :, 128:, 0] = 64.0
+    Wb = np.zeros_like(inp["params"]["Wb"])
+    Wb[:, 0] = 8.0
+    inp["params"]["Wb"] = Wb
+    got = H.run_forward(w, inp, mode)[0]
+    if mode & tb.TRI_ATTN_ENDING_NODE:
+        ref = O.forward_ending(inp["x"], inp["pair_mask"], inp["params"], w.h, mode & 1)
+    else:
+        ref = O.forward(inp["x"], inp["pair_mask"], inp["params"], w.h, mode)
+    H.assert_parity(w, got, ref)
