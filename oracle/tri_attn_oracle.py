@@ -172,14 +172,19 @@ def forward_rows(x, pair_mask, params, h, rows, mask_mode=MASK_ROW_KEY):
 
     The bias plane needs every cell; q, k, v and g are needed only for the
     cells of the requested rows."""
-    x = _f64(x)
     P = {k: _f64(v) for k, v in params.items()}
     B, N, _, D = x.shape
-    x_hat_all = layer_norm(x, P["gamma"], P["beta"])
-    bias = bias_plane(linear(x_hat_all, P["Wb"]))
+    h_out = P["Wb"].shape[0]
+    # The per-cell bias, one grid row at a time (the same per-cell LayerNorm and
+    # projection; only the memory held at once is bounded).
+    bias_cells = np.empty((B, N, N, h_out))
+    for b in range(B):
+        for r in range(N):
+            bias_cells[b, r] = linear(layer_norm(_f64(x[b, r]), P["gamma"], P["beta"]), P["Wb"])
+    bias = bias_plane(bias_cells)
     out = np.empty((len(rows), N, D))
     for n, (b, i) in enumerate(rows):
-        q_i, k_i, v_i, g_i, _ = project(x_hat_all[b, i], P)
+        q_i, k_i, v_i, g_i, _ = project(layer_norm(_f64(x[b, i]), P["gamma"], P["beta"]), P)
         keep = keep_matrix(pair_mask, b, i, mask_mode)
         o_i = row_attention(q_i, k_i, v_i, bias[b], keep, h)
         out[n] = output_projection(g_i, o_i, P)

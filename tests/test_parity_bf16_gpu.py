@@ -128,3 +128,16 @@ def test_bf16_logits_rising_past_the_reference_max(mode):
     else:
         ref = O.forward(inp["x"], inp["pair_mask"], inp["params"], w.h, mode)
     H.assert_parity(w, got, ref)
+
+
+def test_bf16_large_grid_sampled_rows():
+    """N = 2048 with 2000 residues kept: 32 key tiles per unit and 43 712 work
+    units over the 152-CTA grid; whole rows at the edges, tile and row-group
+    boundaries and the padding are compared with the oracle."""
+    w = W.custom(1, 2048, 128, 4, "bf16", "padded", n_valid=2000, seed=81)
+    inp = W.make_inputs(w)
+    got = H.run_forward(w, inp, 0)[0]
+    rows = sorted({(0, i) for i in (0, 1, 63, 64, 127, 128, 1023, 1024, 1999, 2000, 2046, 2047)})
+    ref = O.forward_rows(inp["x"], inp["pair_mask"], inp["params"], w.h, rows, 0)
+    H.assert_parity(w, np.stack([got[b, i] for b, i in rows]), ref)
+    assert np.all(np.isfinite(got))
