@@ -1065,7 +1065,11 @@ constexpr uint32_t T_BYTES = BM * KD * 2;           // 32 KB tile (two K-halves)
 constexpr uint32_t OFF_W = 0;                       // Wo, 32 KB
 constexpr uint32_t OFF_G = OFF_W + T_BYTES;         // g tiles [2]; become the A operand
 constexpr uint32_t OFF_O = OFF_G + 2 * T_BYTES;     // o tiles [2]
-constexpr uint32_t OFF_BO = OFF_O + 2 * T_BYTES;    // bo fp32 [128]
+// Output staging: per epilogue warp two 32-row x 32-channel bf16 tiles (64-byte
+// rows, 64-byte swizzle), each written by one TMA store.
+constexpr uint32_t STG_BYTES = 32 * 64;
+constexpr uint32_t OFF_STG = OFF_O + 2 * T_BYTES;   // [4 warps][2]
+constexpr uint32_t OFF_BO = OFF_STG + 4 * 2 * STG_BYTES;   // bo fp32 [128]
 constexpr uint32_t OFF_BAR = OFF_BO + KD * 4;
 constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
 
@@ -1079,14 +1083,14 @@ struct Params {
   long long cells;
   int ntiles;
   const float* bo;
-  __nv_bfloat16* out;
   unsigned int* dev_err;
   long long polls;
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
 gate_out_tc(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUtensorMap map_o,
-            const __grid_constant__ CUtensorMap map_wo, const Params p) {
+            const __grid_constant__ CUtensorMap map_wo, const __grid_constant__ CUtensorMap map_out,
+            const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   Bars* bars = (Bars*)(smem + OFF_BAR);
@@ -1190,13 +1194,17 @@ gate_out_tc(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ C
       tc::mbar_arrive(&bars->a_ready[b]);
     }
   } else if (warp < 8) {
-    // ---------------- epilogue: cell row = TMEM lane of this warp's quarter
+    // ---------------- epilogue: cell row = TMEM lane of this warp's quarter;
+    // each 32-row x 32-channel chunk leaves through a swizzled staging tile and
+    // one TMA store (rows past the last cell are clipped by the tensor bounds).
     const int q4 = warp & 3;
+    uint8_t* const stg0 = smem + OFF_STG + q4 * 2 * STG_BYTES;
+    int nst = 0;                                  // TMA stores issued by this warp
     for (int it = 0; it < my_tiles; ++it) {
       const int b = it & 1;
       if (!warp_wait_or_abort(&bars->acc_full[b], (it >> 1) & 1, ab)) break;
       tc::tc_fence_after();
-      const long long cell = (long long)(blockIdx.x + it * gridDim.x) * BM + q4 * 32 + lane;
+      const int row0 = (blockIdx.x + it * gridDim.x) * BM + q4 * 32;
       // Chunk ch + 1 is loaded from TMEM while chunk ch is converted and stored.
       uint32_t accb[2][32];
       tc::tmem_ld32(tc::tmem_addr(tmem, q4 * 32, b * 128), accb[0]);
@@ -1210,15 +1218,27 @@ gate_out_tc(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ C
         for (int e = 0; e < 16; ++e)
           pk[e] = tc::pack_bf16x2(__uint_as_float(acc[2 * e]) + s_bo[ch * 32 + 2 * e],
                                   __uint_as_float(acc[2 * e + 1]) + s_bo[ch * 32 + 2 * e + 1]);
-        if (cell < p.cells) {
-          uint4* dst = (uint4*)(p.out + cell * KD + ch * 32);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        uint8_t* stg = stg0 + (nst & 1) * STG_BYTES;
+        if (nst >= 2) {                           // the store two back has read this tile
+          if (lane == 0) tc::tma_store_wait_read<1>();
+          __syncwarp();
         }
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          *(uint4*)(stg + tc::swz_offset(lane, e, 64)) =
+              make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tc::tma_store_2d(&map_out, stg, ch * 32, row0);
+          tc::tma_store_commit();
+        }
+        ++nst;
       }
       tc::tc_fence_before();
       tc::mbar_arrive(&bars->acc_empty[b]);
     }
+    if (lane == 0) tc::tma_store_wait_all<0>();
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -1471,10 +1491,20 @@ cudaError_t tri_tc_forward(tri_attn_s* t, cudaStream_t s, const void* x, const i
                                                       st->map_os, p2);
   tri_mark(t, s, mark++, "row_attn_tc");
 
+  CUtensorMap map_out;                      // (cells, 128) bf16, 32 x 32 store boxes
+  {
+    cuuint64_t dims[2] = {128, (cuuint64_t)cells};
+    cuuint64_t strides[1] = {256};
+    cuuint32_t box[2] = {32, 32};
+    if (!make_map(&map_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, dims, strides, box,
+                  CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
+  }
   k3::Params p3;
-  p3.cells = cells; p3.ntiles = ntiles; p3.bo = t->bo; p3.out = (__nv_bfloat16*)out;
+  p3.cells = cells; p3.ntiles = ntiles; p3.bo = t->bo;
   p3.dev_err = t->dev_err; p3.polls = t->wait_limit;
-  k3::gate_out_tc<<<grid_rows, k3::kThreads, k3::SMEM, s>>>(st->map_g, st->map_o, st->map_wo, p3);
+  k3::gate_out_tc<<<grid_rows, k3::kThreads, k3::SMEM, s>>>(st->map_g, st->map_o, st->map_wo,
+                                                            map_out, p3);
   tri_mark(t, s, mark++, "gate_out_tc");
   return cudaGetLastError();
 }
