@@ -401,6 +401,16 @@ def run_native(args, rank, world):
         roof = {"bound": "hbm", "achieved": kw["bytes"] / t_s / 1e9, "peak": hbm, "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["kernel"] = top
+    if kernel_key(top) == "row_attn" and w.dtype == "bf16":
+        # The attention kernel's three floors: tensor FLOPs, HBM bytes and the
+        # special-function unit's exp2 rate (one exp2 per line, head, query and
+        # key; 32 per clock per SM as measured on this GPU, at the maximum clock).
+        sm_mhz = clk.summary().get("sm_max_mhz") or 2070.0
+        sfu_rate = torch.cuda.get_device_properties(dev).multi_processor_count * 32 * sm_mhz * 1e6
+        t_sfu = w.B * w.h * w.N ** 3 / sfu_rate
+        roof["floors_ms"] = {"tensor": round(t_flops * 1e3, 4), "hbm": round(t_bytes * 1e3, 4),
+                             "sfu": round(t_sfu * 1e3, 4)}
+        roof["sfu_frac"] = round(t_sfu / t_s, 4)
     roof["peak_source"] = (peak_src + " (burst)" if fbound == "tensor" or t_bytes > t_flops
                            else "derived: SMs x 128 FFMA lanes x 2 x max SM clock")
     roof["traffic"] = measured_traffic(top, w.cells) if w.dtype == "bf16" else None
