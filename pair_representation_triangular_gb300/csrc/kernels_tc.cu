@@ -888,6 +888,12 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       const uint2 bits0 = nx_bits;
       if (ui + 1 < my_units) unit_loads(nxu, nx_any, nx_bits);
       float m_used = -INFINITY, l_run = 0.f;
+      // Whether any lane of the warp has a key-keeping query row in this unit
+      // (warp-uniform, one vote per unit), and whether those lanes have taken
+      // their reference max yet: their first live tile is the same tile, since
+      // a tile's keep bits are shared by the whole warp.
+      const bool unit_live = __any_sync(0xffffffffu, !uni);
+      bool have_mu = false;
       const uint32_t* mrow = p.mbits + ((long long)un.b * N + (i < N ? i : 0)) * p.words;
       const bool use_bits = p.mask_mode == TRI_ATTN_MASK_ROW_KEY && !uni;
       uint2 nbits = use_bits ? bits0 : make_uint2(0xffffffffu, 0xffffffffu);
@@ -899,7 +905,8 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         const uint32_t rl0 = real_bits(left, 0), rl1 = real_bits(left, 1);
         const uint32_t bw0 = rl0 & mb.x, bw1 = rl1 & mb.y;
         const bool all_kept = (bw0 & bw1) == 0xffffffffu;
-        const bool live = !uni && (bw0 | bw1) != 0u;
+        const bool tile_keys = (bw0 | bw1) != 0u;      // warp-uniform
+        const bool live = !uni && tile_keys;
         // Bias row jr of the stage (128-byte swizzle: 16-byte chunk q of the row
         // sits at chunk q ^ (jr & 7)); the row base is 128-byte aligned.
         const uint32_t brow = tc::smem_addr(smem + OFF_STAGE + s * STAGE_BYTES + STAGE_KV) +
@@ -911,7 +918,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         if (!okk) okk = wait_or_abort_slow(&bars->kv_full[s], its.sph, ab);
         if (okk && !oks) oks = wait_or_abort_slow(&bars->s_ready[r][c & 1], (c >> 1) & 1, ab);
         if (!__all_sync(0xffffffffu, okk && oks)) { ok = false; break; }
-        const bool any_live = __any_sync(0xffffffffu, live);
+        const bool any_live = unit_live && tile_keys;
         tc::tc_fence_after();
         const uint32_t tsb = tb + (c & 1) * TM_S1;     // S(c), then P(c) over it
         float2 x2[BK / 2];
@@ -935,12 +942,10 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         // A lane's reference max mu is set on its first live tile and moves only
         // when a tile's sum of P reaches 2^32 (its logits rose by more than
         // about 26), so P stays finite and O, l never overflow in fp32.
-        if (any_live) {
-          const bool need_max = live && m_used == -INFINITY;
-          if (__builtin_expect(__any_sync(0xffffffffu, need_max), 0)) {
-            const float mt = tile_max(x2, brow, sc2);
-            if (need_max) m_used = mt;
-          }
+        if (__builtin_expect(any_live && !have_mu, 0)) {
+          const float mt = tile_max(x2, brow, sc2);
+          if (live) m_used = mt;
+          have_mu = true;
         }
         const float mu = m_used == -INFINITY ? 0.f : m_used;
         const uint32_t w0 = uni ? rl0 : 0u, w1 = uni ? rl1 : 0u;
