@@ -489,10 +489,11 @@ constexpr uint32_t STAGE_KV = R * 2 * KV_BYTES;      // [R] K then V
 constexpr uint32_t STAGE_BYTES = STAGE_KV + BIAS_BYTES;
 constexpr uint32_t OFF_STAGE = OFF_Q + 2 * R * Q_BYTES;
 // o of a unit leaves through one TMA store per softmax warp: 32 queries x one
-// head (64 bytes), staged with the 64-byte swizzle.
+// head (64 bytes), staged with the 64-byte swizzle, two staging tiles per warp
+// so that a unit waits only for the store of two units before.
 constexpr uint32_t OST_BYTES = 32 * DH * 2;
 constexpr uint32_t OFF_OST = OFF_STAGE + STAGES * STAGE_BYTES;
-constexpr uint32_t OFF_BAR = OFF_OST + 3 * 4 * OST_BYTES;
+constexpr uint32_t OFF_BAR = OFF_OST + 2 * 3 * 4 * OST_BYTES;
 constexpr uint32_t SMEM = OFF_BAR + 512 + 1024;
 
 struct Bars {
@@ -842,8 +843,8 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     // clipped by the store; rows past N and warps whose 32 queries all lie
     // past N skip it). One 16-byte shared store per lane and chunk replaces
     // 32 scattered 16-byte global stores per warp instruction.
-    uint8_t* const ostg = smem + OFF_OST + (warp - 4) * OST_BYTES;
-    bool ost_pending = false;
+    uint8_t* const ostg0 = smem + OFF_OST + (warp - 4) * 2 * OST_BYTES;
+    int n_ost = 0;
     auto finish_unit = [&](const Unit& fu, int clast, float l) -> bool {
       if (!warp_wait_or_abort(&bars->p_free[r][clast & 1], (clast >> 1) & 1, ab)) return false;
       tc::tc_fence_after();
@@ -855,13 +856,14 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       tc::mbar_arrive(&bars->o_free[r]);
       const int fi = fu.rg * R + r, fj = fu.j0 + (warp & 3) * 32;
       if (fi < N && fj < N) {
-        const float inv = __frcp_rn(l);
+        const float inv = __fdividef(1.0f, l);   // l lies in [1, 2^40): the fast form is exact enough
         uint32_t po[16];
 #pragma unroll
         for (int e = 0; e < DH; e += 2)
           po[e / 2] = tc::pack_bf16x2(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
-        if (ost_pending) {                 // the previous store has read the staging tile
-          if (lane == 0) tc::tma_store_wait_read<0>();
+        uint8_t* const ostg = ostg0 + (n_ost & 1) * OST_BYTES;
+        if (n_ost >= 2) {                  // the store two back has read this staging tile
+          if (lane == 0) tc::tma_store_wait_read<1>();
           __syncwarp();
         }
 #pragma unroll
@@ -874,7 +876,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
           tc::tma_store_4d(&map_o, ostg, fu.t * DH, fj, fi, fu.b);
           tc::tma_store_commit();
         }
-        ost_pending = true;
+        ++n_ost;
       }
       return true;
     };
