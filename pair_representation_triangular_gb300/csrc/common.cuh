@@ -89,5 +89,10 @@ cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const voi
 void tri_tc_release(tri_attn_s* t);
 cudaError_t tri_tc_forward(tri_attn_s* t, cudaStream_t s, const void* x,
                            const int32_t* mask, void* out);
+// Host buffers xh, maskh, outh through the device staging buffers dx, dmask,
+// dout, with the copies overlapped with the first and last kernels; queued on s.
+cudaError_t tri_tc_forward_host(tri_attn_s* t, cudaStream_t s, const void* xh,
+                                const int32_t* maskh, void* outh, void* dx, int32_t* dmask,
+                                void* dout);
 size_t tri_tc_extra_bytes(int B, int N, int D, int h);
 int tri_tc_bias_row_stride(const tri_attn_s* t);

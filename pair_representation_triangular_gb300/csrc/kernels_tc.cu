@@ -31,6 +31,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -172,7 +174,8 @@ struct Consts {
 
 struct Params {
   long long cells;
-  int N, Nb, h, mask_mode, ntiles;
+  int N, Nb, h, mask_mode, ntiles;   // this launch: tiles tile0 .. tile0 + ntiles - 1
+  int tile0;
   int ending;                  // bias of cell (r, c) goes to plane row c, column r
   const int32_t* mask;
   __nv_bfloat16 *q, *k, *v, *g;
@@ -242,7 +245,7 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
       for (int it = 0; it < my_tiles; ++it) {
         const int b = it & 1;
         if (it >= 2 && !wait_or_abort(&bars->x_empty[b], ((it >> 1) - 1) & 1, ab)) break;
-        const int tile = blockIdx.x + it * gridDim.x;
+        const int tile = p.tile0 + blockIdx.x + it * gridDim.x;
         uint8_t* xs = smem + OFF_X + b * X_BYTES;
         tc::mbar_arrive_expect_tx(&bars->x_full[b], X_BYTES);
         tc::tma_load_2d(xs, &map_x, &bars->x_full[b], 0, tile * BM);
@@ -287,7 +290,7 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
     for (int it = 0; ok && it < my_tiles; ++it) {
       const int b = it & 1;
       if (!warp_wait_or_abort(&bars->x_full[b], (it >> 1) & 1, ab)) { ok = false; break; }
-      const int tile = blockIdx.x + it * gridDim.x;
+      const int tile = p.tile0 + blockIdx.x + it * gridDim.x;
       const long long cell = (long long)tile * BM + r;
       uint8_t* xs = smem + OFF_X + b * X_BYTES;
       auto chunk = [&](int c) -> uint4 {
@@ -377,7 +380,7 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
     uint8_t* stg0 = smem + OFF_STG + ew * 2 * STG_BYTES;
     int nst = 0;                                  // TMA stores issued by this warp
     auto epilogue = [&](int it) -> bool {
-      const int tile = blockIdx.x + it * gridDim.x;
+      const int tile = p.tile0 + blockIdx.x + it * gridDim.x;
       const int row0 = tile * BM + q4 * 32;
 #pragma unroll 1
       for (int nh = 0; nh < 2; ++nh) {
@@ -513,7 +516,8 @@ struct UnitStep {
 };
 
 struct Params {
-  int B, N, h, mask_mode, row_groups, jtiles, words, units;
+  int B, N, h, mask_mode, row_groups, jtiles, words;
+  int unit0, units;               // this launch: units unit0 .. unit0 + units - 1
   UnitStep step;                  // gridDim.x in unit digits
   const uint32_t* mbits;          // (B*N rows, words): bit k = pair_mask[b, r, k] != 0, k < N
   const unsigned char* row_any;   // (B*N rows): the mask row keeps some key
@@ -735,7 +739,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       tc::tma_prefetch_desc(&map_v);
       tc::tma_prefetch_desc(&map_b);
       bool ok = true;
-      Unit un = decode_unit(blockIdx.x, p);
+      Unit un = decode_unit(p.unit0 + blockIdx.x, p);
       for (int ui = 0; ok && ui < my_units; ++ui, step_unit(un, p)) {
         const int a0 = un.rg * R;
         const int qb = ui & 1;
@@ -836,7 +840,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     };
     unsigned nx_any = 0u;
     uint2 nx_bits = make_uint2(0u, 0u);
-    Unit nxu = decode_unit(blockIdx.x, p);          // the unit after the current one
+    Unit nxu = decode_unit(p.unit0 + blockIdx.x, p);   // the unit after the current one
     if (my_units > 0) unit_loads(nxu, nx_any, nx_bits);
     // Unit epilogue: o = O / l once the unit's last P V has landed, staged in
     // shared memory and written by one TMA store per warp (queries past N are
@@ -1088,7 +1092,7 @@ struct Bars {
 
 struct Params {
   long long cells;
-  int ntiles;
+  int ntiles, tile0;              // this launch: tiles tile0 .. tile0 + ntiles - 1
   const float* bo;
   unsigned int* dev_err;
   long long polls;
@@ -1141,7 +1145,7 @@ gate_out_tc(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ C
       for (int it = 0; it < my_tiles; ++it) {
         const int b = it & 1;
         if (it >= 2 && !wait_or_abort(&bars->in_empty[b], ((it >> 1) - 1) & 1, ab)) break;
-        const int row = (blockIdx.x + it * gridDim.x) * BM;
+        const int row = (p.tile0 + blockIdx.x + it * gridDim.x) * BM;
         uint8_t* gs = smem + OFF_G + b * T_BYTES;
         uint8_t* os = smem + OFF_O + b * T_BYTES;
         tc::mbar_arrive_expect_tx(&bars->in_full[b], 2 * T_BYTES);
@@ -1211,7 +1215,7 @@ gate_out_tc(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ C
       const int b = it & 1;
       if (!warp_wait_or_abort(&bars->acc_full[b], (it >> 1) & 1, ab)) break;
       tc::tc_fence_after();
-      const int row0 = (blockIdx.x + it * gridDim.x) * BM + q4 * 32;
+      const int row0 = (p.tile0 + blockIdx.x + it * gridDim.x) * BM + q4 * 32;
       // Chunk ch + 1 is loaded from TMEM while chunk ch is converted and stored.
       uint32_t accb[2][32];
       tc::tmem_ld32(tc::tmem_addr(tmem, q4 * 32, b * 128), accb[0]);
@@ -1314,6 +1318,11 @@ bool map_lines(CUtensorMap* m, const void* base, int B, int N, int box_x, bool e
                   CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
+// The host-buffer forward moves x and out in this many chunks; its events are
+// start, mask copied, one per x chunk copied, one per out chunk formed, done.
+constexpr int kHostChunks = 4;
+constexpr int kHostEvents = 3 + 2 * kHostChunks;
+
 struct TcState {
   k1::Consts consts;                        // LayerNorm / gate-bias / pair-bias weights (fp32)
   CUtensorMap map_w, map_q, map_k, map_v, map_b, map_g, map_o, map_wo;
@@ -1324,6 +1333,9 @@ struct TcState {
   int words;
   int num_sms;
   int Nb;
+  // Host-buffer pipeline (created at its first use): copy streams and events.
+  cudaStream_t copy_in, copy_out;
+  cudaEvent_t ev[kHostEvents];
 };
 
 int round_up(int a, int b) { return (a + b - 1) / b * b; }
@@ -1436,51 +1448,68 @@ void tri_tc_release(tri_attn_s* t) {
   if (!st) return;
   if (st->row_any) cudaFree(st->row_any);
   if (st->mbits) cudaFree(st->mbits);
+  if (st->copy_in) cudaStreamDestroy(st->copy_in);
+  if (st->copy_out) cudaStreamDestroy(st->copy_out);
+  for (int i = 0; i < kHostEvents; ++i)
+    if (st->ev[i]) cudaEventDestroy(st->ev[i]);
   free(st);
   t->tc = nullptr;
 }
 
-cudaError_t tri_tc_forward(tri_attn_s* t, cudaStream_t s, const void* x, const int32_t* mask,
-                           void* out) {
-  TcState* st = (TcState*)t->tc;
-  const int B = t->B, N = t->N, h = t->h;
-  const long long cells = t->cells;
-  const int ntiles = (int)((cells + 127) / 128);
-  const int grid_rows = ntiles < st->num_sms ? ntiles : st->num_sms;
-  CUtensorMap map_x;
-  if (!map_rows_bf16(&map_x, x, cells, 128)) return cudaErrorInvalidValue;
+namespace {
 
+int num_tiles(const tri_attn_s* t) { return (int)((t->cells + 127) / 128); }
+
+// K1 over tiles tile0 .. tile0 + n - 1 of the grid's cells.
+cudaError_t launch_k1(tri_attn_s* t, cudaStream_t s, const CUtensorMap& map_x,
+                      const int32_t* mask, int tile0, int n) {
+  TcState* st = (TcState*)t->tc;
   k1::Params p1;
-  p1.cells = cells; p1.N = N; p1.Nb = st->Nb; p1.h = h; p1.mask_mode = t->mask_mode;
+  p1.cells = t->cells; p1.N = t->N; p1.Nb = st->Nb; p1.h = t->h; p1.mask_mode = t->mask_mode;
   p1.ending = t->ending ? 1 : 0;
-  p1.ntiles = ntiles;
+  p1.ntiles = n; p1.tile0 = tile0;
   p1.mask = mask;
   p1.q = (__nv_bfloat16*)t->q; p1.k = (__nv_bfloat16*)t->k; p1.v = (__nv_bfloat16*)t->v;
   p1.g = (__nv_bfloat16*)t->g; p1.bias = (__half*)t->bias; p1.dev_err = t->dev_err;
   p1.polls = t->wait_limit;
-  int mark = 0;
-  tri_mark(t, s, mark++, nullptr);
-  k1::ln_proj_tc<<<grid_rows, k1::kThreads, k1::SMEM, s>>>(map_x, st->map_w, st->st_q, st->st_k,
-                                                           st->st_v, st->st_g, p1, st->consts);
-  tri_mark(t, s, mark++, "ln_proj_tc");
+  const int grid = n < st->num_sms ? n : st->num_sms;
+  k1::ln_proj_tc<<<grid, k1::kThreads, k1::SMEM, s>>>(map_x, st->map_w, st->st_q, st->st_k,
+                                                      st->st_v, st->st_g, p1, st->consts);
+  return cudaGetLastError();
+}
 
-  {
-    const long long rows = (long long)B * N;
-    if (!t->ending) {
-      k2::mask_summary<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(mask, N, rows, st->words,
-                                                                st->mbits, st->row_any);
-      tri_mark(t, s, mark++, "mask_summary");
-    } else {
-      const unsigned blocks = (unsigned)(B * (long long)((N + 31) / 32));
-      k2::mask_summary_cols<<<blocks, 256, 0, s>>>(mask, N, st->words, st->mbits, st->row_any);
-      tri_mark(t, s, mark++, "mask_summary_cols");
-    }
+// The mask summary of every line.
+cudaError_t launch_mask(tri_attn_s* t, cudaStream_t s, const int32_t* mask, int& mark) {
+  TcState* st = (TcState*)t->tc;
+  const int B = t->B, N = t->N;
+  const long long rows = (long long)B * N;
+  if (!t->ending) {
+    k2::mask_summary<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(mask, N, rows, st->words,
+                                                              st->mbits, st->row_any);
+    tri_mark(t, s, mark++, "mask_summary");
+  } else {
+    const unsigned blocks = (unsigned)(B * (long long)((N + 31) / 32));
+    k2::mask_summary_cols<<<blocks, 256, 0, s>>>(mask, N, st->words, st->mbits, st->row_any);
+    tri_mark(t, s, mark++, "mask_summary_cols");
   }
+  return cudaGetLastError();
+}
+
+// K2's work units are (b, row group, head, query tile), query tile fastest.
+int k2_row_groups(const tri_attn_s* t) { return (t->N + k2::R - 1) / k2::R; }
+int k2_units_per_group(const tri_attn_s* t) { return t->h * ((t->N + k2::BQ - 1) / k2::BQ); }
+
+// K2 over the units of the (b, row group) pairs g0 .. g0 + ng - 1 (row groups
+// counted across the batch).
+cudaError_t launch_k2(tri_attn_s* t, cudaStream_t s, int g0, int ng) {
+  TcState* st = (TcState*)t->tc;
+  const int N = t->N, h = t->h;
   k2::Params p2;
-  p2.B = B; p2.N = N; p2.h = h; p2.mask_mode = t->mask_mode;
-  p2.row_groups = (N + k2::R - 1) / k2::R;
+  p2.B = t->B; p2.N = N; p2.h = h; p2.mask_mode = t->mask_mode;
+  p2.row_groups = k2_row_groups(t);
   p2.jtiles = (N + k2::BQ - 1) / k2::BQ;
-  p2.units = B * p2.row_groups * h * p2.jtiles;
+  p2.unit0 = g0 * k2_units_per_group(t);
+  p2.units = ng * k2_units_per_group(t);
   p2.words = st->words;
   p2.mbits = st->mbits; p2.row_any = st->row_any;
   p2.dev_err = t->dev_err;
@@ -1488,30 +1517,157 @@ cudaError_t tri_tc_forward(tri_attn_s* t, cudaStream_t s, const void* x, const i
   p2.scale_log2 = kLog2e / sqrtf((float)t->d);
   const unsigned g2 = (unsigned)(p2.units < st->num_sms ? p2.units : st->num_sms);
   {
-    const int g1 = (int)g2 / p2.jtiles, g0 = g1 / h;
+    const int g1 = (int)g2 / p2.jtiles, gq = g1 / h;
     p2.step.jt = (int)g2 % p2.jtiles;
     p2.step.t = g1 % h;
-    p2.step.rg = g0 % p2.row_groups;
-    p2.step.b = g0 / p2.row_groups;
+    p2.step.rg = gq % p2.row_groups;
+    p2.step.b = gq / p2.row_groups;
   }
   k2::row_attn_tc<<<g2, k2::kThreads, k2::SMEM, s>>>(st->map_q, st->map_k, st->map_v, st->map_b,
                                                       st->map_os, p2);
-  tri_mark(t, s, mark++, "row_attn_tc");
-
-  CUtensorMap map_out;                      // (cells, 128) bf16, 32 x 32 store boxes
-  {
-    cuuint64_t dims[2] = {128, (cuuint64_t)cells};
-    cuuint64_t strides[1] = {256};
-    cuuint32_t box[2] = {32, 32};
-    if (!make_map(&map_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, dims, strides, box,
-                  CU_TENSOR_MAP_SWIZZLE_64B))
-      return cudaErrorInvalidValue;
-  }
-  k3::Params p3;
-  p3.cells = cells; p3.ntiles = ntiles; p3.bo = t->bo;
-  p3.dev_err = t->dev_err; p3.polls = t->wait_limit;
-  k3::gate_out_tc<<<grid_rows, k3::kThreads, k3::SMEM, s>>>(st->map_g, st->map_o, st->map_wo,
-                                                            map_out, p3);
-  tri_mark(t, s, mark++, "gate_out_tc");
   return cudaGetLastError();
+}
+
+// Store map of a (cells, 128) bf16 output: 32 x 32 boxes.
+bool map_out_rows(CUtensorMap* m, void* out, long long cells) {
+  cuuint64_t dims[2] = {128, (cuuint64_t)cells};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {32, 32};
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, dims, strides, box,
+                  CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+// K3 over tiles tile0 .. tile0 + n - 1.
+cudaError_t launch_k3(tri_attn_s* t, cudaStream_t s, const CUtensorMap& map_out, int tile0,
+                      int n) {
+  TcState* st = (TcState*)t->tc;
+  k3::Params p3;
+  p3.cells = t->cells; p3.ntiles = n; p3.tile0 = tile0; p3.bo = t->bo;
+  p3.dev_err = t->dev_err; p3.polls = t->wait_limit;
+  const int grid = n < st->num_sms ? n : st->num_sms;
+  k3::gate_out_tc<<<grid, k3::kThreads, k3::SMEM, s>>>(st->map_g, st->map_o, st->map_wo,
+                                                       map_out, p3);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t tri_tc_forward(tri_attn_s* t, cudaStream_t s, const void* x, const int32_t* mask,
+                           void* out) {
+  const int ntiles = num_tiles(t);
+  CUtensorMap map_x, map_out;
+  if (!map_rows_bf16(&map_x, x, t->cells, 128) || !map_out_rows(&map_out, out, t->cells))
+    return cudaErrorInvalidValue;
+  int mark = 0;
+  tri_mark(t, s, mark++, nullptr);
+  cudaError_t e = launch_k1(t, s, map_x, mask, 0, ntiles);
+  tri_mark(t, s, mark++, "ln_proj_tc");
+  if (e == cudaSuccess) e = launch_mask(t, s, mask, mark);
+  if (e == cudaSuccess) e = launch_k2(t, s, 0, t->B * k2_row_groups(t));
+  tri_mark(t, s, mark++, "row_attn_tc");
+  if (e == cudaSuccess) e = launch_k3(t, s, map_out, 0, ntiles);
+  tri_mark(t, s, mark++, "gate_out_tc");
+  return e;
+}
+
+// Host buffers in and out, pipelined: x arrives in chunks on a copy stream
+// while K1 works on the chunks already on the device; K2 then runs in chunks
+// of row groups, and after each chunk K3 forms the out tiles of its finished
+// rows, which are copied back while the next chunk runs. dx, dmask, dout are
+// the handle's device staging buffers.
+cudaError_t tri_tc_forward_host(tri_attn_s* t, cudaStream_t s, const void* xh,
+                                const int32_t* maskh, void* outh, void* dx, int32_t* dmask,
+                                void* dout) {
+  TcState* st = (TcState*)t->tc;
+  cudaError_t e = cudaSuccess;
+  if (!st->copy_in) {
+    e = cudaStreamCreateWithFlags(&st->copy_in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&st->copy_out, cudaStreamNonBlocking);
+    for (int i = 0; i < kHostEvents && e == cudaSuccess; ++i)
+      e = cudaEventCreateWithFlags(&st->ev[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) return e;
+  }
+  const int ntiles = num_tiles(t);
+  const int nch = ntiles < kHostChunks ? ntiles : kHostChunks;
+  const int per = (ntiles + nch - 1) / nch;
+  const size_t row_bytes = (size_t)t->D * 2;
+  CUtensorMap map_x, map_out;
+  if (!map_rows_bf16(&map_x, dx, t->cells, 128) || !map_out_rows(&map_out, dout, t->cells))
+    return cudaErrorInvalidValue;
+  cudaEvent_t* ev = st->ev;          // [0] start, [1] mask in, [2 ..] x chunks in, out chunks done
+  cudaEvent_t* ev_x = ev + 2;
+  cudaEvent_t* ev_o = ev + 2 + kHostChunks;
+  cudaEvent_t ev_done = ev[2 + 2 * kHostChunks];
+  // The copies start after the work already queued on s.
+  e = cudaEventRecord(ev[0], s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st->copy_in, ev[0], 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st->copy_out, ev[0], 0);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(dmask, maskh, (size_t)t->cells * sizeof(int32_t), cudaMemcpyHostToDevice,
+                        st->copy_in);
+  if (e == cudaSuccess) e = cudaEventRecord(ev[1], st->copy_in);
+  for (int i = 0; i < nch && e == cudaSuccess; ++i) {
+    const long long c0 = (long long)i * per * 128;
+    const long long c1 = std::min((long long)(i + 1) * per * 128, t->cells);
+    if (c0 >= c1) break;
+    e = cudaMemcpyAsync((char*)dx + c0 * row_bytes, (const char*)xh + c0 * row_bytes,
+                        (size_t)(c1 - c0) * row_bytes, cudaMemcpyHostToDevice, st->copy_in);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_x[i], st->copy_in);
+  }
+  for (int i = 0; i < nch && e == cudaSuccess; ++i) {
+    const int t0 = i * per, n = std::min(per, ntiles - t0);
+    if (n <= 0) break;
+    e = cudaStreamWaitEvent(s, ev_x[i], 0);
+    if (e == cudaSuccess) e = launch_k1(t, s, map_x, dmask, t0, n);
+  }
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev[1], 0);
+  int mark = 0;
+  if (e == cudaSuccess) e = launch_mask(t, s, dmask, mark);
+  // K3 over tiles lo .. hi - 1, then their out leaves on the copy-out stream.
+  int n_out = 0;
+  auto emit = [&](int lo, int hi) {
+    if (e != cudaSuccess || hi <= lo || n_out >= kHostChunks) return;
+    e = launch_k3(t, s, map_out, lo, hi - lo);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_o[n_out], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st->copy_out, ev_o[n_out], 0);
+    const long long c0 = (long long)lo * 128, c1 = std::min((long long)hi * 128, t->cells);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync((char*)outh + c0 * row_bytes, (const char*)dout + c0 * row_bytes,
+                          (size_t)(c1 - c0) * row_bytes, cudaMemcpyDeviceToHost, st->copy_out);
+    ++n_out;
+  };
+  const int groups = t->B * k2_row_groups(t);
+  if (t->ending) {
+    // K2's lines are columns here, so no row of out is done before K2 ends:
+    // one K2 launch, then K3 and the copies in chunks.
+    if (e == cudaSuccess) e = launch_k2(t, s, 0, groups);
+    for (int i = 0; i < nch; ++i) emit(std::min(i * per, ntiles), std::min((i + 1) * per, ntiles));
+  } else {
+    // K2 in chunks of row groups; after each, K3 forms the 128-cell tiles whose
+    // rows are all done, and their out leaves while the next chunk runs.
+    const int gch = groups < kHostChunks ? groups : kHostChunks;
+    const int gper = (groups + gch - 1) / gch;
+    const int rgs = k2_row_groups(t);
+    const long long NN = (long long)t->N * t->N;
+    int tile_done = 0;
+    for (int i = 0; i < gch && e == cudaSuccess; ++i) {
+      const int g0 = i * gper, ng = std::min(gper, groups - g0);
+      if (ng <= 0) break;
+      e = launch_k2(t, s, g0, ng);
+      // grid rows (b, i) before the chunk's end are consecutive cells
+      const int gend = g0 + ng;
+      const long long bend = gend / rgs;
+      const long long rend = std::min((long long)(gend % rgs) * k2::R, (long long)t->N);
+      const long long cells_done = std::min(bend * NN + rend * t->N, t->cells);
+      const int tile_end = gend == groups ? ntiles : (int)(cells_done / 128);
+      if (tile_end > tile_done) {
+        emit(tile_done, tile_end);
+        tile_done = tile_end;
+      }
+    }
+  }
+  // s finishes only once the last chunk of out is on the host.
+  if (e == cudaSuccess) e = cudaEventRecord(ev_done, st->copy_out);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_done, 0);
+  return e;
 }

@@ -141,3 +141,28 @@ def test_bf16_large_grid_sampled_rows():
     ref = O.forward_rows(inp["x"], inp["pair_mask"], inp["params"], w.h, rows, 0)
     H.assert_parity(w, np.stack([got[b, i] for b, i in rows]), ref)
     assert np.all(np.isfinite(got))
+
+
+@pytest.mark.parametrize("B,mode", [(2, 1), (1, 0), (1, 2)])
+def test_bf16_forward_host_pipelined_matches_device(B, mode):
+    """The host-buffer entry point moves x in four chunks overlapped with the
+    first kernel, runs the attention kernel in four chunks of row groups (a
+    chunk boundary inside the second batch entry when B = 2) and copies each
+    chunk's finished rows back while the next runs; for the ending node the
+    attention runs whole and the output leaves in four chunks. 131 or 262
+    tiles, the last one ragged; in query-key mode the first kernel also reads
+    the mask, which must have landed. The result must equal the device-buffer
+    forward bit for bit."""
+    w = W.custom(B, 129, 128, 4, "bf16", "bernoulli", seed=43)
+    inp = W.make_inputs(w)
+    mod = tb.TriangularAttention(w.B, w.N, w.D, w.h, tb.TRI_ATTN_BF16, mode, H.device_params(inp, w))
+    try:
+        xh = torch.from_numpy(inp["x"]).to(torch.bfloat16).pin_memory()
+        mh = torch.from_numpy(inp["pair_mask"]).pin_memory()
+        oh = torch.full_like(xh, float("nan")).pin_memory()
+        mod.forward_host(xh, mh, oh)
+        od = mod.forward(xh.cuda(), mh.cuda())
+        assert mod.sync_check() == tb.TRI_ATTN_OK
+        assert torch.equal(oh, od.cpu())
+    finally:
+        mod.close()
