@@ -1318,9 +1318,10 @@ bool map_lines(CUtensorMap* m, const void* base, int B, int N, int box_x, bool e
                   CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-// The host-buffer forward moves x and out in this many chunks; its events are
-// start, mask copied, one per x chunk copied, one per out chunk formed, done.
-constexpr int kHostChunks = 4;
+// The host-buffer forward moves x and out in 4 to kHostChunks chunks (about
+// 16 MB of x each, measured best); its events are start, mask copied, one per
+// x chunk copied, one per out chunk formed, done.
+constexpr int kHostChunks = 8;
 constexpr int kHostEvents = 3 + 2 * kHostChunks;
 
 struct TcState {
@@ -1588,9 +1589,11 @@ cudaError_t tri_tc_forward_host(tri_attn_s* t, cudaStream_t s, const void* xh,
     if (e != cudaSuccess) return e;
   }
   const int ntiles = num_tiles(t);
-  const int nch = ntiles < kHostChunks ? ntiles : kHostChunks;
-  const int per = (ntiles + nch - 1) / nch;
   const size_t row_bytes = (size_t)t->D * 2;
+  const long long want = std::min<long long>(
+      kHostChunks, std::max<long long>(4, (long long)(t->cells * row_bytes >> 24)));
+  const int nch = (int)std::min<long long>(ntiles, want);
+  const int per = (ntiles + nch - 1) / nch;
   CUtensorMap map_x, map_out;
   if (!map_rows_bf16(&map_x, dx, t->cells, 128) || !map_out_rows(&map_out, dout, t->cells))
     return cudaErrorInvalidValue;
@@ -1645,7 +1648,7 @@ cudaError_t tri_tc_forward_host(tri_attn_s* t, cudaStream_t s, const void* xh,
   } else {
     // K2 in chunks of row groups; after each, K3 forms the 128-cell tiles whose
     // rows are all done, and their out leaves while the next chunk runs.
-    const int gch = groups < kHostChunks ? groups : kHostChunks;
+    const int gch = groups < nch ? groups : nch;
     const int gper = (groups + gch - 1) / gch;
     const int rgs = k2_row_groups(t);
     const long long NN = (long long)t->N * t->N;
