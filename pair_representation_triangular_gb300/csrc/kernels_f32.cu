@@ -191,25 +191,35 @@ row_attn_f32(const float* __restrict__ q, const float* __restrict__ k,
       Mrow[tid] = tid < nk ? mask[line0 + (long long)(k0 + tid) * sx] : 0;
     __syncthreads();
 
+    // Keys two at a time: two independent dot-product chains, one rescale.
 #pragma unroll 1
-    for (int kk = 0; kk < nk; ++kk) {
-      float dot = 0.f;
+    for (int kk = 0; kk < nk; kk += 2) {
+      const bool two = kk + 1 < nk;
+      float dot0 = 0.f, dot1 = 0.f;
 #pragma unroll
-      for (int e = 0; e < MAXD; ++e) dot = fmaf(qv[e], Ks[kk][e], dot);
-      float lg = dot * scale + Bs[tid][kk];
-      const int keep = mask_mode == TRI_ATTN_MASK_ROW_KEY ? Mrow[kk] : Ms[tid][kk];
-      if (!keep) lg = -1e9f;                      // replacement by -1e9
-      if (lg > m) {                               // running maximum moved: rescale
-        const float alpha = expf(m - lg);         // exp(-inf) = 0 before the first key
+      for (int e = 0; e < MAXD; ++e) {
+        dot0 = fmaf(qv[e], Ks[kk][e], dot0);
+        dot1 = fmaf(qv[e], Ks[kk + 1][e], dot1);     // row kk + 1 exists: KC is even
+      }
+      float lg0 = dot0 * scale + Bs[tid][kk];
+      float lg1 = dot1 * scale + Bs[tid][kk + 1];
+      const int keep0 = mask_mode == TRI_ATTN_MASK_ROW_KEY ? Mrow[kk] : Ms[tid][kk];
+      const int keep1 = mask_mode == TRI_ATTN_MASK_ROW_KEY ? Mrow[kk + 1] : Ms[tid][kk + 1];
+      if (!keep0) lg0 = -1e9f;                    // replacement by -1e9
+      if (!keep1) lg1 = -1e9f;
+      if (!two) lg1 = -INFINITY;                  // past N: weight 0
+      const float mn = fmaxf(lg0, lg1);
+      if (mn > m) {                               // running maximum moved: rescale
+        const float alpha = expf(m - mn);         // exp(-inf) = 0 before the first key
         l *= alpha;
 #pragma unroll
         for (int e = 0; e < MAXD; ++e) acc[e] *= alpha;
-        m = lg;
+        m = mn;
       }
-      const float p = expf(lg - m);
-      l += p;
+      const float p0 = expf(lg0 - m), p1 = expf(lg1 - m);
+      l += p0 + p1;
 #pragma unroll
-      for (int e = 0; e < MAXD; ++e) acc[e] = fmaf(p, Vs[kk][e], acc[e]);
+      for (int e = 0; e < MAXD; ++e) acc[e] = fmaf(p1, Vs[kk + 1][e], fmaf(p0, Vs[kk][e], acc[e]));
     }
   }
   if (active) {
