@@ -140,7 +140,7 @@ def kernel_key(name: str) -> str:
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """Samples nvidia-smi clocks and throttle reasons every 200 ms."""
+    """Samples nvidia-smi clocks and throttle reasons every 25 ms."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -154,7 +154,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "25"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -327,6 +327,14 @@ def run_native(args, rank, world):
     barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(dev.index) as clk:
+        # Keep the GPU under load until the sampler reports (at most ~2 s), so
+        # that its samples cover the loaded clocks around the timed steps.
+        t_wait = time.perf_counter()
+        while clk.proc is not None and len(clk.rows) < 2 and time.perf_counter() - t_wait < 2.0:
+            mod.forward(x, m, out)
+            torch.cuda.synchronize(dev)
+        barrier()
+        torch.cuda.synchronize(dev)
         for s in range(args.steps):
             flush.fill_(float(s))                       # evict L2 (outside the timed pair)
             ev[s][0].record(stream)
