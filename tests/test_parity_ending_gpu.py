@@ -93,3 +93,28 @@ def test_ending_differs_from_starting():
     start = H.run_forward(w, inp, 0)[0]
     end = H.run_forward(w, inp, END)[0]
     assert float(np.max(np.abs(start - end))) > 10 * H.TOL_BF16_MAX_ABS
+
+
+def _sweep_cases():
+    rng = np.random.default_rng(2026)
+    cases = []
+    for _ in range(12):
+        B = int(rng.integers(1, 4))
+        N = int(rng.integers(1, 260))
+        mode = int(rng.integers(0, 4))                 # mask reading | ending-node flag
+        cases.append((B, N, mode))
+    return cases
+
+
+@pytest.mark.parametrize("B,N,mode", _sweep_cases())
+def test_bf16_seeded_shape_sweep(B, N, mode):
+    """Seeded random shapes (B 1-3, N 1-259, both nodes, both mask readings)
+    on the tensor-core path against the oracle."""
+    w = W.custom(B, N, 128, 4, "bf16", "bernoulli", seed=7000 + 31 * N + B)
+    inp = W.make_inputs(w)
+    got = H.run_forward(w, inp, mode)[0]
+    if mode & END:
+        ref = O.forward_ending(inp["x"], inp["pair_mask"], inp["params"], w.h, mode & 1)
+    else:
+        ref = O.forward(inp["x"], inp["pair_mask"], inp["params"], w.h, mode)
+    H.assert_parity(w, got, ref)
