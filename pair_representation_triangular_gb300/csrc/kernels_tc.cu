@@ -674,16 +674,16 @@ __device__ __forceinline__ float redo_tile(const float2 (&x2)[BK / 2], uint32_t 
   return ts2.x + ts2.y;
 }
 
-// Persistent: CTA c serves work units c, c + G, ... A unit is (b, head t, R = 3
-// rows i, 128 queries j); it streams 64-key tiles, each stage holding the K
-// and V tiles of the three rows and the fp16 bias tile they share. Softmax
-// warpgroup r owns row r; S = Q K^T of the next tile is computed into the
-// row's S columns as soon as the softmax has loaded the current one. The
-// softmax adds the bias, drops masked keys and writes P = 2^(x - mu) (bf16)
-// to the row's P columns in one pass; O += P V accumulates in TMEM. The
-// reference mu of a query row is the max of its first live tile and moves
-// (rescaling O in TMEM) only when a tile's sum of P reaches 2^32, so no
-// per-tile max is taken in the common case.
+// Persistent: CTA c serves work units unit0 + c, + G, ... A unit is (b, head
+// t, R = 3 lines, 128 queries); it streams 64-key tiles, each stage holding
+// the K and V tiles of the three lines and the fp16 bias tile they share.
+// Softmax warpgroup r owns line r; tile c's S = Q K^T lands in the line's S
+// buffer c & 1, and the softmax adds the bias, drops masked keys and writes
+// P = 2^(x - mu) (bf16) over it in one pass; the line's MMA thread then issues
+// O += P V(c) and S(c + 2) into the same buffer. The reference mu of a query
+// row is the max of its first live tile and moves (rescaling O in TMEM) only
+// when a tile's sum of P reaches 2^32, so no per-tile max is taken in the
+// common case.
 __global__ void __launch_bounds__(kThreads, 1)
 row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
             const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_b,
