@@ -82,11 +82,12 @@ def algorithmic_work(w):
 # DRAM traffic per pair cell (dram__bytes_read.sum + dram__bytes_write.sum of
 # one launch, divided by its B*N^2 cells) from the ncu capture of the B=1,
 # N=384 bf16 workload summarised in profiles/kernels_b1-n384-d128-h4-bf16-pad320.md.
-# It holds for the tensor-core kernel sources whose SHA-256 prefix is recorded
-# here; for any other source the bench reports traffic as null.
+# It holds for the tensor-core kernel code whose SHA-256 prefix (comments
+# removed) is recorded here; for any other code the bench reports traffic as
+# null.
 TRAFFIC_SOURCES = ("kernels_tc.cu", "tc_ptx.cuh", "common.cuh")
 TRAFFIC_PER_CELL = {
-    "source_sha256": "917f9d3ad075f3fb",
+    "source_sha256": "cf2a551c22f2749e",
     "capture": "b1-n384-d128-h4-bf16-pad320",
     "ln_proj_tc": (37.938688e6 + 96.419840e6) / 147456,
     "row_attn_tc": (114.521088e6 + 17.288192e6) / 147456,
@@ -94,12 +95,27 @@ TRAFFIC_PER_CELL = {
 }
 
 
-def kernel_source_sha() -> str:
+def code_lines(text: str) -> str:
+    """Source text without // comments, trailing blanks and empty lines, so that
+    a change of comments keeps the hash of the code."""
+    out = []
+    for line in text.splitlines():
+        line = line.split("//", 1)[0].rstrip()
+        if line:
+            out.append(line)
+    return "\n".join(out)
+
+
+def kernel_source_sha(read=None) -> str:
     import hashlib
     h = hashlib.sha256()
     for name in TRAFFIC_SOURCES:
-        with open(os.path.join(ROOT, "pair_representation_triangular_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        if read is None:
+            with open(os.path.join(ROOT, "pair_representation_triangular_gb300", "csrc", name)) as f:
+                text = f.read()
+        else:
+            text = read(name)
+        h.update(code_lines(text).encode())
     return h.hexdigest()[:16]
 
 
