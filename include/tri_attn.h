@@ -63,6 +63,7 @@ typedef struct tri_attn_s* tri_attn_t;
 enum { TRI_ATTN_F32 = 0, TRI_ATTN_BF16 = 1 };
 enum { TRI_ATTN_MASK_ROW_KEY = 0, TRI_ATTN_MASK_QUERY_KEY = 1 };
 enum { TRI_ATTN_STARTING_NODE = 0, TRI_ATTN_ENDING_NODE = 2 };
+enum { TRI_ATTN_PATH_SIMT = 0, TRI_ATTN_PATH_TENSOR_CORE = 1 };
 
 enum {
   TRI_ATTN_OK = 0,
@@ -77,10 +78,14 @@ enum {
 /* Build a handle for one problem shape and one set of weights.
  *
  * B, N, D, h: batch, pair-grid side, channels, heads; D % h == 0. Supported:
- *   TRI_ATTN_F32  any B, N >= 1, even D <= 256 with d = D/h <= 128;
- *   TRI_ATTN_BF16 the tensor-core path: D == 128, h == 4 (d == 32), any B,
- *                 1 <= N <= 8192, B*N*N < 2^31.
- *   Other shapes return TRI_ATTN_ERR_UNSUPPORTED (there is no fallback path).
+ *   TRI_ATTN_F32  any B, N >= 1, even D <= 256 with d = D/h <= 128, on the fp32
+ *                 SIMT kernels;
+ *   TRI_ATTN_BF16 the tensor-core kernels for D == 128, h == 4 (d == 32), any B,
+ *                 1 <= N <= 8192, B*N*N < 2^31; other shapes within the fp32
+ *                 limits run on the fp32 SIMT kernels, with pair_repr converted
+ *                 to fp32 and out rounded to bf16 on the device (see
+ *                 tri_attn_kernel_path).
+ *   Other shapes return TRI_ATTN_ERR_UNSUPPORTED (nothing runs on the host).
  * mode: a mask reading (TRI_ATTN_MASK_ROW_KEY or TRI_ATTN_MASK_QUERY_KEY),
  *   OR-ed with TRI_ATTN_ENDING_NODE for the ending-node variant (see above);
  *   any other bit gives TRI_ATTN_ERR_INVALID_ARG.
@@ -129,6 +134,10 @@ int tri_attn_sync_check(tri_attn_t t, void* stream);
  * uses the handle is still running. NULL is accepted. */
 int tri_attn_destroy(tri_attn_t t);
 
+/* Which kernels a handle runs: TRI_ATTN_PATH_TENSOR_CORE or TRI_ATTN_PATH_SIMT
+ * (negative status for a NULL handle). */
+int tri_attn_kernel_path(tri_attn_t t);
+
 /* Human-readable name of a status code (static storage). */
 const char* tri_attn_status_string(int status);
 
@@ -150,15 +159,16 @@ int tri_attn_kernel_times(tri_attn_t t, float* ms, const char** names, int* n);
 
 /* Diagnostic access to the handle's intermediates (valid until destroy; they
  * hold the results of the most recent forward once it has finished):
- *   "q", "k", "v", "g", "o"  (B*N*N, D) in the handle's dtype: per cell the
- *                           projections, the post-sigmoid gate and the
- *                           attention output before the gate;
+ *   "q", "k", "v", "g", "o"  (B*N*N, D) per cell the projections, the
+ *                           post-sigmoid gate and the attention output before
+ *                           the gate: bf16 on the tensor-core path, fp32 on the
+ *                           SIMT path;
  *   "bias"                  (B, h, N, row_stride) pair-bias plane indexed
  *                           [b, t, query, key]: bias[b,t,j,k] for the starting
  *                           node, bias[b,t,k,i] at [b,t,i,k] for the ending
- *                           node; fp32 on the fp32 path; on the bf16 path fp16
- *                           holding log2(e) * bias, and -inf where the
- *                           query-key mask drops the key.
+ *                           node; fp32 on the SIMT path; on the tensor-core
+ *                           path fp16 holding log2(e) * bias, and -inf where
+ *                           the query-key mask drops the key.
  * Returns the device pointer, or NULL for an unknown name or handle;
  * *row_stride (may be NULL) receives the innermost row stride in elements. */
 void* tri_attn_debug_tensor(tri_attn_t t, const char* name, int64_t* row_stride);

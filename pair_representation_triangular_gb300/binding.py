@@ -22,6 +22,8 @@ TRI_ATTN_MASK_ROW_KEY = 0
 TRI_ATTN_MASK_QUERY_KEY = 1
 TRI_ATTN_STARTING_NODE = 0
 TRI_ATTN_ENDING_NODE = 2        # OR-ed into the mode: attention along columns
+TRI_ATTN_PATH_SIMT = 0
+TRI_ATTN_PATH_TENSOR_CORE = 1
 
 TRI_ATTN_OK = 0
 TRI_ATTN_ERR_INVALID_ARG = 1
@@ -75,6 +77,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.tri_attn_set_wait_limit.argtypes = [vp, i64]
     lib.tri_attn_enable_kernel_timing.argtypes = [vp, i32]
     lib.tri_attn_debug_tensor.argtypes = [vp, ctypes.c_char_p, ctypes.POINTER(i64)]
+    lib.tri_attn_kernel_path.argtypes = [vp]
+    lib.tri_attn_kernel_path.restype = i32
     lib.tri_attn_debug_tensor.restype = vp
     lib.tri_attn_forward_noalloc.argtypes = [i32, i32, i32, i32, i32] + [vp] * 14
     lib.tri_attn_forward_noalloc.restype = i32
@@ -186,6 +190,10 @@ def tri_attn_forward_noalloc(B, N, D, h, mode, params: dict, stream,
            "tri_attn_forward_noalloc")
 
 
+def tri_attn_kernel_path(handle) -> int:
+    return load_library().tri_attn_kernel_path(handle)
+
+
 def tri_attn_debug_tensor(handle, name: str):
     """(device pointer, innermost row stride in elements) of an intermediate;
     (None, 0) for an unknown name."""
@@ -241,19 +249,20 @@ class TriangularAttention:
 
     def intermediate(self, name: str) -> torch.Tensor:
         """Copy of an intermediate of the most recent forward (see
-        tri_attn_debug_tensor): q, k, v, g, o as (B, N, N, D) in the handle's dtype
-        (bf16 is returned as its raw bits reinterpreted); bias as (B, h, N, N) fp32
-        (stored in fp16 on the bf16 path)."""
+        tri_attn_debug_tensor): q, k, v, g, o as (B, N, N, D), bf16 on the
+        tensor-core path (its raw bits reinterpreted) and fp32 on the SIMT path;
+        bias as (B, h, N, N) fp32 (stored in fp16 on the tensor-core path)."""
         ptr, ld = tri_attn_debug_tensor(self.handle, name)
         if not ptr:
             raise KeyError(name)
         torch.cuda.synchronize()
+        simt = tri_attn_kernel_path(self.handle) == TRI_ATTN_PATH_SIMT
         if name == "bias":
-            ts = "<f4" if self.dtype == TRI_ATTN_F32 else "<f2"
+            ts = "<f4" if simt else "<f2"
             view = _DeviceView(ptr, (self.B, self.h, self.N, ld), ts)
             return torch.as_tensor(view, device="cuda")[..., :self.N].float()
         shape = (self.B, self.N, self.N, self.D)
-        if self.torch_dtype == torch.float32:
+        if simt:
             return torch.as_tensor(_DeviceView(ptr, shape, "<f4"), device="cuda").clone()
         raw = torch.as_tensor(_DeviceView(ptr, shape, "<i2"), device="cuda").clone()
         return raw.view(torch.bfloat16)

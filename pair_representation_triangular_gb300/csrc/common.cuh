@@ -27,6 +27,8 @@ inline bool tri_ending(int mode) { return (mode & TRI_ATTN_ENDING_NODE) != 0; }
 struct tri_attn_s {
   int B, N, D, h, d, dtype, mask_mode;
   bool ending;                     // ending-node variant (attention along columns)
+  bool simt;                       // fp32 SIMT kernels (fp32 handles, and bf16 shapes the
+                                   // tensor-core path does not cover)
   long long cells;                 // B * N * N
   int device;
   // Packed weights (owned).
@@ -41,6 +43,8 @@ struct tri_attn_s {
   long long wait_limit;
   // Host-buffer staging (forward_host), allocated on first use.
   void* stage_x; int32_t* stage_mask; void* stage_out;
+  // bf16 handle on the SIMT kernels: fp32 copies of pair_repr and out.
+  float* x32; float* out32;
   // Tensor-core path state (opaque to the f32 path).
   void* tc;
   size_t bytes_owned;

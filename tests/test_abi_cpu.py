@@ -50,7 +50,8 @@ def test_create_rejects_bad_arguments_before_cuda(lib):
     assert _create(lib, 1, 8, 64, 4, 0, ptr=24) == tb.TRI_ATTN_ERR_INVALID_ARG  # misaligned
     assert _create(lib, 1, 8, 512, 4, 0) == tb.TRI_ATTN_ERR_UNSUPPORTED     # f32 D > 256
     assert _create(lib, 1, 8, 33, 3, 0) == tb.TRI_ATTN_ERR_UNSUPPORTED      # f32 odd D
-    assert _create(lib, 1, 8, 96, 4, 1) == tb.TRI_ATTN_ERR_UNSUPPORTED      # bf16 needs D=128
+    assert _create(lib, 1, 8, 512, 4, 1) == tb.TRI_ATTN_ERR_UNSUPPORTED     # bf16 D > 256
+    assert _create(lib, 1, 8, 33, 3, 1) == tb.TRI_ATTN_ERR_UNSUPPORTED      # bf16 odd D
 
 
 def test_null_handle_calls(lib):

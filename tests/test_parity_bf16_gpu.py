@@ -166,3 +166,34 @@ def test_bf16_forward_host_pipelined_matches_device(B, mode):
         assert torch.equal(oh, od.cpu())
     finally:
         mod.close()
+
+
+@pytest.mark.parametrize("B,N,D,h,mode", [(1, 40, 64, 4, 0), (2, 33, 128, 2, 1), (1, 17, 96, 3, 2),
+                                          (1, 50, 128, 8, 3), (1, 70, 32, 1, 0)])
+def test_bf16_shapes_outside_the_tensor_core_path(B, N, D, h, mode):
+    """bf16 handles whose shape the tensor-core kernels do not cover run on the
+    fp32 SIMT kernels (pair_repr widened to fp32 and out rounded to bf16 on the
+    device), and still meet the bf16 bar."""
+    w = W.custom(B, N, D, h, "bf16", "bernoulli", seed=9000 + N + D + h)
+    inp = W.make_inputs(w)
+    mod = tb.TriangularAttention(B, N, D, h, tb.TRI_ATTN_BF16, mode, H.device_params(inp, w))
+    try:
+        assert tb.tri_attn_kernel_path(mod.handle) == tb.TRI_ATTN_PATH_SIMT
+    finally:
+        mod.close()
+    got = H.run_forward(w, inp, mode)[0]
+    if mode & tb.TRI_ATTN_ENDING_NODE:
+        ref = O.forward_ending(inp["x"], inp["pair_mask"], inp["params"], h, mode & 1)
+    else:
+        ref = O.forward(inp["x"], inp["pair_mask"], inp["params"], h, mode)
+    H.assert_parity(w, got, ref)
+
+
+def test_bf16_benchmark_shape_takes_the_tensor_core_path():
+    w = W.custom(1, 8, 128, 4, "bf16", "ones", seed=1)
+    inp = W.make_inputs(w)
+    mod = tb.TriangularAttention(1, 8, 128, 4, tb.TRI_ATTN_BF16, 0, H.device_params(inp, w))
+    try:
+        assert tb.tri_attn_kernel_path(mod.handle) == tb.TRI_ATTN_PATH_TENSOR_CORE
+    finally:
+        mod.close()
