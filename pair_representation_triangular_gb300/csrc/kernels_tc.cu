@@ -28,6 +28,7 @@
 // Passages followed: POPCORNBENCH "Kimi-K2.6 l2_p6", forward op list steps
 // 1-18 and layer definitions; "FW-GLM-5-1 l2_p6", quoted Model.forward.
 #include <math.h>
+#include <stddef.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -168,9 +169,11 @@ struct Bars {
 // gw[t][c] = gamma[c] Wb[t][c], gws[t] = sum_c gw[t][c], bw[t] = sum_c beta[c] Wb[t][c]:
 // with t_c = (x_c - mean) rstd, bias[t] = sum_c x_hat_c Wb[t][c]
 // = rstd (sum_c (x_c - K) gw[t][c] - (mean - K) gws[t]) + bw[t] for any shift K.
-struct Consts {
+struct alignas(16) Consts {     // 16-byte aligned: rows are read as float2 pairs
   float gamma[KD], beta[KD], bg[KD], gw[4][KD], gws[4], bw[4];
 };
+static_assert(offsetof(Consts, gw) % 16 == 0 && offsetof(Consts, beta) % 16 == 0,
+              "parameter rows must stay 8-byte aligned");
 
 struct Params {
   long long cells;
@@ -285,6 +288,11 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
     // ---------------- LayerNorm: cell row r, channel half hh
     const int q4 = warp & 3, hh = warp >> 2;
     const int r = q4 * 32 + lane;
+    // Parameter pairs (one 8-byte constant load each): this thread's two bias
+    // heads and the LayerNorm affine.
+    const float2* gw2[2] = {(const float2*)cst.gw[2 * hh], (const float2*)cst.gw[2 * hh + 1]};
+    const float2* gamma2 = (const float2*)cst.gamma;
+    const float2* beta2 = (const float2*)cst.beta;
     const long long NN = (long long)p.N * p.N;
     bool ok = true;
     for (int it = 0; ok && it < my_tiles; ++it) {
@@ -315,7 +323,7 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
           q2 = __ffma2_rn(d, d, q2);
 #pragma unroll
           for (int t2 = 0; t2 < 2; ++t2)
-            bp[t2] = __ffma2_rn(d, make_float2(cst.gw[2 * hh + t2][i0], cst.gw[2 * hh + t2][i0 + 1]), bp[t2]);
+            bp[t2] = __ffma2_rn(d, gw2[t2][i0 / 2], bp[t2]);
         }
       }
       const float S1 = (s2.x + s2.y) * (1.0f / KD);             // mean of x - K
@@ -337,8 +345,7 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
         for (int e = 0; e < 4; ++e) {
           const int i0 = hh * 64 + c * 8 + 2 * e;
           const float2 t = __ffma2_rn(make_float2(bf16_lo(in4[e]), bf16_hi(in4[e])), rs2, nm2);
-          const float2 y = __ffma2_rn(t, make_float2(s_gamma[i0], s_gamma[i0 + 1]),
-                                      make_float2(s_beta[i0], s_beta[i0 + 1]));
+          const float2 y = __ffma2_rn(t, gamma2[i0 / 2], beta2[i0 / 2]);
           mine[c * 4 + e] = tc::pack_bf16x2(y.x, y.y);
         }
       }
