@@ -204,8 +204,6 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   Bars* bars = (Bars*)(smem + OFF_BAR);
-  const float* s_gamma = cst.gamma;
-  const float* s_beta = cst.beta;
   const float* s_bg = cst.bg;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const Abort ab{&bars->abort, p.dev_err, p.polls};
