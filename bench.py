@@ -87,11 +87,11 @@ def algorithmic_work(w):
 # null.
 TRAFFIC_SOURCES = ("kernels_tc.cu", "tc_ptx.cuh", "common.cuh")
 TRAFFIC_PER_CELL = {
-    "source_sha256": "cf2a551c22f2749e",
+    "source_sha256": "86435f0ecc819913",
     "capture": "b1-n384-d128-h4-bf16-pad320",
-    "ln_proj_tc": (37.938688e6 + 96.419840e6) / 147456,
-    "row_attn_tc": (114.521088e6 + 17.288192e6) / 147456,
-    "gate_out_tc": (75.560960e6 + 5.831424e6) / 147456,
+    "ln_proj_tc": (37.949696e6 + 96.857088e6) / 147456,
+    "row_attn_tc": (114.522112e6 + 17.055744e6) / 147456,
+    "gate_out_tc": (75.561216e6 + 5.678848e6) / 147456,
 }
 
 
