@@ -50,7 +50,7 @@ __device__ __forceinline__ void tile_gemm(const float* __restrict__ xt, int c0, 
   for (int i = 0; i < 2; ++i)
 #pragma unroll
     for (int c = 0; c < CT; ++c) acc[i][c] = 0.f;
-#pragma unroll 2
+#pragma unroll 4
   for (int e = 0; e < D; ++e) {
     const float2 w = *(const float2*)(Wt + (size_t)e * ld + o0);
     float xv[CT];
