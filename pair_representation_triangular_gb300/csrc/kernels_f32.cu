@@ -191,24 +191,21 @@ row_attn_f32(const float* __restrict__ q, const float* __restrict__ k,
       Mrow[tid] = tid < nk ? mask[line0 + (long long)(k0 + tid) * sx] : 0;
     __syncthreads();
 
-    // Keys two at a time: two independent dot-product chains, one rescale.
+    // Keys four at a time: four independent dot-product chains, one rescale.
 #pragma unroll 1
-    for (int kk = 0; kk < nk; kk += 2) {
-      const bool two = kk + 1 < nk;
-      float dot0 = 0.f, dot1 = 0.f;
+    for (int kk = 0; kk < nk; kk += 4) {
+      float lg[4];
 #pragma unroll
-      for (int e = 0; e < MAXD; ++e) {
-        dot0 = fmaf(qv[e], Ks[kk][e], dot0);
-        dot1 = fmaf(qv[e], Ks[kk + 1][e], dot1);     // row kk + 1 exists: KC is even
+      for (int u = 0; u < 4; ++u) {
+        float dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < MAXD; ++e) dot = fmaf(qv[e], Ks[kk + u][e], dot);   // KC % 4 == 0
+        float v = dot * scale + Bs[tid][kk + u];
+        const int keep = mask_mode == TRI_ATTN_MASK_ROW_KEY ? Mrow[kk + u] : Ms[tid][kk + u];
+        if (!keep) v = -1e9f;                     // replacement by -1e9
+        lg[u] = kk + u < nk ? v : -INFINITY;      // past N: weight 0
       }
-      float lg0 = dot0 * scale + Bs[tid][kk];
-      float lg1 = dot1 * scale + Bs[tid][kk + 1];
-      const int keep0 = mask_mode == TRI_ATTN_MASK_ROW_KEY ? Mrow[kk] : Ms[tid][kk];
-      const int keep1 = mask_mode == TRI_ATTN_MASK_ROW_KEY ? Mrow[kk + 1] : Ms[tid][kk + 1];
-      if (!keep0) lg0 = -1e9f;                    // replacement by -1e9
-      if (!keep1) lg1 = -1e9f;
-      if (!two) lg1 = -INFINITY;                  // past N: weight 0
-      const float mn = fmaxf(lg0, lg1);
+      const float mn = fmaxf(fmaxf(lg[0], lg[1]), fmaxf(lg[2], lg[3]));
       if (mn > m) {                               // running maximum moved: rescale
         const float alpha = expf(m - mn);         // exp(-inf) = 0 before the first key
         l *= alpha;
@@ -216,10 +213,16 @@ row_attn_f32(const float* __restrict__ q, const float* __restrict__ k,
         for (int e = 0; e < MAXD; ++e) acc[e] *= alpha;
         m = mn;
       }
-      const float p0 = expf(lg0 - m), p1 = expf(lg1 - m);
-      l += p0 + p1;
+      float pk[4];
 #pragma unroll
-      for (int e = 0; e < MAXD; ++e) acc[e] = fmaf(p1, Vs[kk + 1][e], fmaf(p0, Vs[kk][e], acc[e]));
+      for (int u = 0; u < 4; ++u) {
+        pk[u] = expf(lg[u] - m);
+        l += pk[u];
+      }
+#pragma unroll
+      for (int e = 0; e < MAXD; ++e)
+        acc[e] = fmaf(pk[3], Vs[kk + 3][e], fmaf(pk[2], Vs[kk + 2][e],
+                 fmaf(pk[1], Vs[kk + 1][e], fmaf(pk[0], Vs[kk][e], acc[e]))));
     }
   }
   if (active) {
