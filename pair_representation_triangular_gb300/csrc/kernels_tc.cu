@@ -1098,10 +1098,23 @@ struct Bars {
 struct Params {
   long long cells;
   int ntiles, tile0;              // this launch: tiles tile0 .. tile0 + ntiles - 1
+  // Tile order. cols = 0: tile t is cells t*128 .. t*128 + 127 in memory order
+  // (maps (channel, cell, 1, 1)). cols = 1: tile t is rows x .. x + 127 of one
+  // column j of the grid of batch b, with tpl tiles per column (maps (channel,
+  // i, j, b)), so a run of tiles covers whole columns.
+  int cols, N, tpl;
   const float* bo;
   unsigned int* dev_err;
   long long polls;
 };
+
+// TMA coordinates (x, y, z) of tile `tile` after the channel coordinate.
+struct TileAt { int x, y, z; };
+__device__ __forceinline__ TileAt tile_at(const Params& p, int tile) {
+  if (!p.cols) return {tile * BM, 0, 0};
+  const int line = tile / p.tpl;
+  return {(tile - line * p.tpl) * BM, line % p.N, line / p.N};
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 gate_out_tc(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUtensorMap map_o,
@@ -1150,14 +1163,14 @@ gate_out_tc(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ C
       for (int it = 0; it < my_tiles; ++it) {
         const int b = it & 1;
         if (it >= 2 && !wait_or_abort(&bars->in_empty[b], ((it >> 1) - 1) & 1, ab)) break;
-        const int row = (p.tile0 + blockIdx.x + it * gridDim.x) * BM;
+        const TileAt at = tile_at(p, p.tile0 + blockIdx.x + it * gridDim.x);
         uint8_t* gs = smem + OFF_G + b * T_BYTES;
         uint8_t* os = smem + OFF_O + b * T_BYTES;
         tc::mbar_arrive_expect_tx(&bars->in_full[b], 2 * T_BYTES);
-        tc::tma_load_2d(gs, &map_g, &bars->in_full[b], 0, row);
-        tc::tma_load_2d(gs + 16384, &map_g, &bars->in_full[b], 64, row);
-        tc::tma_load_2d(os, &map_o, &bars->in_full[b], 0, row);
-        tc::tma_load_2d(os + 16384, &map_o, &bars->in_full[b], 64, row);
+        tc::tma_load_4d(gs, &map_g, &bars->in_full[b], 0, at.x, at.y, at.z);
+        tc::tma_load_4d(gs + 16384, &map_g, &bars->in_full[b], 64, at.x, at.y, at.z);
+        tc::tma_load_4d(os, &map_o, &bars->in_full[b], 0, at.x, at.y, at.z);
+        tc::tma_load_4d(os + 16384, &map_o, &bars->in_full[b], 64, at.x, at.y, at.z);
         issued = it + 1;
       }
     }
@@ -1212,7 +1225,8 @@ gate_out_tc(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ C
   } else if (warp < 8) {
     // ---------------- epilogue: cell row = TMEM lane of this warp's quarter;
     // each 32-row x 32-channel chunk leaves through a swizzled staging tile and
-    // one TMA store (rows past the last cell are clipped by the tensor bounds).
+    // one TMA store (rows past the last cell, or past the end of a column, are
+    // clipped by the tensor bounds).
     const int q4 = warp & 3;
     uint8_t* const stg0 = smem + OFF_STG + q4 * 2 * STG_BYTES;
     int nst = 0;                                  // TMA stores issued by this warp
@@ -1220,7 +1234,7 @@ gate_out_tc(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ C
       const int b = it & 1;
       if (!warp_wait_or_abort(&bars->acc_full[b], (it >> 1) & 1, ab)) break;
       tc::tc_fence_after();
-      const int row0 = (p.tile0 + blockIdx.x + it * gridDim.x) * BM + q4 * 32;
+      const TileAt at = tile_at(p, p.tile0 + blockIdx.x + it * gridDim.x);
       // Chunk ch + 1 is loaded from TMEM while chunk ch is converted and stored.
       uint32_t accb[2][32];
       tc::tmem_ld32(tc::tmem_addr(tmem, q4 * 32, b * 128), accb[0]);
@@ -1246,7 +1260,7 @@ gate_out_tc(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ C
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tc::tma_store_2d(&map_out, stg, ch * 32, row0);
+          tc::tma_store_4d(&map_out, stg, ch * 32, at.x + q4 * 32, at.y, at.z);
           tc::tma_store_commit();
         }
         ++nst;
@@ -1323,15 +1337,34 @@ bool map_lines(CUtensorMap* m, const void* base, int B, int N, int box_x, bool e
                   CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-// The host-buffer forward moves x and out in 4 to kHostChunks chunks (about
-// 16 MB of x each, measured best); its events are start, mask copied, one per
-// x chunk copied, one per out chunk formed, done.
-constexpr int kHostChunks = 8;
+// K3's view of a (B, N, N, 128) bf16 activation as (channel, x, y, z): in cell
+// order (x = cell, y = z = 0) or by columns (x = grid row i, y = column j,
+// z = batch b). Box: box_ch channels x box_x positions along x.
+bool map_k3(CUtensorMap* m, const void* base, const tri_attn_s* t, bool cols, int box_ch,
+            int box_x, CUtensorMapSwizzle swz) {
+  const cuuint64_t cell = 256, row = (cuuint64_t)t->N * 256, cells = (cuuint64_t)t->cells;
+  const cuuint64_t dims_flat[4] = {128, cells, 1, 1}, strides_flat[3] = {cell, cell * cells,
+                                                                         cell * cells};
+  const cuuint64_t dims_cols[4] = {128, (cuuint64_t)t->N, (cuuint64_t)t->N, (cuuint64_t)t->B};
+  const cuuint64_t strides_cols[3] = {row, cell, row * (cuuint64_t)t->N};
+  cuuint32_t box[4] = {(cuuint32_t)box_ch, (cuuint32_t)box_x, 1, 1};
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, cols ? dims_cols : dims_flat,
+                  cols ? strides_cols : strides_flat, box, swz);
+}
+
+// The host-buffer forward moves x in 4 to kXChunks chunks (about 16 MB each,
+// measured best) and K2, K3 and out in up to kHostChunks chunks; its events
+// are start, mask copied, one per x chunk copied, one per out chunk formed,
+// done.
+constexpr int kXChunks = 8;
+constexpr int kHostChunks = 12;
 constexpr int kHostEvents = 3 + 2 * kHostChunks;
 
 struct TcState {
   k1::Consts consts;                        // LayerNorm / gate-bias / pair-bias weights (fp32)
-  CUtensorMap map_w, map_q, map_k, map_v, map_b, map_g, map_o, map_wo;
+  CUtensorMap map_w, map_q, map_k, map_v, map_b, map_wo;
+  CUtensorMap map_g, map_o;                // K3 loads, cell-order tiles
+  CUtensorMap map_gc, map_oc;              // K3 loads, column tiles
   CUtensorMap st_q, st_k, st_v, st_g;      // K1 output stores: (cells, 128) bf16, 32 x 32 boxes
   CUtensorMap map_os;                      // K2 output stores: one head x 32 queries of a row
   unsigned char* row_any;    // (B*N) mask rows keeping some key
@@ -1421,7 +1454,8 @@ cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const voi
     ok = ok && make_map(&st->map_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, t->bias, dims, strides,
                         box, CU_TENSOR_MAP_SWIZZLE_128B);
   }
-  ok = ok && map_rows_bf16(&st->map_g, t->g, cells, 128);
+  ok = ok && map_k3(&st->map_g, t->g, t, false, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && map_k3(&st->map_gc, t->g, t, true, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   {
     void* outs[4] = {t->q, t->k, t->v, t->g};
     CUtensorMap* maps[4] = {&st->st_q, &st->st_k, &st->st_v, &st->st_g};
@@ -1433,7 +1467,8 @@ cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const voi
                     CU_TENSOR_MAP_SWIZZLE_64B);
     }
   }
-  ok = ok && map_rows_bf16(&st->map_o, t->o, cells, 128);
+  ok = ok && map_k3(&st->map_o, t->o, t, false, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && map_k3(&st->map_oc, t->o, t, true, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && map_rows_bf16(&st->map_wo, t->w_out, 128, 128);
   if (!ok) return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(k1::ln_proj_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, k1::SMEM);
@@ -1505,17 +1540,17 @@ cudaError_t launch_mask(tri_attn_s* t, cudaStream_t s, const int32_t* mask, int&
 int k2_row_groups(const tri_attn_s* t) { return (t->N + k2::R - 1) / k2::R; }
 int k2_units_per_group(const tri_attn_s* t) { return t->h * ((t->N + k2::BQ - 1) / k2::BQ); }
 
-// K2 over the units of the (b, row group) pairs g0 .. g0 + ng - 1 (row groups
-// counted across the batch).
-cudaError_t launch_k2(tri_attn_s* t, cudaStream_t s, int g0, int ng) {
+// K2 over units u0 .. u0 + nu - 1 (any range; the units of one (b, row group)
+// pair are consecutive).
+cudaError_t launch_k2(tri_attn_s* t, cudaStream_t s, int u0, int nu) {
   TcState* st = (TcState*)t->tc;
   const int N = t->N, h = t->h;
   k2::Params p2;
   p2.B = t->B; p2.N = N; p2.h = h; p2.mask_mode = t->mask_mode;
   p2.row_groups = k2_row_groups(t);
   p2.jtiles = (N + k2::BQ - 1) / k2::BQ;
-  p2.unit0 = g0 * k2_units_per_group(t);
-  p2.units = ng * k2_units_per_group(t);
+  p2.unit0 = u0;
+  p2.units = nu;
   p2.words = st->words;
   p2.mbits = st->mbits; p2.row_any = st->row_any;
   p2.dev_err = t->dev_err;
@@ -1534,25 +1569,27 @@ cudaError_t launch_k2(tri_attn_s* t, cudaStream_t s, int g0, int ng) {
   return cudaGetLastError();
 }
 
-// Store map of a (cells, 128) bf16 output: 32 x 32 boxes.
-bool map_out_rows(CUtensorMap* m, void* out, long long cells) {
-  cuuint64_t dims[2] = {128, (cuuint64_t)cells};
-  cuuint64_t strides[1] = {256};
-  cuuint32_t box[2] = {32, 32};
-  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, dims, strides, box,
-                  CU_TENSOR_MAP_SWIZZLE_64B);
+// Store map of K3's bf16 output (cell order or by columns): 32 x 32 boxes.
+bool map_out_k3(CUtensorMap* m, void* out, const tri_attn_s* t, bool cols) {
+  return map_k3(m, out, t, cols, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-// K3 over tiles tile0 .. tile0 + n - 1.
+// K3's tiles per grid column in column order.
+int k3_tiles_per_col(const tri_attn_s* t) { return (t->N + k3::BM - 1) / k3::BM; }
+
+// K3 over tiles tile0 .. tile0 + n - 1, in cell order or in column order
+// (map_out made with the same order).
 cudaError_t launch_k3(tri_attn_s* t, cudaStream_t s, const CUtensorMap& map_out, int tile0,
-                      int n) {
+                      int n, bool cols) {
   TcState* st = (TcState*)t->tc;
   k3::Params p3;
   p3.cells = t->cells; p3.ntiles = n; p3.tile0 = tile0; p3.bo = t->bo;
+  p3.cols = cols ? 1 : 0; p3.N = t->N; p3.tpl = k3_tiles_per_col(t);
   p3.dev_err = t->dev_err; p3.polls = t->wait_limit;
   const int grid = n < st->num_sms ? n : st->num_sms;
-  k3::gate_out_tc<<<grid, k3::kThreads, k3::SMEM, s>>>(st->map_g, st->map_o, st->map_wo,
-                                                       map_out, p3);
+  k3::gate_out_tc<<<grid, k3::kThreads, k3::SMEM, s>>>(cols ? st->map_gc : st->map_g,
+                                                       cols ? st->map_oc : st->map_o,
+                                                       st->map_wo, map_out, p3);
   return cudaGetLastError();
 }
 
@@ -1562,25 +1599,28 @@ cudaError_t tri_tc_forward(tri_attn_s* t, cudaStream_t s, const void* x, const i
                            void* out) {
   const int ntiles = num_tiles(t);
   CUtensorMap map_x, map_out;
-  if (!map_rows_bf16(&map_x, x, t->cells, 128) || !map_out_rows(&map_out, out, t->cells))
+  if (!map_rows_bf16(&map_x, x, t->cells, 128) || !map_out_k3(&map_out, out, t, false))
     return cudaErrorInvalidValue;
   int mark = 0;
   tri_mark(t, s, mark++, nullptr);
   cudaError_t e = launch_k1(t, s, map_x, mask, 0, ntiles);
   tri_mark(t, s, mark++, "ln_proj_tc");
   if (e == cudaSuccess) e = launch_mask(t, s, mask, mark);
-  if (e == cudaSuccess) e = launch_k2(t, s, 0, t->B * k2_row_groups(t));
+  if (e == cudaSuccess) e = launch_k2(t, s, 0, t->B * k2_row_groups(t) * k2_units_per_group(t));
   tri_mark(t, s, mark++, "row_attn_tc");
-  if (e == cudaSuccess) e = launch_k3(t, s, map_out, 0, ntiles);
+  if (e == cudaSuccess) e = launch_k3(t, s, map_out, 0, ntiles, false);
   tri_mark(t, s, mark++, "gate_out_tc");
   return e;
 }
 
-// Host buffers in and out, pipelined: x arrives in chunks on a copy stream
-// while K1 works on the chunks already on the device; K2 then runs in chunks
-// of row groups, and after each chunk K3 forms the out tiles of its finished
-// rows, which are copied back while the next chunk runs. dx, dmask, dout are
-// the handle's device staging buffers.
+// Host buffers in and out, pipelined. x arrives in chunks on a copy stream
+// while K1 works on the chunks already on the device (the mask summary runs
+// first, during the first copy). Every line's attention needs the whole bias
+// plane, so K2 starts after the last K1 chunk; it then runs in chunks of line
+// groups, and after each chunk K3 forms the out tiles of the finished lines,
+// which are copied back while the next chunk runs: grid rows for the starting
+// node, grid columns (a strided copy per batch) for the ending node. dx, dmask,
+// dout are the handle's device staging buffers.
 cudaError_t tri_tc_forward_host(tri_attn_s* t, cudaStream_t s, const void* xh,
                                 const int32_t* maskh, void* outh, void* dx, int32_t* dmask,
                                 void* dout) {
@@ -1593,14 +1633,15 @@ cudaError_t tri_tc_forward_host(tri_attn_s* t, cudaStream_t s, const void* xh,
       e = cudaEventCreateWithFlags(&st->ev[i], cudaEventDisableTiming);
     if (e != cudaSuccess) return e;
   }
+  const bool cols = t->ending;
   const int ntiles = num_tiles(t);
   const size_t row_bytes = (size_t)t->D * 2;
   const long long want = std::min<long long>(
-      kHostChunks, std::max<long long>(4, (long long)(t->cells * row_bytes >> 24)));
+      kXChunks, std::max<long long>(4, (long long)(t->cells * row_bytes >> 24)));
   const int nch = (int)std::min<long long>(ntiles, want);
   const int per = (ntiles + nch - 1) / nch;
   CUtensorMap map_x, map_out;
-  if (!map_rows_bf16(&map_x, dx, t->cells, 128) || !map_out_rows(&map_out, dout, t->cells))
+  if (!map_rows_bf16(&map_x, dx, t->cells, 128) || !map_out_k3(&map_out, dout, t, cols))
     return cudaErrorInvalidValue;
   cudaEvent_t* ev = st->ev;          // [0] start, [1] mask in, [2 ..] x chunks in, out chunks done
   cudaEvent_t* ev_x = ev + 2;
@@ -1622,56 +1663,87 @@ cudaError_t tri_tc_forward_host(tri_attn_s* t, cudaStream_t s, const void* xh,
                         (size_t)(c1 - c0) * row_bytes, cudaMemcpyHostToDevice, st->copy_in);
     if (e == cudaSuccess) e = cudaEventRecord(ev_x[i], st->copy_in);
   }
+  int mark = 0;
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev[1], 0);
+  if (e == cudaSuccess) e = launch_mask(t, s, dmask, mark);
   for (int i = 0; i < nch && e == cudaSuccess; ++i) {
     const int t0 = i * per, n = std::min(per, ntiles - t0);
     if (n <= 0) break;
     e = cudaStreamWaitEvent(s, ev_x[i], 0);
     if (e == cudaSuccess) e = launch_k1(t, s, map_x, dmask, t0, n);
   }
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev[1], 0);
-  int mark = 0;
-  if (e == cudaSuccess) e = launch_mask(t, s, dmask, mark);
-  // K3 over tiles lo .. hi - 1, then their out leaves on the copy-out stream.
-  int n_out = 0;
-  auto emit = [&](int lo, int hi) {
-    if (e != cudaSuccess || hi <= lo || n_out >= kHostChunks) return;
-    e = launch_k3(t, s, map_out, lo, hi - lo);
-    if (e == cudaSuccess) e = cudaEventRecord(ev_o[n_out], s);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(st->copy_out, ev_o[n_out], 0);
-    const long long c0 = (long long)lo * 128, c1 = std::min((long long)hi * 128, t->cells);
-    if (e == cudaSuccess)
-      e = cudaMemcpyAsync((char*)outh + c0 * row_bytes, (const char*)dout + c0 * row_bytes,
-                          (size_t)(c1 - c0) * row_bytes, cudaMemcpyDeviceToHost, st->copy_out);
-    ++n_out;
-  };
+  // K2 chunk boundaries in work units, in whole waves of CTAs (a partial wave
+  // takes as long as a full one). The first chunk is small (one wave, or 1/48
+  // of the work) so that the copy back starts early; each later one is about
+  // 1.3 times the one before, so that K2 (about 0.7 of the copy-back time per
+  // line at N = 768) keeps ahead of the copy stream, up to 1/6 of the work, so
+  // that little of the copy back is left once K2 ends where K2 is the slower
+  // side (large N); the last takes what is left. A chunk finishes the lines of
+  // the row groups whose units it completes.
   const int groups = t->B * k2_row_groups(t);
-  if (t->ending) {
-    // K2's lines are columns here, so no row of out is done before K2 ends:
-    // one K2 launch, then K3 and the copies in chunks.
-    if (e == cudaSuccess) e = launch_k2(t, s, 0, groups);
-    for (int i = 0; i < nch; ++i) emit(std::min(i * per, ntiles), std::min((i + 1) * per, ntiles));
-  } else {
-    // K2 in chunks of row groups; after each, K3 forms the 128-cell tiles whose
-    // rows are all done, and their out leaves while the next chunk runs.
-    const int gch = groups < nch ? groups : nch;
-    const int gper = (groups + gch - 1) / gch;
-    const int rgs = k2_row_groups(t);
-    const long long NN = (long long)t->N * t->N;
-    int tile_done = 0;
-    for (int i = 0; i < gch && e == cudaSuccess; ++i) {
-      const int g0 = i * gper, ng = std::min(gper, groups - g0);
-      if (ng <= 0) break;
-      e = launch_k2(t, s, g0, ng);
-      // grid rows (b, i) before the chunk's end are consecutive cells
-      const int gend = g0 + ng;
-      const long long bend = gend / rgs;
-      const long long rend = std::min((long long)(gend % rgs) * k2::R, (long long)t->N);
-      const long long cells_done = std::min(bend * NN + rend * t->N, t->cells);
-      const int tile_end = gend == groups ? ntiles : (int)(cells_done / 128);
-      if (tile_end > tile_done) {
-        emit(tile_done, tile_end);
-        tile_done = tile_end;
+  const int upg = k2_units_per_group(t);
+  const int units = groups * upg;
+  const int wave = st->num_sms;
+  int bound[kHostChunks + 1];
+  int nk2 = 0;
+  {
+    const int cap = std::max(1, (units + 6 * wave - 1) / (6 * wave));
+    double waves = std::max(1, (units + 48 * wave - 1) / (48 * wave));
+    bound[0] = 0;
+    while (bound[nk2] < units) {
+      const int left = units - bound[nk2];
+      const int w = std::max(1, std::min(cap, (int)(waves + 0.5)));
+      const int take = nk2 == kHostChunks - 1 ? left : std::min(left, w * wave);
+      bound[nk2 + 1] = bound[nk2] + take;
+      ++nk2;
+      waves *= 1.3;
+    }
+  }
+  // Lines (b, a), counted as b * N + a, that the groups before group g cover.
+  const int rgs = k2_row_groups(t);
+  auto lines_before = [&](int g) -> long long {
+    if (g >= groups) return (long long)t->B * t->N;
+    return (long long)(g / rgs) * t->N + std::min((g % rgs) * k2::R, t->N);
+  };
+  const long long NN = (long long)t->N * t->N;
+  const int tpl = k3_tiles_per_col(t);
+  long long lines_done = 0;
+  int tile_done = 0;
+  for (int i = 0; i < nk2 && e == cudaSuccess; ++i) {
+    e = launch_k2(t, s, bound[i], bound[i + 1] - bound[i]);
+    const long long lend = lines_before(bound[i + 1] / upg);
+    if (e != cudaSuccess || lend <= lines_done) continue;
+    if (cols) {
+      // Column tiles of the finished columns, then one strided copy per batch.
+      e = launch_k3(t, s, map_out, (int)(lines_done * tpl), (int)((lend - lines_done) * tpl), true);
+      if (e == cudaSuccess) e = cudaEventRecord(ev_o[i], s);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(st->copy_out, ev_o[i], 0);
+      const size_t pitch = (size_t)t->N * row_bytes;
+      for (long long b = lines_done / t->N; b * t->N < lend && e == cudaSuccess; ++b) {
+        const long long j0 = std::max(lines_done - b * t->N, 0LL);
+        const long long j1 = std::min(lend - b * t->N, (long long)t->N);
+        const size_t off = (size_t)(b * NN + j0) * row_bytes;
+        e = cudaMemcpy2DAsync((char*)outh + off, pitch, (const char*)dout + off, pitch,
+                              (size_t)(j1 - j0) * row_bytes, (size_t)t->N,
+                              cudaMemcpyDeviceToHost, st->copy_out);
       }
+      lines_done = lend;
+    } else {
+      // Cell-order tiles whose grid rows are all finished (the last chunk
+      // takes the rest), then one contiguous copy.
+      const int tile_end = lend == (long long)t->B * t->N
+                               ? ntiles : (int)(std::min(lend * t->N, t->cells) / 128);
+      lines_done = lend;
+      if (tile_end <= tile_done) continue;
+      e = launch_k3(t, s, map_out, tile_done, tile_end - tile_done, false);
+      if (e == cudaSuccess) e = cudaEventRecord(ev_o[i], s);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(st->copy_out, ev_o[i], 0);
+      const long long c0 = (long long)tile_done * 128;
+      const long long c1 = std::min((long long)tile_end * 128, t->cells);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync((char*)outh + c0 * row_bytes, (const char*)dout + c0 * row_bytes,
+                            (size_t)(c1 - c0) * row_bytes, cudaMemcpyDeviceToHost, st->copy_out);
+      tile_done = tile_end;
     }
   }
   // s finishes only once the last chunk of out is on the host.

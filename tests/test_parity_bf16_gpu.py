@@ -143,17 +143,19 @@ def test_bf16_large_grid_sampled_rows():
     assert np.all(np.isfinite(got))
 
 
-@pytest.mark.parametrize("B,mode", [(2, 1), (1, 0), (1, 2)])
-def test_bf16_forward_host_pipelined_matches_device(B, mode):
+@pytest.mark.parametrize("B,N,mode", [(2, 129, 1), (1, 129, 0), (1, 129, 2), (2, 129, 2),
+                                      (2, 129, 3), (1, 300, 2)])
+def test_bf16_forward_host_pipelined_matches_device(B, N, mode):
     """The host-buffer entry point moves x in four chunks overlapped with the
-    first kernel, runs the attention kernel in four chunks of row groups (a
-    chunk boundary inside the second batch entry when B = 2) and copies each
-    chunk's finished rows back while the next runs; for the ending node the
-    attention runs whole and the output leaves in four chunks. 131 or 262
-    tiles, the last one ragged; in query-key mode the first kernel also reads
-    the mask, which must have landed. The result must equal the device-buffer
-    forward bit for bit."""
-    w = W.custom(B, 129, 128, 4, "bf16", "bernoulli", seed=43)
+    first kernel, then runs the attention kernel in chunks of line groups (six
+    or seven here, a boundary inside the second batch entry when B = 2) and
+    copies each chunk's finished lines back while the next runs: grid rows in
+    cell order for the starting node; for the ending node grid columns, formed
+    by the output kernel in column-ordered tiles (ragged at the column's end:
+    129 or 300 rows) and copied back with one strided copy per batch entry. In
+    query-key mode the first kernel also reads the mask, which must have
+    landed. The result must equal the device-buffer forward bit for bit."""
+    w = W.custom(B, N, 128, 4, "bf16", "bernoulli", seed=43)
     inp = W.make_inputs(w)
     mod = tb.TriangularAttention(w.B, w.N, w.D, w.h, tb.TRI_ATTN_BF16, mode, H.device_params(inp, w))
     try:
