@@ -1672,33 +1672,19 @@ cudaError_t tri_tc_forward_host(tri_attn_s* t, cudaStream_t s, const void* xh,
     e = cudaStreamWaitEvent(s, ev_x[i], 0);
     if (e == cudaSuccess) e = launch_k1(t, s, map_x, dmask, t0, n);
   }
-  // K2 chunk boundaries in work units, in whole waves of CTAs (a partial wave
-  // takes as long as a full one). The first chunk is small (one wave, or 1/48
-  // of the work) so that the copy back starts early; each later one is about
-  // 1.3 times the one before, so that K2 (about 0.7 of the copy-back time per
-  // line at N = 768) keeps ahead of the copy stream, up to 1/6 of the work, so
-  // that little of the copy back is left once K2 ends where K2 is the slower
-  // side (large N); the last takes what is left. A chunk finishes the lines of
-  // the row groups whose units it completes.
+  // K2 chunk boundaries in work units: up to eight equal chunks of whole
+  // waves of CTAs (a partial wave takes as long as a full one), the last
+  // taking what is left. Each chunk adds a K2 ramp and a K3 launch (~20 us at
+  // N = 768) to the K2 -> K3 chain on s, which runs about as fast as the copy
+  // back, so a short first chunk gains nothing (a timeline of one-wave-first
+  // chunks growing 1.3 times showed the copy stream waiting on that chain). A
+  // chunk finishes the lines of the row groups whose units it completes.
   const int groups = t->B * k2_row_groups(t);
   const int upg = k2_units_per_group(t);
   const int units = groups * upg;
   const int wave = st->num_sms;
-  int bound[kHostChunks + 1];
-  int nk2 = 0;
-  {
-    const int cap = std::max(1, (units + 6 * wave - 1) / (6 * wave));
-    double waves = std::max(1, (units + 48 * wave - 1) / (48 * wave));
-    bound[0] = 0;
-    while (bound[nk2] < units) {
-      const int left = units - bound[nk2];
-      const int w = std::max(1, std::min(cap, (int)(waves + 0.5)));
-      const int take = nk2 == kHostChunks - 1 ? left : std::min(left, w * wave);
-      bound[nk2 + 1] = bound[nk2] + take;
-      ++nk2;
-      waves *= 1.3;
-    }
-  }
+  const int chunk = wave * std::max(1, (units + 8 * wave - 1) / (8 * wave));
+  const int nk2 = (units + chunk - 1) / chunk;
   // Lines (b, a), counted as b * N + a, that the groups before group g cover.
   const int rgs = k2_row_groups(t);
   auto lines_before = [&](int g) -> long long {
@@ -1710,8 +1696,9 @@ cudaError_t tri_tc_forward_host(tri_attn_s* t, cudaStream_t s, const void* xh,
   long long lines_done = 0;
   int tile_done = 0;
   for (int i = 0; i < nk2 && e == cudaSuccess; ++i) {
-    e = launch_k2(t, s, bound[i], bound[i + 1] - bound[i]);
-    const long long lend = lines_before(bound[i + 1] / upg);
+    const int u0 = i * chunk, u1 = std::min(units, u0 + chunk);
+    e = launch_k2(t, s, u0, u1 - u0);
+    const long long lend = lines_before(u1 / upg);
     if (e != cudaSuccess || lend <= lines_done) continue;
     if (cols) {
       // Column tiles of the finished columns, then one strided copy per batch.

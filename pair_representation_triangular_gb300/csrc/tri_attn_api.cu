@@ -272,7 +272,7 @@ int tri_attn_forward_host(tri_attn_t t, void* stream, const void* pair_repr_host
     t->bytes_owned += 2 * xbytes + mbytes;
   }
   if (t->dtype == TRI_ATTN_BF16 && !t->simt && !t->timing) {
-    // Copies overlapped with the first and last kernels (chunked).
+    // Copies overlapped with the kernels (chunked).
     e = tri_tc_forward_host(t, s, pair_repr_host, pair_mask_host, out_host, t->stage_x,
                             t->stage_mask, t->stage_out);
     if (e != cudaSuccess) return cuda_status(e);

@@ -147,8 +147,9 @@ def test_bf16_large_grid_sampled_rows():
                                       (2, 129, 3), (1, 300, 2)])
 def test_bf16_forward_host_pipelined_matches_device(B, N, mode):
     """The host-buffer entry point moves x in four chunks overlapped with the
-    first kernel, then runs the attention kernel in chunks of line groups (six
-    or seven here, a boundary inside the second batch entry when B = 2) and
+    first kernel, then runs the attention kernel in chunks of whole waves of
+    its work units (three to eight here, one spanning both batch entries when
+    B = 2; a chunk finishes the lines of the row groups it completes) and
     copies each chunk's finished lines back while the next runs: grid rows in
     cell order for the starting node; for the ending node grid columns, formed
     by the output kernel in column-ordered tiles (ragged at the column's end:
