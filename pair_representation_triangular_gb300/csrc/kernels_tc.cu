@@ -1736,5 +1736,12 @@ cudaError_t tri_tc_forward_host(tri_attn_s* t, cudaStream_t s, const void* xh,
   // s finishes only once the last chunk of out is on the host.
   if (e == cudaSuccess) e = cudaEventRecord(ev_done, st->copy_out);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_done, 0);
+  if (e != cudaSuccess) {
+    // Copies already queued may still read or write the caller's host buffers:
+    // let them finish before the error reaches the caller.
+    cudaStreamSynchronize(st->copy_in);
+    cudaStreamSynchronize(st->copy_out);
+    cudaStreamSynchronize(s);
+  }
   return e;
 }

@@ -281,11 +281,17 @@ int tri_attn_forward_host(tri_attn_t t, void* stream, const void* pair_repr_host
   e = cudaMemcpyAsync(t->stage_x, pair_repr_host, xbytes, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(t->stage_mask, pair_mask_host, mbytes, cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess) return cuda_status(e);
-  int st = tri_attn_forward(t, stream, t->stage_x, t->stage_mask, t->stage_out);
-  if (st) return st;
-  e = cudaMemcpyAsync(out_host, t->stage_out, xbytes, cudaMemcpyDeviceToHost, s);
-  if (e != cudaSuccess) return cuda_status(e);
+  int st = e == cudaSuccess ? tri_attn_forward(t, stream, t->stage_x, t->stage_mask, t->stage_out)
+                            : cuda_status(e);
+  if (st == TRI_ATTN_OK) {
+    e = cudaMemcpyAsync(out_host, t->stage_out, xbytes, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) st = cuda_status(e);
+  }
+  if (st != TRI_ATTN_OK) {
+    // Copies already queued may still touch the caller's host buffers.
+    cudaStreamSynchronize(s);
+    return st;
+  }
   return tri_attn_sync_check(t, stream);
 }
 
