@@ -44,3 +44,36 @@ def test_two_ranks_take_the_slowest_time():
 def test_single_process_is_unchanged():
     assert bench.max_over_ranks(3.5, "cpu") == 3.5
     assert bench.whole_job_rate(589824, 1, 1.0) == pytest.approx(589824e3)
+
+
+def test_traffic_hash_covers_the_kernels_and_not_the_host_pipeline():
+    """bench.py reports the captured DRAM traffic only while a hash of the
+    tensor-core kernel sources (comments removed) matches the capture's. The
+    host-buffer pipeline that closes kernels_tc.cu launches the same kernels for
+    the other entry point and is left out; any change to the kernels, their
+    device-buffer launches or the shared headers changes the hash."""
+    csrc = os.path.join(bench.ROOT, "pair_representation_triangular_gb300", "csrc")
+    src = {}
+    for name in bench.TRAFFIC_SOURCES:
+        with open(os.path.join(csrc, name)) as f:
+            src[name] = f.read()
+    base = bench.kernel_source_sha(src.__getitem__)
+    assert base == bench.kernel_source_sha()
+
+    def sha_with(name, text):
+        edited = dict(src)
+        edited[name] = text
+        return bench.kernel_source_sha(edited.__getitem__)
+
+    k = src["kernels_tc.cu"]
+    cut = k.index(bench.HOST_PIPELINE_START)
+    assert sha_with("kernels_tc.cu", k + "\nstatic int after_the_pipeline = 1;\n") == base
+    assert sha_with("kernels_tc.cu", k[:cut] + k[cut:].replace("8 * wave", "6 * wave")) == base
+    assert sha_with("kernels_tc.cu", "// a comment line\n" + k) == base
+    kernel_line = "constexpr int BM = 128;"
+    assert kernel_line in k[:cut]
+    assert sha_with("kernels_tc.cu", k.replace(kernel_line, "constexpr int BM = 64;", 1)) != base
+    launch = "launch_k3(t, s, map_out, 0, ntiles, false)"
+    assert launch in k[:cut]
+    assert sha_with("kernels_tc.cu", k.replace(launch, "launch_k3(t, s, map_out, 0, ntiles, true)", 1)) != base
+    assert sha_with("tc_ptx.cuh", src["tc_ptx.cuh"] + "\n#define ANOTHER 1\n") != base
