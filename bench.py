@@ -1,6 +1,8 @@
-"""Benchmark: forward passes of starting-node triangular self-attention on GB300.
+"""Benchmark: forward passes of triangular self-attention (starting node, or the
+ending node with --node ending) on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--node starting|ending] [--mask-mode 0|1] [--impl reference]
 
 One step is one full forward pass (LayerNorm + projections, row attention, gate +
 output projection) over one batch of seeded synthetic input, the default being
@@ -9,8 +11,8 @@ residues kept). Prints one JSON line (rank 0).
 
 value      pair-cells/s = B*N^2 / (device time per forward), inputs resident in
            HBM, L2 flushed (256 MB write) before every timed step.
-e2e        the same metric through tri_attn_forward_host: pageable->pinned
-           host buffers are reused; every step copies pair_repr and pair_mask
+e2e        the same metric through tri_attn_forward_host: pinned host buffers
+           (filled once) are reused; every step copies pair_repr and pair_mask
            host->device and the output device->host inside the timed region.
 roofline   the dominant kernel (largest share of device time) against its
            algorithmic bytes or FLOPs per launch.

@@ -4,7 +4,9 @@ Every function has the name and argument order of its C entry point; tensors
 are passed as device (or host) pointers taken from torch tensors, and the
 stream is a ``torch.cuda.Stream`` (or None for the current stream). No step of
 the computation runs here. If the library is missing or cannot be loaded, the
-first call raises ``TriAttnError``: there is no fallback path.
+first call raises ``RuntimeError`` (``OSError`` from ctypes for a library that
+does not load): there is no fallback path. Calls that the library refuses raise
+``TriAttnError`` with its status code.
 """
 from __future__ import annotations
 
@@ -251,7 +253,9 @@ class TriangularAttention:
         """Copy of an intermediate of the most recent forward (see
         tri_attn_debug_tensor): q, k, v, g, o as (B, N, N, D), bf16 on the
         tensor-core path (its raw bits reinterpreted) and fp32 on the SIMT path;
-        bias as (B, h, N, N) fp32 (stored in fp16 on the tensor-core path)."""
+        bias as (B, h, N, N) fp32. On the tensor-core path the plane is stored
+        in fp16 as log2(e) * bias, with -inf where the query-key mask drops a
+        key; it is returned as stored, widened to fp32."""
         ptr, ld = tri_attn_debug_tensor(self.handle, name)
         if not ptr:
             raise KeyError(name)
