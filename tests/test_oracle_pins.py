@@ -191,6 +191,28 @@ def pin_hand_worked_example():
             np.testing.assert_allclose(out[0, i, j], [0.5 * o0, -0.5 * o0], rtol=0, atol=1e-14)
 
 
+def pin_hand_worked_example_ending():
+    """The same 2 x 2 grid through the ending node, derived by hand in the
+    fixture: cell (i, j) attends along column j,
+    l[k] = sqrt(2) c0^2 s[i][j] s[k][j] + c0 s[k][i],
+    out[i,j] = 0.5 * sum_k softmax_k(l) s[k][j] c0 (1, -1). The signs are not
+    symmetric, so this differs from the starting node's result."""
+    with open(os.path.join(GOLDEN, "hand_worked_2x2.json")) as f:
+        ex = json.load(f)
+    s = ex["signs"]
+    x = np.array([[[[s[r][c], -s[r][c]] for c in range(2)] for r in range(2)]], np.float64)
+    P = {k: np.array(v, np.float64) for k, v in ex["params"].items()}
+    out = O.forward_ending(x, None, P, 1)
+    c0 = 1.0 / math.sqrt(1.0 + 1e-5)
+    for i in range(2):
+        for j in range(2):
+            l = [math.sqrt(2) * c0 * c0 * s[i][j] * s[k][j] + c0 * s[k][i] for k in range(2)]
+            z = sum(math.exp(a) for a in l)
+            o0 = sum(math.exp(l[k]) / z * s[k][j] * c0 for k in range(2))
+            np.testing.assert_allclose(out[0, i, j], [0.5 * o0, -0.5 * o0], rtol=0, atol=1e-14)
+    assert np.max(np.abs(out - O.forward(x, None, P, 1))) > 1e-2
+
+
 # --------------------------------------------------------- ending-node pins
 
 def _swap(a):
@@ -276,8 +298,9 @@ PINS = {f.__name__: f for f in (
     pin_n1_closed_form, pin_rows_sum_to_one, pin_all_ones_mask_is_no_mask,
     pin_relabelling_equivariance, pin_single_kept_key, pin_zero_query_weights,
     pin_mean_of_kept_values, pin_zero_value_weights, pin_torch_library_module,
-    pin_hand_worked_example, pin_ending_is_module_on_swapped_grid,
-    pin_ending_n1_closed_form, pin_ending_single_kept_key, pin_ending_zero_query_weights)}
+    pin_hand_worked_example, pin_hand_worked_example_ending,
+    pin_ending_is_module_on_swapped_grid, pin_ending_n1_closed_form,
+    pin_ending_single_kept_key, pin_ending_zero_query_weights)}
 
 
 @pytest.mark.parametrize("name", list(PINS))
