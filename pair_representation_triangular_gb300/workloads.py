@@ -1,4 +1,4 @@
-"""Seeded synthetic workloads for starting-node triangular self-attention.
+"""Seeded synthetic workloads for triangular self-attention (both node variants).
 
 This module only draws inputs. It holds none of the method's arithmetic, so both
 the CUDA path and the CPU oracle can take their inputs from it without sharing
