@@ -119,10 +119,14 @@ int tri_attn_forward(tri_attn_t t, void* stream, const void* pair_repr,
 
 /* The same forward pass on HOST buffers: copies pair_repr and pair_mask to the
  * device (into staging buffers the handle owns; allocated at the first call),
- * runs the forward pass and copies the result back into `out_host`, all on
- * `stream`, then synchronises `stream` and reports device-side errors like
- * tri_attn_sync_check. Host buffers should be page-locked for full copy speed;
- * pageable memory works but copies synchronously. */
+ * runs the forward pass and copies the result back into `out_host`, ordered
+ * after the work already queued on `stream`, then synchronises `stream` and
+ * reports device-side errors like tri_attn_sync_check. On the tensor-core path
+ * the copies run on two internal streams in chunks, overlapped with the
+ * kernels (rows of x in, finished lines of out back); the result is bit-for-bit
+ * that of tri_attn_forward. Host buffers should be page-locked for full copy
+ * speed; pageable memory works but copies synchronously. On an error return no
+ * copy that touches the host buffers is still running. */
 int tri_attn_forward_host(tri_attn_t t, void* stream, const void* pair_repr_host,
                           const int32_t* pair_mask_host, void* out_host);
 
