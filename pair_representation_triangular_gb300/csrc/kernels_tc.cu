@@ -23,7 +23,13 @@
 //                over S (mu: a lazily moved reference max); O += P V
 //                accumulates in TMEM. The (B, N, h, N, N) logits never exist.
 //   gate_out_tc  g * o formed in shared memory as the A operand of the output
-//                projection GEMM; the epilogue adds bo and stores bf16.
+//                projection GEMM; the epilogue adds bo and stores bf16. Tiles
+//                are 128 cells in memory order, or 128 rows of one grid
+//                column (the host-buffer forward of the ending node).
+//
+// The file ends with the host side: tensor maps, launchers, the device-buffer
+// forward and the host-buffer pipeline that overlaps the host copies with
+// chunks of the same kernels.
 //
 // Passages followed: POPCORNBENCH "Kimi-K2.6 l2_p6", forward op list steps
 // 1-18 and layer definitions; "FW-GLM-5-1 l2_p6", quoted Model.forward.
