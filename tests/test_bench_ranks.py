@@ -77,3 +77,45 @@ def test_traffic_hash_covers_the_kernels_and_not_the_host_pipeline():
     assert launch in k[:cut]
     assert sha_with("kernels_tc.cu", k.replace(launch, "launch_k3(t, s, map_out, 0, ntiles, true)", 1)) != base
     assert sha_with("tc_ptx.cuh", src["tc_ptx.cuh"] + "\n#define ANOTHER 1\n") != base
+
+
+def _run_bench(args, env=None, timeout=240):
+    import subprocess
+    import sys
+    full_env = dict(os.environ)
+    full_env.update(env or {})
+    return subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), *args],
+                          capture_output=True, text=True, timeout=timeout, env=full_env)
+
+
+def test_reference_arm_prints_one_contract_line():
+    """--impl reference times the CPU oracle on this host and prints exactly one
+    JSON line with the native arm's metric, unit and config, the oracle's own
+    cpu_baseline and an e2e block with no host<->device bytes."""
+    import json
+    r = _run_bench(["--impl", "reference", "--workload", "b2-n32-d64-h4-f32",
+                    "--steps", "2", "--warmup", "1"])
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference"
+    assert rec["metric"] == bench.METRIC and rec["unit"] == "pair-cells/s"
+    assert rec["value"] > 0 and rec["higher_is_better"] is True
+    assert (rec["n_gpus"], rec["steps"], rec["warmup"]) == (1, 2, 1)
+    assert rec["ms_per_step"] == pytest.approx(2 * 32 * 32 / rec["value"] * 1e3)
+    assert rec["config"]["workload"] == "b2-n32-d64-h4-f32"
+    cb = rec["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == rec["value"]
+    assert "rows" in cb["sample"]
+    assert rec["e2e"] == {"value": rec["value"], "unit": "pair-cells/s",
+                          "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    """Under torchrun only rank 0 runs the reference arm; the others exit 0
+    without output or work."""
+    r = _run_bench(["--impl", "reference", "--workload", "b2-n32-d64-h4-f32",
+                    "--steps", "1", "--warmup", "0"], env={"RANK": "1", "WORLD_SIZE": "2"})
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == ""
