@@ -119,3 +119,24 @@ def test_reference_arm_other_ranks_exit_quietly():
                     "--steps", "1", "--warmup", "0"], env={"RANK": "1", "WORLD_SIZE": "2"})
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_clock_summary_reports_median_and_throttle_reasons():
+    """The sampler's rows are nvidia-smi CSV fields (index, clocks.sm,
+    clocks.max.sm, power, active mask, hw_slowdown, hw_thermal_slowdown,
+    sw_thermal_slowdown, sw_power_cap); the summary gives the median SM clock,
+    the maximum clock and every throttle reason seen Active at least once."""
+    clk = bench.ClockSampler(0)
+    assert clk.summary()["reasons"] == ["clock sampling unavailable"]
+    idle = ["Not Active"] * 4
+    clk.rows = [["0", "2070", "2070", "700.1", "0x0", *idle],
+                ["0", "1980", "2070", "1390.0", "0x4", "Not Active", "Not Active", "Not Active",
+                 "Active"],
+                ["0", "2070", "2070", "900.0", "0x0", *idle],
+                ["0", "[N/A]", "2070", "900.0", "0x0", *idle]]
+    s = clk.summary()
+    assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 4
+    clk.rows.append(["0", "1500", "2070", "800.0", "0x8", "Active", "Not Active", "Active",
+                     "Not Active"])
+    assert clk.summary()["reasons"] == ["sw_power_cap", "hw_slowdown", "sw_thermal_slowdown"]
