@@ -1,0 +1,84 @@
+"""Resource checks of the tensor-core kernels from the compiler's own report
+(``nvcc -Xptxas -v``: register, stack and spill counts only). No kernel spills
+registers or uses a stack frame; every kernel's registers at launch fit its
+block on one SM; and the attention kernel's ``setmaxnreg`` split (control warps
+down, softmax warps up) adds up to no more than the registers its block was
+launched with, since a split above that would wait forever at ``setmaxnreg.inc``.
+Runs on the CPU: nvcc cross-compiles for sm_103a without a GPU."""
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+from pair_representation_triangular_gb300 import build as tbuild
+
+SRC = os.path.join(tbuild.CSRC, "kernels_tc.cu")
+REGS_PER_SM = 65536
+# Threads per block of each kernel (the kThreads of its namespace; 256 for the
+# mask summaries).
+THREADS = {"ln_proj_tc": 576, "row_attn_tc": 512, "gate_out_tc": 320,
+           "mask_summary": 256, "mask_summary_cols": 256}
+
+
+@pytest.fixture(scope="module")
+def report():
+    try:
+        cc = tbuild.nvcc()
+    except RuntimeError:
+        pytest.skip("nvcc not available")
+    with tempfile.TemporaryDirectory() as d:
+        r = subprocess.run([cc, *tbuild.ARCH, *tbuild.CFLAGS, "-Xptxas", "-v", "-c", SRC,
+                            "-o", os.path.join(d, "k.o")],
+                           capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-2000:]
+    kernels, cur = {}, None
+    for line in (r.stdout + r.stderr).splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            cur = m.group(1)
+            kernels[cur] = {}
+            continue
+        if cur is None:
+            continue
+        m = re.search(r"(\d+) bytes stack frame, (\d+) bytes spill stores, (\d+) bytes spill loads",
+                      line)
+        if m:
+            kernels[cur].update(stack=int(m[1]), spill_st=int(m[2]), spill_ld=int(m[3]))
+        m = re.search(r"Used (\d+) registers", line)
+        if m:
+            kernels[cur]["regs"] = int(m[1])
+    return kernels
+
+
+def _kernel(report, name):
+    """The report of kernel `name` (mangled as <length><name>E...)."""
+    hits = [v for k, v in report.items() if f"{len(name)}{name}E" in k]
+    assert len(hits) == 1, (name, list(report))
+    return hits[0]
+
+
+@pytest.mark.parametrize("name", list(THREADS))
+def test_no_spills_and_registers_fit(report, name):
+    k = _kernel(report, name)
+    assert k["stack"] == 0 and k["spill_st"] == 0 and k["spill_ld"] == 0, k
+    assert k["regs"] * THREADS[name] <= REGS_PER_SM, k
+
+
+def test_attention_register_split_fits_the_launch(report):
+    with open(SRC) as f:
+        src = f.read()
+    m = re.search(r"constexpr int kRegsCtl = (\d+), kRegsSoftmax = (\d+);", src)
+    assert m, "register split constants not found"
+    ctl, sm = int(m[1]), int(m[2])
+    # Roles: warps 0-3 (TMA producer, MMA issuers) lower to kRegsCtl, the other
+    # warps (three softmax warpgroups) raise to kRegsSoftmax.
+    assert re.search(r"if \(warp < 4\) \{\s*tc::regs_dec<kRegsCtl>\(\);", src)
+    assert re.search(r"\} else \{\s*//[^\n]*\n\s*tc::regs_inc<kRegsSoftmax>\(\);", src)
+    launch = _kernel(report, "row_attn_tc")["regs"]
+    warps = THREADS["row_attn_tc"] // 32
+    for n in (ctl, sm):
+        assert n % 8 == 0 and 24 <= n <= 256
+    assert ctl <= launch <= sm
+    assert 32 * (4 * ctl + (warps - 4) * sm) <= launch * THREADS["row_attn_tc"]
