@@ -1,9 +1,10 @@
-"""Resource checks of the tensor-core kernels from the compiler's own report
+"""Resource checks of the kernels from the compiler's own report
 (``nvcc -Xptxas -v``: register, stack and spill counts only). No kernel spills
 registers or uses a stack frame; every kernel's registers at launch fit its
 block on one SM; and the attention kernel's ``setmaxnreg`` split (control warps
 down, softmax warps up) adds up to no more than the registers its block was
 launched with, since a split above that would wait forever at ``setmaxnreg.inc``.
+The fp32 kernels of the two fp32 benchmark configurations do not spill either.
 Runs on the CPU: nvcc cross-compiles for sm_103a without a GPU."""
 import os
 import re
@@ -82,3 +83,35 @@ def test_attention_register_split_fits_the_launch(report):
         assert n % 8 == 0 and 24 <= n <= 256
     assert ctl <= launch <= sm
     assert 32 * (4 * ctl + (warps - 4) * sm) <= launch * THREADS["row_attn_tc"]
+
+
+F32_SRC = os.path.join(tbuild.CSRC, "kernels_f32.cu")
+# fp32 kernels of the two fp32 benchmark configurations (d = 16 and d = 32,
+# starting node; d = 32 ending node), by a unique piece of their mangled names.
+F32_SPILL_FREE = ("11ln_proj_f32E", "12gate_out_f32E", "row_attn_f32ILi16ELi32ELb0EE",
+                  "row_attn_f32ILi32ELi32ELb0EE", "row_attn_f32ILi32ELi32ELb1EE")
+
+
+def test_fp32_benchmark_kernels_do_not_spill():
+    try:
+        cc = tbuild.nvcc()
+    except RuntimeError:
+        pytest.skip("nvcc not available")
+    with tempfile.TemporaryDirectory() as d:
+        r = subprocess.run([cc, *tbuild.ARCH, *tbuild.CFLAGS, "-Xptxas", "-v", "-c", F32_SRC,
+                            "-o", os.path.join(d, "k.o")],
+                           capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-2000:]
+    spills, cur = {}, None
+    for line in (r.stdout + r.stderr).splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            cur = m.group(1)
+            continue
+        m = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", line)
+        if m and cur:
+            spills[cur] = int(m[1]) + int(m[2])
+    for key in F32_SPILL_FREE:
+        hits = [v for k, v in spills.items() if key in k]
+        assert len(hits) == 1, (key, list(spills))
+        assert hits[0] == 0, (key, hits[0])
