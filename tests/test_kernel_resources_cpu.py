@@ -1,5 +1,5 @@
 """Resource checks of the kernels from the compiler's own report
-(``nvcc -Xptxas -v``: register, stack and spill counts only). No kernel spills
+(``nvcc -Xptxas -v``: register, stack and spill counts only). No tensor-core kernel spills
 registers or uses a stack frame; every kernel's registers at launch fit its
 block on one SM; and the attention kernel's ``setmaxnreg`` split (control warps
 down, softmax warps up) adds up to no more than the registers its block was
