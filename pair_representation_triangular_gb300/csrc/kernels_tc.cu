@@ -191,6 +191,7 @@ struct Params {
   __half* bias;                // (B, h, N, Nb) fp16, scaled by log2(e)
   unsigned int* dev_err;
   long long polls;
+  float q_scale;               // q is stored times log2(e) / sqrt(d)
 };
 
 // Persistent: CTA c serves 128-cell tiles c, c + G, ... [Wq;Wk;Wv;Wg] (bf16,
@@ -423,6 +424,13 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
               const float z1 = __uint_as_float(acc[2 * e + 1]) + s_bg[cg + 1];
               packed[e] = tc::pack_bf16x2(sigmoid_approx(z0), sigmoid_approx(z1));
             }
+          } else if (sect == 0) {
+            // q leaves in the log2 domain of the attention's exponentials,
+            // scaled by log2(e) / sqrt(d) before its one rounding to bf16.
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              packed[e] = tc::pack_bf16x2(__uint_as_float(acc[2 * e]) * p.q_scale,
+                                          __uint_as_float(acc[2 * e + 1]) * p.q_scale);
           } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e)
@@ -477,45 +485,49 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
 // K2: flash row attention
 // ---------------------------------------------------------------------------
 namespace k2 {
-constexpr int R = 3;                    // rows i per work unit = softmax warpgroups
+constexpr int R = 3;                    // lines per work unit = softmax warpgroups
 constexpr int BQ = 128;                 // queries j per unit
-constexpr int BK = 64;                  // keys per tile
+constexpr int BK = 64;                  // keys per sub-tile (one S buffer)
+constexpr int KVK = 128;                // keys per K/V stage (two sub-tiles)
 constexpr int DH = 32;                  // head dim
-constexpr int STAGES = 3;
-constexpr int kIssuers = R;             // MMA issuer warps, one row each
-// Warpgroup 0: warp 0 TMA, warp 1 + r issues the MMAs of row r; warpgroup
-// w = 1..3 runs the softmax of row w - 1 of the unit. Registers move from the
-// control warpgroup to the softmax ones: 512 x 128 >= 128 x 48 + 384 x 152.
+constexpr int KV_STAGES = 2;
+constexpr int B_STAGES = 3;
+constexpr int kIssuers = R;             // MMA issuer warps, one line each
+constexpr int kSoftmaxWarps = 4 * R;
+// Warpgroup 0: warp 0 TMA, warp 1 + r issues the MMAs of line r (both roles
+// run as whole warps; one elected lane issues); warpgroup w = 1..3 runs the
+// softmax of line w - 1. Registers move from the control warpgroup to the
+// softmax ones: 512 x 128 >= 128 x 48 + 384 x 152.
 constexpr int kThreads = 512;
 constexpr int kRegsCtl = 48, kRegsSoftmax = 152;
-// TMEM per row: S0 | S1 (64 fp32 columns each) | O (32). Tile c's S lands in
-// buffer c & 1 and its P (bf16 pairs, 32 columns) is written over it; the MMA
-// thread issues P V(c) and then S(c + 2) into the same buffer, so the tensor
-// pipe's issue order keeps them apart and S(c + 1) is already waiting in the
-// other buffer while tile c's softmax runs.
+// TMEM per line: S0 | S1 (64 fp32 columns each) | O (32). Sub-tile c's S lands
+// in buffer c & 1 and its P (bf16 pairs, 32 columns) is written over it; the
+// MMA warp issues P V(c) and then S(c + 2) into the same buffer, so the tensor
+// pipe's issue order keeps them apart.
 constexpr int kTmemPerRow = 160;
 constexpr int TM_S1 = 64, TM_O = 128;
-constexpr uint32_t Q_BYTES = BQ * DH * 2;            // 8 KB per row
-constexpr uint32_t KV_BYTES = BK * DH * 2;           // 4 KB each of K and V
-constexpr uint32_t BIAS_BYTES = BQ * BK * 2;         // 16 KB fp16 bias tile
+constexpr uint32_t Q_BYTES = BQ * DH * 2;            // 8 KB per line
+constexpr uint32_t KVT_BYTES = KVK * DH * 2;         // 8 KB: K or V of one line, 128 keys
+constexpr uint32_t KV_STAGE = R * 2 * KVT_BYTES;     // 48 KB: [R] K then V
+constexpr uint32_t HALF_KV = BK * DH * 2;            // 4 KB: one sub-tile inside a K/V tile
+constexpr uint32_t BIAS_BYTES = BQ * BK * 2;         // 16 KB fp16 bias sub-tile
+constexpr uint32_t OST_BYTES = 32 * DH * 2;          // 2 KB o staging per softmax warp
 constexpr uint32_t OFF_Q = 0;                        // [2][R] Q tiles
-constexpr uint32_t STAGE_KV = R * 2 * KV_BYTES;      // [R] K then V
-constexpr uint32_t STAGE_BYTES = STAGE_KV + BIAS_BYTES;
-constexpr uint32_t OFF_STAGE = OFF_Q + 2 * R * Q_BYTES;
-// o of a unit leaves through one TMA store per softmax warp: 32 queries x one
-// head (64 bytes), staged with the 64-byte swizzle, two staging tiles per warp
-// so that a unit waits only for the store of two units before.
-constexpr uint32_t OST_BYTES = 32 * DH * 2;
-constexpr uint32_t OFF_OST = OFF_STAGE + STAGES * STAGE_BYTES;
-constexpr uint32_t OFF_BAR = OFF_OST + 2 * 3 * 4 * OST_BYTES;
+constexpr uint32_t OFF_KV = OFF_Q + 2 * R * Q_BYTES;
+constexpr uint32_t OFF_BIAS = OFF_KV + KV_STAGES * KV_STAGE;
+constexpr uint32_t OFF_OST = OFF_BIAS + B_STAGES * BIAS_BYTES;
+constexpr uint32_t OFF_BAR = OFF_OST + kSoftmaxWarps * OST_BYTES;
 constexpr uint32_t SMEM = OFF_BAR + 512 + 1024;
+static_assert(OFF_KV % 1024 == 0 && OFF_BIAS % 1024 == 0 && OFF_OST % 1024 == 0,
+              "swizzled tiles need 1024-byte alignment");
 
 struct Bars {
-  uint64_t q_full[2], q_empty[2], kv_full[STAGES], kv_empty[STAGES];
-  // s_ready and p_full follow the S/P buffer (tile parity): a warp with no live
-  // lanes runs ahead, and its arrivals for tile c + 1 must not complete the
-  // phase of tile c.
-  uint64_t s_ready[R][2], p_full[R][2], p_free[R][2], o_free[R], drain;
+  uint64_t q_full[2], q_empty[2], kv_full[KV_STAGES], kv_empty[KV_STAGES];
+  uint64_t b_full[B_STAGES], b_empty[B_STAGES];
+  // s_ready and p_full follow the S/P buffer (sub-tile parity): a warp with no
+  // live lanes runs ahead, and its arrivals for sub-tile c + 1 must not complete
+  // the phase of sub-tile c.
+  uint64_t s_ready[R][2], p_full[R][2], p_free[R][2], o_free[R], drain[R];
   uint32_t tmem_base;
   int abort;
 };
@@ -534,7 +546,13 @@ struct Params {
   const unsigned char* row_any;   // (B*N rows): the mask row keeps some key
   unsigned int* dev_err;
   long long polls;
-  float scale_log2;               // log2(e) / sqrt(d)
+  // The same q, k, v and bias plane as raw tensors, for the exact recomputation
+  // of a query row whose sums left the fp32 range: element (b, line a, position
+  // x, channel e) of q, k or v sits at b * sb + a * sl + x * sx + e.
+  const __nv_bfloat16 *q, *k, *v;
+  long long sb, sl, sx;
+  const __half* bias;             // (B, h, N, Nb) fp16, log2(e) * bias, -inf where dropped
+  int Nb;
 };
 
 struct Unit {
@@ -568,48 +586,78 @@ __device__ __forceinline__ void step_unit(Unit& u, const Params& p) {
   u.j0 = u.jt * BQ;
 }
 
-// Position of the tile stream of one MMA thread: global tile c, its unit ui,
-// key tile kt, stage s and the stage ring's phase, advanced without dividing.
-struct TileIt {
-  int c, ui, kt, s, sph;
+// Position in a stream of sub-tiles: global sub-tile c, its unit ui and key
+// sub-tile kt, the K/V stage slot and phase, and the bias slot and phase,
+// advanced without dividing.
+struct SubIt {
+  int c, ui, kt, kvs, kvph, bs, bph;
 };
-__device__ __forceinline__ void advance(TileIt& it, int KT) {
+__device__ __forceinline__ void advance(SubIt& it, int KT) {
   ++it.c;
+  const bool stage_end = (it.kt & 1) || it.kt == KT - 1;
   if (++it.kt == KT) { it.kt = 0; ++it.ui; }
-  if (++it.s == STAGES) { it.s = 0; it.sph ^= 1; }
+  if (stage_end && ++it.kvs == KV_STAGES) { it.kvs = 0; it.kvph ^= 1; }
+  if (++it.bs == B_STAGES) { it.bs = 0; it.bph ^= 1; }
 }
 
-// Real-key bits of word w (keys 32w..32w+31 of a tile with `left` keys left).
+// The softmax's position in its sub-tile stream: global sub-tile c, key
+// sub-tile kt and the bias slot and phase.
+struct SoftIt {
+  int c, kt, bs, bph;
+};
+__device__ __forceinline__ void advance(SoftIt& it, int KT) {
+  ++it.c;
+  if (++it.kt == KT) it.kt = 0;
+  if (++it.bs == B_STAGES) { it.bs = 0; it.bph ^= 1; }
+}
+
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// Real-key bits of word w (keys 32w..32w+31 of a sub-tile with `left` keys left).
 __device__ __forceinline__ uint32_t real_bits(int left, int w) {
   const int n = left - 32 * w;
   return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
 }
 
-// P = 2^(S sc + bias - mu) of one 32-key half (keys 32 hf ..; bh = its 32 fp16
-// biases), packed in bf16 pairs, and its sum; a lane that is not live writes 1
-// on every real key of a uniform row or query (`w` = that half's real-key
-// bits), else 0.
-__device__ __forceinline__ float2 p_half(const float2 (&x2)[BK / 2], const uint4 (&bh)[4], int hf,
-                                         float2 sc2, float mu, bool live, uint32_t w,
-                                         uint32_t (&pk)[16]) {
+// The 32 fp16 biases of half hf of a sub-tile row (brow: the row's swizzled
+// base, 16-byte chunk q at brow ^ (q << 4)).
+__device__ __forceinline__ void load_bias_half(uint32_t brow, int hf, uint4 (&bh)[4]) {
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) bh[q4] = tc::lds128(brow ^ ((hf * 4 + q4) << 4));
+}
+
+// Common path of one 32-key half: P = 2^(S + bias) (S in log2 units, the
+// reference mu = 0 and every lane live), packed in bf16 pairs; returns the
+// sum of P in two partial sums.
+__device__ __forceinline__ float2 p_half_fast(const float2 (&x2)[BK / 2], const uint4 (&bh)[4],
+                                              int hf, uint32_t (&pk)[16]) {
   float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
-  if (live) {
-    const float2 nmu2 = make_float2(-mu, -mu);
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      const int q = hf * 4 + q4;
-      const uint32_t hw[4] = {bh[q4].x, bh[q4].y, bh[q4].z, bh[q4].w};
+  for (int q4 = 0; q4 < 4; ++q4) {
+    const uint32_t hw[4] = {bh[q4].x, bh[q4].y, bh[q4].z, bh[q4].w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 y = __ffma2_rn(x2[q * 4 + e], sc2, nmu2);
-        const float2 p2 = make_float2(ex2_approx(add_f16lo_f32(hw[e], y.x)),
-                                      ex2_approx(add_f16hi_f32(hw[e], y.y)));
-        if (e & 1) sb = __fadd2_rn(sb, p2);
-        else sa = __fadd2_rn(sa, p2);
-        pk[q4 * 4 + e] = tc::pack_bf16x2(p2.x, p2.y);
-      }
+    for (int e = 0; e < 4; ++e) {
+      const float2 x = x2[(hf * 4 + q4) * 4 + e];
+      const float2 p2 = make_float2(ex2_approx(add_f16lo_f32(hw[e], x.x)),
+                                    ex2_approx(add_f16hi_f32(hw[e], x.y)));
+      if (e & 1) sb = __fadd2_rn(sb, p2);
+      else sa = __fadd2_rn(sa, p2);
+      pk[q4 * 4 + e] = tc::pack_bf16x2(p2.x, p2.y);
     }
-  } else if (w == 0u || w == 0xffffffffu) {
+  }
+  return __fadd2_rn(sa, sb);
+}
+
+// P of one 32-key half of a lane that is not live: 1 on every real key of a
+// uniform row or query (`w` = that half's real-key bits), else 0.
+__device__ __forceinline__ void p_half_const(uint32_t w, uint32_t (&pk)[16]) {
+  if (w == 0u || w == 0xffffffffu) {
     const uint32_t v = w ? 0x3F803F80u : 0u;
 #pragma unroll
     for (int k = 0; k < 16; ++k) pk[k] = v;
@@ -618,83 +666,106 @@ __device__ __forceinline__ float2 p_half(const float2 (&x2)[BK / 2], const uint4
     for (int k = 0; k < 16; ++k)
       pk[k] = (((w >> (2 * k)) & 1u) ? 0x3F80u : 0u) | (((w >> (2 * k + 1)) & 1u) ? 0x3F800000u : 0u);
   }
-  return __fadd2_rn(sa, sb);
 }
 
-// The 32 fp16 biases of half hf of a tile row (brow: the row's swizzled base,
-// 16-byte chunk q at brow ^ (q << 4)).
-__device__ __forceinline__ void load_bias_half(uint32_t brow, int hf, uint4 (&bh)[4]) {
-#pragma unroll
-  for (int q4 = 0; q4 < 4; ++q4) bh[q4] = tc::lds128(brow ^ ((hf * 4 + q4) << 4));
-}
-
-// Largest logit x = S sc + bias of a 64-key tile, in log2 units.
-__device__ __forceinline__ float tile_max(const float2 (&x2)[BK / 2], uint32_t brow, float2 sc2) {
-  float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-  const float2 z2 = make_float2(0.f, 0.f);
-#pragma unroll
-  for (int hf = 0; hf < 2; ++hf) {
-    uint4 bh[4];
-    load_bias_half(brow, hf, bh);
+// General path of one 32-key half: P = 2^(S + bias - mu) for a live lane; a
+// lane that is not live writes 1 on every real key of a uniform row or query
+// (`w` = that half's real-key bits), else 0.
+__device__ __forceinline__ float2 p_half(const float2 (&x2)[BK / 2], const uint4 (&bh)[4], int hf,
+                                         float mu, bool live, uint32_t w, uint32_t (&pk)[16]) {
+  float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
+  if (live) {
+    const float2 nmu2 = make_float2(-mu, -mu);
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4) {
       const uint32_t hw[4] = {bh[q4].x, bh[q4].y, bh[q4].z, bh[q4].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float2 y = __ffma2_rn(x2[(hf * 4 + q4) * 4 + e], sc2, z2);
-        mx[e] = fmax3(mx[e], add_f16lo_f32(hw[e], y.x), add_f16hi_f32(hw[e], y.y));
+        const float2 y = __fadd2_rn(x2[(hf * 4 + q4) * 4 + e], nmu2);
+        const float2 p2 = make_float2(ex2_approx(add_f16lo_f32(hw[e], y.x)),
+                                      ex2_approx(add_f16hi_f32(hw[e], y.y)));
+        if (e & 1) sb = __fadd2_rn(sb, p2);
+        else sa = __fadd2_rn(sa, p2);
+        pk[q4 * 4 + e] = tc::pack_bf16x2(p2.x, p2.y);
       }
     }
+  } else {
+    p_half_const(w, pk);
   }
-  return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+  return __fadd2_rn(sa, sb);
 }
 
-// Rare path: some lane's sum of P over the tile reached 2^32. Those lanes raise mu to
-// the tile max; O (in TMEM, at tb + TM_O, when it holds this unit's sum: o_live) and
-// l are rescaled, and the tile's P is recomputed and stored again at tp. Called by
-// whole warps once the P V that last read P and O has completed. Returns the new
-// sum of P of the tile.
-__device__ __forceinline__ float redo_tile(const float2 (&x2)[BK / 2], uint32_t brow, uint32_t tb,
-                                        uint32_t tp, float2 sc2, bool live, bool ovf, bool o_live,
-                                        uint32_t w0, uint32_t w1, float& m_used, float& l_run) {
-  const float mt = tile_max(x2, brow, sc2);
-  float alpha = 1.f;
-  if (ovf) {
-    alpha = ex2_approx(m_used - mt);
-    m_used = mt;
-    l_run *= alpha;
-  }
-  tc::tmem_st_wait();
-#pragma unroll 1
-  for (int oh = 0; o_live && oh < 2; ++oh) {
-    uint32_t ov[16];
-    tc::tmem_ld16(tb + TM_O + 16 * oh, ov);
-    tc::tmem_ld_wait();
+// A query row whose sum l left [2^-90, 2^100) (logits beyond about +-100 in
+// log2 units, where P = 2^x with the fixed reference 0 loses range) is
+// recomputed exactly on the CUDA cores: two passes over the line's keys, the
+// first for the row max m, the second for l = sum 2^(x - m) and
+// o = sum 2^(x - m) v / l, in fp32. qrow: the row's q (head t); kl, vl: key 0
+// of the line's k and v (head t), sx: the stride between keys; brow: the row
+// of the bias plane; keys come from the line's mask bits (row reading; mrow)
+// or from the finite biases (query reading, mrow = null: the plane holds -inf
+// for dropped keys). o leaves as 16 bf16 pairs in the lane's row of the
+// 64-byte-swizzled staging tile at stg.
+__device__ __noinline__ void exact_row(const __nv_bfloat16* qrow, const __nv_bfloat16* kl,
+                                       const __nv_bfloat16* vl, long long sx,
+                                       const __half* brow, const uint32_t* mrow, int N,
+                                       uint8_t* stg, int lane) {
+  float q[DH];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-    tc::tmem_st16(tb + TM_O + 16 * oh, ov);
+  for (int e = 0; e < DH; ++e) q[e] = __bfloat162float(qrow[e]);
+  float m = -INFINITY;
+  for (int kk = 0; kk < N; ++kk) {
+    if (mrow && !((__ldg(mrow + (kk >> 5)) >> (kk & 31)) & 1u)) continue;
+    const float bb = __half2float(brow[kk]);
+    if (bb == -INFINITY) continue;
+    const __nv_bfloat16* kr = kl + (long long)kk * sx;
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < DH; ++e) s = fmaf(q[e], __bfloat162float(kr[e]), s);
+    m = fmaxf(m, s + bb);
   }
-  uint32_t pk[16];
-  uint4 bh[4];
-  load_bias_half(brow, 0, bh);
-  float2 ts2 = p_half(x2, bh, 0, sc2, m_used, live, w0, pk);
-  tc::tmem_st16(tp, pk);
-  load_bias_half(brow, 1, bh);
-  ts2 = __fadd2_rn(ts2, p_half(x2, bh, 1, sc2, m_used, live, w1, pk));
-  tc::tmem_st16(tp + 16, pk);
-  return ts2.x + ts2.y;
+  float l = 0.f, o[DH];
+#pragma unroll
+  for (int e = 0; e < DH; ++e) o[e] = 0.f;
+  for (int kk = 0; kk < N; ++kk) {
+    if (mrow && !((__ldg(mrow + (kk >> 5)) >> (kk & 31)) & 1u)) continue;
+    const float bb = __half2float(brow[kk]);
+    if (bb == -INFINITY) continue;
+    const __nv_bfloat16* kr = kl + (long long)kk * sx;
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < DH; ++e) s = fmaf(q[e], __bfloat162float(kr[e]), s);
+    const float w = exp2f(s + bb - m);
+    l += w;
+    const __nv_bfloat16* vr = vl + (long long)kk * sx;
+#pragma unroll
+    for (int e = 0; e < DH; ++e) o[e] = fmaf(w, __bfloat162float(vr[e]), o[e]);
+  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+  for (int qc = 0; qc < 4; ++qc) {
+    uint32_t w4[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      w4[e] = tc::pack_bf16x2(o[8 * qc + 2 * e] * inv, o[8 * qc + 2 * e + 1] * inv);
+    *(uint4*)(stg + tc::swz_offset(lane, qc, 64)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  }
 }
 
 // Persistent: CTA c serves work units unit0 + c, + G, ... A unit is (b, head
-// t, R = 3 lines, 128 queries); it streams 64-key tiles, each stage holding
-// the K and V tiles of the three lines and the fp16 bias tile they share.
-// Softmax warpgroup r owns line r; tile c's S = Q K^T lands in the line's S
-// buffer c & 1, and the softmax adds the bias, drops masked keys and writes
-// P = 2^(x - mu) (bf16) over it in one pass; the line's MMA thread then issues
-// O += P V(c) and S(c + 2) into the same buffer. The reference mu of a query
-// row is the max of its first live tile and moves (rescaling O in TMEM) only
-// when a tile's sum of P reaches 2^32, so no per-tile max is taken in the
-// common case.
+// t, R = 3 lines, 128 queries); it streams 64-key sub-tiles. The K and V tiles
+// of the three lines arrive 128 keys at a time (one stage serves two
+// sub-tiles); the fp16 bias sub-tile they share has a ring of its own.
+// Softmax warpgroup r owns line r; sub-tile c's S = Q K^T lands in the line's
+// S buffer c & 1 in log2 units (q carries the factor log2(e)/sqrt(d)), and the
+// softmax adds the bias, drops masked keys and writes P = 2^x (bf16) over it
+// in one pass; the line's MMA warp then issues O += P V(c) and S(c + 2) into
+// the same buffer. The reference of the exponentials is fixed at 0: no max is
+// taken, and fp32 and bf16 hold 2^x with full relative precision for
+// |x| < ~100, far beyond the logits of layer-normalised activations; a query
+// row whose sum l ends outside [2^-90, 2^100) is recomputed exactly in the
+// unit epilogue (exact_row). A unit's o = O / l is read and stored after the
+// next unit's first sub-tile, which hides the completion of the unit's last
+// P V.
 __global__ void __launch_bounds__(kThreads, 1)
 row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
             const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_b,
@@ -703,7 +774,8 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
   uint8_t* smem = align1024(smem_raw);
   Bars* bars = (Bars*)(smem + OFF_BAR);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const Abort ab{&bars->abort, p.dev_err, p.polls};
+  // The abort context is rebuilt from the kernel parameters at each use.
+#define ab (Abort{&bars->abort, p.dev_err, p.polls})
   const int N = p.N;
   const int KT = (N + BK - 1) / BK;
   int my_units = 0;
@@ -714,20 +786,23 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       tc::mbar_init(&bars->q_full[q], 1);
       tc::mbar_init(&bars->q_empty[q], kIssuers);    // one commit per issuer
     }
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < KV_STAGES; ++s) {
       tc::mbar_init(&bars->kv_full[s], 1);
       tc::mbar_init(&bars->kv_empty[s], kIssuers);
+    }
+    for (int s = 0; s < B_STAGES; ++s) {
+      tc::mbar_init(&bars->b_full[s], 1);
+      tc::mbar_init(&bars->b_empty[s], kSoftmaxWarps);   // one arrive per softmax warp
     }
     for (int r = 0; r < R; ++r) {
       for (int b = 0; b < 2; ++b) {
         tc::mbar_init(&bars->s_ready[r][b], 1);
         tc::mbar_init(&bars->p_full[r][b], 128);
+        tc::mbar_init(&bars->p_free[r][b], 1);
       }
-      tc::mbar_init(&bars->p_free[r][0], 1);
-      tc::mbar_init(&bars->p_free[r][1], 1);
       tc::mbar_init(&bars->o_free[r], 128);
+      tc::mbar_init(&bars->drain[r], 1);
     }
-    tc::mbar_init(&bars->drain, kIssuers);
     bars->abort = 0;
     tc::fence_mbar_init();
   }
@@ -739,88 +814,119 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  int q_issued = 0, kg_issued = 0;          // producer: units / key tiles whose loads were issued
+  int q_issued = 0, kv_issued = 0, b_issued = 0;    // producer: loads issued
 
   if (warp < 4) {
     tc::regs_dec<kRegsCtl>();
-    if (warp == 0 && lane == 0) {
-      // ---------------- TMA producer
-      tc::tma_prefetch_desc(&map_q);
-      tc::tma_prefetch_desc(&map_k);
-      tc::tma_prefetch_desc(&map_v);
-      tc::tma_prefetch_desc(&map_b);
-      bool ok = true;
+    if (warp == 0) {
+      // ---------------- TMA producer (whole warp; one elected lane issues)
+      if (elect_one()) {
+        tc::tma_prefetch_desc(&map_q);
+        tc::tma_prefetch_desc(&map_k);
+        tc::tma_prefetch_desc(&map_v);
+        tc::tma_prefetch_desc(&map_b);
+      }
+      __syncwarp();
       Unit un = decode_unit(p.unit0 + blockIdx.x, p);
+      int kvs = 0, kvph = 0, bs = 0, bph = 0;
+      bool ok = true;
       for (int ui = 0; ok && ui < my_units; ++ui, step_unit(un, p)) {
         const int a0 = un.rg * R;
         const int qb = ui & 1;
-        if (ui >= 2 && !wait_or_abort(&bars->q_empty[qb], ((ui >> 1) - 1) & 1, ab)) break;
-        tc::mbar_arrive_expect_tx(&bars->q_full[qb], R * Q_BYTES);
-        for (int r = 0; r < R; ++r)
-          tc::tma_load_4d(smem + OFF_Q + (qb * R + r) * Q_BYTES, &map_q, &bars->q_full[qb],
-                          un.t * DH, un.j0, a0 + r, un.b);
+        if (ui >= 2 && !warp_wait_or_abort(&bars->q_empty[qb], ((ui >> 1) - 1) & 1, ab)) break;
+        if (elect_one()) {
+          tc::mbar_arrive_expect_tx(&bars->q_full[qb], R * Q_BYTES);
+          for (int r = 0; r < R; ++r)
+            tc::tma_load_4d(smem + OFF_Q + (qb * R + r) * Q_BYTES, &map_q, &bars->q_full[qb],
+                            un.t * DH, un.j0, a0 + r, un.b);
+        }
+        __syncwarp();
         q_issued = ui + 1;
         for (int kt = 0; kt < KT; ++kt) {
-          const int kg = kg_issued, s = kg % STAGES;
-          if (kg >= STAGES && !wait_or_abort(&bars->kv_empty[s], ((kg / STAGES) - 1) & 1, ab)) {
+          if ((kt & 1) == 0) {
+            if (kv_issued >= KV_STAGES && !warp_wait_or_abort(&bars->kv_empty[kvs], kvph ^ 1, ab)) {
+              ok = false;
+              break;
+            }
+            if (elect_one()) {
+              uint8_t* st = smem + OFF_KV + kvs * KV_STAGE;
+              tc::mbar_arrive_expect_tx(&bars->kv_full[kvs], KV_STAGE);
+              for (int r = 0; r < R; ++r) {
+                tc::tma_load_4d(st + r * 2 * KVT_BYTES, &map_k, &bars->kv_full[kvs], un.t * DH,
+                                kt * BK, a0 + r, un.b);
+                tc::tma_load_4d(st + r * 2 * KVT_BYTES + KVT_BYTES, &map_v, &bars->kv_full[kvs],
+                                un.t * DH, kt * BK, a0 + r, un.b);
+              }
+            }
+            __syncwarp();
+            ++kv_issued;
+            if (++kvs == KV_STAGES) { kvs = 0; kvph ^= 1; }
+          }
+          if (b_issued >= B_STAGES && !warp_wait_or_abort(&bars->b_empty[bs], bph ^ 1, ab)) {
             ok = false;
             break;
           }
-          uint8_t* st = smem + OFF_STAGE + s * STAGE_BYTES;
-          tc::mbar_arrive_expect_tx(&bars->kv_full[s], STAGE_BYTES);
-          for (int r = 0; r < R; ++r) {
-            tc::tma_load_4d(st + r * 2 * KV_BYTES, &map_k, &bars->kv_full[s], un.t * DH, kt * BK,
-                            a0 + r, un.b);
-            tc::tma_load_4d(st + r * 2 * KV_BYTES + KV_BYTES, &map_v, &bars->kv_full[s],
-                            un.t * DH, kt * BK, a0 + r, un.b);
+          if (elect_one()) {
+            tc::mbar_arrive_expect_tx(&bars->b_full[bs], BIAS_BYTES);
+            tc::tma_load_3d(smem + OFF_BIAS + bs * BIAS_BYTES, &map_b, &bars->b_full[bs], kt * BK,
+                            un.j0, un.b * p.h + un.t);
           }
-          tc::tma_load_3d(st + STAGE_KV, &map_b, &bars->kv_full[s], kt * BK, un.j0,
-                          un.b * p.h + un.t);
-          kg_issued = kg + 1;
+          __syncwarp();
+          ++b_issued;
+          if (++bs == B_STAGES) { bs = 0; bph ^= 1; }
         }
       }
-    } else if (warp >= 1 && warp <= R && lane == 0) {
-      // ---------------- MMA issuer of row r = warp - 1
+    } else {
+      // ---------------- MMA issuer of line r = warp - 1 (whole warp; one elected lane issues)
       const int r = warp - 1;
       const uint32_t tr = tmem + r * kTmemPerRow;
       constexpr uint32_t id_qk = tc::idesc_bf16_f32(128, BK, 0, 0);
       constexpr uint32_t id_pv = tc::idesc_bf16_f32(128, DH, 0, 1);
-      const uint32_t q0 = tc::smem_addr(smem + OFF_Q);
-      const uint32_t st0 = tc::smem_addr(smem + OFF_STAGE);
-      const int total = my_units * KT;     // one item per key tile
-      // S(0), S(1); then per tile c, once P(c) is written: P V(c) from buffer
-      // c & 1, then S(c + 2) into the same buffer.
-      auto qk = [&](const TileIt& it) -> bool {
+      // Descriptors of this line's first Q tile and first K tile; every other
+      // operand sits a multiple of 16 bytes further (the start-address field
+      // holds address / 16 and stays below 2^14).
+      const uint64_t dq0 = tc::smem_desc(tc::smem_addr(smem + OFF_Q + r * Q_BYTES), 16, 512, tc::SWZ_64B);
+      const uint64_t dk0 =
+          tc::smem_desc(tc::smem_addr(smem + OFF_KV + r * 2 * KVT_BYTES), 16, 512, tc::SWZ_64B);
+      const int total = my_units * KT;     // one item per key sub-tile
+      auto qk = [&](const SubIt& it) -> bool {
         const int c = it.c;
-        if (it.kt == 0 && !wait_or_abort(&bars->q_full[it.ui & 1], (it.ui >> 1) & 1, ab)) return false;
-        if (!wait_or_abort(&bars->kv_full[it.s], it.sph, ab)) return false;
+        if (it.kt == 0 && !warp_wait_or_abort(&bars->q_full[it.ui & 1], (it.ui >> 1) & 1, ab)) return false;
+        if ((it.kt & 1) == 0 && !warp_wait_or_abort(&bars->kv_full[it.kvs], it.kvph, ab)) return false;
         tc::tc_fence_after();
-        const uint32_t qa = q0 + ((it.ui & 1) * R + r) * Q_BYTES;
-        const uint32_t ka = st0 + it.s * STAGE_BYTES + r * 2 * KV_BYTES;
-        for (int ks = 0; ks < DH / 16; ++ks)
-          tc::mma_bf16_ss(tr + (c & 1) * TM_S1, tc::smem_desc(qa + ks * 32, 16, 512, tc::SWZ_64B),
-                          tc::smem_desc(ka + ks * 32, 16, 512, tc::SWZ_64B), id_qk, ks > 0);
-        tc::mma_commit(&bars->s_ready[r][c & 1]);
-        if (it.kt == KT - 1) tc::mma_commit(&bars->q_empty[it.ui & 1]);
+        if (elect_one()) {
+          const uint64_t qd = dq0 + (uint64_t)(((it.ui & 1) * R * Q_BYTES) >> 4);
+          const uint64_t kd = dk0 + (uint64_t)((it.kvs * KV_STAGE + (it.kt & 1) * HALF_KV) >> 4);
+#pragma unroll
+          for (int ks = 0; ks < DH / 16; ++ks)
+            tc::mma_bf16_ss(tr + (c & 1) * TM_S1, qd + 2 * ks, kd + 2 * ks, id_qk, ks > 0);
+          tc::mma_commit(&bars->s_ready[r][c & 1]);
+          if (it.kt == KT - 1) tc::mma_commit(&bars->q_empty[it.ui & 1]);
+        }
+        __syncwarp();
         return true;
       };
-      auto pv = [&](const TileIt& it) -> bool {
+      auto pv = [&](const SubIt& it) -> bool {
         const int c = it.c;
-        if (!wait_or_abort(&bars->p_full[r][c & 1], (c >> 1) & 1, ab)) return false;
-        if (it.kt == 0 && it.ui >= 1 && !wait_or_abort(&bars->o_free[r], (it.ui - 1) & 1, ab))
+        if (!warp_wait_or_abort(&bars->p_full[r][c & 1], (c >> 1) & 1, ab)) return false;
+        if (it.kt == 0 && it.ui >= 1 && !warp_wait_or_abort(&bars->o_free[r], (it.ui - 1) & 1, ab))
           return false;
         tc::tc_fence_after();
-        const uint32_t va = st0 + it.s * STAGE_BYTES + r * 2 * KV_BYTES + KV_BYTES;
-        for (int ks = 0; ks < BK / 16; ++ks)
-          tc::mma_bf16_ts(tr + TM_O, tr + (c & 1) * TM_S1 + ks * 8,
-                          tc::smem_desc(va + ks * 1024, 16, 512, tc::SWZ_64B), id_pv,
-                          (it.kt > 0 || ks > 0) ? 1u : 0u);
-        tc::mma_commit(&bars->p_free[r][c & 1]);
-        tc::mma_commit(&bars->kv_empty[it.s]);
+        if (elect_one()) {
+          const uint64_t vd =
+              dk0 + (uint64_t)((it.kvs * KV_STAGE + KVT_BYTES + (it.kt & 1) * HALF_KV) >> 4);
+#pragma unroll
+          for (int ks = 0; ks < BK / 16; ++ks)
+            tc::mma_bf16_ts(tr + TM_O, tr + (c & 1) * TM_S1 + ks * 8, vd + 64 * ks, id_pv,
+                            (it.kt > 0 || ks > 0) ? 1u : 0u);
+          tc::mma_commit(&bars->p_free[r][c & 1]);
+          if ((it.kt & 1) || it.kt == KT - 1) tc::mma_commit(&bars->kv_empty[it.kvs]);
+        }
+        __syncwarp();
         return true;
       };
       bool ok = true;
-      TileIt itq{0, 0, 0, 0, 0}, itp{0, 0, 0, 0, 0};
+      SubIt itq{0, 0, 0, 0, 0, 0, 0}, itp{0, 0, 0, 0, 0, 0, 0};
       for (; ok && itq.c < 2 && itq.c < total; advance(itq, KT)) ok = qk(itq);
       for (; ok && itp.c < total; advance(itp, KT)) {
         ok = pv(itp);
@@ -829,177 +935,192 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
           advance(itq, KT);
         }
       }
-      tc::mma_commit(&bars->drain);
-      drain_wait(&bars->drain, 0);
+      if (elect_one()) tc::mma_commit(&bars->drain[r]);
+      __syncwarp();
+      drain_wait(&bars->drain[r], 0);
     }
   } else {
-    // ---------------- softmax warpgroups: row r of each unit, thread = query row
+    // ---------------- softmax warpgroups: line r of each unit, thread = query row
     tc::regs_inc<kRegsSoftmax>();
     const int r = (warp >> 2) - 1;
+    const int sw = warp - 4;                         // softmax warp index
     const int jr = (warp & 3) * 32 + lane;          // query row of the tile = TMEM lane
     const uint32_t tb = tmem + ((uint32_t)((warp & 3) * 32) << 16) + r * kTmemPerRow;
-    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-    // A unit's mask summary (its query row's or key row's "keeps some key"
-    // flag, and the row's first mask word) is loaded one unit ahead.
-    auto unit_loads = [&](const Unit& nu, unsigned& any, uint2& bits0) {
+    // Bias row jr of a stage (128-byte swizzle: 16-byte chunk q of the row sits
+    // at chunk q ^ (jr & 7)); the row base is 128-byte aligned.
+    const uint32_t brow0 = tc::smem_addr(smem + OFF_BIAS) + jr * 128u + ((jr & 7u) << 4);
+    const bool qk_mode = p.mask_mode == TRI_ATTN_MASK_QUERY_KEY;
+    // A unit's mask summary: the "keeps some key" flag of this lane's query
+    // row (query-key) or of the line (row-key), and the mask row whose bits
+    // give the keys this lane keeps. Loaded one unit ahead.
+    auto unit_loads = [&](const Unit& nu, unsigned& any, const uint32_t*& mrow) {
       const int nj = nu.j0 + jr, ni = nu.rg * R + r;
-      if (p.mask_mode == TRI_ATTN_MASK_QUERY_KEY)
-        any = nj < N ? __ldg(p.row_any + (long long)nu.b * N + nj) : 0u;
-      else
-        any = ni < N ? __ldg(p.row_any + (long long)nu.b * N + ni) : 0u;
-      bits0 = __ldg((const uint2*)(p.mbits + ((long long)nu.b * N + (ni < N ? ni : 0)) * p.words));
+      const int mr = qk_mode ? nj : ni;
+      // Queries past N produce nothing (their stores are clipped): they count
+      // as keeping keys so that they never force the general path.
+      any = mr < N ? __ldg(p.row_any + (long long)nu.b * N + mr) : (qk_mode ? 1u : 0u);
+      mrow = p.mbits + ((long long)nu.b * N + (mr < N ? mr : 0)) * p.words;
     };
     unsigned nx_any = 0u;
-    uint2 nx_bits = make_uint2(0u, 0u);
-    Unit nxu = decode_unit(p.unit0 + blockIdx.x, p);   // the unit after the current one
-    if (my_units > 0) unit_loads(nxu, nx_any, nx_bits);
+    const uint32_t* nx_mrow = p.mbits;
+    if (my_units > 0) unit_loads(decode_unit(p.unit0 + blockIdx.x, p), nx_any, nx_mrow);
     // Unit epilogue: o = O / l once the unit's last P V has landed, staged in
     // shared memory and written by one TMA store per warp (queries past N are
-    // clipped by the store; rows past N and warps whose 32 queries all lie
-    // past N skip it). One 16-byte shared store per lane and chunk replaces
-    // 32 scattered 16-byte global stores per warp instruction.
-    uint8_t* const ostg0 = smem + OFF_OST + (warp - 4) * 2 * OST_BYTES;
-    int n_ost = 0;
-    auto finish_unit = [&](const Unit& fu, int clast, float l) -> bool {
+    // clipped by the store; lines past N and warps whose 32 queries all lie
+    // past N skip it).
+    uint8_t* const ostg = smem + OFF_OST + sw * OST_BYTES;
+    auto finish_unit = [&](int ui, int clast, float l) -> bool {
       if (!warp_wait_or_abort(&bars->p_free[r][clast & 1], (clast >> 1) & 1, ab)) return false;
       tc::tc_fence_after();
       uint32_t ov[32];
       tc::tmem_ld32(tb + TM_O, ov);
       tc::tmem_ld_wait();
-      // O is in registers: its columns may take the next unit.
+      // O is in registers: its columns may take the next unit's sums.
       tc::tc_fence_before();
       tc::mbar_arrive(&bars->o_free[r]);
+      const Unit fu = decode_unit(p.unit0 + blockIdx.x + ui * gridDim.x, p);
       const int fi = fu.rg * R + r, fj = fu.j0 + (warp & 3) * 32;
       if (fi < N && fj < N) {
-        const float inv = __fdividef(1.0f, l);   // l lies in [1, 2^40): the fast form is exact enough
+        // A query row has l in [2^-90, 2^100) unless its logits reached about
+        // +-100 (a uniform row or query has l = its count of real keys): those
+        // rows are recomputed exactly.
+        const bool exact = fj + lane < N && !(l >= 0x1p-90f && l < 0x1p100f);
+        const float inv = __fdividef(1.0f, l);   // l lies in [2^-90, 2^100): the fast form is exact enough
         uint32_t po[16];
 #pragma unroll
         for (int e = 0; e < DH; e += 2)
           po[e / 2] = tc::pack_bf16x2(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
-        uint8_t* const ostg = ostg0 + (n_ost & 1) * OST_BYTES;
-        if (n_ost >= 2) {                  // the store two back has read this staging tile
-          if (lane == 0) tc::tma_store_wait_read<1>();
-          __syncwarp();
-        }
+        // The previous store (if any) has read the staging tile.
+        if (lane == 0) tc::tma_store_wait_read<0>();
+        __syncwarp();
+        if (__builtin_expect(exact, 0)) {
+          const long long base = (long long)fu.b * p.sb + (long long)fi * p.sl + fu.t * DH;
+          exact_row(p.q + base + (long long)(fj + lane) * p.sx, p.k + base, p.v + base, p.sx,
+                    p.bias + (((long long)fu.b * p.h + fu.t) * N + fj + lane) * p.Nb,
+                    p.mask_mode == TRI_ATTN_MASK_QUERY_KEY
+                        ? nullptr
+                        : p.mbits + ((long long)fu.b * N + fi) * p.words,
+                    N, ostg, lane);
+        } else {
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *(uint4*)(ostg + tc::swz_offset(lane, q, 64)) =
-              make_uint4(po[4 * q], po[4 * q + 1], po[4 * q + 2], po[4 * q + 3]);
+          for (int q = 0; q < 4; ++q)
+            *(uint4*)(ostg + tc::swz_offset(lane, q, 64)) =
+                make_uint4(po[4 * q], po[4 * q + 1], po[4 * q + 2], po[4 * q + 3]);
+        }
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           tc::tma_store_4d(&map_o, ostg, fu.t * DH, fj, fi, fu.b);
           tc::tma_store_commit();
         }
-        ++n_ost;
       }
       return true;
     };
     bool ok = true;
-    TileIt its{0, 0, 0, 0, 0};                      // this warp's tile stream
+    SoftIt its{0, 0, 0, 0};                         // this warp's sub-tile stream
+    float l_prev = 0.f;
     for (int ui = 0; ok && ui < my_units; ++ui) {
-      const Unit un = nxu;
-      step_unit(nxu, p);
-      const int i = un.rg * R + r;
       const bool uni = nx_any == 0u;
-      const uint2 bits0 = nx_bits;
-      if (ui + 1 < my_units) unit_loads(nxu, nx_any, nx_bits);
-      float m_used = -INFINITY, l_run = 0.f;
-      // Whether any lane of the warp has a key-keeping query row in this unit
-      // (warp-uniform, one vote per unit), and whether those lanes have taken
-      // their reference max yet: their first live tile is the same tile, since
-      // a tile's keep bits are shared by the whole warp.
+      const uint32_t* mrow = nx_mrow;
+      if (ui + 1 < my_units)
+        unit_loads(decode_unit(p.unit0 + blockIdx.x + (ui + 1) * gridDim.x, p), nx_any, nx_mrow);
+      float l_run = 0.f;
+      // Warp-uniform unit state: whether any lane has a key-keeping query row,
+      // and whether every lane has one.
       const bool unit_live = __any_sync(0xffffffffu, !uni);
-      bool have_mu = false;
-      const uint32_t* mrow = p.mbits + ((long long)un.b * N + (i < N ? i : 0)) * p.words;
-      const bool use_bits = p.mask_mode == TRI_ATTN_MASK_ROW_KEY && !uni;
-      uint2 nbits = use_bits ? bits0 : make_uint2(0xffffffffu, 0xffffffffu);
+      const bool all_live = __all_sync(0xffffffffu, !uni);
+      uint2 nbits = __ldg((const uint2*)mrow);
       for (int kt = 0; ok && kt < KT; ++kt, advance(its, KT)) {
-        const int c = its.c, s = its.s;
+        const int c = its.c;
         const uint2 mb = nbits;
-        if (use_bits && kt + 1 < KT) nbits = __ldg((const uint2*)(mrow + 2 * (kt + 1)));
+        if (kt + 1 < KT) nbits = __ldg((const uint2*)(mrow + 2 * (kt + 1)));
         const int left = N - kt * BK;
         const uint32_t rl0 = real_bits(left, 0), rl1 = real_bits(left, 1);
-        const uint32_t bw0 = rl0 & mb.x, bw1 = rl1 & mb.y;
-        const bool all_kept = (bw0 & bw1) == 0xffffffffu;
-        const bool tile_keys = (bw0 | bw1) != 0u;      // warp-uniform
+        // Keys kept by this lane (query-key: its own query row; row-key: the
+        // line, the same for the whole warp).
+        const uint32_t kb0 = rl0 & mb.x, kb1 = rl1 & mb.y;
+        // Row-key: S of a dropped key is set to -inf. Query-key: the bias plane
+        // already holds -inf there.
+        const uint32_t bw0 = qk_mode ? rl0 : kb0, bw1 = qk_mode ? rl1 : kb1;
+        const bool all_kept = (bw0 & bw1) == 0xffffffffu;      // warp-uniform
+        const bool tile_keys = (bw0 | bw1) != 0u;              // warp-uniform
         const bool live = !uni && tile_keys;
-        // Bias row jr of the stage (128-byte swizzle: 16-byte chunk q of the row
-        // sits at chunk q ^ (jr & 7)); the row base is 128-byte aligned.
-        const uint32_t brow = tc::smem_addr(smem + OFF_STAGE + s * STAGE_BYTES + STAGE_KV) +
-                              jr * 128u + ((jr & 7u) << 4);
-        // The stage (its bias tile) and S(c): both barriers are polled back to
-        // back so that their latencies overlap, then one vote settles them.
-        bool okk = tc::mbar_try_wait(&bars->kv_full[s], its.sph);
+        const uint32_t brow = brow0 + its.bs * BIAS_BYTES;
+        // The bias stage and S(c): both barriers are polled back to back so
+        // that their latencies overlap, then one vote settles them.
+        bool okk = tc::mbar_try_wait(&bars->b_full[its.bs], its.bph);
         bool oks = tc::mbar_try_wait(&bars->s_ready[r][c & 1], (c >> 1) & 1);
-        if (!okk) okk = wait_or_abort_slow(&bars->kv_full[s], its.sph, ab);
+        if (!okk) okk = wait_or_abort_slow(&bars->b_full[its.bs], its.bph, ab);
         if (okk && !oks) oks = wait_or_abort_slow(&bars->s_ready[r][c & 1], (c >> 1) & 1, ab);
         if (!__all_sync(0xffffffffu, okk && oks)) { ok = false; break; }
         const bool any_live = unit_live && tile_keys;
         tc::tc_fence_after();
         const uint32_t tsb = tb + (c & 1) * TM_S1;     // S(c), then P(c) over it
         float2 x2[BK / 2];
-        uint4 bh[4];                                   // 32 fp16 biases of one half
+        uint4 bh0[4], bh1[4];
+        float tsum = 0.f;
         if (any_live) {
           tc::tmem_ld32(tsb, *(uint32_t(*)[32])&x2[0]);
           tc::tmem_ld32(tsb + 32, *(uint32_t(*)[32])&x2[16]);
-          load_bias_half(brow, 0, bh);
+          load_bias_half(brow, 0, bh0);
+          load_bias_half(brow, 1, bh1);
           tc::tmem_ld_wait();
-        }
-        if (any_live && !all_kept) {
-          // Dropped keys: S = -inf, which the bias add keeps at -inf (P = 0).
+          if (!all_kept) {
+            // Dropped keys: S = -inf, which the bias add keeps at -inf (P = 0).
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            if (!((bw0 >> (2 * k)) & 1u)) x2[k].x = -INFINITY;
-            if (!((bw0 >> (2 * k + 1)) & 1u)) x2[k].y = -INFINITY;
-            if (!((bw1 >> (2 * k)) & 1u)) x2[16 + k].x = -INFINITY;
-            if (!((bw1 >> (2 * k + 1)) & 1u)) x2[16 + k].y = -INFINITY;
+            for (int k = 0; k < 16; ++k) {
+              if (!((bw0 >> (2 * k)) & 1u)) x2[k].x = -INFINITY;
+              if (!((bw0 >> (2 * k + 1)) & 1u)) x2[k].y = -INFINITY;
+              if (!((bw1 >> (2 * k)) & 1u)) x2[16 + k].x = -INFINITY;
+              if (!((bw1 >> (2 * k + 1)) & 1u)) x2[16 + k].y = -INFINITY;
+            }
           }
-        }
-        // A lane's reference max mu is set on its first live tile and moves only
-        // when a tile's sum of P reaches 2^32 (its logits rose by more than
-        // about 26), so P stays finite and O, l never overflow in fp32.
-        if (__builtin_expect(any_live && !have_mu, 0)) {
-          const float mt = tile_max(x2, brow, sc2);
-          if (live) m_used = mt;
-          have_mu = true;
-        }
-        const float mu = m_used == -INFINITY ? 0.f : m_used;
-        const uint32_t w0 = uni ? rl0 : 0u, w1 = uni ? rl1 : 0u;
-        uint32_t pk[16];
-        float2 ts2 = p_half(x2, bh, 0, sc2, mu, live, w0, pk);
-        tc::tmem_st16(tsb, pk);
-        if (any_live) load_bias_half(brow, 1, bh);
-        ts2 = __fadd2_rn(ts2, p_half(x2, bh, 1, sc2, mu, live, w1, pk));
-        tc::tmem_st16(tsb + 16, pk);
-        float tsum = ts2.x + ts2.y;
-        if (any_live) {
-          const bool ovf = live && !(tsum < 4294967296.f);
-          if (__builtin_expect(__any_sync(0xffffffffu, ovf), 0)) {
-            // O is stable once P V(c - 1), the last MMA on it, has landed
-            // (S(c) landing implied P V(c - 2)).
-            // On a unit's first tile O holds no sum of this unit yet.
-            if (kt >= 1 && !warp_wait_or_abort(&bars->p_free[r][(c - 1) & 1], ((c - 1) >> 1) & 1, ab)) { ok = false; break; }
-            tc::tc_fence_after();
-            tsum = redo_tile(x2, brow, tb, tsb, sc2, live, ovf, kt >= 1, w0, w1, m_used, l_run);
+          uint32_t pk[16];
+          float2 ts2;
+          if (all_live) {
+            ts2 = p_half_fast(x2, bh0, 0, pk);
+            tc::tmem_st16(tsb, pk);
+            ts2 = __fadd2_rn(ts2, p_half_fast(x2, bh1, 1, pk));
+            tc::tmem_st16(tsb + 16, pk);
+          } else {
+            const uint32_t w0 = uni ? rl0 : 0u, w1 = uni ? rl1 : 0u;
+            ts2 = p_half(x2, bh0, 0, 0.f, live, w0, pk);
+            tc::tmem_st16(tsb, pk);
+            ts2 = __fadd2_rn(ts2, p_half(x2, bh1, 1, 0.f, live, w1, pk));
+            tc::tmem_st16(tsb + 16, pk);
           }
+          tsum = ts2.x + ts2.y;
+        } else {
+          // No lane of the warp keeps a key of this sub-tile: P is 1 on the real
+          // keys of a uniform row or query, else 0.
+          uint32_t pk[16];
+          p_half_const(uni ? rl0 : 0u, pk);
+          tc::tmem_st16(tsb, pk);
+          p_half_const(uni ? rl1 : 0u, pk);
+          tc::tmem_st16(tsb + 16, pk);
         }
+        // The bias stage is read: release it.
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bars->b_empty[its.bs]);
         if (live) {
           l_run += tsum;
         } else if (uni) {
-          m_used = 0.f;
           l_run += (float)(__popc(rl0) + __popc(rl1));
         }
         tc::tmem_st_wait();
         tc::tc_fence_before();
         tc::mbar_arrive(&bars->p_full[r][c & 1]);
+        if (kt == 0 && ui >= 1) {
+          // The previous unit's epilogue, after this unit's first sub-tile.
+          if (!finish_unit(ui - 1, c - 1, l_prev)) { ok = false; break; }
+        }
       }
       if (!ok) break;
-      if (!finish_unit(un, ui * KT + KT - 1, l_run)) { ok = false; break; }
+      l_prev = l_run;
     }
+    if (ok && my_units > 0) finish_unit(my_units - 1, my_units * KT - 1, l_prev);
     if (lane == 0) tc::tma_store_wait_all<0>();
   }
-
 
   // ---------------- teardown
   tc::tc_fence_before();
@@ -1007,12 +1128,15 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
   if (warp == 0 && lane == 0) {
     for (int ui = q_issued - 1; ui >= 0 && ui >= q_issued - 2; --ui)
       drain_wait(&bars->q_full[ui & 1], (ui >> 1) & 1);
-    for (int kg = kg_issued - 1; kg >= 0 && kg >= kg_issued - STAGES; --kg)
-      drain_wait(&bars->kv_full[kg % STAGES], (kg / STAGES) & 1);
+    for (int g = kv_issued - 1; g >= 0 && g >= kv_issued - KV_STAGES; --g)
+      drain_wait(&bars->kv_full[g % KV_STAGES], (g / KV_STAGES) & 1);
+    for (int g = b_issued - 1; g >= 0 && g >= b_issued - B_STAGES; --g)
+      drain_wait(&bars->b_full[g % B_STAGES], (g / B_STAGES) & 1);
   }
   __syncthreads();
   tc::tc_fence_after();
   if (warp == 1) tc::tmem_dealloc(tmem, 512);
+#undef ab
 }
 
 // One warp per mask row (b, r): bit k of word k/32 is pair_mask[b, r, k] != 0
@@ -1450,8 +1574,8 @@ cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const voi
   const long long cells = t->cells;
   bool ok = map_rows_bf16(&st->map_w, t->w_proj, 512, 256);
   ok = ok && map_lines(&st->map_q, t->q, B, N, k2::BQ, t->ending);
-  ok = ok && map_lines(&st->map_k, t->k, B, N, k2::BK, t->ending);
-  ok = ok && map_lines(&st->map_v, t->v, B, N, k2::BK, t->ending);
+  ok = ok && map_lines(&st->map_k, t->k, B, N, k2::KVK, t->ending);
+  ok = ok && map_lines(&st->map_v, t->v, B, N, k2::KVK, t->ending);
   ok = ok && map_lines(&st->map_os, t->o, B, N, 32, t->ending);
   {
     cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)N, (cuuint64_t)B * h};
@@ -1519,6 +1643,7 @@ cudaError_t launch_k1(tri_attn_s* t, cudaStream_t s, const CUtensorMap& map_x,
   p1.q = (__nv_bfloat16*)t->q; p1.k = (__nv_bfloat16*)t->k; p1.v = (__nv_bfloat16*)t->v;
   p1.g = (__nv_bfloat16*)t->g; p1.bias = (__half*)t->bias; p1.dev_err = t->dev_err;
   p1.polls = t->wait_limit;
+  p1.q_scale = kLog2e / sqrtf((float)t->d);
   const int grid = n < st->num_sms ? n : st->num_sms;
   k1::ln_proj_tc<<<grid, k1::kThreads, k1::SMEM, s>>>(map_x, st->map_w, st->st_q, st->st_k,
                                                       st->st_v, st->st_g, p1, st->consts);
@@ -1561,7 +1686,14 @@ cudaError_t launch_k2(tri_attn_s* t, cudaStream_t s, int u0, int nu) {
   p2.mbits = st->mbits; p2.row_any = st->row_any;
   p2.dev_err = t->dev_err;
   p2.polls = t->wait_limit;
-  p2.scale_log2 = kLog2e / sqrtf((float)t->d);
+  p2.q = (const __nv_bfloat16*)t->q;
+  p2.k = (const __nv_bfloat16*)t->k;
+  p2.v = (const __nv_bfloat16*)t->v;
+  p2.sb = (long long)N * N * t->D;
+  p2.sl = t->ending ? (long long)t->D : (long long)N * t->D;     // line a: row (starting) or column
+  p2.sx = t->ending ? (long long)N * t->D : (long long)t->D;     // position along the line
+  p2.bias = (const __half*)t->bias;
+  p2.Nb = st->Nb;
   const unsigned g2 = (unsigned)(p2.units < st->num_sms ? p2.units : st->num_sms);
   {
     const int g1 = (int)g2 / p2.jtiles, gq = g1 / h;

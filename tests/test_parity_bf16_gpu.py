@@ -102,14 +102,14 @@ def test_bf16_forward_host_matches_device():
 
 @pytest.mark.parametrize("mode", [0, 1, 2])
 def test_bf16_logits_rising_past_the_reference_max(mode):
-    """The kernel's reference max comes from a query row's first live tile and
-    moves only when a later tile's sum of P reaches 2^32. Here the pair bias of
-    keys 64..127 sits 56..80 log2 units and that of keys >= 128 at ~115, against
-    at most ~42 in the first tile, so query rows take the rescaling path, most
-    of them twice (mode 2: the ending node, where the same construction on the
-    grid's rows feeds the bias of the column lines). x and Wb are bf16-exact:
-    channel 0 carries a spike of 8 (keys 64..127) or 64 (keys >= 128), and Wb
-    reads channel 0 alone (8.0 per head)."""
+    """The kernel's exponentials use the fixed reference 0 (P = 2^x); a query
+    row whose sum leaves [2^-90, 2^100) is recomputed exactly in the unit
+    epilogue. Here the pair bias of keys 64..127 sits 56..80 log2 units and
+    that of keys >= 128 at ~115, so every row's sum overflows that range and
+    takes the exact path (mode 2: the ending node, where the same construction
+    on the grid's rows feeds the bias of the column lines). x and Wb are
+    bf16-exact: channel 0 carries a spike of 8 (keys 64..127) or 64 (keys
+    >= 128), and Wb reads channel 0 alone (8.0 per head)."""
     w = W.custom(1, 200, 128, 4, "bf16", "bernoulli", seed=61)
     inp = W.make_inputs(w)
     x = inp["x"]
@@ -119,6 +119,28 @@ def test_bf16_logits_rising_past_the_reference_max(mode):
     else:
         x[0, :, 64:128, 0] = 8.0
         x[0, :, 128:, 0] = 64.0
+    Wb = np.zeros_like(inp["params"]["Wb"])
+    Wb[:, 0] = 8.0
+    inp["params"]["Wb"] = Wb
+    got = H.run_forward(w, inp, mode)[0]
+    if mode & tb.TRI_ATTN_ENDING_NODE:
+        ref = O.forward_ending(inp["x"], inp["pair_mask"], inp["params"], w.h, mode & 1)
+    else:
+        ref = O.forward(inp["x"], inp["pair_mask"], inp["params"], w.h, mode)
+    H.assert_parity(w, got, ref)
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_bf16_logits_far_below_zero(mode):
+    """Every pair bias about -141 log2 units: with the fixed reference 0, P =
+    2^x underflows and the row sums fall below 2^-90, so every query row is
+    recomputed exactly (two passes, its own max) in the unit epilogue. The
+    bias is the same for every key of a row, so the weights follow S alone.
+    Channel 0 of every cell carries -64 (bf16-exact) and Wb reads channel 0
+    alone (8.0 per head)."""
+    w = W.custom(1, 150, 128, 4, "bf16", "bernoulli", seed=62)
+    inp = W.make_inputs(w)
+    inp["x"][..., 0] = -64.0
     Wb = np.zeros_like(inp["params"]["Wb"])
     Wb[:, 0] = 8.0
     inp["params"]["Wb"] = Wb
