@@ -194,17 +194,21 @@ int tri_attn_set_wait_limit(tri_attn_t t, long long spins);
  * Everything is a caller pointer (device, fp32, 16-byte aligned; pair_mask
  * int32): the weights in nn.Linear layout as for tri_attn_create, pair_repr
  * (B, N, N, D), pair_mask (B, N, N) and out (B, N, N, D). The intermediates live
- * in one fixed 16 MiB device array inside the library, which every GPU that
- * loads the library holds until the process exits. A problem needs
+ * in one fixed 16 MiB device array inside the library, which every device the
+ * library's code is loaded on holds until the process exits. A problem needs
  *   4 * (P * D + D * D + 5 * B * N * N * D + B * h * N * N) bytes, P = 4D + h
  * rounded up to an even count (each of those seven regions rounded up to 256);
  * larger problems return TRI_ATTN_ERR_UNSUPPORTED without launching anything.
  * Other shape rules are those of TRI_ATTN_F32 in tri_attn_create; `mode` is as
  * there.
  *
- * The call is asynchronous on `stream`. The first call on each device looks up
- * the array's device address (cudaGetSymbolAddress, with that device current),
- * so make that first call before any stream capture. All calls share the one
+ * The call is asynchronous on `stream`. CUDA loads a library's device code
+ * lazily: the first call on each device (each context) loads it, which
+ * reserves the 16 MiB array in device memory and may synchronise, so make that
+ * first call before any stream capture and outside any region that forbids
+ * allocations; later calls allocate nothing. Every call looks up the array's
+ * device address in the current context (cudaGetSymbolAddress), so a context
+ * that was reset or re-created is served at its own address. All calls share the one
  * array and it keeps the previous call's contents (every byte a call reads is
  * written earlier in the same call, so nothing is cleared): calls that can
  * overlap on the GPU, on different streams or from different threads, race on

@@ -10,37 +10,25 @@
 // every weight, input and output as a caller pointer and keeps all intermediates
 // (packed weights, q, k, v, g, o and the bias plane) in one fixed, file-scope
 // device array, so it allocates nothing.
-#include <mutex>
-
 #include "common.cuh"
 
 namespace {
 
-// Fixed scratch of the no-allocation entry point. Every GPU that loads the
-// library holds this array until the process exits.
+// Fixed scratch of the no-allocation entry point. Every device the library's
+// code is loaded on (lazily, at the first call there) holds this array until
+// the process exits.
 constexpr size_t kNoAllocScratchBytes = 16u << 20;   // 16 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of the array for each device, looked up once per device with
-// that device current. In host code the array's name is only a host-side
-// stand-in, so kernels must be given this address instead.
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-unsigned char* g_scratch_addr[kMaxDevices] = {};
-
+// Device address of the array in the current context. In host code the
+// array's name is only a host-side stand-in, so kernels must be given this
+// address. It is looked up at every call (cheap once the code is loaded), so a
+// context that was reset or re-created never receives a stale address.
 cudaError_t scratch_address(unsigned char** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = (unsigned char*)p;
-  }
-  *out = g_scratch_addr[dev];
+  *out = (unsigned char*)p;
   return cudaSuccess;
 }
 

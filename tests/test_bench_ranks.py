@@ -91,7 +91,10 @@ def _run_bench(args, env=None, timeout=240):
 def test_reference_arm_prints_one_contract_line():
     """--impl reference times the CPU oracle on this host and prints exactly one
     JSON line with the native arm's metric, unit and config, the oracle's own
-    cpu_baseline and an e2e block with no host<->device bytes."""
+    cpu_baseline and an e2e block with no host<->device bytes. A step is one
+    bounded sample: ms_per_step is its measured wall time (so steps x
+    ms_per_step is the work the arm did), and at this tiny size the sample
+    covers every row, so it is one whole forward and value = cells / time."""
     import json
     r = _run_bench(["--impl", "reference", "--workload", "b2-n32-d64-h4-f32",
                     "--steps", "2", "--warmup", "1"])
@@ -103,7 +106,8 @@ def test_reference_arm_prints_one_contract_line():
     assert rec["metric"] == bench.METRIC and rec["unit"] == "pair-cells/s"
     assert rec["value"] > 0 and rec["higher_is_better"] is True
     assert (rec["n_gpus"], rec["steps"], rec["warmup"]) == (1, 2, 1)
-    assert rec["ms_per_step"] == pytest.approx(2 * 32 * 32 / rec["value"] * 1e3)
+    assert rec["step"].startswith("one bounded sample")
+    assert rec["ms_per_step"] == pytest.approx(2 * 32 * 32 / rec["value"] * 1e3, rel=1e-3)
     assert rec["config"]["workload"] == "b2-n32-d64-h4-f32"
     cb = rec["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == rec["value"]

@@ -3,12 +3,15 @@ allocate device memory (memory pools or custom allocators that forbid outside
 allocations, plugins given only their input and output buffers). It keeps its
 intermediates in the library's fixed device scratch instead of a handle's
 workspace. Checked through the C ABI against the handle-based tri_attn_forward
-on two calls in a row with different inputs, so a call that read stale scratch
-from the one before would show; and a problem beyond the fixed scratch must be
-refused. This file is collected last on purpose."""
+and against the CPU oracle on two calls in a row with different inputs, so a
+call that read stale scratch from the one before would show; and a problem
+beyond the fixed scratch must be refused. This file is collected last on
+purpose."""
 import numpy as np
 import pytest
 import torch
+
+import oracle.tri_attn_oracle as O
 
 from pair_representation_triangular_gb300 import binding as tb
 from pair_representation_triangular_gb300 import workloads as W
@@ -44,6 +47,11 @@ def test_noalloc_matches_forward_on_two_calls(mode):
         got, want = out.double().cpu().numpy(), ref.double().cpu().numpy()
         assert np.all(np.isfinite(got))
         assert float(np.max(np.abs(got - want))) <= H.TOL_F32_MAX_ABS
+        if mode & tb.TRI_ATTN_ENDING_NODE:
+            oracle = O.forward_ending(inp["x"], inp["pair_mask"], inp["params"], w.h, mode & 1)
+        else:
+            oracle = O.forward(inp["x"], inp["pair_mask"], inp["params"], w.h, mode)
+        H.assert_parity(w, got, oracle)
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch():
