@@ -253,9 +253,10 @@ class TriangularAttention:
         """Copy of an intermediate of the most recent forward (see
         tri_attn_debug_tensor): q, k, v, g, o as (B, N, N, D), bf16 on the
         tensor-core path (its raw bits reinterpreted) and fp32 on the SIMT path;
-        bias as (B, h, N, N) fp32. On the tensor-core path the plane is stored
-        in fp16 as log2(e) * bias, with -inf where the query-key mask drops a
-        key; it is returned as stored, widened to fp32."""
+        bias as (B, h, N, N) fp32. On the tensor-core path the plane the
+        attention reads is stored in fp16 as log2(e) * (bias minus the largest
+        kept entry of its (head, query) row), with -inf where the query-key
+        mask drops a key; it is returned as stored, widened to fp32."""
         ptr, ld = tri_attn_debug_tensor(self.handle, name)
         if not ptr:
             raise KeyError(name)

@@ -10,8 +10,12 @@
 //                the epilogue writes q, k, v and sigmoid(g + bg) in bf16. The
 //                h pair-bias outputs (Wb x_hat, with gamma and beta folded into
 //                Wb) come out of the LayerNorm's statistics pass on the CUDA
-//                cores and go, scaled by log2(e), to the fp16 bias plane
-//                (B, h, N, Nb), indexed [query, key] along the attended line.
+//                cores and go, scaled by log2(e), to an fp32 plane in cell
+//                order.
+//   bias_rows    the attention's fp16 bias plane (B, h, N, Nb), indexed
+//                [query, key] along the attended line: each (head, query) row
+//                minus its largest entry (the softmax is unchanged, and fp16
+//                is then precise where the weights are large).
 //   mask_summary / mask_summary_cols
 //                keep bits and a "keeps some key" flag of every line.
 //   row_attn_tc  flash-style line attention, persistent: a work unit is
@@ -183,12 +187,11 @@ static_assert(offsetof(Consts, gw) % 16 == 0 && offsetof(Consts, beta) % 16 == 0
 
 struct Params {
   long long cells;
-  int N, Nb, h, mask_mode, ntiles;   // this launch: tiles tile0 .. tile0 + ntiles - 1
+  int N, h, mask_mode, ntiles;       // this launch: tiles tile0 .. tile0 + ntiles - 1
   int tile0;
-  int ending;                  // bias of cell (r, c) goes to plane row c, column r
   const int32_t* mask;
   __nv_bfloat16 *q, *k, *v, *g;
-  __half* bias;                // (B, h, N, Nb) fp16, scaled by log2(e)
+  float* bias32;               // (B, h, N, N) fp32 in cell order, scaled by log2(e)
   unsigned int* dev_err;
   long long polls;
   float q_scale;               // q is stored times log2(e) / sqrt(d)
@@ -364,18 +367,18 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(&bars->a_ready[b]);
       if (cell < p.cells) {
+        // The pair bias of the cell, in cell order (consecutive threads,
+        // consecutive cells): bias_rows turns the plane into the attention's
+        // [query, key] layout.
         const long long bb = cell / NN;
         const long long rc = cell - bb * NN;
-        const long long rr = rc / p.N, cc = rc - rr * p.N;
         bool keep = true;
         if (p.mask_mode == TRI_ATTN_MASK_QUERY_KEY) keep = p.mask[cell] != 0;
-        const long long pr = p.ending ? cc : rr, pc = p.ending ? rr : cc;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           const int head = 2 * hh + t;
           if (head < p.h)
-            p.bias[((bb * p.h + head) * p.N + pr) * p.Nb + pc] =
-                __float2half_rn(keep ? bsum[t] * kLog2e : -INFINITY);
+            p.bias32[(bb * p.h + head) * NN + rc] = keep ? bsum[t] * kLog2e : -INFINITY;
         }
       }
     }
@@ -1139,6 +1142,74 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
 #undef ab
 }
 
+// The attention's bias plane from K1's cell-order plane C (fp32, log2(e) *
+// bias, -inf where the query-key reading drops the key): row (b, t, query a)
+// holds the biases of the keys along line a, which is row a of C (starting
+// node) or column a (ending node: the bias of key k for query a is that of
+// cell (k, a)). Each row is stored in fp16 minus its largest entry: the softmax
+// over keys is unchanged by a per-row constant, and the entries that carry the
+// weight (near the row's largest) are then small in magnitude, where fp16 is
+// precise. A block takes 8 rows of one (b, t) plane, one warp per row, and
+// walks the keys 128 at a time (4 per lane), once for the row maximum and once
+// to write; for the ending node each step first moves a 128-key x 8-query
+// block of C (32 contiguous bytes per key) through shared memory. A row with
+// every key dropped stays -inf.
+__global__ void __launch_bounds__(256)
+bias_rows(const float* __restrict__ C, int N, int Nb, int ending, __half* __restrict__ P) {
+  __shared__ float tile[8][132];
+  const int a0 = blockIdx.x * 8;
+  const long long plane = blockIdx.y;
+  const float* Cp = C + plane * N * N;
+  __half* Pp = P + plane * N * Nb;
+  const int wq = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int a = a0 + wq;                          // this warp's row
+  float m = -INFINITY;
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+#pragma unroll 1
+    for (int k0 = 0; k0 < N; k0 += 128) {
+      float v[4];
+      if (ending) {
+        // Thread i moves C[k0 + i / 2][a0 + 4 (i & 1) .. + 3] to tile[query][key].
+        const int kk = k0 + (threadIdx.x >> 1), qa = 4 * (threadIdx.x & 1);
+        __syncthreads();                          // the previous step has read the tile
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          tile[qa + e][threadIdx.x >> 1] =
+              (kk < N && a0 + qa + e < N) ? Cp[(long long)kk * N + a0 + qa + e] : -INFINITY;
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = tile[wq][4 * lane + e];
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int k = k0 + 4 * lane + e;
+          v[e] = (k < N && a < N) ? Cp[(long long)a * N + k] : -INFINITY;
+        }
+      }
+      if (pass == 0) {
+        m = fmaxf(fmaxf(m, fmaxf(v[0], v[1])), fmaxf(v[2], v[3]));
+      } else if (a < N) {
+        const int k = k0 + 4 * lane;
+        __half hv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) hv[e] = __float2half_rn(m == -INFINITY ? -INFINITY : v[e] - m);
+        if (k + 3 < N) {                          // 8-byte store: Nb and k are multiples of 4
+          *(uint2*)(Pp + (long long)a * Nb + k) = *(const uint2*)hv;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (k + e < N) Pp[(long long)a * Nb + k + e] = hv[e];
+        }
+      }
+    }
+    if (pass == 0) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    }
+  }
+}
+
 // One warp per mask row (b, r): bit k of word k/32 is pair_mask[b, r, k] != 0
 // for k < N (0 beyond, up to `words` words), and any[row] says whether the row
 // keeps some key.
@@ -1497,6 +1568,7 @@ struct TcState {
   CUtensorMap map_gc, map_oc;              // K3 loads, column tiles
   CUtensorMap st_q, st_k, st_v, st_g;      // K1 output stores: (cells, 128) bf16, 32 x 32 boxes
   CUtensorMap map_os;                      // K2 output stores: one head x 32 queries of a row
+  float* bias32;             // (B, h, N, N) fp32 pair bias in cell order (K1's output)
   unsigned char* row_any;    // (B*N) mask rows keeping some key
   uint32_t* mbits;           // (B*N, words) mask bits
   int words;
@@ -1519,11 +1591,11 @@ bool tri_tc_supported(int B, int N, int D, int h) {
 }
 
 size_t tri_tc_extra_bytes(int B, int N, int, int h) {
-  // the fp16 bias plane (rows padded to Nb) replaces the fp32 one; plus the mask summary
+  // the attention's fp16 bias plane (rows padded to Nb) beside K1's fp32 one;
+  // plus the mask summary
   const size_t Nb = (size_t)round_up(N, 8);
-  const size_t f16 = (size_t)B * h * N * Nb * 2, f32 = (size_t)B * h * N * N * 4;
-  return (f16 > f32 ? f16 - f32 : 0) + (size_t)B * N +
-         (size_t)B * N * 2 * ((N + 63) / 64) * 4 + 512;
+  return (size_t)B * h * N * Nb * 2 + (size_t)B * N + (size_t)B * N * 2 * ((N + 63) / 64) * 4 +
+         512;
 }
 
 cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const void* Wv,
@@ -1534,10 +1606,11 @@ cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const voi
   const int B = t->B, N = t->N, D = t->D, h = t->h;
   st->Nb = round_up(N, 8);
   cudaError_t e = cudaDeviceGetAttribute(&st->num_sms, cudaDevAttrMultiProcessorCount, t->device);
-  // This path keeps the bias plane in fp16 with rows padded to Nb (TMA strides
-  // are multiples of 16 bytes).
+  // K1 writes the fp32 plane the handle allocated (cell order); the attention
+  // reads an fp16 plane with rows padded to Nb (TMA strides are multiples of 16
+  // bytes), which takes the handle's bias pointer.
   if (e == cudaSuccess) {
-    cudaFree(t->bias);
+    st->bias32 = t->bias;
     t->bias = nullptr;
     e = cudaMalloc((void**)&t->bias, (size_t)B * h * N * st->Nb * 2);
   }
@@ -1617,6 +1690,7 @@ int tri_tc_bias_row_stride(const tri_attn_s* t) {
 void tri_tc_release(tri_attn_s* t) {
   TcState* st = (TcState*)t->tc;
   if (!st) return;
+  if (st->bias32) cudaFree(st->bias32);
   if (st->row_any) cudaFree(st->row_any);
   if (st->mbits) cudaFree(st->mbits);
   if (st->copy_in) cudaStreamDestroy(st->copy_in);
@@ -1636,12 +1710,11 @@ cudaError_t launch_k1(tri_attn_s* t, cudaStream_t s, const CUtensorMap& map_x,
                       const int32_t* mask, int tile0, int n) {
   TcState* st = (TcState*)t->tc;
   k1::Params p1;
-  p1.cells = t->cells; p1.N = t->N; p1.Nb = st->Nb; p1.h = t->h; p1.mask_mode = t->mask_mode;
-  p1.ending = t->ending ? 1 : 0;
+  p1.cells = t->cells; p1.N = t->N; p1.h = t->h; p1.mask_mode = t->mask_mode;
   p1.ntiles = n; p1.tile0 = tile0;
   p1.mask = mask;
   p1.q = (__nv_bfloat16*)t->q; p1.k = (__nv_bfloat16*)t->k; p1.v = (__nv_bfloat16*)t->v;
-  p1.g = (__nv_bfloat16*)t->g; p1.bias = (__half*)t->bias; p1.dev_err = t->dev_err;
+  p1.g = (__nv_bfloat16*)t->g; p1.bias32 = st->bias32; p1.dev_err = t->dev_err;
   p1.polls = t->wait_limit;
   p1.q_scale = kLog2e / sqrtf((float)t->d);
   const int grid = n < st->num_sms ? n : st->num_sms;
@@ -1664,6 +1737,16 @@ cudaError_t launch_mask(tri_attn_s* t, cudaStream_t s, const int32_t* mask, int&
     k2::mask_summary_cols<<<blocks, 256, 0, s>>>(mask, N, st->words, st->mbits, st->row_any);
     tri_mark(t, s, mark++, "mask_summary_cols");
   }
+  return cudaGetLastError();
+}
+
+// The attention's bias plane from K1's (after every K1 tile).
+cudaError_t launch_bias_rows(tri_attn_s* t, cudaStream_t s, int& mark) {
+  TcState* st = (TcState*)t->tc;
+  const dim3 grid((unsigned)((t->N + 7) / 8), (unsigned)(t->B * t->h));
+  k2::bias_rows<<<grid, 256, 0, s>>>(st->bias32, t->N, st->Nb, t->ending ? 1 : 0,
+                                      (__half*)t->bias);
+  tri_mark(t, s, mark++, "bias_rows");
   return cudaGetLastError();
 }
 
@@ -1744,6 +1827,7 @@ cudaError_t tri_tc_forward(tri_attn_s* t, cudaStream_t s, const void* x, const i
   cudaError_t e = launch_k1(t, s, map_x, mask, 0, ntiles);
   tri_mark(t, s, mark++, "ln_proj_tc");
   if (e == cudaSuccess) e = launch_mask(t, s, mask, mark);
+  if (e == cudaSuccess) e = launch_bias_rows(t, s, mark);
   if (e == cudaSuccess) e = launch_k2(t, s, 0, t->B * k2_row_groups(t) * k2_units_per_group(t));
   tri_mark(t, s, mark++, "row_attn_tc");
   if (e == cudaSuccess) e = launch_k3(t, s, map_out, 0, ntiles, false);
@@ -1810,6 +1894,7 @@ cudaError_t tri_tc_forward_host(tri_attn_s* t, cudaStream_t s, const void* xh,
     e = cudaStreamWaitEvent(s, ev_x[i], 0);
     if (e == cudaSuccess) e = launch_k1(t, s, map_x, dmask, t0, n);
   }
+  if (e == cudaSuccess) e = launch_bias_rows(t, s, mark);
   // K2 chunk boundaries in work units: up to eight equal chunks of whole
   // waves of CTAs (a partial wave takes as long as a full one), the last
   // taking what is left. Each chunk adds a K2 ramp and a K3 launch (~20 us at

@@ -148,17 +148,19 @@ def test_clock_summary_reports_median_and_throttle_reasons():
 
 def test_algorithmic_work_matches_the_per_cell_figures(monkeypatch):
     """The roofline's algorithmic work per cell at the N = 768 bf16 workload:
-    K1 reads x and writes q, k, v, g and the fp16 bias (2D + 8D + 2h = 1288 B);
-    K2 reads q, k, v and the bias and writes o (6D + 2h + 2D = 1032 B) plus the
-    mask bit rows, for 4 B N^3 D FLOPs; K3 reads g and o and writes out (768 B);
-    the mask summary reads the int32 mask. The captured traffic is reported only
+    K1 reads x and writes q, k, v, g and the fp32 bias (2D + 8D + 4h = 1296 B);
+    bias_rows reads that plane and writes the fp16 one (6h = 24 B); K2 reads
+    q, k, v and the fp16 bias and writes o (6D + 2h + 2D = 1032 B) plus the mask
+    bit rows, for 4 B N^3 D FLOPs; K3 reads g and o and writes out (768 B); the
+    mask summary reads the int32 mask. The captured traffic is reported only
     while the kernel sources hash to the capture's."""
     from pair_representation_triangular_gb300 import workloads as W
     w = W.WORKLOADS["b1-n768-d128-h4-bf16-pad700"]
     P, N, D, h = w.cells, w.N, w.D, w.h
     work = bench.algorithmic_work(w)
     bits = N * (1 + 8 * ((N + 63) // 64))
-    assert work["ln_proj"]["bytes"] == 1288 * P
+    assert work["ln_proj"]["bytes"] == 1296 * P
+    assert work["bias_rows"]["bytes"] == 24 * P
     assert work["ln_proj"]["flops"] == 2.0 * P * D * (4 * D + h)
     assert work["row_attn"]["bytes"] == 1032 * P + bits
     assert work["row_attn"]["flops"] == 4.0 * N ** 3 * D
