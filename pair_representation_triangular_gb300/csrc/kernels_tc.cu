@@ -554,8 +554,8 @@ struct Params {
   // x, channel e) of q, k or v sits at b * sb + a * sl + x * sx + e.
   const __nv_bfloat16 *q, *k, *v;
   long long sb, sl, sx;
-  const __half* bias;             // (B, h, N, Nb) fp16, log2(e) * bias, -inf where dropped
-  int Nb;
+  const float* bias32;            // (B, h, N, N) fp32 cell order, log2(e) * bias, -inf where dropped
+  int ending;                     // the key k of query a is cell (k, a) instead of (a, k)
 };
 
 struct Unit {
@@ -698,27 +698,30 @@ __device__ __forceinline__ float2 p_half(const float2 (&x2)[BK / 2], const uint4
   return __fadd2_rn(sa, sb);
 }
 
-// A query row whose sum l left [2^-90, 2^100) (logits beyond about +-100 in
-// log2 units, where P = 2^x with the fixed reference 0 loses range) is
-// recomputed exactly on the CUDA cores: two passes over the line's keys, the
-// first for the row max m, the second for l = sum 2^(x - m) and
-// o = sum 2^(x - m) v / l, in fp32. qrow: the row's q (head t); kl, vl: key 0
-// of the line's k and v (head t), sx: the stride between keys; brow: the row
-// of the bias plane; keys come from the line's mask bits (row reading; mrow)
-// or from the finite biases (query reading, mrow = null: the plane holds -inf
-// for dropped keys). o leaves as 16 bf16 pairs in the lane's row of the
-// 64-byte-swizzled staging tile at stg.
+// A query row whose sum l left [2^-16, 2^100) is recomputed exactly on the
+// CUDA cores: its logits reached about +100 in log2 units (P = 2^x with the
+// fixed reference 0 loses range), or every key it keeps lies more than 16
+// below its (head, query) row's largest bias, which may sit at a key the line
+// drops (the row-key reading), where the fp16 plane's rounding is no longer
+// small. Two passes over the line's keys, the first for the row max m, the
+// second for l = sum 2^(x - m) and o = sum 2^(x - m) v / l, in fp32 with the
+// fp32 bias. qrow: the row's q (head t); kl, vl: key 0 of the line's k and v
+// (head t), sx: the stride between keys; brow: the bias of the row's key 0 in
+// the fp32 cell-order plane and bs the stride between keys; keys come from the
+// line's mask bits (row reading; mrow) or from the finite biases (query
+// reading, mrow = null: the plane holds -inf for dropped keys). o leaves as 16
+// bf16 pairs in the lane's row of the 64-byte-swizzled staging tile at stg.
 __device__ __noinline__ void exact_row(const __nv_bfloat16* qrow, const __nv_bfloat16* kl,
                                        const __nv_bfloat16* vl, long long sx,
-                                       const __half* brow, const uint32_t* mrow, int N,
-                                       uint8_t* stg, int lane) {
+                                       const float* brow, long long bs, const uint32_t* mrow,
+                                       int N, uint8_t* stg, int lane) {
   float q[DH];
 #pragma unroll
   for (int e = 0; e < DH; ++e) q[e] = __bfloat162float(qrow[e]);
   float m = -INFINITY;
   for (int kk = 0; kk < N; ++kk) {
     if (mrow && !((__ldg(mrow + (kk >> 5)) >> (kk & 31)) & 1u)) continue;
-    const float bb = __half2float(brow[kk]);
+    const float bb = brow[(long long)kk * bs];
     if (bb == -INFINITY) continue;
     const __nv_bfloat16* kr = kl + (long long)kk * sx;
     float s = 0.f;
@@ -731,7 +734,7 @@ __device__ __noinline__ void exact_row(const __nv_bfloat16* qrow, const __nv_bfl
   for (int e = 0; e < DH; ++e) o[e] = 0.f;
   for (int kk = 0; kk < N; ++kk) {
     if (mrow && !((__ldg(mrow + (kk >> 5)) >> (kk & 31)) & 1u)) continue;
-    const float bb = __half2float(brow[kk]);
+    const float bb = brow[(long long)kk * bs];
     if (bb == -INFINITY) continue;
     const __nv_bfloat16* kr = kl + (long long)kk * sx;
     float s = 0.f;
@@ -765,7 +768,7 @@ __device__ __noinline__ void exact_row(const __nv_bfloat16* qrow, const __nv_bfl
 // the same buffer. The reference of the exponentials is fixed at 0: no max is
 // taken, and fp32 and bf16 hold 2^x with full relative precision for
 // |x| < ~100, far beyond the logits of layer-normalised activations; a query
-// row whose sum l ends outside [2^-90, 2^100) is recomputed exactly in the
+// row whose sum l ends outside [2^-16, 2^100) is recomputed exactly in the
 // unit epilogue (exact_row). A unit's o = O / l is read and stored after the
 // next unit's first sub-tile, which hides the completion of the unit's last
 // P V.
@@ -984,11 +987,11 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       const Unit fu = decode_unit(p.unit0 + blockIdx.x + ui * gridDim.x, p);
       const int fi = fu.rg * R + r, fj = fu.j0 + (warp & 3) * 32;
       if (fi < N && fj < N) {
-        // A query row has l in [2^-90, 2^100) unless its logits reached about
-        // +-100 (a uniform row or query has l = its count of real keys): those
-        // rows are recomputed exactly.
-        const bool exact = fj + lane < N && !(l >= 0x1p-90f && l < 0x1p100f);
-        const float inv = __fdividef(1.0f, l);   // l lies in [2^-90, 2^100): the fast form is exact enough
+        // A query row has l in [2^-16, 2^100) unless its logits left that range
+        // (a uniform row or query has l = its count of real keys): those rows
+        // are recomputed exactly.
+        const bool exact = fj + lane < N && !(l >= 0x1p-16f && l < 0x1p100f);
+        const float inv = __fdividef(1.0f, l);   // l lies in [2^-16, 2^100): the fast form is exact enough
         uint32_t po[16];
 #pragma unroll
         for (int e = 0; e < DH; e += 2)
@@ -998,8 +1001,11 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         __syncwarp();
         if (__builtin_expect(exact, 0)) {
           const long long base = (long long)fu.b * p.sb + (long long)fi * p.sl + fu.t * DH;
-          exact_row(p.q + base + (long long)(fj + lane) * p.sx, p.k + base, p.v + base, p.sx,
-                    p.bias + (((long long)fu.b * p.h + fu.t) * N + fj + lane) * p.Nb,
+          const long long plane = ((long long)fu.b * p.h + fu.t) * N * N;
+          const int a = fj + lane;             // the query's position along the line
+          exact_row(p.q + base + (long long)a * p.sx, p.k + base, p.v + base, p.sx,
+                    p.bias32 + plane + (p.ending ? (long long)a : (long long)a * N),
+                    p.ending ? (long long)N : 1ll,
                     p.mask_mode == TRI_ATTN_MASK_QUERY_KEY
                         ? nullptr
                         : p.mbits + ((long long)fu.b * N + fi) * p.words,
@@ -1775,8 +1781,8 @@ cudaError_t launch_k2(tri_attn_s* t, cudaStream_t s, int u0, int nu) {
   p2.sb = (long long)N * N * t->D;
   p2.sl = t->ending ? (long long)t->D : (long long)N * t->D;     // line a: row (starting) or column
   p2.sx = t->ending ? (long long)N * t->D : (long long)t->D;     // position along the line
-  p2.bias = (const __half*)t->bias;
-  p2.Nb = st->Nb;
+  p2.bias32 = st->bias32;
+  p2.ending = t->ending ? 1 : 0;
   const unsigned g2 = (unsigned)(p2.units < st->num_sms ? p2.units : st->num_sms);
   {
     const int g1 = (int)g2 / p2.jtiles, gq = g1 / h;

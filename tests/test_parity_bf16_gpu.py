@@ -87,13 +87,13 @@ def test_bf16_forward_host_matches_device():
 
 @pytest.mark.parametrize("mode", [0, 1, 2])
 def test_bf16_logits_rising_past_the_reference_max(mode):
-    """The kernel's exponentials use the fixed reference 0 (P = 2^x); a query
-    row whose sum leaves [2^-90, 2^100) is recomputed exactly in the unit
-    epilogue. Here the pair bias of keys 64..127 sits 56..80 log2 units and
-    that of keys >= 128 at ~115, so every row's sum overflows that range and
-    takes the exact path (mode 2: the ending node, where the same construction
-    on the grid's rows feeds the bias of the column lines). x and Wb are
-    bf16-exact: channel 0 carries a spike of 8 (keys 64..127) or 64 (keys
+    """Large pair biases rising along the keys: those of keys 64..127 sit
+    56..80 log2 units above the first tile's and those of keys >= 128 at ~115
+    (mode 2: the ending node, where the same construction on the grid's rows
+    feeds the bias of the column lines). The bias plane holds each (head,
+    query) row minus its largest entry and the exponentials use the fixed
+    reference 0, so the weights come out right without any rescaling. x and Wb
+    are bf16-exact: channel 0 carries a spike of 8 (keys 64..127) or 64 (keys
     >= 128), and Wb reads channel 0 alone (8.0 per head)."""
     w = W.custom(1, 200, 128, 4, "bf16", "bernoulli", seed=61)
     inp = W.make_inputs(w)
@@ -117,12 +117,10 @@ def test_bf16_logits_rising_past_the_reference_max(mode):
 
 @pytest.mark.parametrize("mode", [0, 1, 2])
 def test_bf16_logits_far_below_zero(mode):
-    """Every pair bias about -141 log2 units: with the fixed reference 0, P =
-    2^x underflows and the row sums fall below 2^-90, so every query row is
-    recomputed exactly (two passes, its own max) in the unit epilogue. The
-    bias is the same for every key of a row, so the weights follow S alone.
-    Channel 0 of every cell carries -64 (bf16-exact) and Wb reads channel 0
-    alone (8.0 per head)."""
+    """Every pair bias about -141 log2 units, nearly the same for every key of
+    a row: the plane subtracts each row's largest entry, so the weights follow
+    S alone without any underflow. Channel 0 of every cell carries -64
+    (bf16-exact) and Wb reads channel 0 alone (8.0 per head)."""
     w = W.custom(1, 150, 128, 4, "bf16", "bernoulli", seed=62)
     inp = W.make_inputs(w)
     inp["x"][..., 0] = -64.0
@@ -154,6 +152,67 @@ def test_bf16_pair_bias_spread_wide(mode):
     inp["x"][..., 0] = (mag * sign).reshape(w.B, w.N, w.N).astype(inp["x"].dtype)
     Wb = np.zeros_like(inp["params"]["Wb"])
     Wb[:, 0] = 16.0
+    inp["params"]["Wb"] = Wb
+    got = H.run_forward(w, inp, mode)[0]
+    if mode & tb.TRI_ATTN_ENDING_NODE:
+        ref = O.forward_ending(inp["x"], inp["pair_mask"], inp["params"], w.h, mode & 1)
+    else:
+        ref = O.forward(inp["x"], inp["pair_mask"], inp["params"], w.h, mode)
+    H.assert_parity(w, got, ref)
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_bf16_exact_rows_for_logits_beyond_range(mode):
+    """One key of every line carries S = q.k/sqrt(d) of about +180 log2 units
+    for head 0 (q reads channel 0 = 2 of every cell, k reads channel 1, which
+    is 0 except a spike of 64 at one key position): P = 2^x overflows, the row
+    sum leaves [2^-16, 2^100) and the unit epilogue recomputes those rows
+    exactly (its own max, fp32). The weights are then one-hot on that key, so
+    bf16 rounding of q and k does not matter. Other heads have q = k = 0."""
+    w = W.custom(1, 130, 128, 4, "bf16", "bernoulli", seed=66)
+    inp = W.make_inputs(w)
+    x = inp["x"]
+    x[..., 0] = 2.0
+    x[..., 1] = 0.0
+    spike = 37                                   # key position carrying the spike
+    if mode & tb.TRI_ATTN_ENDING_NODE:
+        x[0, spike, :, 1] = 64.0                 # keys of column lines are grid rows
+    else:
+        x[0, :, spike, 1] = 64.0
+    P = inp["params"]
+    d = w.D // w.h
+    P["Wq"] = np.zeros_like(P["Wq"])
+    P["Wk"] = np.zeros_like(P["Wk"])
+    P["Wq"][:d, 0] = 1.0
+    P["Wk"][:d, 1] = 1.0
+    got = H.run_forward(w, inp, mode)[0]
+    if mode & tb.TRI_ATTN_ENDING_NODE:
+        ref = O.forward_ending(inp["x"], inp["pair_mask"], inp["params"], w.h, mode & 1)
+    else:
+        ref = O.forward(inp["x"], inp["pair_mask"], inp["params"], w.h, mode)
+    H.assert_parity(w, got, ref)
+
+
+@pytest.mark.parametrize("mode", [0, 2])
+def test_bf16_kept_keys_far_below_a_dropped_maximum(mode):
+    """Row-key reading, padded mask (the first 100 of 130 residues kept): keys
+    >= 100 of every query carry a pair bias of about +88 (natural units) and
+    the kept keys about -88. The bias plane's row maximum sits at a dropped
+    key, so every kept key lies about 250 log2 units below it: P underflows,
+    the row sums fall below 2^-16 and the unit epilogue recomputes those rows
+    exactly from the fp32 bias (the fp16 plane would be too coarse there).
+    Channel 2 carries +-40 (bf16-exact) and Wb reads it alone (8.0 per head)."""
+    w = W.custom(1, 130, 128, 4, "bf16", "padded", n_valid=100, seed=67)
+    inp = W.make_inputs(w)
+    x = inp["x"]
+    if mode & tb.TRI_ATTN_ENDING_NODE:           # key k of column j is cell (k, j)
+        x[0, :100, :, 2] = -40.0
+        x[0, 100:, :, 2] = 40.0
+    else:                                        # key k of row i is cell (j, k) for query j
+        x[0, :, :100, 2] = -40.0
+        x[0, :, 100:, 2] = 40.0
+    Wb = np.zeros_like(inp["params"]["Wb"])
+    Wb[:, 2] = 8.0
     inp["params"]["Wb"] = Wb
     got = H.run_forward(w, inp, mode)[0]
     if mode & tb.TRI_ATTN_ENDING_NODE:
