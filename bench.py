@@ -90,7 +90,8 @@ def algorithmic_work(w):
 # It holds for the tensor-core kernel code whose SHA-256 prefix (comments
 # removed) is recorded here; for any other code the bench reports traffic as
 # null.
-TRAFFIC_SOURCES = ("kernels_tc.cu", "tc_ptx.cuh", "common.cuh")
+TRAFFIC_SOURCES = ("kernels_tc.cu", "tc_k1.cu", "tc_k2.cu", "tc_k3.cu", "tc_kernels.cuh",
+                   "tc_device.cuh", "tc_shapes.h", "tc_ptx.cuh", "common.cuh")
 # The host-buffer pipeline closes kernels_tc.cu: it launches the same kernels
 # for the host-buffer entry point and leaves the device-buffer forward that the
 # capture measured unchanged, so the hash stops where it begins.

@@ -252,7 +252,8 @@ class TriangularAttention:
     def intermediate(self, name: str) -> torch.Tensor:
         """Copy of an intermediate of the most recent forward (see
         tri_attn_debug_tensor): q, k, v, g, o as (B, N, N, D), bf16 on the
-        tensor-core path (its raw bits reinterpreted) and fp32 on the SIMT path;
+        tensor-core path of bf16 handles (its raw bits reinterpreted) and fp32
+        on the SIMT path of fp32 handles;
         bias as (B, h, N, N) fp32. On the tensor-core path the plane the
         attention reads is stored in fp16 as log2(e) * (bias minus the largest
         kept entry of its (head, query) row), with -inf where the query-key

@@ -27,8 +27,7 @@ inline bool tri_ending(int mode) { return (mode & TRI_ATTN_ENDING_NODE) != 0; }
 struct tri_attn_s {
   int B, N, D, h, d, dtype, mask_mode;
   bool ending;                     // ending-node variant (attention along columns)
-  bool simt;                       // fp32 SIMT kernels (fp32 handles, and bf16 shapes the
-                                   // tensor-core path does not cover)
+  bool simt;                       // fp32 SIMT kernels (fp32 handles)
   long long cells;                 // B * N * N
   int device;
   // Packed weights (owned).
@@ -43,8 +42,6 @@ struct tri_attn_s {
   long long wait_limit;
   // Host-buffer staging (forward_host), allocated on first use.
   void* stage_x; int32_t* stage_mask; void* stage_out;
-  // bf16 handle on the SIMT kernels: fp32 copies of pair_repr and out.
-  float* x32; float* out32;
   // Tensor-core path state (opaque to the f32 path).
   void* tc;
   size_t bytes_owned;
@@ -86,7 +83,7 @@ struct TriF32Raw {
 };
 cudaError_t tri_f32_forward_raw(const TriF32Raw& a, cudaStream_t s);
 
-// ---- bf16 tensor-core path (kernels_tc.cu)
+// ---- bf16 tensor-core path (kernels_tc.cu; kernels in tc_k1.cu, tc_k2.cu, tc_k3.cu)
 bool tri_tc_supported(int B, int N, int D, int h);
 cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const void* Wv,
                         const void* Wg, const void* Wb, const void* Wo, cudaStream_t s);

@@ -1,0 +1,112 @@
+// Device helpers shared by the bf16 tensor-core kernels: bounded waits with a
+// CTA-wide abort flag, special-function approximations, packed-fp16 adds and
+// swizzled shared-memory addressing.
+#pragma once
+
+#include <math.h>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+#include "tc_shapes.h"
+
+namespace tri_tc {
+
+struct Abort {
+  int* flag;              // shared-memory flag: nonzero once any role gave up
+  unsigned int* dev_err;  // handle's device error word
+  long long polls;        // poll cap of ordinary waits
+};
+
+// Bounded wait; on time-out or when another role has already aborted, raises
+// the abort flag (and records a time-out) and returns false.
+__device__ __forceinline__ bool wait_or_abort_slow(uint64_t* bar, uint32_t parity, const Abort a) {
+  const uint64_t t0 = tc::global_timer_ns();
+  for (long long n = 1; n < a.polls; ++n) {
+    // Sleeps up to 20 us per poll instead of spinning; the phase wakes it.
+    if (tc::mbar_try_wait_hint(bar, parity, 20000u)) return true;
+    if (tc::lds_volatile(a.flag)) return false;
+    if ((n & 15) == 0 && tc::global_timer_ns() - t0 > 2000000000ull) break;
+  }
+  *(volatile int*)a.flag = 1;
+  atomicOr(a.dev_err, TRI_DEV_ERR_TIMEOUT);
+  return false;
+}
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const Abort& a) {
+  if (tc::mbar_try_wait(bar, parity)) return true;
+  return wait_or_abort_slow(bar, parity, a);
+}
+
+// Warp-uniform form for warps that go on to issue warp-collective tcgen05
+// loads: every lane waits, and the warp proceeds only if all lanes succeeded.
+__device__ __forceinline__ bool warp_wait_or_abort(uint64_t* bar, uint32_t parity, const Abort& a) {
+  const bool ok = wait_or_abort(bar, parity, a);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Drain wait used at teardown: ignores the abort flag and the poll cap so that
+// copies and MMAs still in flight land before the CTA releases its memory.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  tc::mbar_wait(bar, parity, 1ll << 40);
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Logistic function for the gate, 1/(1 + e^-z) = (1 + tanh(z/2)) / 2, with the
+// hardware tanh approximation (one special-function operation; its error is
+// well below the bf16 rounding the gate gets).
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float sigmoid_approx(float z) {
+  return fmaf(0.5f, tanh_approx(0.5f * z), 0.5f);
+}
+
+// fp16 half of a packed pair plus an fp32 value, rounded once in fp32.
+__device__ __forceinline__ float add_f16lo_f32(uint32_t h2, float c) {
+  float d;
+  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, lo, %2;\n\t}"
+      : "=f"(d) : "r"(h2), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float add_f16hi_f32(uint32_t h2, float c) {
+  float d;
+  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, hi, %2;\n\t}"
+      : "=f"(d) : "r"(h2), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
+}
+
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// Shared-memory descriptor swizzle mode for rows of `bytes` (32, 64 or 128).
+__host__ __device__ constexpr uint32_t swz_mode(int bytes) {
+  return bytes == 128 ? tc::SWZ_128B : bytes == 64 ? tc::SWZ_64B : tc::SWZ_32B;
+}
+
+// Byte offset of 16-byte chunk `chunk` of row `row` in a tile whose rows are
+// `row_bytes` (32, 64 or 128) long, swizzled as TMA writes it with the swizzle
+// of the same span: address bits 4.. XOR the bits 7.. of the same address.
+__host__ __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk, uint32_t row_bytes) {
+  return row_bytes == 32 ? row * 32u + ((chunk ^ ((row >> 2) & 1u)) << 4)
+                         : tc::swz_offset(row, chunk, row_bytes);
+}
+
+}  // namespace tri_tc

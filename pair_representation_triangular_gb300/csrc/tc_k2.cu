@@ -1,0 +1,828 @@
+// K2 of the bf16 tensor-core path: flash-style line attention with the pair
+// bias, the mask and the softmax, plus its small companions:
+//
+//   row_attn_tc  persistent: a work unit is (b, head t, R lines, 128 queries)
+//                streaming 64-key tiles. Lines are grid rows (starting node)
+//                or columns (ending node); only the tensor maps tell them
+//                apart. S = Q K^T goes to TMEM; one softmax warpgroup per line
+//                adds the shared fp16 bias tile, drops masked keys and writes
+//                P = 2^x in bf16 over S; O += P V accumulates in TMEM. The
+//                (B, N, h, N, N) logits never exist. Instantiated for d = 16,
+//                32 and 64.
+//   bias_rows    the attention's fp16 bias plane (B, h, N, Nb), indexed
+//                [query, key] along the attended line: each (head, query) row
+//                minus its largest entry (the softmax is unchanged, and fp16
+//                is then precise where the weights are large).
+//   mask_summary / mask_summary_cols
+//                keep bits and a "keeps some key" flag of every line.
+//
+// Passages followed: POPCORNBENCH "Kimi-K2.6 l2_p6", forward op list steps
+// 10-16 (scaled logits, pair bias, mask, softmax, weighted sum of v);
+// "FW-GLM-5-1 l2_p6", quoted Model.forward (the mask broadcast).
+#include "tc_device.cuh"
+#include "tc_kernels.cuh"
+
+namespace tri_tc {
+namespace k2 {
+
+template <int R>
+struct Bars {
+  uint64_t q_full[2], q_empty[2], kv_full[KV_STAGES], kv_empty[KV_STAGES];
+  uint64_t b_full[B_STAGES], b_empty[B_STAGES];
+  // s_ready and p_full follow the S/P buffer (sub-tile parity): a warp with no
+  // live lanes runs ahead, and its arrivals for sub-tile c + 1 must not complete
+  // the phase of sub-tile c.
+  uint64_t s_ready[R][2], p_full[R][2], p_free[R][2], o_free[R], drain[R];
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct Unit {
+  int b, t, rg, jt, j0;
+};
+
+__device__ __forceinline__ Unit decode_unit(int u, const Params& p) {
+  Unit un;
+  un.jt = u % p.jtiles;
+  un.t = (u / p.jtiles) % p.h;
+  const int rgb = u / (p.jtiles * p.h);
+  un.rg = rgb % p.row_groups;
+  un.b = rgb / p.row_groups;
+  un.j0 = un.jt * BQ;
+  return un;
+}
+
+// The unit gridDim.x further on: digit-wise addition with carries (each digit
+// of the step is below its radix, so one subtraction per digit suffices).
+__device__ __forceinline__ void step_unit(Unit& u, const Params& p) {
+  int v = u.jt + p.step.jt;
+  int c = v >= p.jtiles;
+  u.jt = c ? v - p.jtiles : v;
+  v = u.t + p.step.t + c;
+  c = v >= p.h;
+  u.t = c ? v - p.h : v;
+  v = u.rg + p.step.rg + c;
+  c = v >= p.row_groups;
+  u.rg = c ? v - p.row_groups : v;
+  u.b += p.step.b + c;
+  u.j0 = u.jt * BQ;
+}
+
+// Position in a stream of sub-tiles: global sub-tile c, its unit ui and key
+// sub-tile kt, the K/V stage slot and phase, and the bias slot and phase,
+// advanced without dividing.
+struct SubIt {
+  int c, ui, kt, kvs, kvph, bs, bph;
+};
+template <int SPS>
+__device__ __forceinline__ void advance(SubIt& it, int KT) {
+  ++it.c;
+  const bool stage_end = (it.kt % SPS) == SPS - 1 || it.kt == KT - 1;
+  if (++it.kt == KT) { it.kt = 0; ++it.ui; }
+  if (stage_end && ++it.kvs == KV_STAGES) { it.kvs = 0; it.kvph ^= 1; }
+  if (++it.bs == B_STAGES) { it.bs = 0; it.bph ^= 1; }
+}
+
+// The softmax's position in its sub-tile stream: global sub-tile c, key
+// sub-tile kt and the bias slot and phase.
+struct SoftIt {
+  int c, kt, bs, bph;
+};
+__device__ __forceinline__ void advance_soft(SoftIt& it, int KT) {
+  ++it.c;
+  if (++it.kt == KT) it.kt = 0;
+  if (++it.bs == B_STAGES) { it.bs = 0; it.bph ^= 1; }
+}
+
+// Real-key bits of word w (keys 32w..32w+31 of a sub-tile with `left` keys left).
+__device__ __forceinline__ uint32_t real_bits(int left, int w) {
+  const int n = left - 32 * w;
+  return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
+}
+
+// The 32 fp16 biases of half hf of a sub-tile row (brow: the row's swizzled
+// base, 16-byte chunk q at brow ^ (q << 4)).
+__device__ __forceinline__ void load_bias_half(uint32_t brow, int hf, uint4 (&bh)[4]) {
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) bh[q4] = tc::lds128(brow ^ ((hf * 4 + q4) << 4));
+}
+
+// Common path of one 32-key half: P = 2^(S + bias) (S in log2 units, the
+// reference mu = 0 and every lane live), packed in bf16 pairs; returns the
+// sum of P in two partial sums.
+__device__ __forceinline__ float2 p_half_fast(const float2 (&x2)[BK / 2], const uint4 (&bh)[4],
+                                              int hf, uint32_t (&pk)[16]) {
+  float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    const uint32_t hw[4] = {bh[q4].x, bh[q4].y, bh[q4].z, bh[q4].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 x = x2[(hf * 4 + q4) * 4 + e];
+      const float2 p2 = make_float2(ex2_approx(add_f16lo_f32(hw[e], x.x)),
+                                    ex2_approx(add_f16hi_f32(hw[e], x.y)));
+      if (e & 1) sb = __fadd2_rn(sb, p2);
+      else sa = __fadd2_rn(sa, p2);
+      pk[q4 * 4 + e] = tc::pack_bf16x2(p2.x, p2.y);
+    }
+  }
+  return __fadd2_rn(sa, sb);
+}
+
+// P of one 32-key half of a lane that is not live: 1 on every real key of a
+// uniform row or query (`w` = that half's real-key bits), else 0.
+__device__ __forceinline__ void p_half_const(uint32_t w, uint32_t (&pk)[16]) {
+  if (w == 0u || w == 0xffffffffu) {
+    const uint32_t v = w ? 0x3F803F80u : 0u;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) pk[k] = v;
+  } else {
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+      pk[k] = (((w >> (2 * k)) & 1u) ? 0x3F80u : 0u) | (((w >> (2 * k + 1)) & 1u) ? 0x3F800000u : 0u);
+  }
+}
+
+// General path of one 32-key half: P = 2^(S + bias - mu) for a live lane; a
+// lane that is not live writes 1 on every real key of a uniform row or query
+// (`w` = that half's real-key bits), else 0.
+__device__ __forceinline__ float2 p_half(const float2 (&x2)[BK / 2], const uint4 (&bh)[4], int hf,
+                                         float mu, bool live, uint32_t w, uint32_t (&pk)[16]) {
+  float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
+  if (live) {
+    const float2 nmu2 = make_float2(-mu, -mu);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const uint32_t hw[4] = {bh[q4].x, bh[q4].y, bh[q4].z, bh[q4].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 y = __fadd2_rn(x2[(hf * 4 + q4) * 4 + e], nmu2);
+        const float2 p2 = make_float2(ex2_approx(add_f16lo_f32(hw[e], y.x)),
+                                      ex2_approx(add_f16hi_f32(hw[e], y.y)));
+        if (e & 1) sb = __fadd2_rn(sb, p2);
+        else sa = __fadd2_rn(sa, p2);
+        pk[q4 * 4 + e] = tc::pack_bf16x2(p2.x, p2.y);
+      }
+    }
+  } else {
+    p_half_const(w, pk);
+  }
+  return __fadd2_rn(sa, sb);
+}
+
+// A query row whose sum l left [2^-16, 2^100) is recomputed exactly on the
+// CUDA cores: its logits reached about +100 in log2 units (P = 2^x with the
+// fixed reference 0 loses range), or every key it keeps lies more than 16
+// below its (head, query) row's largest bias, which may sit at a key the line
+// drops (the row-key reading), where the fp16 plane's rounding is no longer
+// small. Two passes over the line's keys, the first for the row max m, the
+// second for l = sum 2^(x - m) and o = sum 2^(x - m) v / l, in fp32 with the
+// fp32 bias. qrow: the row's q (head t); kl, vl: key 0 of the line's k and v
+// (head t), sx: the stride between keys; brow: the bias of the row's key 0 in
+// the fp32 cell-order plane and bs the stride between keys; keys come from the
+// line's mask bits (row reading; mrow) or from the finite biases (query
+// reading, mrow = null: the plane holds -inf for dropped keys). o leaves as 16
+// bf16 pairs in the lane's row of the swizzled staging tile at stg (rows of
+// 2 d bytes).
+template <int DH>
+__device__ __noinline__ void exact_row(const __nv_bfloat16* qrow, const __nv_bfloat16* kl,
+                                       const __nv_bfloat16* vl, long long sx,
+                                       const float* brow, long long bs, const uint32_t* mrow,
+                                       int N, uint8_t* stg, int lane) {
+  float q[DH];
+#pragma unroll
+  for (int e = 0; e < DH; ++e) q[e] = __bfloat162float(qrow[e]);
+  float m = -INFINITY;
+  for (int kk = 0; kk < N; ++kk) {
+    if (mrow && !((__ldg(mrow + (kk >> 5)) >> (kk & 31)) & 1u)) continue;
+    const float bb = brow[(long long)kk * bs];
+    if (bb == -INFINITY) continue;
+    const __nv_bfloat16* kr = kl + (long long)kk * sx;
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < DH; ++e) s = fmaf(q[e], __bfloat162float(kr[e]), s);
+    m = fmaxf(m, s + bb);
+  }
+  float l = 0.f, o[DH];
+#pragma unroll
+  for (int e = 0; e < DH; ++e) o[e] = 0.f;
+  for (int kk = 0; kk < N; ++kk) {
+    if (mrow && !((__ldg(mrow + (kk >> 5)) >> (kk & 31)) & 1u)) continue;
+    const float bb = brow[(long long)kk * bs];
+    if (bb == -INFINITY) continue;
+    const __nv_bfloat16* kr = kl + (long long)kk * sx;
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < DH; ++e) s = fmaf(q[e], __bfloat162float(kr[e]), s);
+    const float w = exp2f(s + bb - m);
+    l += w;
+    const __nv_bfloat16* vr = vl + (long long)kk * sx;
+#pragma unroll
+    for (int e = 0; e < DH; ++e) o[e] = fmaf(w, __bfloat162float(vr[e]), o[e]);
+  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+  for (int qc = 0; qc < DH / 8; ++qc) {
+    uint32_t w4[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      w4[e] = tc::pack_bf16x2(o[8 * qc + 2 * e] * inv, o[8 * qc + 2 * e + 1] * inv);
+    *(uint4*)(stg + swz(lane, qc, 2 * DH)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  }
+}
+
+// Persistent: CTA c serves work units unit0 + c, + G, ... A unit is (b, head
+// t, R lines, 128 queries), R = 3 (d = 16, 32) or 2 (d = 64, whose three
+// lines would not fit tensor memory); it streams 64-key sub-tiles. The K and
+// V tiles of the R lines arrive KVK keys at a time (128: one stage serves two
+// sub-tiles; 64 for d = 64, where shared memory is short); the fp16 bias
+// sub-tile they share has a ring of its own. Warpgroup 0: warp 0 TMA, warp
+// 1 + r issues the MMAs of line r (both roles run as whole warps; one elected
+// lane issues); warpgroup 1 + r runs the softmax of line r, with registers
+// moved to it from warpgroup 0 (setmaxnreg). Tensor memory per line: S0 | S1
+// (64 fp32 columns each) | O (d columns from column 128).
+// Softmax warpgroup r owns line r; sub-tile c's S = Q K^T lands in the line's
+// S buffer c & 1 in log2 units (q carries the factor log2(e)/sqrt(d)), and the
+// softmax adds the bias, drops masked keys and writes P = 2^x (bf16) over it
+// in one pass; the line's MMA warp then issues O += P V(c) and S(c + 2) into
+// the same buffer. The reference of the exponentials is fixed at 0: no max is
+// taken, and fp32 and bf16 hold 2^x with full relative precision for
+// |x| < ~100, far beyond the logits of layer-normalised activations; a query
+// row whose sum l ends outside [2^-16, 2^100) is recomputed exactly in the
+// unit epilogue (exact_row). A unit's o = O / l is read and stored after the
+// next unit's first sub-tile, which hides the completion of the unit's last
+// P V.
+template <int DH>
+__global__ void __launch_bounds__(Shape<DH>::kThreads, 1)
+row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+            const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_b,
+            const __grid_constant__ CUtensorMap map_o, const Params p) {
+  using S = Shape<DH>;
+  constexpr int R = S::R, SPS = S::SPS, SW = S::SW;
+  constexpr int kIssuers = S::kIssuers, kSoftmaxWarps = S::kSoftmaxWarps;
+  constexpr int kRegsCtl = S::kRegsCtl, kRegsSoftmax = S::kRegsSoftmax;
+  constexpr int kTmemPerRow = S::kTmemPerRow;
+  constexpr uint32_t Q_BYTES = S::Q_BYTES, KVT_BYTES = S::KVT_BYTES, KV_STAGE = S::KV_STAGE;
+  constexpr uint32_t HALF_KV = S::HALF_KV, OST_BYTES = S::OST_BYTES;
+  constexpr uint32_t OFF_Q = S::OFF_Q, OFF_KV = S::OFF_KV, OFF_BIAS = S::OFF_BIAS;
+  constexpr uint32_t OFF_OST = S::OFF_OST, OFF_BAR = S::OFF_BAR;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  Bars<R>* bars = (Bars<R>*)(smem + OFF_BAR);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // The abort context is rebuilt from the kernel parameters at each use.
+#define ab (Abort{&bars->abort, p.dev_err, p.polls})
+  const int N = p.N;
+  const int KT = (N + BK - 1) / BK;
+  int my_units = 0;
+  for (int u = blockIdx.x; u < p.units; u += gridDim.x) ++my_units;
+
+  if (tid == 0) {
+    for (int q = 0; q < 2; ++q) {
+      tc::mbar_init(&bars->q_full[q], 1);
+      tc::mbar_init(&bars->q_empty[q], kIssuers);    // one commit per issuer
+    }
+    for (int s = 0; s < KV_STAGES; ++s) {
+      tc::mbar_init(&bars->kv_full[s], 1);
+      tc::mbar_init(&bars->kv_empty[s], kIssuers);
+    }
+    for (int s = 0; s < B_STAGES; ++s) {
+      tc::mbar_init(&bars->b_full[s], 1);
+      tc::mbar_init(&bars->b_empty[s], kSoftmaxWarps);   // one arrive per softmax warp
+    }
+    for (int r = 0; r < R; ++r) {
+      for (int b = 0; b < 2; ++b) {
+        tc::mbar_init(&bars->s_ready[r][b], 1);
+        tc::mbar_init(&bars->p_full[r][b], 128);
+        tc::mbar_init(&bars->p_free[r][b], 1);
+      }
+      tc::mbar_init(&bars->o_free[r], 128);
+      tc::mbar_init(&bars->drain[r], 1);
+    }
+    bars->abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&bars->tmem_base, 512);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  int q_issued = 0, kv_issued = 0, b_issued = 0;    // producer: loads issued
+
+  if (warp < 4) {
+    tc::regs_dec<kRegsCtl>();
+    if (warp == 0) {
+      // ---------------- TMA producer (whole warp; one elected lane issues)
+      if (elect_one()) {
+        tc::tma_prefetch_desc(&map_q);
+        tc::tma_prefetch_desc(&map_k);
+        tc::tma_prefetch_desc(&map_v);
+        tc::tma_prefetch_desc(&map_b);
+      }
+      __syncwarp();
+      Unit un = decode_unit(p.unit0 + blockIdx.x, p);
+      int kvs = 0, kvph = 0, bs = 0, bph = 0;
+      bool ok = true;
+      for (int ui = 0; ok && ui < my_units; ++ui, step_unit(un, p)) {
+        const int a0 = un.rg * R;
+        const int qb = ui & 1;
+        if (ui >= 2 && !warp_wait_or_abort(&bars->q_empty[qb], ((ui >> 1) - 1) & 1, ab)) break;
+        if (elect_one()) {
+          tc::mbar_arrive_expect_tx(&bars->q_full[qb], R * Q_BYTES);
+          for (int r = 0; r < R; ++r)
+            tc::tma_load_4d(smem + OFF_Q + (qb * R + r) * Q_BYTES, &map_q, &bars->q_full[qb],
+                            un.t * DH, un.j0, a0 + r, un.b);
+        }
+        __syncwarp();
+        q_issued = ui + 1;
+        for (int kt = 0; kt < KT; ++kt) {
+          if (kt % SPS == 0) {
+            if (kv_issued >= KV_STAGES && !warp_wait_or_abort(&bars->kv_empty[kvs], kvph ^ 1, ab)) {
+              ok = false;
+              break;
+            }
+            if (elect_one()) {
+              uint8_t* st = smem + OFF_KV + kvs * KV_STAGE;
+              tc::mbar_arrive_expect_tx(&bars->kv_full[kvs], KV_STAGE);
+              for (int r = 0; r < R; ++r) {
+                tc::tma_load_4d(st + r * 2 * KVT_BYTES, &map_k, &bars->kv_full[kvs], un.t * DH,
+                                kt * BK, a0 + r, un.b);
+                tc::tma_load_4d(st + r * 2 * KVT_BYTES + KVT_BYTES, &map_v, &bars->kv_full[kvs],
+                                un.t * DH, kt * BK, a0 + r, un.b);
+              }
+            }
+            __syncwarp();
+            ++kv_issued;
+            if (++kvs == KV_STAGES) { kvs = 0; kvph ^= 1; }
+          }
+          if (b_issued >= B_STAGES && !warp_wait_or_abort(&bars->b_empty[bs], bph ^ 1, ab)) {
+            ok = false;
+            break;
+          }
+          if (elect_one()) {
+            tc::mbar_arrive_expect_tx(&bars->b_full[bs], BIAS_BYTES);
+            tc::tma_load_3d(smem + OFF_BIAS + bs * BIAS_BYTES, &map_b, &bars->b_full[bs], kt * BK,
+                            un.j0, un.b * p.h + un.t);
+          }
+          __syncwarp();
+          ++b_issued;
+          if (++bs == B_STAGES) { bs = 0; bph ^= 1; }
+        }
+      }
+    } else if (warp - 1 < R) {
+      // ---------------- MMA issuer of line r = warp - 1 (whole warp; one elected lane
+      // issues). With R = 2, warp 3 has no role and goes straight to the teardown.
+      const int r = warp - 1;
+      const uint32_t tr = tmem + r * kTmemPerRow;
+      constexpr uint32_t id_qk = tc::idesc_bf16_f32(128, BK, 0, 0);
+      constexpr uint32_t id_pv = tc::idesc_bf16_f32(128, DH, 0, 1);
+      // Descriptors of this line's first Q tile and first K tile; every other
+      // operand sits a multiple of 16 bytes further (the start-address field
+      // holds address / 16 and stays below 2^14).
+      const uint64_t dq0 = tc::smem_desc(tc::smem_addr(smem + OFF_Q + r * Q_BYTES), 16, 8 * SW, swz_mode(SW));
+      const uint64_t dk0 =
+          tc::smem_desc(tc::smem_addr(smem + OFF_KV + r * 2 * KVT_BYTES), 16, 8 * SW, swz_mode(SW));
+      const int total = my_units * KT;     // one item per key sub-tile
+      auto qk = [&](const SubIt& it) -> bool {
+        const int c = it.c;
+        if (it.kt == 0 && !warp_wait_or_abort(&bars->q_full[it.ui & 1], (it.ui >> 1) & 1, ab)) return false;
+        if (it.kt % SPS == 0 && !warp_wait_or_abort(&bars->kv_full[it.kvs], it.kvph, ab)) return false;
+        tc::tc_fence_after();
+        if (elect_one()) {
+          const uint64_t qd = dq0 + (uint64_t)(((it.ui & 1) * R * Q_BYTES) >> 4);
+          const uint64_t kd = dk0 + (uint64_t)((it.kvs * KV_STAGE + (it.kt % SPS) * HALF_KV) >> 4);
+#pragma unroll
+          for (int ks = 0; ks < DH / 16; ++ks)
+            tc::mma_bf16_ss(tr + (c & 1) * TM_S1, qd + 2 * ks, kd + 2 * ks, id_qk, ks > 0);
+          tc::mma_commit(&bars->s_ready[r][c & 1]);
+          if (it.kt == KT - 1) tc::mma_commit(&bars->q_empty[it.ui & 1]);
+        }
+        __syncwarp();
+        return true;
+      };
+      auto pv = [&](const SubIt& it) -> bool {
+        const int c = it.c;
+        if (!warp_wait_or_abort(&bars->p_full[r][c & 1], (c >> 1) & 1, ab)) return false;
+        if (it.kt == 0 && it.ui >= 1 && !warp_wait_or_abort(&bars->o_free[r], (it.ui - 1) & 1, ab))
+          return false;
+        tc::tc_fence_after();
+        if (elect_one()) {
+          const uint64_t vd =
+              dk0 + (uint64_t)((it.kvs * KV_STAGE + KVT_BYTES + (it.kt % SPS) * HALF_KV) >> 4);
+#pragma unroll
+          for (int ks = 0; ks < BK / 16; ++ks)
+            tc::mma_bf16_ts(tr + TM_O, tr + (c & 1) * TM_S1 + ks * 8, vd + SW * ks, id_pv,
+                            (it.kt > 0 || ks > 0) ? 1u : 0u);
+          tc::mma_commit(&bars->p_free[r][c & 1]);
+          if (it.kt % SPS == SPS - 1 || it.kt == KT - 1) tc::mma_commit(&bars->kv_empty[it.kvs]);
+        }
+        __syncwarp();
+        return true;
+      };
+      bool ok = true;
+      SubIt itq{0, 0, 0, 0, 0, 0, 0}, itp{0, 0, 0, 0, 0, 0, 0};
+      for (; ok && itq.c < 2 && itq.c < total; advance<SPS>(itq, KT)) ok = qk(itq);
+      for (; ok && itp.c < total; advance<SPS>(itp, KT)) {
+        ok = pv(itp);
+        if (ok && itq.c < total) {
+          ok = qk(itq);
+          advance<SPS>(itq, KT);
+        }
+      }
+      if (elect_one()) tc::mma_commit(&bars->drain[r]);
+      __syncwarp();
+      drain_wait(&bars->drain[r], 0);
+    }
+  } else {
+    // ---------------- softmax warpgroups: line r of each unit, thread = query row
+    tc::regs_inc<kRegsSoftmax>();
+    const int r = (warp >> 2) - 1;
+    const int sw = warp - 4;                         // softmax warp index
+    const int jr = (warp & 3) * 32 + lane;          // query row of the tile = TMEM lane
+    const uint32_t tb = tmem + ((uint32_t)((warp & 3) * 32) << 16) + r * kTmemPerRow;
+    // Bias row jr of a stage (128-byte swizzle: 16-byte chunk q of the row sits
+    // at chunk q ^ (jr & 7)); the row base is 128-byte aligned.
+    const uint32_t brow0 = tc::smem_addr(smem + OFF_BIAS) + jr * 128u + ((jr & 7u) << 4);
+    const bool qk_mode = p.mask_mode == TRI_ATTN_MASK_QUERY_KEY;
+    // A unit's mask summary: the "keeps some key" flag of this lane's query
+    // row (query-key) or of the line (row-key), and the mask row whose bits
+    // give the keys this lane keeps. Loaded one unit ahead.
+    auto unit_loads = [&](const Unit& nu, unsigned& any, const uint32_t*& mrow) {
+      const int nj = nu.j0 + jr, ni = nu.rg * R + r;
+      const int mr = qk_mode ? nj : ni;
+      // Queries past N produce nothing (their stores are clipped): they count
+      // as keeping keys so that they never force the general path.
+      any = mr < N ? __ldg(p.row_any + (long long)nu.b * N + mr) : (qk_mode ? 1u : 0u);
+      mrow = p.mbits + ((long long)nu.b * N + (mr < N ? mr : 0)) * p.words;
+    };
+    unsigned nx_any = 0u;
+    const uint32_t* nx_mrow = p.mbits;
+    if (my_units > 0) unit_loads(decode_unit(p.unit0 + blockIdx.x, p), nx_any, nx_mrow);
+    // Unit epilogue: o = O / l once the unit's last P V has landed, staged in
+    // shared memory and written by one TMA store per warp (queries past N are
+    // clipped by the store; lines past N and warps whose 32 queries all lie
+    // past N skip it).
+    uint8_t* const ostg = smem + OFF_OST + sw * OST_BYTES;
+    auto finish_unit = [&](int ui, int clast, float l) -> bool {
+      if (!warp_wait_or_abort(&bars->p_free[r][clast & 1], (clast >> 1) & 1, ab)) return false;
+      tc::tc_fence_after();
+      uint32_t ov[DH];
+      if constexpr (DH == 16) {
+        tc::tmem_ld16(tb + TM_O, *(uint32_t(*)[16])ov);
+      } else {
+#pragma unroll
+        for (int hc = 0; hc < DH / 32; ++hc)
+          tc::tmem_ld32(tb + TM_O + 32 * hc, *(uint32_t(*)[32]) & ov[32 * hc]);
+      }
+      tc::tmem_ld_wait();
+      // O is in registers: its columns may take the next unit's sums.
+      tc::tc_fence_before();
+      tc::mbar_arrive(&bars->o_free[r]);
+      const Unit fu = decode_unit(p.unit0 + blockIdx.x + ui * gridDim.x, p);
+      const int fi = fu.rg * R + r, fj = fu.j0 + (warp & 3) * 32;
+      if (fi < N && fj < N) {
+        // A query row has l in [2^-16, 2^100) unless its logits left that range
+        // (a uniform row or query has l = its count of real keys): those rows
+        // are recomputed exactly.
+        const bool exact = fj + lane < N && !(l >= 0x1p-16f && l < 0x1p100f);
+        const float inv = __fdividef(1.0f, l);   // l lies in [2^-16, 2^100): the fast form is exact enough
+        uint32_t po[DH / 2];
+#pragma unroll
+        for (int e = 0; e < DH; e += 2)
+          po[e / 2] = tc::pack_bf16x2(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
+        // The previous store (if any) has read the staging tile.
+        if (lane == 0) tc::tma_store_wait_read<0>();
+        __syncwarp();
+        if (__builtin_expect(exact, 0)) {
+          const long long base = (long long)fu.b * p.sb + (long long)fi * p.sl + fu.t * DH;
+          const long long plane = ((long long)fu.b * p.h + fu.t) * N * N;
+          const int a = fj + lane;             // the query's position along the line
+          exact_row<DH>(p.q + base + (long long)a * p.sx, p.k + base, p.v + base, p.sx,
+                    p.bias32 + plane + (p.ending ? (long long)a : (long long)a * N),
+                    p.ending ? (long long)N : 1ll,
+                    p.mask_mode == TRI_ATTN_MASK_QUERY_KEY
+                        ? nullptr
+                        : p.mbits + ((long long)fu.b * N + fi) * p.words,
+                    N, ostg, lane);
+        } else {
+#pragma unroll
+          for (int q = 0; q < DH / 8; ++q)
+            *(uint4*)(ostg + swz(lane, q, SW)) =
+                make_uint4(po[4 * q], po[4 * q + 1], po[4 * q + 2], po[4 * q + 3]);
+        }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tc::tma_store_4d(&map_o, ostg, fu.t * DH, fj, fi, fu.b);
+          tc::tma_store_commit();
+        }
+      }
+      return true;
+    };
+    bool ok = true;
+    SoftIt its{0, 0, 0, 0};                         // this warp's sub-tile stream
+    float l_prev = 0.f;
+    for (int ui = 0; ok && ui < my_units; ++ui) {
+      const bool uni = nx_any == 0u;
+      const uint32_t* mrow = nx_mrow;
+      if (ui + 1 < my_units)
+        unit_loads(decode_unit(p.unit0 + blockIdx.x + (ui + 1) * gridDim.x, p), nx_any, nx_mrow);
+      float l_run = 0.f;
+      // Warp-uniform unit state: whether any lane has a key-keeping query row,
+      // and whether every lane has one.
+      const bool unit_live = __any_sync(0xffffffffu, !uni);
+      const bool all_live = __all_sync(0xffffffffu, !uni);
+      uint2 nbits = __ldg((const uint2*)mrow);
+      for (int kt = 0; ok && kt < KT; ++kt, advance_soft(its, KT)) {
+        const int c = its.c;
+        const uint2 mb = nbits;
+        if (kt + 1 < KT) nbits = __ldg((const uint2*)(mrow + 2 * (kt + 1)));
+        const int left = N - kt * BK;
+        const uint32_t rl0 = real_bits(left, 0), rl1 = real_bits(left, 1);
+        // Keys kept by this lane (query-key: its own query row; row-key: the
+        // line, the same for the whole warp).
+        const uint32_t kb0 = rl0 & mb.x, kb1 = rl1 & mb.y;
+        // Row-key: S of a dropped key is set to -inf. Query-key: the bias plane
+        // already holds -inf there.
+        const uint32_t bw0 = qk_mode ? rl0 : kb0, bw1 = qk_mode ? rl1 : kb1;
+        const bool all_kept = (bw0 & bw1) == 0xffffffffu;      // warp-uniform
+        const bool tile_keys = (bw0 | bw1) != 0u;              // warp-uniform
+        const bool live = !uni && tile_keys;
+        const uint32_t brow = brow0 + its.bs * BIAS_BYTES;
+        // The bias stage and S(c): both barriers are polled back to back so
+        // that their latencies overlap, then one vote settles them.
+        bool okk = tc::mbar_try_wait(&bars->b_full[its.bs], its.bph);
+        bool oks = tc::mbar_try_wait(&bars->s_ready[r][c & 1], (c >> 1) & 1);
+        if (!okk) okk = wait_or_abort_slow(&bars->b_full[its.bs], its.bph, ab);
+        if (okk && !oks) oks = wait_or_abort_slow(&bars->s_ready[r][c & 1], (c >> 1) & 1, ab);
+        if (!__all_sync(0xffffffffu, okk && oks)) { ok = false; break; }
+        const bool any_live = unit_live && tile_keys;
+        tc::tc_fence_after();
+        const uint32_t tsb = tb + (c & 1) * TM_S1;     // S(c), then P(c) over it
+        float2 x2[BK / 2];
+        uint4 bh0[4], bh1[4];
+        float tsum = 0.f;
+        if (any_live) {
+          tc::tmem_ld32(tsb, *(uint32_t(*)[32])&x2[0]);
+          tc::tmem_ld32(tsb + 32, *(uint32_t(*)[32])&x2[16]);
+          load_bias_half(brow, 0, bh0);
+          load_bias_half(brow, 1, bh1);
+          tc::tmem_ld_wait();
+          if (!all_kept) {
+            // Dropped keys: S = -inf, which the bias add keeps at -inf (P = 0).
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              if (!((bw0 >> (2 * k)) & 1u)) x2[k].x = -INFINITY;
+              if (!((bw0 >> (2 * k + 1)) & 1u)) x2[k].y = -INFINITY;
+              if (!((bw1 >> (2 * k)) & 1u)) x2[16 + k].x = -INFINITY;
+              if (!((bw1 >> (2 * k + 1)) & 1u)) x2[16 + k].y = -INFINITY;
+            }
+          }
+          uint32_t pk[16];
+          float2 ts2;
+          if (all_live) {
+            ts2 = p_half_fast(x2, bh0, 0, pk);
+            tc::tmem_st16(tsb, pk);
+            ts2 = __fadd2_rn(ts2, p_half_fast(x2, bh1, 1, pk));
+            tc::tmem_st16(tsb + 16, pk);
+          } else {
+            const uint32_t w0 = uni ? rl0 : 0u, w1 = uni ? rl1 : 0u;
+            ts2 = p_half(x2, bh0, 0, 0.f, live, w0, pk);
+            tc::tmem_st16(tsb, pk);
+            ts2 = __fadd2_rn(ts2, p_half(x2, bh1, 1, 0.f, live, w1, pk));
+            tc::tmem_st16(tsb + 16, pk);
+          }
+          tsum = ts2.x + ts2.y;
+        } else {
+          // No lane of the warp keeps a key of this sub-tile: P is 1 on the real
+          // keys of a uniform row or query, else 0.
+          uint32_t pk[16];
+          p_half_const(uni ? rl0 : 0u, pk);
+          tc::tmem_st16(tsb, pk);
+          p_half_const(uni ? rl1 : 0u, pk);
+          tc::tmem_st16(tsb + 16, pk);
+        }
+        // The bias stage is read: release it.
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bars->b_empty[its.bs]);
+        if (live) {
+          l_run += tsum;
+        } else if (uni) {
+          l_run += (float)(__popc(rl0) + __popc(rl1));
+        }
+        tc::tmem_st_wait();
+        tc::tc_fence_before();
+        tc::mbar_arrive(&bars->p_full[r][c & 1]);
+        if (kt == 0 && ui >= 1) {
+          // The previous unit's epilogue, after this unit's first sub-tile.
+          if (!finish_unit(ui - 1, c - 1, l_prev)) { ok = false; break; }
+        }
+      }
+      if (!ok) break;
+      l_prev = l_run;
+    }
+    if (ok && my_units > 0) finish_unit(my_units - 1, my_units * KT - 1, l_prev);
+    if (lane == 0) tc::tma_store_wait_all<0>();
+  }
+
+  // ---------------- teardown
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0 && lane == 0) {
+    for (int ui = q_issued - 1; ui >= 0 && ui >= q_issued - 2; --ui)
+      drain_wait(&bars->q_full[ui & 1], (ui >> 1) & 1);
+    for (int g = kv_issued - 1; g >= 0 && g >= kv_issued - KV_STAGES; --g)
+      drain_wait(&bars->kv_full[g % KV_STAGES], (g / KV_STAGES) & 1);
+    for (int g = b_issued - 1; g >= 0 && g >= b_issued - B_STAGES; --g)
+      drain_wait(&bars->b_full[g % B_STAGES], (g / B_STAGES) & 1);
+  }
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == 1) tc::tmem_dealloc(tmem, 512);
+#undef ab
+}
+
+// The attention's bias plane from K1's cell-order plane C (fp32, log2(e) *
+// bias, -inf where the query-key reading drops the key): row (b, t, query a)
+// holds the biases of the keys along line a, which is row a of C (starting
+// node) or column a (ending node: the bias of key k for query a is that of
+// cell (k, a)). Each row is stored in fp16 minus its largest entry: the softmax
+// over keys is unchanged by a per-row constant, and the entries that carry the
+// weight (near the row's largest) are then small in magnitude, where fp16 is
+// precise. A block takes 8 rows of one (b, t) plane, one warp per row, and
+// walks the keys 128 at a time (4 per lane), once for the row maximum and once
+// to write; for the ending node each step first moves a 128-key x 8-query
+// block of C (32 contiguous bytes per key) through shared memory. A row with
+// every key dropped stays -inf.
+__global__ void __launch_bounds__(256)
+bias_rows(const float* __restrict__ C, int N, int Nb, int ending, __half* __restrict__ P) {
+  __shared__ float tile[8][132];
+  const int a0 = blockIdx.x * 8;
+  const long long plane = blockIdx.y;
+  const float* Cp = C + plane * N * N;
+  __half* Pp = P + plane * N * Nb;
+  const int wq = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int a = a0 + wq;                          // this warp's row
+  float m = -INFINITY;
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+#pragma unroll 1
+    for (int k0 = 0; k0 < N; k0 += 128) {
+      float v[4];
+      if (ending) {
+        // Thread i moves C[k0 + i / 2][a0 + 4 (i & 1) .. + 3] to tile[query][key].
+        const int kk = k0 + (threadIdx.x >> 1), qa = 4 * (threadIdx.x & 1);
+        __syncthreads();                          // the previous step has read the tile
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          tile[qa + e][threadIdx.x >> 1] =
+              (kk < N && a0 + qa + e < N) ? Cp[(long long)kk * N + a0 + qa + e] : -INFINITY;
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = tile[wq][4 * lane + e];
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int k = k0 + 4 * lane + e;
+          v[e] = (k < N && a < N) ? Cp[(long long)a * N + k] : -INFINITY;
+        }
+      }
+      if (pass == 0) {
+        m = fmaxf(fmaxf(m, fmaxf(v[0], v[1])), fmaxf(v[2], v[3]));
+      } else if (a < N) {
+        const int k = k0 + 4 * lane;
+        __half hv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) hv[e] = __float2half_rn(m == -INFINITY ? -INFINITY : v[e] - m);
+        if (k + 3 < N) {                          // 8-byte store: Nb and k are multiples of 4
+          *(uint2*)(Pp + (long long)a * Nb + k) = *(const uint2*)hv;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (k + e < N) Pp[(long long)a * Nb + k + e] = hv[e];
+        }
+      }
+    }
+    if (pass == 0) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    }
+  }
+}
+
+// One warp per mask row (b, r): bit k of word k/32 is pair_mask[b, r, k] != 0
+// for k < N (0 beyond, up to `words` words), and any[row] says whether the row
+// keeps some key.
+__global__ void mask_summary(const int32_t* __restrict__ mask, int N, long long rows, int words,
+                             uint32_t* __restrict__ bits, unsigned char* __restrict__ any) {
+  const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int lane = threadIdx.x & 31;
+  unsigned found = 0;
+  for (int wd = 0; wd < words; ++wd) {
+    const int k = wd * 32 + lane;
+    const bool keep = k < N && mask[row * N + k] != 0;
+    const unsigned w = __ballot_sync(0xffffffffu, keep);
+    found |= w;
+    if (lane == 0) bits[row * words + wd] = w;
+  }
+  if (lane == 0) any[row] = found != 0;
+}
+
+// Ending node: line (b, a) is column a of the mask (key k = grid row k). A
+// block takes 32 columns of one batch, lane = column a; warp wp forms the
+// words w = wp, wp + 8, ... (bit kk of word w: pair_mask[b, 32 w + kk, a] != 0,
+// each of its 32 loads one coalesced 128-byte row segment across the warp),
+// and the block ORs them into the column's "keeps some key" flag.
+__global__ void __launch_bounds__(256)
+mask_summary_cols(const int32_t* __restrict__ mask, int N, int words, uint32_t* __restrict__ bits,
+                  unsigned char* __restrict__ any) {
+  __shared__ uint32_t found[8][32];
+  const int cblocks = (N + 31) >> 5;
+  const long long b = blockIdx.x / cblocks;
+  const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
+  const int a = (int)(blockIdx.x % cblocks) * 32 + lane;
+  uint32_t acc = 0;
+  if (a < N) {
+    const int32_t* col = mask + b * N * N + a;
+    for (int w = wp; w < words; w += 8) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int kk = 0; kk < 32; ++kk) {
+        const int k = 32 * w + kk;
+        if (k < N && col[(long long)k * N] != 0) word |= 1u << kk;
+      }
+      bits[(b * N + a) * words + w] = word;
+      acc |= word;
+    }
+  }
+  found[wp][lane] = acc;
+  __syncthreads();
+  if (wp == 0 && a < N) {
+#pragma unroll
+    for (int i = 1; i < 8; ++i) acc |= found[i][lane];
+    any[b * N + a] = acc != 0;
+  }
+}
+
+template <int DH>
+cudaError_t launch(int grid, cudaStream_t s, const Maps& m, const Params& p) {
+  row_attn_tc<DH><<<grid, Shape<DH>::kThreads, Shape<DH>::SMEM, s>>>(m.q, m.k, m.v, m.b, m.o, p);
+  return cudaGetLastError();
+}
+
+template <int DH>
+cudaError_t set_smem() {
+  return cudaFuncSetAttribute(row_attn_tc<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Shape<DH>::SMEM);
+}
+
+}  // namespace k2
+
+cudaError_t k2_init() {
+  cudaError_t e = k2::set_smem<16>();
+  if (e == cudaSuccess) e = k2::set_smem<32>();
+  if (e == cudaSuccess) e = k2::set_smem<64>();
+  return e;
+}
+
+int k2_lines_per_unit(int d) {
+  return d == 16 ? k2::Shape<16>::R : d == 32 ? k2::Shape<32>::R : k2::Shape<64>::R;
+}
+
+int k2_keys_per_stage(int d) {
+  return d == 16 ? k2::Shape<16>::KVK : d == 32 ? k2::Shape<32>::KVK : k2::Shape<64>::KVK;
+}
+
+cudaError_t k2_launch(int d, int grid, cudaStream_t s, const k2::Maps& m, const k2::Params& p) {
+  switch (d) {
+    case 16: return k2::launch<16>(grid, s, m, p);
+    case 32: return k2::launch<32>(grid, s, m, p);
+    case 64: return k2::launch<64>(grid, s, m, p);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t k2_mask_summary(const int32_t* mask, int B, int N, bool ending, int words,
+                            uint32_t* bits, unsigned char* any, cudaStream_t s) {
+  const long long rows = (long long)B * N;
+  if (!ending) {
+    k2::mask_summary<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(mask, N, rows, words, bits, any);
+  } else {
+    const unsigned blocks = (unsigned)(B * (long long)((N + 31) / 32));
+    k2::mask_summary_cols<<<blocks, 256, 0, s>>>(mask, N, words, bits, any);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t k2_bias_rows(const float* C, int B, int h, int N, int Nb, bool ending, __half* P,
+                         cudaStream_t s) {
+  const dim3 grid((unsigned)((N + 7) / 8), (unsigned)(B * h));
+  k2::bias_rows<<<grid, 256, 0, s>>>(C, N, Nb, ending ? 1 : 0, P);
+  return cudaGetLastError();
+}
+
+}  // namespace tri_tc

@@ -1,5 +1,6 @@
 // C ABI of libtriattn: argument checks, ownership of weights and workspace,
-// dispatch to the fp32 SIMT path or the bf16 tensor-core path.
+// dispatch by dtype: fp32 handles run the fp32 SIMT kernels, bf16 handles the
+// tensor-core kernels (bf16 shapes those do not cover are refused at create).
 #include <stdlib.h>
 #include <string.h>
 
@@ -30,45 +31,12 @@ cudaError_t to_f32(const void* src, int dtype, int n, float* dst, cudaStream_t s
   return cudaGetLastError();
 }
 
-// bf16 <-> fp32 over n elements (n a multiple of 2; rounding to nearest even).
-__global__ void bf16_to_f32_kernel(const __nv_bfloat162* __restrict__ src, long long n2,
-                                   float2* __restrict__ dst) {
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n2;
-       i += (long long)gridDim.x * blockDim.x)
-    dst[i] = __bfloat1622float2(src[i]);
-}
-__global__ void f32_to_bf16_kernel(const float2* __restrict__ src, long long n2,
-                                   __nv_bfloat162* __restrict__ dst) {
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n2;
-       i += (long long)gridDim.x * blockDim.x)
-    dst[i] = __float22bfloat162_rn(src[i]);
-}
-
-// Shapes the SIMT kernels take: even D <= 256, d <= 128.
+// Shapes the fp32 SIMT kernels take: even D <= 256, d <= 128.
 bool simt_shape(int D, int h) { return D <= 256 && D / h <= 128 && !(D & 1); }
-
-// The bf16 weights of a handle on the SIMT kernels, converted to fp32 and packed.
-cudaError_t pack_bf16_for_simt(tri_attn_s* t, const void* const (&w)[6], cudaStream_t s) {
-  const int D = t->D, h = t->h;
-  const int n[6] = {D * D, D * D, D * D, D * D, h * D, D * D};
-  float* tmp[6] = {};
-  cudaError_t e = cudaSuccess;
-  for (int i = 0; i < 6 && e == cudaSuccess; ++i) {
-    e = cudaMalloc((void**)&tmp[i], (size_t)n[i] * sizeof(float));
-    if (e == cudaSuccess) e = to_f32(w[i], TRI_ATTN_BF16, n[i], tmp[i], s);
-  }
-  if (e == cudaSuccess) e = tri_f32_pack_weights(t, tmp[0], tmp[1], tmp[2], tmp[3], tmp[4], tmp[5], s);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  for (float* p : tmp)
-    if (p) cudaFree(p);
-  return e;
-}
 
 void free_all(tri_attn_s* t) {
   if (!t) return;
   if (t->tc) tri_tc_release(t);
-  if (t->x32) cudaFree(t->x32);
-  if (t->out32) cudaFree(t->out32);
   if (t->timing)
     for (int i = 0; i < 8; ++i) cudaEventDestroy(t->marks[i]);
   void* ptrs[] = {t->w_proj, t->w_out, t->gamma, t->beta, t->bg, t->bo, t->wb_f32,
@@ -84,29 +52,25 @@ int check_shape(int B, int N, int D, int h, int dtype) {
   if (dtype != TRI_ATTN_F32 && dtype != TRI_ATTN_BF16) return TRI_ATTN_ERR_INVALID_ARG;
   const long long cells = (long long)B * N * N;
   if (cells * (long long)D > (1ll << 40)) return TRI_ATTN_ERR_INVALID_ARG;
-  if (dtype == TRI_ATTN_F32) {
-    if (!simt_shape(D, h)) return TRI_ATTN_ERR_UNSUPPORTED;
-  } else if (!tri_tc_supported(B, N, D, h) && !simt_shape(D, h)) {
+  // bf16 runs on the tensor-core kernels alone: D in {32, 64, 128} and
+  // d = D / h in {16, 32, 64}, with B N^2 below 2^31 cells; there is no other
+  // bf16 backend.
+  if (dtype == TRI_ATTN_F32 ? !simt_shape(D, h) : !tri_tc_supported(B, N, D, h))
     return TRI_ATTN_ERR_UNSUPPORTED;
-  }
   return TRI_ATTN_OK;
 }
 
-// Whether a handle of this shape and dtype runs on the fp32 SIMT kernels.
-bool uses_simt(int B, int N, int D, int h, int dtype) {
-  return dtype == TRI_ATTN_F32 || !tri_tc_supported(B, N, D, h);
-}
+// Whether a handle of this dtype runs on the fp32 SIMT kernels.
+bool uses_simt(int dtype) { return dtype == TRI_ATTN_F32; }
 
 size_t base_bytes(int B, int N, int D, int h, int dtype) {
-  const bool simt = uses_simt(B, N, D, h, dtype);
-  const size_t es = simt ? sizeof(float) : tri_elem_size(dtype);     // weights, intermediates
+  const size_t es = tri_elem_size(dtype);                              // weights, intermediates
   const size_t cells = (size_t)B * N * N;
   size_t bytes = 0;
   bytes += (size_t)(4 * D + h + 16) * D * es + (size_t)D * D * es;   // packed weights
   bytes += (size_t)(5 * D + h) * sizeof(float);                       // gamma beta bg bo Wb
   bytes += 5 * cells * D * es;                                         // q k v g o
   bytes += (size_t)B * h * N * N * sizeof(float);                      // bias plane
-  if (simt && dtype == TRI_ATTN_BF16) bytes += 2 * cells * D * sizeof(float);   // x, out
   return bytes + 256;
 }
 
@@ -134,7 +98,7 @@ int tri_attn_workspace_bytes(int B, int N, int D, int h, int dtype, size_t* byte
   int st = check_shape(B, N, D, h, dtype);
   if (st) return st;
   *bytes = base_bytes(B, N, D, h, dtype) +
-           (uses_simt(B, N, D, h, dtype) ? 0 : tri_tc_extra_bytes(B, N, D, h));
+           (uses_simt(dtype) ? 0 : tri_tc_extra_bytes(B, N, D, h));
   return TRI_ATTN_OK;
 }
 
@@ -158,10 +122,10 @@ int tri_attn_create(tri_attn_t* out, int B, int N, int D, int h, int dtype, int 
   t->dtype = dtype; t->mask_mode = tri_mask_mode(mode); t->ending = tri_ending(mode);
   t->cells = (long long)B * N * N;
   t->wait_limit = TRI_DEFAULT_WAIT_LIMIT;
-  t->simt = uses_simt(B, N, D, h, dtype);
+  t->simt = uses_simt(dtype);
   cudaError_t e = cudaGetDevice(&t->device);
 
-  const size_t es = t->simt ? sizeof(float) : tri_elem_size(dtype);
+  const size_t es = tri_elem_size(dtype);
   const size_t act = (size_t)t->cells * D * es;
   const size_t nproj_pad = (size_t)4 * D + h + 16;
   auto alloc = [&](void** p, size_t n) {
@@ -178,10 +142,6 @@ int tri_attn_create(tri_attn_t* out, int B, int N, int D, int h, int dtype, int 
   alloc(&t->q, act); alloc(&t->k, act); alloc(&t->v, act); alloc(&t->g, act); alloc(&t->o, act);
   alloc((void**)&t->bias, (size_t)B * h * N * N * sizeof(float));
   alloc((void**)&t->dev_err, 256);
-  if (t->simt && dtype == TRI_ATTN_BF16) {
-    alloc((void**)&t->x32, (size_t)t->cells * D * sizeof(float));
-    alloc((void**)&t->out32, (size_t)t->cells * D * sizeof(float));
-  }
   if (e == cudaSuccess) e = cudaMemsetAsync(t->dev_err, 0, 256, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(t->w_proj, 0, nproj_pad * D * es, s);
   if (e == cudaSuccess) e = to_f32(ln_gamma, dtype, D, t->gamma, s);
@@ -192,9 +152,6 @@ int tri_attn_create(tri_attn_t* out, int B, int N, int D, int h, int dtype, int 
   if (e == cudaSuccess) {
     if (dtype == TRI_ATTN_F32) {
       e = tri_f32_pack_weights(t, Wq, Wk, Wv, Wg, Wb, Wo, s);
-    } else if (t->simt) {
-      const void* const w[6] = {Wq, Wk, Wv, Wg, Wb, Wo};
-      e = pack_bf16_for_simt(t, w, s);
     } else {
       e = tri_tc_init(t, Wq, Wk, Wv, Wg, Wb, Wo, s);
     }
@@ -224,17 +181,6 @@ int tri_attn_forward(tri_attn_t t, void* stream, const void* pair_repr, const in
   cudaError_t e;
   if (t->dtype == TRI_ATTN_F32) {
     e = tri_f32_forward(t, s, (const float*)pair_repr, pair_mask, (float*)out);
-  } else if (t->simt) {
-    // bf16 in and out around the fp32 kernels.
-    const long long n2 = t->cells * t->D / 2;
-    const unsigned grid = (unsigned)std::min<long long>((n2 + 255) / 256, 4096);
-    bf16_to_f32_kernel<<<grid, 256, 0, s>>>((const __nv_bfloat162*)pair_repr, n2, (float2*)t->x32);
-    e = cudaGetLastError();
-    if (e == cudaSuccess) e = tri_f32_forward(t, s, t->x32, pair_mask, t->out32);
-    if (e == cudaSuccess) {
-      f32_to_bf16_kernel<<<grid, 256, 0, s>>>((const float2*)t->out32, n2, (__nv_bfloat162*)out);
-      e = cudaGetLastError();
-    }
   } else {
     e = tri_tc_forward(t, s, pair_repr, pair_mask, out);
   }
@@ -271,7 +217,7 @@ int tri_attn_forward_host(tri_attn_t t, void* stream, const void* pair_repr_host
     if (e != cudaSuccess) return cuda_status(e);
     t->bytes_owned += 2 * xbytes + mbytes;
   }
-  if (t->dtype == TRI_ATTN_BF16 && !t->simt && !t->timing) {
+  if (t->dtype == TRI_ATTN_BF16 && !t->timing) {
     // Copies overlapped with the kernels (chunked).
     e = tri_tc_forward_host(t, s, pair_repr_host, pair_mask_host, out_host, t->stage_x,
                             t->stage_mask, t->stage_out);

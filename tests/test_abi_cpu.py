@@ -54,6 +54,30 @@ def test_create_rejects_bad_arguments_before_cuda(lib):
     assert _create(lib, 1, 8, 33, 3, 1) == tb.TRI_ATTN_ERR_UNSUPPORTED      # bf16 odd D
 
 
+# bf16 runs on the tensor-core kernels alone: D in {32, 64, 128} and
+# d = D / h in {16, 32, 64}. Every other bf16 shape is refused before any CUDA
+# call (there is no other bf16 backend); fp32 handles of those shapes are taken.
+BF16_SHAPES = [(32, 2), (32, 1), (64, 4), (64, 2), (64, 1), (128, 8), (128, 4), (128, 2)]
+BF16_REFUSED = [(96, 3), (96, 2), (128, 1), (256, 4), (64, 8), (32, 4), (48, 3), (128, 16), (16, 1)]
+
+
+@pytest.mark.parametrize("D,h", BF16_REFUSED)
+def test_bf16_shapes_outside_the_tensor_core_set_are_refused(lib, D, h):
+    assert _create(lib, 1, 8, D, h, tb.TRI_ATTN_BF16) == tb.TRI_ATTN_ERR_UNSUPPORTED
+    with pytest.raises(tb.TriAttnError) as e:
+        tb.tri_attn_workspace_bytes(1, 8, D, h, tb.TRI_ATTN_BF16)
+    assert e.value.status == tb.TRI_ATTN_ERR_UNSUPPORTED
+    if D <= 256 and D // h <= 128 and D % 2 == 0:
+        assert tb.tri_attn_workspace_bytes(1, 8, D, h, tb.TRI_ATTN_F32) > 0
+
+
+@pytest.mark.parametrize("D,h", BF16_SHAPES)
+def test_bf16_tensor_core_shapes_are_accepted(lib, D, h):
+    n = tb.tri_attn_workspace_bytes(2, 40, D, h, tb.TRI_ATTN_BF16)
+    cells = 2 * 40 * 40
+    assert n >= 5 * cells * D * 2 + 2 * h * 40 * 40 * (4 + 2)
+
+
 def test_null_handle_calls(lib):
     assert lib.tri_attn_forward(None, None, 16, 16, 16) == tb.TRI_ATTN_ERR_INVALID_ARG
     assert lib.tri_attn_forward_host(None, None, 16, 16, 16) == tb.TRI_ATTN_ERR_INVALID_ARG

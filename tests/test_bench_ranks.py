@@ -70,9 +70,12 @@ def test_traffic_hash_covers_the_kernels_and_not_the_host_pipeline():
     assert sha_with("kernels_tc.cu", k + "\nstatic int after_the_pipeline = 1;\n") == base
     assert sha_with("kernels_tc.cu", k[:cut] + k[cut:].replace("8 * wave", "6 * wave")) == base
     assert sha_with("kernels_tc.cu", "// a comment line\n" + k) == base
+    shapes = src["tc_shapes.h"]
     kernel_line = "constexpr int BM = 128;"
-    assert kernel_line in k[:cut]
-    assert sha_with("kernels_tc.cu", k.replace(kernel_line, "constexpr int BM = 64;", 1)) != base
+    assert kernel_line in shapes
+    assert sha_with("tc_shapes.h", shapes.replace(kernel_line, "constexpr int BM = 64;", 1)) != base
+    k2 = src["tc_k2.cu"]
+    assert sha_with("tc_k2.cu", k2.replace("SPS == SPS - 1", "SPS == 0", 1)) != base
     launch = "launch_k3(t, s, map_out, 0, ntiles, false)"
     assert launch in k[:cut]
     assert sha_with("kernels_tc.cu", k.replace(launch, "launch_k3(t, s, map_out, 0, ntiles, true)", 1)) != base

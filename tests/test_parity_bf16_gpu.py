@@ -301,25 +301,48 @@ def test_bf16_large_common_offset(mode):
     H.assert_parity(w, got, ref)
 
 
-@pytest.mark.parametrize("B,N,D,h,mode", [(1, 40, 64, 4, 0), (2, 33, 128, 2, 1), (1, 17, 96, 3, 2),
-                                          (1, 50, 128, 8, 3), (1, 70, 32, 1, 0)])
-def test_bf16_shapes_outside_the_tensor_core_path(B, N, D, h, mode):
-    """bf16 handles whose shape the tensor-core kernels do not cover run on the
-    fp32 SIMT kernels (pair_repr widened to fp32 and out rounded to bf16 on the
-    device), and still meet the bf16 bar."""
-    w = W.custom(B, N, D, h, "bf16", "bernoulli", seed=9000 + N + D + h)
+# Every (D, h) the tensor-core kernels are built for: D in {32, 64, 128} and
+# d = D / h in {16, 32, 64} (R = 3 lines per attention unit for d = 16, 32;
+# R = 2 and 64-key K/V stages for d = 64).
+TC_SHAPES = [(32, 2), (32, 1), (64, 4), (64, 2), (64, 1), (128, 8), (128, 4), (128, 2)]
+
+
+def _oracle(inp, w, mode):
+    if mode & tb.TRI_ATTN_ENDING_NODE:
+        return O.forward_ending(inp["x"], inp["pair_mask"], inp["params"], w.h, mode & 1)
+    return O.forward(inp["x"], inp["pair_mask"], inp["params"], w.h, mode)
+
+
+@pytest.mark.parametrize("D,h", TC_SHAPES)
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+def test_bf16_every_tensor_core_shape(D, h, mode):
+    """Each shape of the tensor-core kernels, both mask readings, both nodes, at
+    N = 130: two 128-query tiles, three 64-key sub-tiles, 133 cell tiles, each
+    with a ragged tail."""
+    B = 2 if D == 32 else 1
+    w = W.custom(B, 130, D, h, "bf16", "bernoulli", seed=9100 + D + h)
     inp = W.make_inputs(w)
-    mod = tb.TriangularAttention(B, N, D, h, tb.TRI_ATTN_BF16, mode, H.device_params(inp, w))
+    mod = tb.TriangularAttention(B, w.N, D, h, tb.TRI_ATTN_BF16, mode, H.device_params(inp, w))
     try:
-        assert tb.tri_attn_kernel_path(mod.handle) == tb.TRI_ATTN_PATH_SIMT
+        assert tb.tri_attn_kernel_path(mod.handle) == tb.TRI_ATTN_PATH_TENSOR_CORE
     finally:
         mod.close()
     got = H.run_forward(w, inp, mode)[0]
-    if mode & tb.TRI_ATTN_ENDING_NODE:
-        ref = O.forward_ending(inp["x"], inp["pair_mask"], inp["params"], h, mode & 1)
-    else:
-        ref = O.forward(inp["x"], inp["pair_mask"], inp["params"], h, mode)
-    H.assert_parity(w, got, ref)
+    H.assert_parity(w, got, _oracle(inp, w, mode))
+
+
+@pytest.mark.parametrize("D,h", [(64, 4), (64, 1), (32, 2)])
+@pytest.mark.parametrize("N", [1, 3, 65, 129, 200])
+def test_bf16_tensor_core_shapes_ragged(D, h, N):
+    """The head dimensions 16 and 64 and the smallest pair dimension at sizes
+    from a single cell to several tiles plus a tail (starting node with the
+    query-key reading on odd N, the ending node with the row-key reading on
+    even N)."""
+    mode = 1 if N % 2 else 2
+    w = W.custom(1 + (N % 2), N, D, h, "bf16", "bernoulli", seed=9300 + N + D + h)
+    inp = W.make_inputs(w)
+    got = H.run_forward(w, inp, mode)[0]
+    H.assert_parity(w, got, _oracle(inp, w, mode))
 
 
 def test_bf16_benchmark_shape_takes_the_tensor_core_path():

@@ -49,6 +49,10 @@ def _run(w, mode):
 CASES = [(W.custom(1, 130, 128, 4, "bf16", "bernoulli", seed=71), 0),
          (W.custom(1, 130, 128, 4, "bf16", "bernoulli", seed=72), 1),
          (W.custom(2, 33, 64, 4, "f32", "bernoulli", seed=73), 0)]
+# The other tensor-core shapes (D, h): each kernel's instantiation on its own.
+CASES += [(W.custom(1, 130, D, h, "bf16", "bernoulli", seed=74 + i), i % 2)
+          for i, (D, h) in enumerate([(32, 2), (32, 1), (64, 4), (64, 2), (64, 1), (128, 8),
+                                      (128, 2)])]
 
 
 @pytest.mark.parametrize("w,mode", CASES, ids=[f"{w.name}-m{m}" for w, m in CASES])
