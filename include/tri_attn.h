@@ -68,24 +68,26 @@ enum { TRI_ATTN_PATH_SIMT = 0, TRI_ATTN_PATH_TENSOR_CORE = 1 };
 enum {
   TRI_ATTN_OK = 0,
   TRI_ATTN_ERR_INVALID_ARG = 1,    /* bad pointer, shape, alignment or handle       */
-  TRI_ATTN_ERR_UNSUPPORTED = 2,    /* valid but not built (e.g. bf16 with D != 128) */
+  TRI_ATTN_ERR_UNSUPPORTED = 2,    /* valid but not built (e.g. bf16 with d = 128)  */
   TRI_ATTN_ERR_CUDA = 3,           /* a CUDA runtime call failed                     */
   TRI_ATTN_ERR_OOM = 4,            /* device allocation failed                       */
   TRI_ATTN_ERR_DEVICE_TIMEOUT = 5, /* a kernel's bounded wait ran out                */
   TRI_ATTN_ERR_DEVICE_CHECK = 6    /* a kernel's own bounds/alignment check failed   */
 };
 
-/* Build a handle for one problem shape and one set of weights.
+/* Build a handle for one problem shape and one set of weights: the module's
+ * constructor, ModelNew(pair_dim = D, num_heads = h, dropout) on
+ * "Kimi-K2.6 l2_p6" (layer definitions), with the dropout of the inference
+ * forward, the identity (no dropout argument).
  *
  * B, N, D, h: batch, pair-grid side, channels, heads; D % h == 0. Supported:
  *   TRI_ATTN_F32  any B, N >= 1, even D <= 256 with d = D/h <= 128, on the fp32
  *                 SIMT kernels;
- *   TRI_ATTN_BF16 the tensor-core kernels for D == 128, h == 4 (d == 32), any B,
- *                 1 <= N <= 8192, B*N*N < 2^31; other shapes within the fp32
- *                 limits run on the fp32 SIMT kernels, with pair_repr converted
- *                 to fp32 and out rounded to bf16 on the device (see
- *                 tri_attn_kernel_path).
- *   Other shapes return TRI_ATTN_ERR_UNSUPPORTED (nothing runs on the host).
+ *   TRI_ATTN_BF16 the tensor-core kernels, for D in {32, 64, 128} and
+ *                 d = D/h in {16, 32, 64} (D = 128, h = 4 among them), any B,
+ *                 1 <= N <= 8192, B*N*N < 2^31.
+ *   Other shapes return TRI_ATTN_ERR_UNSUPPORTED before any CUDA call: there is
+ *   no second bf16 backend and nothing runs on the host.
  * mode: a mask reading (TRI_ATTN_MASK_ROW_KEY or TRI_ATTN_MASK_QUERY_KEY),
  *   OR-ed with TRI_ATTN_ENDING_NODE for the ending-node variant (see above);
  *   any other bit gives TRI_ATTN_ERR_INVALID_ARG.
@@ -106,7 +108,10 @@ int tri_attn_create(tri_attn_t* out, int B, int N, int D, int h, int dtype, int 
                     const void* Wg, const void* bg, const void* Wb,
                     const void* Wo, const void* bo, void* stream);
 
-/* One forward pass, asynchronous on `stream`; allocates nothing.
+/* One forward pass, asynchronous on `stream`; allocates nothing. The module's
+ * forward(pair_repr, pair_mask) on "Kimi-K2.6 l2_p6" (forward op list steps
+ * 1-18; the mask broadcast as in the Model.forward quoted on
+ * "FW-GLM-5-1 l2_p6"), computed as written at the top of this header.
  *
  * pair_repr: device (B, N, N, D) of the handle's dtype, 16-byte aligned.
  * pair_mask: device (B, N, N) int32, nonzero = keep.
@@ -117,7 +122,9 @@ int tri_attn_create(tri_attn_t* out, int B, int N, int D, int h, int dtype, int 
 int tri_attn_forward(tri_attn_t t, void* stream, const void* pair_repr,
                      const int32_t* pair_mask, void* out);
 
-/* The same forward pass on HOST buffers: copies pair_repr and pair_mask to the
+/* The same forward pass on HOST buffers (the operation of tri_attn_forward;
+ * the pages' forward takes tensors wherever they live, this call is the
+ * host-memory form of it): copies pair_repr and pair_mask to the
  * device (into staging buffers the handle owns; allocated at the first call),
  * runs the forward pass and copies the result back into `out_host`, ordered
  * after the work already queued on `stream`, then synchronises `stream` and
@@ -131,25 +138,33 @@ int tri_attn_forward_host(tri_attn_t t, void* stream, const void* pair_repr_host
                           const int32_t* pair_mask_host, void* out_host);
 
 /* Synchronise `stream`, then report any error the handle's kernels recorded on
- * the device since the last check (and clear it). */
+ * the device since the last check (and clear it). The pages have no
+ * counterpart: their module raises no device-side errors; this reports the
+ * bounded waits and checks of this library's kernels. */
 int tri_attn_sync_check(tri_attn_t t, void* stream);
 
-/* Release everything the handle owns. The caller must make sure no work that
- * uses the handle is still running. NULL is accepted. */
+/* Release everything the handle owns (the end of the module's lifetime; no
+ * counterpart on the pages). The caller must make sure no work that uses the
+ * handle is still running. NULL is accepted. */
 int tri_attn_destroy(tri_attn_t t);
 
-/* Which kernels a handle runs: TRI_ATTN_PATH_TENSOR_CORE or TRI_ATTN_PATH_SIMT
- * (negative status for a NULL handle). */
+/* Which kernels a handle runs: TRI_ATTN_PATH_TENSOR_CORE for every bf16 handle,
+ * TRI_ATTN_PATH_SIMT for every fp32 handle (negative status for a NULL handle).
+ * No counterpart on the pages. */
 int tri_attn_kernel_path(tri_attn_t t);
 
-/* Human-readable name of a status code (static storage). */
+/* Human-readable name of a status code (static storage; no counterpart on the
+ * pages). */
 const char* tri_attn_status_string(int status);
 
-/* Bytes of device memory a handle of this shape owns (weights + workspace). */
+/* Bytes of device memory a handle of this shape owns (weights + workspace); the
+ * same shape rules and status codes as tri_attn_create, checked without any
+ * CUDA call. No counterpart on the pages. */
 int tri_attn_workspace_bytes(int B, int N, int D, int h, int dtype, size_t* bytes);
 
-/* Per-kernel timing. With `enable` nonzero, every later tri_attn_forward records
- * a CUDA event on its stream before its first kernel and after each kernel
+/* Per-kernel timing (instrumentation; no counterpart on the pages). With
+ * `enable` nonzero, every later tri_attn_forward records a CUDA event on its
+ * stream before its first kernel and after each kernel
  * (events the handle owns; a few microseconds of stream work per forward).
  * tri_attn_kernel_times then reports the duration of each kernel of the most
  * recent forward. */
@@ -161,12 +176,16 @@ int tri_attn_enable_kernel_timing(tri_attn_t t, int enable);
  * (0 when timing is off or nothing ran). names[i] receives a static string. */
 int tri_attn_kernel_times(tri_attn_t t, float* ms, const char** names, int* n);
 
-/* Diagnostic access to the handle's intermediates (valid until destroy; they
+/* Diagnostic access to the handle's intermediates, the tensors of the forward
+ * op list on "Kimi-K2.6 l2_p6" before the gate and output projection (valid
+ * until destroy; they
  * hold the results of the most recent forward once it has finished):
  *   "q", "k", "v", "g", "o"  (B*N*N, D) per cell the projections, the
  *                           post-sigmoid gate and the attention output before
- *                           the gate: bf16 on the tensor-core path, fp32 on the
- *                           SIMT path;
+ *                           the gate: bf16 on the tensor-core path (q times
+ *                           log2(e)/sqrt(d); v in fp16, times a power of 2
+ *                           that is 1 unless the weights could drive |v| past
+ *                           2^15), fp32 on the SIMT path;
  *   "bias"                  (B, h, N, row_stride) pair-bias plane indexed
  *                           [b, t, query, key]: bias[b,t,j,k] for the starting
  *                           node, bias[b,t,k,i] at [b,t,i,k] for the ending

@@ -251,9 +251,9 @@ class TriangularAttention:
 
     def intermediate(self, name: str) -> torch.Tensor:
         """Copy of an intermediate of the most recent forward (see
-        tri_attn_debug_tensor): q, k, v, g, o as (B, N, N, D), bf16 on the
-        tensor-core path of bf16 handles (its raw bits reinterpreted) and fp32
-        on the SIMT path of fp32 handles;
+        tri_attn_debug_tensor): q, k, v, g, o as (B, N, N, D), on the
+        tensor-core path of bf16 handles bf16 (v: fp16) with their raw bits
+        reinterpreted, and fp32 on the SIMT path of fp32 handles;
         bias as (B, h, N, N) fp32. On the tensor-core path the plane the
         attention reads is stored in fp16 as log2(e) * (bias minus the largest
         kept entry of its (head, query) row), with -inf where the query-key
@@ -271,7 +271,9 @@ class TriangularAttention:
         if simt:
             return torch.as_tensor(_DeviceView(ptr, shape, "<f4"), device="cuda").clone()
         raw = torch.as_tensor(_DeviceView(ptr, shape, "<i2"), device="cuda").clone()
-        return raw.view(torch.bfloat16)
+        # v is fp16 on the tensor-core path (times a power of 2 that is 1 unless
+        # the weights could drive |v| past 2^15), the others bf16.
+        return raw.view(torch.float16 if name == "v" else torch.bfloat16)
 
     def sync_check(self, stream=None) -> int:
         return tri_attn_sync_check(self.handle, stream)

@@ -87,13 +87,13 @@ bool map_rows_bf16(CUtensorMap* m, const void* base, long long rows, int D, int 
 // its columns (ending node: cell (x, a)). Box: one head (d channels, rows of
 // 2d bytes swizzled over their length) x box_x positions of one line.
 bool map_lines(CUtensorMap* m, const void* base, int B, int N, int D, int d, int box_x,
-               bool ending) {
+               bool ending,
+               CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   const cuuint64_t cell = (cuuint64_t)D * 2, row = (cuuint64_t)N * cell;
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)N, (cuuint64_t)B};
   cuuint64_t strides[3] = {ending ? row : cell, ending ? cell : row, (cuuint64_t)N * row};
   cuuint32_t box[4] = {(cuuint32_t)d, (cuuint32_t)box_x, 1, 1};
-  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box,
-                  swizzle_for(2 * d));
+  return make_map(m, dt, 4, base, dims, strides, box, swizzle_for(2 * d));
 }
 
 // K3's view of a (B, N, N, D) bf16 activation as (channel, x, y, z): in cell
@@ -127,6 +127,7 @@ struct TcState {
   k3::Maps m3;               // K3 maps, cell-order tiles (out is set per forward)
   CUtensorMap map_gc, map_oc;   // K3 loads, column tiles
   int R;                     // K2 lines per work unit
+  float v_scale;             // v is stored in fp16 times this power of 2
   float* bias32;             // (B, h, N, N) fp32 pair bias in cell order (K1's output)
   unsigned char* row_any;    // (B*N) mask rows keeping some key
   uint32_t* mbits;           // (B*N, words) mask bits
@@ -209,12 +210,42 @@ cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const voi
     st->consts.bw[hd] = (float)bs;
   }
 
+  // v = Wv x_hat goes to fp16. Every LayerNorm output obeys |x_hat_c| <=
+  // |gamma_c| sqrt(D - 1) + |beta_c| (no entry of D values lies more than
+  // sqrt(D - 1) standard deviations from their mean), so |v_e| <= sum_c
+  // |Wv[e][c]| (|gamma_c| sqrt(D - 1) + |beta_c|) for any input; v is stored
+  // times the power of 2 that keeps this bound (with a margin for the bf16
+  // rounding of x_hat) below 2^15.
+  {
+    static_assert(sizeof(__nv_bfloat16) == 2, "bf16 weights");
+    uint16_t* wv = (uint16_t*)malloc((size_t)D * D * 2);
+    if (!wv) return cudaErrorMemoryAllocation;
+    e = cudaMemcpy(wv, Wv, (size_t)D * D * 2, cudaMemcpyDeviceToHost);
+    double bound = 0.0;
+    const double sq = sqrt((double)(D - 1));
+    for (int r = 0; r < D && e == cudaSuccess; ++r) {
+      double acc = 0.0;
+      for (int c = 0; c < D; ++c) {
+        uint32_t bits = (uint32_t)wv[(size_t)r * D + c] << 16;
+        float w;
+        memcpy(&w, &bits, 4);
+        acc += fabs((double)w) * (fabs((double)st->consts.gamma[c]) * sq + fabs((double)st->consts.beta[c]));
+      }
+      bound = std::max(bound, acc);
+    }
+    free(wv);
+    if (e != cudaSuccess) return e;
+    bound *= 1.02;
+    st->v_scale = 1.0f;
+    while (bound * st->v_scale >= 32768.0 && st->v_scale > 0x1p-100f) st->v_scale *= 0.5f;
+  }
+
   const long long cells = t->cells;
   const int d = t->d, half_bytes = D >= 64 ? 128 : 2 * D, kvk = k2_keys_per_stage(d);
   bool ok = map_rows_bf16(&st->m1.w, t->w_proj, 4 * D, D, 2 * D);
   ok = ok && map_lines(&st->m2.q, t->q, B, N, D, d, k2::BQ, t->ending);
   ok = ok && map_lines(&st->m2.k, t->k, B, N, D, d, kvk, t->ending);
-  ok = ok && map_lines(&st->m2.v, t->v, B, N, D, d, kvk, t->ending);
+  ok = ok && map_lines(&st->m2.v, t->v, B, N, D, d, kvk, t->ending, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
   ok = ok && map_lines(&st->m2.o, t->o, B, N, D, d, 32, t->ending);
   {
     cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)N, (cuuint64_t)B * h};
@@ -233,8 +264,9 @@ cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const voi
       cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)cells};
       cuuint64_t strides[1] = {(cuuint64_t)D * 2};
       cuuint32_t box[2] = {32, 32};
-      ok = make_map(maps[m], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, outs[m], dims, strides, box,
-                    CU_TENSOR_MAP_SWIZZLE_64B);
+      // v is fp16 (the attention's P V operand), q, k and g bf16.
+      ok = make_map(maps[m], m == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                    2, outs[m], dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
     }
   }
   ok = ok && map_k3(&st->m3.o, t->o, t, false, half_bytes / 2, 128, hsw);
@@ -281,6 +313,7 @@ cudaError_t launch_k1(tri_attn_s* t, cudaStream_t s, const CUtensorMap& map_x,
   p1.bias32 = st->bias32; p1.dev_err = t->dev_err;
   p1.polls = t->wait_limit;
   p1.q_scale = kLog2e / sqrtf((float)t->d);
+  p1.v_scale = st->v_scale;
   const int grid = n < st->num_sms ? n : st->num_sms;
   k1::Maps m = st->m1;
   m.x = map_x;
@@ -329,7 +362,8 @@ cudaError_t launch_k2(tri_attn_s* t, cudaStream_t s, int u0, int nu) {
   p2.polls = t->wait_limit;
   p2.q = (const __nv_bfloat16*)t->q;
   p2.k = (const __nv_bfloat16*)t->k;
-  p2.v = (const __nv_bfloat16*)t->v;
+  p2.v = (const __half*)t->v;
+  p2.v_unscale = 1.0f / st->v_scale;
   p2.sb = (long long)N * N * t->D;
   p2.sl = t->ending ? (long long)t->D : (long long)N * t->D;     // line a: row (starting) or column
   p2.sx = t->ending ? (long long)N * t->D : (long long)t->D;     // position along the line

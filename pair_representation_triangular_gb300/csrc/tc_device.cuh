@@ -81,6 +81,33 @@ __device__ __forceinline__ float add_f16hi_f32(uint32_t h2, float c) {
   return d;
 }
 
+// Packed fp16 arithmetic of the attention's softmax. cvt_f16x2: two fp32
+// values rounded to an fp16 pair (lo in the low half); hadd2: pairwise sum;
+// ex2_f16x2: 2^x of both halves in one special-function operation (relative
+// error about 2^-10, subnormal results kept, 2^-inf = 0).
+__device__ __forceinline__ uint32_t cvt_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t hadd2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+  uint32_t r;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
+// The two halves of an fp16 pair, each widened to fp32, added in fp32.
+__device__ __forceinline__ float f16x2_sum(uint32_t h) {
+  float lo, hi;
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi) : "r"(h));
+  return lo + hi;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 

@@ -1,7 +1,8 @@
 // K1 of the bf16 tensor-core path: LayerNorm as the prologue of one
 // concatenated projection GEMM, x_hat [128 cells x D] . [Wq|Wk|Wv|Wg]^T -> 4D
-// TMEM columns; the epilogue writes q (times log2(e)/sqrt(d)), k, v and
-// sigmoid(g + bg) in bf16. The h pair-bias outputs (Wb x_hat, with gamma and
+// TMEM columns; the epilogue writes q (times log2(e)/sqrt(d)) and k in bf16,
+// v in fp16 (times a power of 2 that keeps it in range; the attention's P V
+// runs on fp16 operands) and sigmoid(g + bg) in bf16. The h pair-bias outputs (Wb x_hat, with gamma and
 // beta folded into Wb) come out of the LayerNorm's statistics pass on the CUDA
 // cores and go, scaled by log2(e), to an fp32 plane in cell order.
 //
@@ -119,7 +120,7 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
             const uint64_t ad = tc::smem_desc(a0 + kh * S::X_HALF + kin * 32, 16, 8 * XSW, swm);
             const uint64_t bd = tc::smem_desc(w0 + kh * S::W_HALF + nh * S::NHALF * XSW + kin * 32,
                                               16, 8 * XSW, swm);
-            tc::mma_bf16_ss(tmem + nh * S::NHALF, ad, bd, idesc, ks > 0);
+            tc::mma_ss(tmem + nh * S::NHALF, ad, bd, idesc, ks > 0);
           }
           tc::mma_commit(&bars->acc_full[nh]);
         }
@@ -284,6 +285,13 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
             for (int e = 0; e < 8; ++e)
               packed[e] = tc::pack_bf16x2(__uint_as_float(acc[2 * e]) * p.q_scale,
                                           __uint_as_float(acc[2 * e + 1]) * p.q_scale);
+          } else if (sect == 2) {
+            // v in fp16, times v_scale: a power of 2 chosen from the weights so
+            // that |v| stays below 2^15 for any input (exact scaling).
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              packed[e] = cvt_f16x2(__uint_as_float(acc[2 * e]) * p.v_scale,
+                                    __uint_as_float(acc[2 * e + 1]) * p.v_scale);
           } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e)

@@ -6,7 +6,8 @@
 //                or columns (ending node); only the tensor maps tell them
 //                apart. S = Q K^T goes to TMEM; one softmax warpgroup per line
 //                adds the shared fp16 bias tile, drops masked keys and writes
-//                P = 2^x in bf16 over S; O += P V accumulates in TMEM. The
+//                P = 2^x in fp16 over S; O += P V (fp16 operands, fp32
+//                accumulator) accumulates in TMEM. The
 //                (B, N, h, N, N) logits never exist. Instantiated for d = 16,
 //                32 and 64.
 //   bias_rows    the attention's fp16 bias plane (B, h, N, Nb), indexed
@@ -107,86 +108,72 @@ __device__ __forceinline__ void load_bias_half(uint32_t brow, int hf, uint4 (&bh
   for (int q4 = 0; q4 < 4; ++q4) bh[q4] = tc::lds128(brow ^ ((hf * 4 + q4) << 4));
 }
 
-// Common path of one 32-key half: P = 2^(S + bias) (S in log2 units, the
-// reference mu = 0 and every lane live), packed in bf16 pairs; returns the
-// sum of P in two partial sums.
-__device__ __forceinline__ float2 p_half_fast(const float2 (&x2)[BK / 2], const uint4 (&bh)[4],
-                                              int hf, uint32_t (&pk)[16]) {
-  float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
+// One 32-key half of a sub-tile row, every lane live: P = 2^(S + bias) with
+// S in log2 units (the reference of the exponentials is 0). S (fp32 pairs) is
+// rounded to fp16 pairs, the fp16 bias pair added and 2^x taken of both halves
+// at once; P leaves as fp16 pairs (the A operand of the P V MMA) and the
+// return value is their sum as one fp16 pair (a tree of pairwise adds).
+__device__ __forceinline__ uint32_t p_half_fast(const float2 (&x2)[BK / 2], const uint4 (&bh)[4],
+                                                int hf, uint32_t (&pk)[16]) {
 #pragma unroll
   for (int q4 = 0; q4 < 4; ++q4) {
     const uint32_t hw[4] = {bh[q4].x, bh[q4].y, bh[q4].z, bh[q4].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float2 x = x2[(hf * 4 + q4) * 4 + e];
-      const float2 p2 = make_float2(ex2_approx(add_f16lo_f32(hw[e], x.x)),
-                                    ex2_approx(add_f16hi_f32(hw[e], x.y)));
-      if (e & 1) sb = __fadd2_rn(sb, p2);
-      else sa = __fadd2_rn(sa, p2);
-      pk[q4 * 4 + e] = tc::pack_bf16x2(p2.x, p2.y);
+      pk[q4 * 4 + e] = ex2_f16x2(hadd2(cvt_f16x2(x.x, x.y), hw[e]));
     }
   }
-  return __fadd2_rn(sa, sb);
+  uint32_t t8[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) t8[k] = hadd2(pk[2 * k], pk[2 * k + 1]);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) t8[k] = hadd2(t8[2 * k], t8[2 * k + 1]);
+  return hadd2(hadd2(t8[0], t8[1]), hadd2(t8[2], t8[3]));
 }
 
 // P of one 32-key half of a lane that is not live: 1 on every real key of a
-// uniform row or query (`w` = that half's real-key bits), else 0.
+// uniform row or query (`w` = that half's real-key bits), else 0 (fp16 pairs).
 __device__ __forceinline__ void p_half_const(uint32_t w, uint32_t (&pk)[16]) {
   if (w == 0u || w == 0xffffffffu) {
-    const uint32_t v = w ? 0x3F803F80u : 0u;
+    const uint32_t v = w ? 0x3C003C00u : 0u;
 #pragma unroll
     for (int k = 0; k < 16; ++k) pk[k] = v;
   } else {
 #pragma unroll
     for (int k = 0; k < 16; ++k)
-      pk[k] = (((w >> (2 * k)) & 1u) ? 0x3F80u : 0u) | (((w >> (2 * k + 1)) & 1u) ? 0x3F800000u : 0u);
+      pk[k] = (((w >> (2 * k)) & 1u) ? 0x3C00u : 0u) | (((w >> (2 * k + 1)) & 1u) ? 0x3C000000u : 0u);
   }
 }
 
-// General path of one 32-key half: P = 2^(S + bias - mu) for a live lane; a
-// lane that is not live writes 1 on every real key of a uniform row or query
-// (`w` = that half's real-key bits), else 0.
-__device__ __forceinline__ float2 p_half(const float2 (&x2)[BK / 2], const uint4 (&bh)[4], int hf,
-                                         float mu, bool live, uint32_t w, uint32_t (&pk)[16]) {
-  float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
-  if (live) {
-    const float2 nmu2 = make_float2(-mu, -mu);
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      const uint32_t hw[4] = {bh[q4].x, bh[q4].y, bh[q4].z, bh[q4].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 y = __fadd2_rn(x2[(hf * 4 + q4) * 4 + e], nmu2);
-        const float2 p2 = make_float2(ex2_approx(add_f16lo_f32(hw[e], y.x)),
-                                      ex2_approx(add_f16hi_f32(hw[e], y.y)));
-        if (e & 1) sb = __fadd2_rn(sb, p2);
-        else sa = __fadd2_rn(sa, p2);
-        pk[q4 * 4 + e] = tc::pack_bf16x2(p2.x, p2.y);
-      }
-    }
-  } else {
-    p_half_const(w, pk);
-  }
-  return __fadd2_rn(sa, sb);
+// General path of one 32-key half: the common path for a live lane; a lane
+// that is not live writes 1 on every real key of a uniform row or query (`w` =
+// that half's real-key bits), else 0, and returns a zero sum.
+__device__ __forceinline__ uint32_t p_half(const float2 (&x2)[BK / 2], const uint4 (&bh)[4], int hf,
+                                           bool live, uint32_t w, uint32_t (&pk)[16]) {
+  if (live) return p_half_fast(x2, bh, hf, pk);
+  p_half_const(w, pk);
+  return 0u;
 }
 
-// A query row whose sum l left [2^-16, 2^100) is recomputed exactly on the
-// CUDA cores: its logits reached about +100 in log2 units (P = 2^x with the
-// fixed reference 0 loses range), or every key it keeps lies more than 16
-// below its (head, query) row's largest bias, which may sit at a key the line
-// drops (the row-key reading), where the fp16 plane's rounding is no longer
-// small. Two passes over the line's keys, the first for the row max m, the
+// A query row whose sum l left [2^-6, 2^100] is recomputed exactly on the
+// CUDA cores: a logit reached 2^16 in P = 2^x (fp16 holds P below 65504, and
+// an infinite or undefined P makes l infinite or NaN), or every key it keeps
+// lies more than 6 below 0 in log2 units, where fp16 P loses relative
+// precision (subnormal below 2^-14) and the fp16 bias plane's rounding is no
+// longer small: the row's largest bias may sit at a key the line drops (the
+// row-key reading). Two passes over the line's keys, the first for the row max m, the
 // second for l = sum 2^(x - m) and o = sum 2^(x - m) v / l, in fp32 with the
 // fp32 bias. qrow: the row's q (head t); kl, vl: key 0 of the line's k and v
 // (head t), sx: the stride between keys; brow: the bias of the row's key 0 in
 // the fp32 cell-order plane and bs the stride between keys; keys come from the
 // line's mask bits (row reading; mrow) or from the finite biases (query
-// reading, mrow = null: the plane holds -inf for dropped keys). o leaves as 16
-// bf16 pairs in the lane's row of the swizzled staging tile at stg (rows of
-// 2 d bytes).
+// reading, mrow = null: the plane holds -inf for dropped keys); v is fp16
+// times 1 / v_unscale. o leaves as d / 2 bf16 pairs in the lane's row of the
+// swizzled staging tile at stg (rows of 2 d bytes).
 template <int DH>
 __device__ __noinline__ void exact_row(const __nv_bfloat16* qrow, const __nv_bfloat16* kl,
-                                       const __nv_bfloat16* vl, long long sx,
+                                       const __half* vl, float v_unscale, long long sx,
                                        const float* brow, long long bs, const uint32_t* mrow,
                                        int N, uint8_t* stg, int lane) {
   float q[DH];
@@ -216,11 +203,11 @@ __device__ __noinline__ void exact_row(const __nv_bfloat16* qrow, const __nv_bfl
     for (int e = 0; e < DH; ++e) s = fmaf(q[e], __bfloat162float(kr[e]), s);
     const float w = exp2f(s + bb - m);
     l += w;
-    const __nv_bfloat16* vr = vl + (long long)kk * sx;
+    const __half* vr = vl + (long long)kk * sx;
 #pragma unroll
-    for (int e = 0; e < DH; ++e) o[e] = fmaf(w, __bfloat162float(vr[e]), o[e]);
+    for (int e = 0; e < DH; ++e) o[e] = fmaf(w, __half2float(vr[e]), o[e]);
   }
-  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const float inv = l > 0.f ? v_unscale / l : 0.f;
 #pragma unroll
   for (int qc = 0; qc < DH / 8; ++qc) {
     uint32_t w4[4];
@@ -243,13 +230,15 @@ __device__ __noinline__ void exact_row(const __nv_bfloat16* qrow, const __nv_bfl
 // (64 fp32 columns each) | O (d columns from column 128).
 // Softmax warpgroup r owns line r; sub-tile c's S = Q K^T lands in the line's
 // S buffer c & 1 in log2 units (q carries the factor log2(e)/sqrt(d)), and the
-// softmax adds the bias, drops masked keys and writes P = 2^x (bf16) over it
-// in one pass; the line's MMA warp then issues O += P V(c) and S(c + 2) into
-// the same buffer. The reference of the exponentials is fixed at 0: no max is
-// taken, and fp32 and bf16 hold 2^x with full relative precision for
-// |x| < ~100, far beyond the logits of layer-normalised activations; a query
-// row whose sum l ends outside [2^-16, 2^100) is recomputed exactly in the
-// unit epilogue (exact_row). A unit's o = O / l is read and stored after the
+// softmax rounds S to fp16 pairs, adds the fp16 bias pair, drops masked keys
+// and writes P = 2^x (fp16, two per 32-bit column) over it in one pass, with
+// one packed 2^x per key pair; the line's MMA warp then issues O += P V(c)
+// (V in fp16) and S(c + 2) into the same buffer. The reference of the
+// exponentials is fixed at 0: no max is taken; fp16 P holds 2^x with 11-bit
+// precision for -14 <= x < 16, beyond the logits of layer-normalised
+// activations (the bias rows are stored minus their maximum); a query row
+// whose sum l ends outside [2^-6, 2^100] is recomputed exactly in the unit
+// epilogue (exact_row). A unit's o = O / l is read and stored after the
 // next unit's first sub-tile, which hides the completion of the unit's last
 // P V.
 template <int DH>
@@ -378,7 +367,8 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       const int r = warp - 1;
       const uint32_t tr = tmem + r * kTmemPerRow;
       constexpr uint32_t id_qk = tc::idesc_bf16_f32(128, BK, 0, 0);
-      constexpr uint32_t id_pv = tc::idesc_bf16_f32(128, DH, 0, 1);
+      // P (fp16, tensor memory) times V (fp16): both operands fp16.
+      constexpr uint32_t id_pv = tc::idesc_f16_f32(128, DH, 0, 1);
       // Descriptors of this line's first Q tile and first K tile; every other
       // operand sits a multiple of 16 bytes further (the start-address field
       // holds address / 16 and stays below 2^14).
@@ -396,7 +386,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
           const uint64_t kd = dk0 + (uint64_t)((it.kvs * KV_STAGE + (it.kt % SPS) * HALF_KV) >> 4);
 #pragma unroll
           for (int ks = 0; ks < DH / 16; ++ks)
-            tc::mma_bf16_ss(tr + (c & 1) * TM_S1, qd + 2 * ks, kd + 2 * ks, id_qk, ks > 0);
+            tc::mma_ss(tr + (c & 1) * TM_S1, qd + 2 * ks, kd + 2 * ks, id_qk, ks > 0);
           tc::mma_commit(&bars->s_ready[r][c & 1]);
           if (it.kt == KT - 1) tc::mma_commit(&bars->q_empty[it.ui & 1]);
         }
@@ -414,7 +404,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
               dk0 + (uint64_t)((it.kvs * KV_STAGE + KVT_BYTES + (it.kt % SPS) * HALF_KV) >> 4);
 #pragma unroll
           for (int ks = 0; ks < BK / 16; ++ks)
-            tc::mma_bf16_ts(tr + TM_O, tr + (c & 1) * TM_S1 + ks * 8, vd + SW * ks, id_pv,
+            tc::mma_ts(tr + TM_O, tr + (c & 1) * TM_S1 + ks * 8, vd + SW * ks, id_pv,
                             (it.kt > 0 || ks > 0) ? 1u : 0u);
           tc::mma_commit(&bars->p_free[r][c & 1]);
           if (it.kt % SPS == SPS - 1 || it.kt == KT - 1) tc::mma_commit(&bars->kv_empty[it.kvs]);
@@ -487,8 +477,10 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         // A query row has l in [2^-16, 2^100) unless its logits left that range
         // (a uniform row or query has l = its count of real keys): those rows
         // are recomputed exactly.
-        const bool exact = fj + lane < N && !(l >= 0x1p-16f && l < 0x1p100f);
-        const float inv = __fdividef(1.0f, l);   // l lies in [2^-16, 2^100): the fast form is exact enough
+        const bool exact = fj + lane < N && !(l >= 0x1p-6f && l <= 0x1p100f);
+        // l lies in [2^-6, 2^100]: the fast form is exact enough. V is stored
+        // times a power of 2, taken out here.
+        const float inv = __fdividef(p.v_unscale, l);
         uint32_t po[DH / 2];
 #pragma unroll
         for (int e = 0; e < DH; e += 2)
@@ -500,7 +492,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
           const long long base = (long long)fu.b * p.sb + (long long)fi * p.sl + fu.t * DH;
           const long long plane = ((long long)fu.b * p.h + fu.t) * N * N;
           const int a = fj + lane;             // the query's position along the line
-          exact_row<DH>(p.q + base + (long long)a * p.sx, p.k + base, p.v + base, p.sx,
+          exact_row<DH>(p.q + base + (long long)a * p.sx, p.k + base, p.v + base, p.v_unscale, p.sx,
                     p.bias32 + plane + (p.ending ? (long long)a : (long long)a * N),
                     p.ending ? (long long)N : 1ll,
                     p.mask_mode == TRI_ATTN_MASK_QUERY_KEY
@@ -564,7 +556,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         const uint32_t tsb = tb + (c & 1) * TM_S1;     // S(c), then P(c) over it
         float2 x2[BK / 2];
         uint4 bh0[4], bh1[4];
-        float tsum = 0.f;
+        uint32_t tsum = 0u;                            // fp16 pair
         if (any_live) {
           tc::tmem_ld32(tsb, *(uint32_t(*)[32])&x2[0]);
           tc::tmem_ld32(tsb + 32, *(uint32_t(*)[32])&x2[16]);
@@ -582,20 +574,18 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
             }
           }
           uint32_t pk[16];
-          float2 ts2;
           if (all_live) {
-            ts2 = p_half_fast(x2, bh0, 0, pk);
+            const uint32_t t0 = p_half_fast(x2, bh0, 0, pk);
             tc::tmem_st16(tsb, pk);
-            ts2 = __fadd2_rn(ts2, p_half_fast(x2, bh1, 1, pk));
+            tsum = hadd2(t0, p_half_fast(x2, bh1, 1, pk));
             tc::tmem_st16(tsb + 16, pk);
           } else {
             const uint32_t w0 = uni ? rl0 : 0u, w1 = uni ? rl1 : 0u;
-            ts2 = p_half(x2, bh0, 0, 0.f, live, w0, pk);
+            const uint32_t t0 = p_half(x2, bh0, 0, live, w0, pk);
             tc::tmem_st16(tsb, pk);
-            ts2 = __fadd2_rn(ts2, p_half(x2, bh1, 1, 0.f, live, w1, pk));
+            tsum = hadd2(t0, p_half(x2, bh1, 1, live, w1, pk));
             tc::tmem_st16(tsb + 16, pk);
           }
-          tsum = ts2.x + ts2.y;
         } else {
           // No lane of the warp keeps a key of this sub-tile: P is 1 on the real
           // keys of a uniform row or query, else 0.
@@ -609,7 +599,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&bars->b_empty[its.bs]);
         if (live) {
-          l_run += tsum;
+          l_run += f16x2_sum(tsum);
         } else if (uni) {
           l_run += (float)(__popc(rl0) + __popc(rl1));
         }

@@ -106,7 +106,7 @@ gate_out_tc(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ C
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t kh = ks / S::KSTEPS_PER_HALF, kin = ks % S::KSTEPS_PER_HALF;
-          tc::mma_bf16_ss(tmem + b * D,
+          tc::mma_ss(tmem + b * D,
                           tc::smem_desc(a0 + kh * S::T_HALF + kin * 32, 16, 8 * XSW, swm),
                           tc::smem_desc(w0 + kh * S::W_HALF + kin * 32, 16, 8 * XSW, swm), idesc,
                           ks > 0);

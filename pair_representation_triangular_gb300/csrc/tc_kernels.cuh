@@ -37,6 +37,7 @@ struct Params {
   unsigned int* dev_err;
   long long polls;
   float q_scale;               // q is stored times log2(e) / sqrt(d)
+  float v_scale;               // v is stored in fp16 times this power of 2
 };
 
 // x: loads (channel, cell), box (channels of one half, 128 cells). w: the
@@ -65,7 +66,9 @@ struct Params {
   // The same q, k, v and bias plane as raw tensors, for the exact recomputation
   // of a query row whose sums left the fp32 range: element (b, line a, position
   // x, channel e) of q, k or v sits at b * sb + a * sl + x * sx + e.
-  const __nv_bfloat16 *q, *k, *v;
+  const __nv_bfloat16 *q, *k;
+  const __half* v;                // fp16, times v_scale (a power of 2)
+  float v_unscale;                // 1 / v_scale
   long long sb, sl, sx;
   const float* bias32;            // (B, h, N, N) fp32 cell order, log2(e) * bias, -inf where dropped
   int ending;                     // the key k of query a is cell (k, a) instead of (a, k)
