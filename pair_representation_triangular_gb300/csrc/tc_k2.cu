@@ -101,59 +101,58 @@ __device__ __forceinline__ uint32_t real_bits(int left, int w) {
   return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
 }
 
-// The 32 fp16 biases of half hf of a sub-tile row (brow: the row's swizzled
-// base, 16-byte chunk q at brow ^ (q << 4)).
-__device__ __forceinline__ void load_bias_half(uint32_t brow, int hf, uint4 (&bh)[4]) {
+// The 64 fp16 biases of a sub-tile row (brow: the row's swizzled base, 16-byte
+// chunk q, keys 8q .. 8q + 7, at brow ^ (q << 4)).
+__device__ __forceinline__ void load_bias(uint32_t brow, uint4 (&bh)[8]) {
 #pragma unroll
-  for (int q4 = 0; q4 < 4; ++q4) bh[q4] = tc::lds128(brow ^ ((hf * 4 + q4) << 4));
+  for (int q = 0; q < 8; ++q) bh[q] = tc::lds128(brow ^ (q << 4));
 }
 
-// One 32-key half of a sub-tile row, every lane live: P = 2^(S + bias) with
-// S in log2 units (the reference of the exponentials is 0). S (fp32 pairs) is
-// rounded to fp16 pairs, the fp16 bias pair added and 2^x taken of both halves
-// at once; P leaves as fp16 pairs (the A operand of the P V MMA) and the
-// return value is their sum as one fp16 pair (a tree of pairwise adds).
-__device__ __forceinline__ uint32_t p_half_fast(const float2 (&x2)[BK / 2], const uint4 (&bh)[4],
-                                                int hf, uint32_t (&pk)[16]) {
+// One 64-key sub-tile row, every lane live: P = 2^(S + bias) with S (fp32
+// bits, sv) in log2 units (the reference of the exponentials is 0). Each key
+// pair of S is rounded to an fp16 pair, the fp16 bias pair added and 2^x taken
+// of both halves at once; P leaves as 32 fp16 pairs (the A operand of the P V
+// MMA) and the return value is their sum as one fp16 pair (a tree of pairwise
+// adds).
+__device__ __forceinline__ uint32_t p_tile_fast(const uint32_t (&sv)[2 * BK / 2], const uint4 (&bh)[8],
+                                                uint32_t (&pk)[BK / 2]) {
 #pragma unroll
-  for (int q4 = 0; q4 < 4; ++q4) {
-    const uint32_t hw[4] = {bh[q4].x, bh[q4].y, bh[q4].z, bh[q4].w};
+  for (int q = 0; q < 8; ++q) {
+    const uint32_t hw[4] = {bh[q].x, bh[q].y, bh[q].z, bh[q].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float2 x = x2[(hf * 4 + q4) * 4 + e];
-      pk[q4 * 4 + e] = ex2_f16x2(hadd2(cvt_f16x2(x.x, x.y), hw[e]));
+      const int m = q * 4 + e;
+      pk[m] = ex2_f16x2(hadd2(cvt_f16x2(__uint_as_float(sv[2 * m]), __uint_as_float(sv[2 * m + 1])), hw[e]));
     }
   }
-  uint32_t t8[8];
+  uint32_t t[16];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) t8[k] = hadd2(pk[2 * k], pk[2 * k + 1]);
+  for (int k = 0; k < 16; ++k) t[k] = hadd2(pk[2 * k], pk[2 * k + 1]);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) t8[k] = hadd2(t8[2 * k], t8[2 * k + 1]);
-  return hadd2(hadd2(t8[0], t8[1]), hadd2(t8[2], t8[3]));
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int k = 0; k < w; ++k) t[k] = hadd2(t[2 * k], t[2 * k + 1]);
+  return t[0];
 }
 
-// P of one 32-key half of a lane that is not live: 1 on every real key of a
-// uniform row or query (`w` = that half's real-key bits), else 0 (fp16 pairs).
-__device__ __forceinline__ void p_half_const(uint32_t w, uint32_t (&pk)[16]) {
-  if (w == 0u || w == 0xffffffffu) {
-    const uint32_t v = w ? 0x3C003C00u : 0u;
+// P of a 64-key sub-tile row of a lane that is not live: 1 on every real key
+// of a uniform row or query (w0, w1: the sub-tile's real-key bits), else 0
+// (fp16 pairs).
+__device__ __forceinline__ void p_tile_const(uint32_t w0, uint32_t w1, uint32_t (&pk)[BK / 2]) {
 #pragma unroll
-    for (int k = 0; k < 16; ++k) pk[k] = v;
-  } else {
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t w = h ? w1 : w0;
+    if (w == 0u || w == 0xffffffffu) {
+      const uint32_t v = w ? 0x3C003C00u : 0u;
 #pragma unroll
-    for (int k = 0; k < 16; ++k)
-      pk[k] = (((w >> (2 * k)) & 1u) ? 0x3C00u : 0u) | (((w >> (2 * k + 1)) & 1u) ? 0x3C000000u : 0u);
+      for (int k = 0; k < 16; ++k) pk[16 * h + k] = v;
+    } else {
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        pk[16 * h + k] = (((w >> (2 * k)) & 1u) ? 0x3C00u : 0u) |
+                         (((w >> (2 * k + 1)) & 1u) ? 0x3C000000u : 0u);
+    }
   }
-}
-
-// General path of one 32-key half: the common path for a live lane; a lane
-// that is not live writes 1 on every real key of a uniform row or query (`w` =
-// that half's real-key bits), else 0, and returns a zero sum.
-__device__ __forceinline__ uint32_t p_half(const float2 (&x2)[BK / 2], const uint4 (&bh)[4], int hf,
-                                           bool live, uint32_t w, uint32_t (&pk)[16]) {
-  if (live) return p_half_fast(x2, bh, hf, pk);
-  p_half_const(w, pk);
-  return 0u;
 }
 
 // A query row whose sum l left [2^-6, 2^100] is recomputed exactly on the
@@ -277,7 +276,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     }
     for (int s = 0; s < B_STAGES; ++s) {
       tc::mbar_init(&bars->b_full[s], 1);
-      tc::mbar_init(&bars->b_empty[s], kSoftmaxWarps);   // one arrive per softmax warp
+      tc::mbar_init(&bars->b_empty[s], 32 * kSoftmaxWarps);   // every softmax thread arrives
     }
     for (int r = 0; r < R; ++r) {
       for (int b = 0; b < 2; ++b) {
@@ -364,8 +363,11 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     } else if (warp - 1 < R) {
       // ---------------- MMA issuer of line r = warp - 1 (whole warp; one elected lane
       // issues). With R = 2, warp 3 has no role and goes straight to the teardown.
-      const int r = warp - 1;
-      const uint32_t tr = tmem + r * kTmemPerRow;
+      // The line index and the tensor-memory base are broadcast from lane 0 so
+      // that the compiler sees every MMA operand as warp-uniform (uniform
+      // registers: the elected lane issues without a per-lane loop).
+      const int r = __shfl_sync(0xffffffffu, warp - 1, 0);
+      const uint32_t tr = __shfl_sync(0xffffffffu, tmem, 0) + r * kTmemPerRow;
       constexpr uint32_t id_qk = tc::idesc_bf16_f32(128, BK, 0, 0);
       // P (fp16, tensor memory) times V (fp16): both operands fp16.
       constexpr uint32_t id_pv = tc::idesc_f16_f32(128, DH, 0, 1);
@@ -439,18 +441,21 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     const bool qk_mode = p.mask_mode == TRI_ATTN_MASK_QUERY_KEY;
     // A unit's mask summary: the "keeps some key" flag of this lane's query
     // row (query-key) or of the line (row-key), and the mask row whose bits
-    // give the keys this lane keeps. Loaded one unit ahead.
-    auto unit_loads = [&](const Unit& nu, unsigned& any, const uint32_t*& mrow) {
+    // give the keys this lane keeps, with its first two words. Loaded one unit
+    // ahead.
+    auto unit_loads = [&](const Unit& nu, unsigned& any, const uint32_t*& mrow, uint2& bits0) {
       const int nj = nu.j0 + jr, ni = nu.rg * R + r;
       const int mr = qk_mode ? nj : ni;
       // Queries past N produce nothing (their stores are clipped): they count
       // as keeping keys so that they never force the general path.
-      any = mr < N ? __ldg(p.row_any + (long long)nu.b * N + mr) : (qk_mode ? 1u : 0u);
+      any = mr < N ? tc::ldg_nc_u8_early(p.row_any + (long long)nu.b * N + mr) : (qk_mode ? 1u : 0u);
       mrow = p.mbits + ((long long)nu.b * N + (mr < N ? mr : 0)) * p.words;
+      bits0 = tc::ldg_nc_v2_early(mrow);
     };
     unsigned nx_any = 0u;
     const uint32_t* nx_mrow = p.mbits;
-    if (my_units > 0) unit_loads(decode_unit(p.unit0 + blockIdx.x, p), nx_any, nx_mrow);
+    uint2 nx_bits0 = make_uint2(0u, 0u);
+    if (my_units > 0) unit_loads(decode_unit(p.unit0 + blockIdx.x, p), nx_any, nx_mrow, nx_bits0);
     // Unit epilogue: o = O / l once the unit's last P V has landed, staged in
     // shared memory and written by one TMA store per warp (queries past N are
     // clipped by the store; lines past N and warps whose 32 queries all lie
@@ -520,18 +525,19 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     for (int ui = 0; ok && ui < my_units; ++ui) {
       const bool uni = nx_any == 0u;
       const uint32_t* mrow = nx_mrow;
+      uint2 nbits = nx_bits0;
       if (ui + 1 < my_units)
-        unit_loads(decode_unit(p.unit0 + blockIdx.x + (ui + 1) * gridDim.x, p), nx_any, nx_mrow);
+        unit_loads(decode_unit(p.unit0 + blockIdx.x + (ui + 1) * gridDim.x, p), nx_any, nx_mrow,
+                   nx_bits0);
       float l_run = 0.f;
       // Warp-uniform unit state: whether any lane has a key-keeping query row,
       // and whether every lane has one.
       const bool unit_live = __any_sync(0xffffffffu, !uni);
       const bool all_live = __all_sync(0xffffffffu, !uni);
-      uint2 nbits = __ldg((const uint2*)mrow);
       for (int kt = 0; ok && kt < KT; ++kt, advance_soft(its, KT)) {
         const int c = its.c;
         const uint2 mb = nbits;
-        if (kt + 1 < KT) nbits = __ldg((const uint2*)(mrow + 2 * (kt + 1)));
+        if (kt + 1 < KT) nbits = tc::ldg_nc_v2_early(mrow + 2 * (kt + 1));
         const int left = N - kt * BK;
         const uint32_t rl0 = real_bits(left, 0), rl1 = real_bits(left, 1);
         // Keys kept by this lane (query-key: its own query row; row-key: the
@@ -554,50 +560,34 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         const bool any_live = unit_live && tile_keys;
         tc::tc_fence_after();
         const uint32_t tsb = tb + (c & 1) * TM_S1;     // S(c), then P(c) over it
-        float2 x2[BK / 2];
-        uint4 bh0[4], bh1[4];
         uint32_t tsum = 0u;                            // fp16 pair
+        uint32_t pk[BK / 2];
         if (any_live) {
-          tc::tmem_ld32(tsb, *(uint32_t(*)[32])&x2[0]);
-          tc::tmem_ld32(tsb + 32, *(uint32_t(*)[32])&x2[16]);
-          load_bias_half(brow, 0, bh0);
-          load_bias_half(brow, 1, bh1);
+          uint32_t sv[BK];
+          uint4 bh[8];
+          tc::tmem_ld64(tsb, sv);
+          load_bias(brow, bh);
           tc::tmem_ld_wait();
           if (!all_kept) {
             // Dropped keys: S = -inf, which the bias add keeps at -inf (P = 0).
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              if (!((bw0 >> (2 * k)) & 1u)) x2[k].x = -INFINITY;
-              if (!((bw0 >> (2 * k + 1)) & 1u)) x2[k].y = -INFINITY;
-              if (!((bw1 >> (2 * k)) & 1u)) x2[16 + k].x = -INFINITY;
-              if (!((bw1 >> (2 * k + 1)) & 1u)) x2[16 + k].y = -INFINITY;
+            for (int k = 0; k < 32; ++k) {
+              if (!((bw0 >> k) & 1u)) sv[k] = 0xff800000u;
+              if (!((bw1 >> k) & 1u)) sv[32 + k] = 0xff800000u;
             }
           }
-          uint32_t pk[16];
-          if (all_live) {
-            const uint32_t t0 = p_half_fast(x2, bh0, 0, pk);
-            tc::tmem_st16(tsb, pk);
-            tsum = hadd2(t0, p_half_fast(x2, bh1, 1, pk));
-            tc::tmem_st16(tsb + 16, pk);
-          } else {
-            const uint32_t w0 = uni ? rl0 : 0u, w1 = uni ? rl1 : 0u;
-            const uint32_t t0 = p_half(x2, bh0, 0, live, w0, pk);
-            tc::tmem_st16(tsb, pk);
-            tsum = hadd2(t0, p_half(x2, bh1, 1, live, w1, pk));
-            tc::tmem_st16(tsb + 16, pk);
-          }
+          if (live)
+            tsum = p_tile_fast(sv, bh, pk);
+          else
+            p_tile_const(uni ? rl0 : 0u, uni ? rl1 : 0u, pk);
         } else {
           // No lane of the warp keeps a key of this sub-tile: P is 1 on the real
           // keys of a uniform row or query, else 0.
-          uint32_t pk[16];
-          p_half_const(uni ? rl0 : 0u, pk);
-          tc::tmem_st16(tsb, pk);
-          p_half_const(uni ? rl1 : 0u, pk);
-          tc::tmem_st16(tsb + 16, pk);
+          p_tile_const(uni ? rl0 : 0u, uni ? rl1 : 0u, pk);
         }
-        // The bias stage is read: release it.
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&bars->b_empty[its.bs]);
+        tc::tmem_st32(tsb, pk);
+        // The bias stage is read: release it (every softmax thread arrives).
+        tc::mbar_arrive(&bars->b_empty[its.bs]);
         if (live) {
           l_run += f16x2_sum(tsum);
         } else if (uni) {
