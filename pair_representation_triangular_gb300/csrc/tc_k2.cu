@@ -28,7 +28,7 @@ namespace k2 {
 
 template <int R>
 struct Bars {
-  uint64_t q_full[2], q_empty[2], kv_full[KV_STAGES], kv_empty[KV_STAGES];
+  uint64_t q_full[2], q_empty[2], kv_full[KV_STAGES_MAX], kv_empty[KV_STAGES_MAX];
   uint64_t b_full[B_STAGES], b_empty[B_STAGES];
   // s_ready and p_full follow the S/P buffer (sub-tile parity): a warp with no
   // live lanes runs ahead, and its arrivals for sub-tile c + 1 must not complete
@@ -75,7 +75,7 @@ __device__ __forceinline__ void step_unit(Unit& u, const Params& p) {
 struct SubIt {
   int c, ui, kt, kvs, kvph, bs, bph;
 };
-template <int SPS>
+template <int SPS, int KV_STAGES>
 __device__ __forceinline__ void advance(SubIt& it, int KT) {
   ++it.c;
   const bool stage_end = (it.kt % SPS) == SPS - 1 || it.kt == KT - 1;
@@ -246,7 +246,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
             const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_b,
             const __grid_constant__ CUtensorMap map_o, const Params p) {
   using S = Shape<DH>;
-  constexpr int R = S::R, SPS = S::SPS, SW = S::SW;
+  constexpr int R = S::R, SPS = S::SPS, SW = S::SW, KV_STAGES = S::KV_STAGES;
   constexpr int kIssuers = S::kIssuers, kSoftmaxWarps = S::kSoftmaxWarps;
   constexpr int kRegsCtl = S::kRegsCtl, kRegsSoftmax = S::kRegsSoftmax;
   constexpr int kTmemPerRow = S::kTmemPerRow;
@@ -416,12 +416,12 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       };
       bool ok = true;
       SubIt itq{0, 0, 0, 0, 0, 0, 0}, itp{0, 0, 0, 0, 0, 0, 0};
-      for (; ok && itq.c < 2 && itq.c < total; advance<SPS>(itq, KT)) ok = qk(itq);
-      for (; ok && itp.c < total; advance<SPS>(itp, KT)) {
+      for (; ok && itq.c < 2 && itq.c < total; advance<SPS, KV_STAGES>(itq, KT)) ok = qk(itq);
+      for (; ok && itp.c < total; advance<SPS, KV_STAGES>(itp, KT)) {
         ok = pv(itp);
         if (ok && itq.c < total) {
           ok = qk(itq);
-          advance<SPS>(itq, KT);
+          advance<SPS, KV_STAGES>(itq, KT);
         }
       }
       if (elect_one()) tc::mma_commit(&bars->drain[r]);

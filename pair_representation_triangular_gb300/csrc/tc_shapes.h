@@ -65,15 +65,18 @@ namespace k2 {
 constexpr int BQ = 128;                 // queries per unit
 constexpr int BK = 64;                  // keys per sub-tile (one S buffer)
 constexpr int B_STAGES = 3;             // bias sub-tile ring
-constexpr int KV_STAGES = 2;            // K/V stage ring
+constexpr int KV_STAGES_MAX = 4;        // K/V stage ring (barrier slots)
 constexpr int TM_S1 = 64, TM_O = 128;   // per line: S0 | S1 | O
 constexpr uint32_t BIAS_BYTES = BQ * BK * 2;
 template <int DH>
 struct Shape {
   // d = 64 fits two lines in tensor memory (S0 | S1 | O = 192 columns each).
   static constexpr int R = DH == 64 ? 2 : 3;
-  // Keys per K/V stage: two sub-tiles, or one where shared memory is short.
-  static constexpr int KVK = DH == 64 ? 64 : 128;
+  // Keys per K/V stage: one sub-tile. A stage is released as soon as the P V
+  // of its sub-tile completes, so four stages keep the copies three to four
+  // sub-tiles ahead of the MMAs (two for d = 64, where shared memory is short).
+  static constexpr int KVK = 64;
+  static constexpr int KV_STAGES = DH == 64 ? 2 : 4;
   static constexpr int SPS = KVK / BK;                // sub-tiles per stage
   static constexpr int SW = 2 * DH;                   // row bytes = swizzle span of Q/K/V/O tiles
   static constexpr int kIssuers = R;
