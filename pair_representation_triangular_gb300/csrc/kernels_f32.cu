@@ -137,8 +137,15 @@ ln_proj_f32(const float* __restrict__ x, long long cells, int N, int D, int h, i
 // of the line is b N^2 + a sa + x sx, (sa, sx) = (N, 1) for the starting node
 // and (1, N) for the ending node (END); the pair bias is read at [b, t, query,
 // key], and the query-key mask at b N^2 + query sa + key sx.
+// Heads wider than 64 take two threads per query (adjacent lanes), each holding
+// half of the head's query and accumulator; the two halves of a dot product
+// meet through one shuffle. A thread then needs 2 x 64 registers for them
+// instead of 2 x 128, which no register file of 255 per thread holds.
+template <int MAXD>
+constexpr int f32_split() { return MAXD >= 128 ? 2 : 1; }
+
 template <int MAXD, int KC, bool END>
-__global__ void __launch_bounds__(kQueriesPerBlock)
+__global__ void __launch_bounds__(kQueriesPerBlock * f32_split<MAXD>())
 row_attn_f32(const float* __restrict__ q, const float* __restrict__ k,
              const float* __restrict__ v, const float* __restrict__ bias,
              const int32_t* __restrict__ mask, int mask_mode,
@@ -150,7 +157,11 @@ row_attn_f32(const float* __restrict__ q, const float* __restrict__ k,
   __shared__ unsigned char Ms[kQueriesPerBlock][KC + 1];
   __shared__ int Mrow[KC];
 
-  const int tid = threadIdx.x;
+  constexpr int SPLIT = f32_split<MAXD>();       // threads per query
+  constexpr int HD = MAXD / SPLIT;               // head channels per thread
+  constexpr int NT = kQueriesPerBlock * SPLIT;   // threads per block
+  const int tid = threadIdx.x / SPLIT;           // the query of the block
+  const int part = threadIdx.x % SPLIT;          // channels part * HD .. + HD - 1
   const long long row = blockIdx.x;              // b * N + a
   const int t = blockIdx.y;
   const long long b = row / N;
@@ -161,10 +172,11 @@ row_attn_f32(const float* __restrict__ q, const float* __restrict__ k,
   const long long NN = (long long)N * N;
   const float scale = 1.0f / sqrtf((float)d);
 
-  float qv[MAXD], acc[MAXD];
+  float qv[HD], acc[HD];
 #pragma unroll
-  for (int e = 0; e < MAXD; ++e) {
-    qv[e] = (active && e < d) ? q[(line0 + (long long)j * sx) * D + t * d + e] : 0.f;
+  for (int e = 0; e < HD; ++e) {
+    const int ee = part * HD + e;
+    qv[e] = (active && ee < d) ? q[(line0 + (long long)j * sx) * D + t * d + ee] : 0.f;
     acc[e] = 0.f;
   }
   float m = -INFINITY, l = 0.f;
@@ -172,14 +184,14 @@ row_attn_f32(const float* __restrict__ q, const float* __restrict__ k,
   for (int k0 = 0; k0 < N; k0 += KC) {
     const int nk = min(KC, N - k0);
     __syncthreads();
-    for (int idx = tid; idx < KC * MAXD; idx += kQueriesPerBlock) {
+    for (int idx = threadIdx.x; idx < KC * MAXD; idx += NT) {
       const int kk = idx / MAXD, e = idx % MAXD;
       const bool in = kk < nk && e < d;
       const long long src = (line0 + (long long)(k0 + kk) * sx) * D + t * d + e;
       Ks[kk][e] = in ? k[src] : 0.f;
       Vs[kk][e] = in ? v[src] : 0.f;
     }
-    for (int idx = tid; idx < kQueriesPerBlock * KC; idx += kQueriesPerBlock) {
+    for (int idx = threadIdx.x; idx < kQueriesPerBlock * KC; idx += NT) {
       const int jj = idx / KC, kk = idx % KC;
       const bool in = (j0 + jj) < N && kk < nk;
       Bs[jj][kk] = in ? bias[(b * h + t) * NN + (long long)(j0 + jj) * N + k0 + kk] : 0.f;
@@ -187,8 +199,8 @@ row_attn_f32(const float* __restrict__ q, const float* __restrict__ k,
         Ms[jj][kk] =
             (in && mask[b * NN + (long long)(j0 + jj) * sa + (long long)(k0 + kk) * sx] != 0) ? 1 : 0;
     }
-    if (mask_mode == TRI_ATTN_MASK_ROW_KEY && tid < KC)
-      Mrow[tid] = tid < nk ? mask[line0 + (long long)(k0 + tid) * sx] : 0;
+    if (mask_mode == TRI_ATTN_MASK_ROW_KEY && threadIdx.x < KC)
+      Mrow[threadIdx.x] = (int)threadIdx.x < nk ? mask[line0 + (long long)(k0 + threadIdx.x) * sx] : 0;
     __syncthreads();
 
     // Keys four at a time: four independent dot-product chains, one rescale.
@@ -199,7 +211,8 @@ row_attn_f32(const float* __restrict__ q, const float* __restrict__ k,
       for (int u = 0; u < 4; ++u) {
         float dot = 0.f;
 #pragma unroll
-        for (int e = 0; e < MAXD; ++e) dot = fmaf(qv[e], Ks[kk + u][e], dot);   // KC % 4 == 0
+        for (int e = 0; e < HD; ++e) dot = fmaf(qv[e], Ks[kk + u][part * HD + e], dot);   // KC % 4 == 0
+        if constexpr (SPLIT == 2) dot += __shfl_xor_sync(0xffffffffu, dot, 1);
         float v = dot * scale + Bs[tid][kk + u];
         const int keep = mask_mode == TRI_ATTN_MASK_ROW_KEY ? Mrow[kk + u] : Ms[tid][kk + u];
         if (!keep) v = -1e9f;                     // replacement by -1e9
@@ -210,7 +223,7 @@ row_attn_f32(const float* __restrict__ q, const float* __restrict__ k,
         const float alpha = expf(m - mn);         // exp(-inf) = 0 before the first key
         l *= alpha;
 #pragma unroll
-        for (int e = 0; e < MAXD; ++e) acc[e] *= alpha;
+        for (int e = 0; e < HD; ++e) acc[e] *= alpha;
         m = mn;
       }
       float pk[4];
@@ -220,16 +233,18 @@ row_attn_f32(const float* __restrict__ q, const float* __restrict__ k,
         l += pk[u];
       }
 #pragma unroll
-      for (int e = 0; e < MAXD; ++e)
-        acc[e] = fmaf(pk[3], Vs[kk + 3][e], fmaf(pk[2], Vs[kk + 2][e],
-                 fmaf(pk[1], Vs[kk + 1][e], fmaf(pk[0], Vs[kk][e], acc[e]))));
+      for (int e = 0; e < HD; ++e) {
+        const int ee = part * HD + e;
+        acc[e] = fmaf(pk[3], Vs[kk + 3][ee], fmaf(pk[2], Vs[kk + 2][ee],
+                 fmaf(pk[1], Vs[kk + 1][ee], fmaf(pk[0], Vs[kk][ee], acc[e]))));
+      }
     }
   }
   if (active) {
     const float inv = 1.0f / l;
 #pragma unroll
-    for (int e = 0; e < MAXD; ++e)
-      if (e < d) o[(line0 + (long long)j * sx) * D + t * d + e] = acc[e] * inv;
+    for (int e = 0; e < HD; ++e)
+      if (part * HD + e < d) o[(line0 + (long long)j * sx) * D + t * d + part * HD + e] = acc[e] * inv;
   }
 }
 
@@ -286,10 +301,12 @@ cudaError_t launch_f32(const F32Launch& a, cudaStream_t s, tri_attn_s* timing) {
 #define TRI_ATTN_F32_CASE(MD)                                                              \
   case MD:                                                                                 \
     if (a.ending)                                                                          \
-      row_attn_f32<MD, (MD >= 128 ? 16 : kKeyChunk), true><<<grid, kQueriesPerBlock, 0, s>>>( \
+      row_attn_f32<MD, (MD >= 128 ? 16 : kKeyChunk), true>                                \
+          <<<grid, kQueriesPerBlock * f32_split<MD>(), 0, s>>>(                            \
           a.q, a.k, a.v, a.bias, a.mask, a.mask_mode, N, D, h, d, a.o);                    \
     else                                                                                   \
-      row_attn_f32<MD, (MD >= 128 ? 16 : kKeyChunk), false><<<grid, kQueriesPerBlock, 0, s>>>( \
+      row_attn_f32<MD, (MD >= 128 ? 16 : kKeyChunk), false>                               \
+          <<<grid, kQueriesPerBlock * f32_split<MD>(), 0, s>>>(                            \
           a.q, a.k, a.v, a.bias, a.mask, a.mask_mode, N, D, h, d, a.o);                    \
     break;
   const int md = d <= 8 ? 8 : d <= 16 ? 16 : d <= 32 ? 32 : d <= 64 ? 64 : 128;

@@ -317,14 +317,14 @@ cudaError_t launch_k1(tri_attn_s* t, cudaStream_t s, const CUtensorMap& map_x,
   const int grid = n < st->num_sms ? n : st->num_sms;
   k1::Maps m = st->m1;
   m.x = map_x;
-  return k1_launch(t->D, t->h, grid, s, m, p1, st->consts);
+  return k1_launch(t->D, t->h, grid, s, !t->timing, m, p1, st->consts);
 }
 
 // The mask summary of every line.
 cudaError_t launch_mask(tri_attn_s* t, cudaStream_t s, const int32_t* mask, int& mark) {
   TcState* st = (TcState*)t->tc;
   const cudaError_t e =
-      k2_mask_summary(mask, t->B, t->N, t->ending, st->words, st->mbits, st->row_any, s);
+      k2_mask_summary(mask, t->B, t->N, t->ending, st->words, st->mbits, st->row_any, s, !t->timing);
   tri_mark(t, s, mark++, t->ending ? "mask_summary_cols" : "mask_summary");
   return e;
 }
@@ -333,7 +333,7 @@ cudaError_t launch_mask(tri_attn_s* t, cudaStream_t s, const int32_t* mask, int&
 cudaError_t launch_bias_rows(tri_attn_s* t, cudaStream_t s, int& mark) {
   TcState* st = (TcState*)t->tc;
   const cudaError_t e =
-      k2_bias_rows(st->bias32, t->B, t->h, t->N, st->Nb, t->ending, (__half*)t->bias, s);
+      k2_bias_rows(st->bias32, t->B, t->h, t->N, st->Nb, t->ending, (__half*)t->bias, s, !t->timing);
   tri_mark(t, s, mark++, "bias_rows");
   return e;
 }
@@ -377,7 +377,7 @@ cudaError_t launch_k2(tri_attn_s* t, cudaStream_t s, int u0, int nu) {
     p2.step.rg = gq % p2.row_groups;
     p2.step.b = gq / p2.row_groups;
   }
-  return k2_launch(t->d, (int)g2, s, st->m2, p2);
+  return k2_launch(t->d, (int)g2, s, !t->timing, st->m2, p2);
 }
 
 // Store map of K3's bf16 output (cell order or by columns): 32 x 32 boxes.
@@ -404,7 +404,7 @@ cudaError_t launch_k3(tri_attn_s* t, cudaStream_t s, const CUtensorMap& map_out,
     m.o = st->map_oc;
   }
   m.out = map_out;
-  return k3_launch(t->D, grid, s, m, p3);
+  return k3_launch(t->D, grid, s, !t->timing, m, p3);
 }
 
 }  // namespace

@@ -123,6 +123,18 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
+// Programmatic dependent launch. Every kernel of the path is launched so that
+// it may start while the previous kernel on the stream is still running; its
+// threads run the prologue that reads nothing another kernel writes (barrier
+// setup, tensor-memory allocation, the resident weights), then pdl_wait()
+// blocks until the previous kernel has completed and its writes are visible.
+// pdl_trigger() lets the next kernel start as soon as every CTA of this one has
+// called it (or exited); it only releases the launch, not the data.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Shared-memory descriptor swizzle mode for rows of `bytes` (32, 64 or 128).
 __host__ __device__ constexpr uint32_t swz_mode(int bytes) {
   return bytes == 128 ? tc::SWZ_128B : bytes == 64 ? tc::SWZ_64B : tc::SWZ_32B;

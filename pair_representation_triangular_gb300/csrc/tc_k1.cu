@@ -78,6 +78,10 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
   int my_tiles = 0;
   for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) ++my_tiles;
   int issued = 0;                          // tile loads issued (producer thread)
+  pdl_trigger();
+  // x, the mask and every output may belong to the previous kernel on the
+  // stream; only the resident weights are loaded before its completion.
+  if (warp != kTmaWarp) pdl_wait();
 
   if (warp == kTmaWarp) {
     // ---------------- TMA producer
@@ -89,6 +93,7 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
         for (int nh = 0; nh < 2; ++nh)
           tc::tma_load_2d(smem + S::OFF_W + kh * S::W_HALF + nh * S::NHALF * XSW, &map_w,
                           &bars->w_full, kh * S::HC, nh * S::NHALF);
+      pdl_wait();
       for (int it = 0; it < my_tiles; ++it) {
         const int b = it & 1;
         if (it >= 2 && !wait_or_abort(&bars->x_empty[b], ((it >> 1) - 1) & 1, ab)) break;
@@ -341,9 +346,10 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
 }
 
 template <int D, int H>
-cudaError_t launch(int grid, cudaStream_t s, const Maps& m, const Params& p, const Consts& c) {
-  ln_proj_tc<D, H><<<grid, kThreads, Shape<D>::SMEM, s>>>(m.x, m.w, m.q, m.k, m.v, m.g, p, c);
-  return cudaGetLastError();
+cudaError_t launch(int grid, cudaStream_t s, bool pdl, const Maps& m, const Params& p,
+                   const Consts& c) {
+  return launch_pdl(pdl, ln_proj_tc<D, H>, dim3(grid), dim3(kThreads), Shape<D>::SMEM, s, m.x, m.w, m.q,
+                    m.k, m.v, m.g, p, c);
 }
 
 template <int D, int H>
@@ -364,9 +370,9 @@ cudaError_t k1_init() {
   return e;
 }
 
-cudaError_t k1_launch(int D, int h, int grid, cudaStream_t s, const k1::Maps& m,
+cudaError_t k1_launch(int D, int h, int grid, cudaStream_t s, bool pdl, const k1::Maps& m,
                       const k1::Params& p, const k1::Consts& c) {
-#define X(DD, HH) if (D == DD && h == HH) return k1::launch<DD, HH>(grid, s, m, p, c);
+#define X(DD, HH) if (D == DD && h == HH) return k1::launch<DD, HH>(grid, s, pdl, m, p, c);
   TRI_K1_SHAPES(X)
 #undef X
   return cudaErrorInvalidValue;

@@ -299,6 +299,10 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
   tc::tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   int q_issued = 0, kv_issued = 0, b_issued = 0;    // producer: loads issued
+  // Every input of the attention comes from the kernels before it on the
+  // stream, and o may still be read by the previous forward's output kernel.
+  pdl_trigger();
+  pdl_wait();
 
   if (warp < 4) {
     tc::regs_dec<kRegsCtl>();
@@ -640,6 +644,8 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
 __global__ void __launch_bounds__(256)
 bias_rows(const float* __restrict__ C, int N, int Nb, int ending, __half* __restrict__ P) {
   __shared__ float tile[8][132];
+  pdl_trigger();
+  pdl_wait();
   const int a0 = blockIdx.x * 8;
   const long long plane = blockIdx.y;
   const float* Cp = C + plane * N * N;
@@ -698,6 +704,8 @@ bias_rows(const float* __restrict__ C, int N, int Nb, int ending, __half* __rest
 // keeps some key.
 __global__ void mask_summary(const int32_t* __restrict__ mask, int N, long long rows, int words,
                              uint32_t* __restrict__ bits, unsigned char* __restrict__ any) {
+  pdl_trigger();
+  pdl_wait();
   const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= rows) return;
   const int lane = threadIdx.x & 31;
@@ -721,6 +729,8 @@ __global__ void __launch_bounds__(256)
 mask_summary_cols(const int32_t* __restrict__ mask, int N, int words, uint32_t* __restrict__ bits,
                   unsigned char* __restrict__ any) {
   __shared__ uint32_t found[8][32];
+  pdl_trigger();
+  pdl_wait();
   const int cblocks = (N + 31) >> 5;
   const long long b = blockIdx.x / cblocks;
   const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
@@ -749,9 +759,9 @@ mask_summary_cols(const int32_t* __restrict__ mask, int N, int words, uint32_t* 
 }
 
 template <int DH>
-cudaError_t launch(int grid, cudaStream_t s, const Maps& m, const Params& p) {
-  row_attn_tc<DH><<<grid, Shape<DH>::kThreads, Shape<DH>::SMEM, s>>>(m.q, m.k, m.v, m.b, m.o, p);
-  return cudaGetLastError();
+cudaError_t launch(int grid, cudaStream_t s, bool pdl, const Maps& m, const Params& p) {
+  return launch_pdl(pdl, row_attn_tc<DH>, dim3(grid), dim3(Shape<DH>::kThreads), Shape<DH>::SMEM, s, m.q,
+                    m.k, m.v, m.b, m.o, p);
 }
 
 template <int DH>
@@ -777,32 +787,30 @@ int k2_keys_per_stage(int d) {
   return d == 16 ? k2::Shape<16>::KVK : d == 32 ? k2::Shape<32>::KVK : k2::Shape<64>::KVK;
 }
 
-cudaError_t k2_launch(int d, int grid, cudaStream_t s, const k2::Maps& m, const k2::Params& p) {
+cudaError_t k2_launch(int d, int grid, cudaStream_t s, bool pdl, const k2::Maps& m,
+                      const k2::Params& p) {
   switch (d) {
-    case 16: return k2::launch<16>(grid, s, m, p);
-    case 32: return k2::launch<32>(grid, s, m, p);
-    case 64: return k2::launch<64>(grid, s, m, p);
+    case 16: return k2::launch<16>(grid, s, pdl, m, p);
+    case 32: return k2::launch<32>(grid, s, pdl, m, p);
+    case 64: return k2::launch<64>(grid, s, pdl, m, p);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t k2_mask_summary(const int32_t* mask, int B, int N, bool ending, int words,
-                            uint32_t* bits, unsigned char* any, cudaStream_t s) {
+                            uint32_t* bits, unsigned char* any, cudaStream_t s, bool pdl) {
   const long long rows = (long long)B * N;
-  if (!ending) {
-    k2::mask_summary<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(mask, N, rows, words, bits, any);
-  } else {
-    const unsigned blocks = (unsigned)(B * (long long)((N + 31) / 32));
-    k2::mask_summary_cols<<<blocks, 256, 0, s>>>(mask, N, words, bits, any);
-  }
-  return cudaGetLastError();
+  if (!ending)
+    return launch_pdl(pdl, k2::mask_summary, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s, mask, N,
+                      rows, words, bits, any);
+  const unsigned blocks = (unsigned)(B * (long long)((N + 31) / 32));
+  return launch_pdl(pdl, k2::mask_summary_cols, dim3(blocks), dim3(256), 0, s, mask, N, words, bits, any);
 }
 
 cudaError_t k2_bias_rows(const float* C, int B, int h, int N, int Nb, bool ending, __half* P,
-                         cudaStream_t s) {
+                         cudaStream_t s, bool pdl) {
   const dim3 grid((unsigned)((N + 7) / 8), (unsigned)(B * h));
-  k2::bias_rows<<<grid, 256, 0, s>>>(C, N, Nb, ending ? 1 : 0, P);
-  return cudaGetLastError();
+  return launch_pdl(pdl, k2::bias_rows, grid, dim3(256), 0, s, C, N, Nb, ending ? 1 : 0, P);
 }
 
 }  // namespace tri_tc

@@ -68,6 +68,10 @@ gate_out_tc(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ C
   int my_tiles = 0;
   for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) ++my_tiles;
   int issued = 0;
+  pdl_trigger();
+  // g, o and out belong to earlier kernels on the stream; only Wo and bo are
+  // read before the previous kernel's completion.
+  if (warp != kTmaWarp) pdl_wait();
 
   if (warp == kTmaWarp) {
     if (lane == 0) {
@@ -77,6 +81,7 @@ gate_out_tc(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ C
       tc::mbar_arrive_expect_tx(&bars->w_full, S::W_BYTES);
       for (int kh = 0; kh < S::KH; ++kh)
         tc::tma_load_2d(smem + S::OFF_W + kh * S::W_HALF, &map_wo, &bars->w_full, kh * S::HC, 0);
+      pdl_wait();
       for (int it = 0; it < my_tiles; ++it) {
         const int b = it & 1;
         if (it >= 2 && !wait_or_abort(&bars->in_empty[b], ((it >> 1) - 1) & 1, ab)) break;
@@ -206,9 +211,9 @@ gate_out_tc(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ C
 }
 
 template <int D>
-cudaError_t launch(int grid, cudaStream_t s, const Maps& m, const Params& p) {
-  gate_out_tc<D><<<grid, kThreads, Shape<D>::SMEM, s>>>(m.g, m.o, m.wo, m.out, p);
-  return cudaGetLastError();
+cudaError_t launch(int grid, cudaStream_t s, bool pdl, const Maps& m, const Params& p) {
+  return launch_pdl(pdl, gate_out_tc<D>, dim3(grid), dim3(kThreads), Shape<D>::SMEM, s, m.g, m.o, m.wo,
+                    m.out, p);
 }
 
 template <int D>
@@ -226,11 +231,12 @@ cudaError_t k3_init() {
   return e;
 }
 
-cudaError_t k3_launch(int D, int grid, cudaStream_t s, const k3::Maps& m, const k3::Params& p) {
+cudaError_t k3_launch(int D, int grid, cudaStream_t s, bool pdl, const k3::Maps& m,
+                      const k3::Params& p) {
   switch (D) {
-    case 32: return k3::launch<32>(grid, s, m, p);
-    case 64: return k3::launch<64>(grid, s, m, p);
-    case 128: return k3::launch<128>(grid, s, m, p);
+    case 32: return k3::launch<32>(grid, s, pdl, m, p);
+    case 64: return k3::launch<64>(grid, s, pdl, m, p);
+    case 128: return k3::launch<128>(grid, s, pdl, m, p);
     default: return cudaErrorInvalidValue;
   }
 }

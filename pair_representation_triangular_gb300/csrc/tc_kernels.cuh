@@ -103,22 +103,46 @@ struct Maps {
 };
 }  // namespace k3
 
+// Launch with the programmatic-stream-serialization attribute: the kernel may
+// begin while the previous kernel on the stream finishes (it waits for that
+// kernel's completion itself, see pdl_wait). After any other stream operation
+// the attribute has no effect and ordering is the stream's usual one.
+template <typename... ExpTypes, typename... ActTypes>
+cudaError_t launch_pdl(bool pdl, void (*kernel)(ExpTypes...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, ActTypes&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<ActTypes&&>(args)...);
+}
+
 // Launchers: each picks the kernel instantiated for the shape and returns the
-// launch status. *_init sets the shared-memory size of every instantiation.
+// launch status; `pdl` requests the programmatic dependent launch (off while
+// events are recorded between the kernels). *_init sets the shared-memory size
+// of every instantiation.
 cudaError_t k1_init();
-cudaError_t k1_launch(int D, int h, int grid, cudaStream_t s, const k1::Maps& m,
+cudaError_t k1_launch(int D, int h, int grid, cudaStream_t s, bool pdl, const k1::Maps& m,
                       const k1::Params& p, const k1::Consts& c);
 
 cudaError_t k2_init();
 int k2_lines_per_unit(int d);
 int k2_keys_per_stage(int d);
-cudaError_t k2_launch(int d, int grid, cudaStream_t s, const k2::Maps& m, const k2::Params& p);
+cudaError_t k2_launch(int d, int grid, cudaStream_t s, bool pdl, const k2::Maps& m,
+                      const k2::Params& p);
 cudaError_t k2_mask_summary(const int32_t* mask, int B, int N, bool ending, int words,
-                            uint32_t* bits, unsigned char* any, cudaStream_t s);
+                            uint32_t* bits, unsigned char* any, cudaStream_t s, bool pdl);
 cudaError_t k2_bias_rows(const float* C, int B, int h, int N, int Nb, bool ending, __half* P,
-                         cudaStream_t s);
+                         cudaStream_t s, bool pdl);
 
 cudaError_t k3_init();
-cudaError_t k3_launch(int D, int grid, cudaStream_t s, const k3::Maps& m, const k3::Params& p);
+cudaError_t k3_launch(int D, int grid, cudaStream_t s, bool pdl, const k3::Maps& m,
+                      const k3::Params& p);
 
 }  // namespace tri_tc

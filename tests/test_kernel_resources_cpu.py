@@ -155,9 +155,12 @@ def test_attention_register_split_fits_the_launch(report, shapes, d):
 
 F32_SRC = os.path.join(tbuild.CSRC, "kernels_f32.cu")
 # fp32 kernels of the two fp32 benchmark configurations (d = 16 and d = 32,
-# starting node; d = 32 ending node), by a unique piece of their mangled names.
+# starting node; d = 32 ending node) and the 128-wide heads, by a unique piece
+# of their mangled names.
 F32_SPILL_FREE = ("11ln_proj_f32E", "12gate_out_f32E", "row_attn_f32ILi16ELi32ELb0EE",
-                  "row_attn_f32ILi32ELi32ELb0EE", "row_attn_f32ILi32ELi32ELb1EE")
+                  "row_attn_f32ILi32ELi32ELb0EE", "row_attn_f32ILi32ELi32ELb1EE",
+                  # d = 128 (two threads per query), both nodes
+                  "row_attn_f32ILi128ELi16ELb0EE", "row_attn_f32ILi128ELi16ELb1EE")
 
 
 def test_fp32_benchmark_kernels_do_not_spill():

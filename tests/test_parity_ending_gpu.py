@@ -62,7 +62,7 @@ def test_ending_bf16_small_shapes(N, mode):
 
 
 @pytest.mark.parametrize("B,N,D,h", [(1, 1, 32, 1), (2, 17, 32, 4), (1, 33, 64, 2),
-                                     (1, 129, 64, 4), (1, 20, 128, 4)])
+                                     (1, 129, 64, 4), (1, 20, 128, 4), (1, 70, 128, 1)])
 @pytest.mark.parametrize("mode", [0, 1])
 def test_ending_f32_small_shapes(B, N, D, h, mode):
     w = W.custom(B, N, D, h, "f32", "bernoulli", seed=6000 + N + D + h)

@@ -29,7 +29,8 @@ def test_f32_workloads(name, mode):
 
 
 SHAPES = [(1, 1, 32, 1), (2, 2, 32, 2), (1, 3, 64, 4), (1, 17, 32, 4), (2, 33, 64, 2),
-          (1, 127, 32, 1), (1, 129, 64, 4), (1, 33, 128, 1), (1, 20, 128, 4), (1, 9, 96, 4)]
+          (1, 127, 32, 1), (1, 129, 64, 4), (1, 33, 128, 1), (1, 20, 128, 4), (1, 9, 96, 4),
+          (1, 130, 256, 2)]   # d = 128: two threads per query, several key chunks
 
 
 @pytest.mark.parametrize("B,N,D,h", SHAPES)
