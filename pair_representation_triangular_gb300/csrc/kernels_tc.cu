@@ -141,6 +141,12 @@ struct TcState {
 
 int round_up(int a, int b) { return (a + b - 1) / b * b; }
 
+// n bf16 values times a power of 2 (exact).
+__global__ void scale_bf16(__nv_bfloat16* p, long long n, float s) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) p[i] = __float2bfloat16_rn(__bfloat162float(p[i]) * s);
+}
+
 
 }  // namespace
 
@@ -238,6 +244,16 @@ cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const voi
     bound *= 1.02;
     st->v_scale = 1.0f;
     while (bound * st->v_scale >= 32768.0 && st->v_scale > 0x1p-100f) st->v_scale *= 0.5f;
+    // The scale goes into the packed Wv rows (rows 2D .. 3D - 1 of [Wq;Wk;Wv;Wg]):
+    // a power of 2, so the bf16 weights scale exactly.
+    if (st->v_scale != 1.0f) {
+      const long long n = (long long)D * D;
+      scale_bf16<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(
+          (__nv_bfloat16*)t->w_proj + 2ll * D * D, n, st->v_scale);
+      e = cudaGetLastError();
+      if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+      if (e != cudaSuccess) return e;
+    }
   }
 
   const long long cells = t->cells;
@@ -313,7 +329,6 @@ cudaError_t launch_k1(tri_attn_s* t, cudaStream_t s, const CUtensorMap& map_x,
   p1.bias32 = st->bias32; p1.dev_err = t->dev_err;
   p1.polls = t->wait_limit;
   p1.q_scale = kLog2e / sqrtf((float)t->d);
-  p1.v_scale = st->v_scale;
   const int grid = n < st->num_sms ? n : st->num_sms;
   k1::Maps m = st->m1;
   m.x = map_x;

@@ -1,8 +1,9 @@
 // K1 of the bf16 tensor-core path: LayerNorm as the prologue of one
 // concatenated projection GEMM, x_hat [128 cells x D] . [Wq|Wk|Wv|Wg]^T -> 4D
 // TMEM columns; the epilogue writes q (times log2(e)/sqrt(d)) and k in bf16,
-// v in fp16 (times a power of 2 that keeps it in range; the attention's P V
-// runs on fp16 operands) and sigmoid(g + bg) in bf16. The h pair-bias outputs (Wb x_hat, with gamma and
+// v in fp16 (times a power of 2, folded into the packed Wv rows, that keeps it
+// in range; the attention's P V runs on fp16 operands) and sigmoid(g + bg) in
+// bf16. The h pair-bias outputs (Wb x_hat, with gamma and
 // beta folded into Wb) come out of the LayerNorm's statistics pass on the CUDA
 // cores and go, scaled by log2(e), to an fp32 plane in cell order.
 //
@@ -291,12 +292,11 @@ ln_proj_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
               packed[e] = tc::pack_bf16x2(__uint_as_float(acc[2 * e]) * p.q_scale,
                                           __uint_as_float(acc[2 * e + 1]) * p.q_scale);
           } else if (sect == 2) {
-            // v in fp16, times v_scale: a power of 2 chosen from the weights so
-            // that |v| stays below 2^15 for any input (exact scaling).
+            // v in fp16 (the resident Wv rows carry the power of 2 that keeps
+            // |v| below 2^15 for any input).
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-              packed[e] = cvt_f16x2(__uint_as_float(acc[2 * e]) * p.v_scale,
-                                    __uint_as_float(acc[2 * e + 1]) * p.v_scale);
+              packed[e] = cvt_f16x2(__uint_as_float(acc[2 * e]), __uint_as_float(acc[2 * e + 1]));
           } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e)

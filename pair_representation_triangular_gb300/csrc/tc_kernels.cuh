@@ -37,7 +37,6 @@ struct Params {
   unsigned int* dev_err;
   long long polls;
   float q_scale;               // q is stored times log2(e) / sqrt(d)
-  float v_scale;               // v is stored in fp16 times this power of 2
 };
 
 // x: loads (channel, cell), box (channels of one half, 128 cells). w: the

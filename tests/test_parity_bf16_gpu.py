@@ -6,6 +6,8 @@ kernels consume. Every workload, the full-size ones included, is compared
 element by element on every cell, in the same launch configuration the
 benchmark uses (the oracle's lines spread over spawned processes).
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -299,6 +301,35 @@ def test_bf16_large_common_offset(mode):
     got = H.run_forward(w, inp, mode)[0]
     ref = O.forward(inp["x"], inp["pair_mask"], inp["params"], w.h, mode)
     H.assert_parity(w, got, ref)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_bf16_value_weights_scaled_into_fp16_range(mode):
+    """Wv times 2^12 and Wo times 2^-12 (both exact in bf16): the output is that
+    of ordinary weights, but the bound on |v| over all inputs exceeds the fp16
+    range, so the library stores v times a power of 2 below 1 (carried by the
+    resident Wv rows) and divides it out of the attention output."""
+    w = W.custom(1, 130, 128, 4, "bf16", "bernoulli", seed=66)
+    inp = W.make_inputs(w)
+    inp["params"]["Wv"] = (inp["params"]["Wv"].astype(np.float64) * 4096.0).astype(np.float32)
+    inp["params"]["Wo"] = (inp["params"]["Wo"].astype(np.float64) / 4096.0).astype(np.float32)
+    mod = tb.TriangularAttention(w.B, w.N, w.D, w.h, tb.TRI_ATTN_BF16, mode, H.device_params(inp, w))
+    try:
+        x = torch.from_numpy(inp["x"]).to("cuda", torch.bfloat16)
+        m = torch.from_numpy(inp["pair_mask"]).cuda()
+        got = mod.forward(x, m).double().cpu().numpy()
+        assert mod.sync_check() == tb.TRI_ATTN_OK
+        v_got = mod.intermediate("v").double().cpu().numpy().reshape(-1, w.D)
+    finally:
+        mod.close()
+    P = {k: v.astype(np.float64) for k, v in inp["params"].items()}
+    x_hat = O.layer_norm(inp["x"].astype(np.float64), P["gamma"], P["beta"])
+    v_ref = O.project(x_hat, P)[2].reshape(-1, w.D)
+    scale = float(np.sum(v_got * v_ref) / np.sum(v_ref * v_ref))
+    k = round(-math.log2(scale))
+    assert k >= 1 and abs(scale * 2.0 ** k - 1.0) < 1e-3, scale
+    assert np.all(np.isfinite(v_got)) and np.abs(v_got).max() < 32768.0
+    H.assert_parity(w, got, O.forward(inp["x"], inp["pair_mask"], inp["params"], w.h, mode))
 
 
 # Every (D, h) the tensor-core kernels are built for: D in {32, 64, 128} and
