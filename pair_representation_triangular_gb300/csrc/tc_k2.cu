@@ -459,13 +459,15 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     unsigned nx_any = 0u;
     const uint32_t* nx_mrow = p.mbits;
     uint2 nx_bits0 = make_uint2(0u, 0u);
-    if (my_units > 0) unit_loads(decode_unit(p.unit0 + blockIdx.x, p), nx_any, nx_mrow, nx_bits0);
+    // Units advance by digit-wise steps: cu is unit ui, pu the unit before it.
+    Unit cu = decode_unit(p.unit0 + blockIdx.x, p), pu = cu;
+    if (my_units > 0) unit_loads(cu, nx_any, nx_mrow, nx_bits0);
     // Unit epilogue: o = O / l once the unit's last P V has landed, staged in
     // shared memory and written by one TMA store per warp (queries past N are
     // clipped by the store; lines past N and warps whose 32 queries all lie
     // past N skip it).
     uint8_t* const ostg = smem + OFF_OST + sw * OST_BYTES;
-    auto finish_unit = [&](int ui, int clast, float l) -> bool {
+    auto finish_unit = [&](const Unit& fu, int clast, float l) -> bool {
       if (!warp_wait_or_abort(&bars->p_free[r][clast & 1], (clast >> 1) & 1, ab)) return false;
       tc::tc_fence_after();
       uint32_t ov[DH];
@@ -480,7 +482,6 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       // O is in registers: its columns may take the next unit's sums.
       tc::tc_fence_before();
       tc::mbar_arrive(&bars->o_free[r]);
-      const Unit fu = decode_unit(p.unit0 + blockIdx.x + ui * gridDim.x, p);
       const int fi = fu.rg * R + r, fj = fu.j0 + (warp & 3) * 32;
       if (fi < N && fj < N) {
         // A query row has l in [2^-16, 2^100) unless its logits left that range
@@ -530,14 +531,12 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       const bool uni = nx_any == 0u;
       const uint32_t* mrow = nx_mrow;
       uint2 nbits = nx_bits0;
-      if (ui + 1 < my_units)
-        unit_loads(decode_unit(p.unit0 + blockIdx.x + (ui + 1) * gridDim.x, p), nx_any, nx_mrow,
-                   nx_bits0);
+      Unit nu = cu;
+      step_unit(nu, p);
+      if (ui + 1 < my_units) unit_loads(nu, nx_any, nx_mrow, nx_bits0);
       float l_run = 0.f;
-      // Warp-uniform unit state: whether any lane has a key-keeping query row,
-      // and whether every lane has one.
+      // Warp-uniform unit state: whether any lane has a key-keeping query row.
       const bool unit_live = __any_sync(0xffffffffu, !uni);
-      const bool all_live = __all_sync(0xffffffffu, !uni);
       for (int kt = 0; ok && kt < KT; ++kt, advance_soft(its, KT)) {
         const int c = its.c;
         const uint2 mb = nbits;
@@ -566,19 +565,29 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         const uint32_t tsb = tb + (c & 1) * TM_S1;     // S(c), then P(c) over it
         uint32_t tsum = 0u;                            // fp16 pair
         uint32_t pk[BK / 2];
-        if (any_live) {
+        // The common sub-tile (every key real and kept) has a copy of its own
+        // without the masking, which slowed it even when skipped.
+        if (any_live && all_kept) {
           uint32_t sv[BK];
           uint4 bh[8];
           tc::tmem_ld64(tsb, sv);
           load_bias(brow, bh);
           tc::tmem_ld_wait();
-          if (!all_kept) {
-            // Dropped keys: S = -inf, which the bias add keeps at -inf (P = 0).
+          if (live)
+            tsum = p_tile_fast(sv, bh, pk);
+          else
+            p_tile_const(uni ? rl0 : 0u, uni ? rl1 : 0u, pk);
+        } else if (any_live) {
+          uint32_t sv[BK];
+          uint4 bh[8];
+          tc::tmem_ld64(tsb, sv);
+          load_bias(brow, bh);
+          tc::tmem_ld_wait();
+          // Dropped keys: S = -inf, which the bias add keeps at -inf (P = 0).
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              if (!((bw0 >> k) & 1u)) sv[k] = 0xff800000u;
-              if (!((bw1 >> k) & 1u)) sv[32 + k] = 0xff800000u;
-            }
+          for (int k = 0; k < 32; ++k) {
+            if (!((bw0 >> k) & 1u)) sv[k] = 0xff800000u;
+            if (!((bw1 >> k) & 1u)) sv[32 + k] = 0xff800000u;
           }
           if (live)
             tsum = p_tile_fast(sv, bh, pk);
@@ -602,13 +611,15 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         tc::mbar_arrive(&bars->p_full[r][c & 1]);
         if (kt == 0 && ui >= 1) {
           // The previous unit's epilogue, after this unit's first sub-tile.
-          if (!finish_unit(ui - 1, c - 1, l_prev)) { ok = false; break; }
+          if (!finish_unit(pu, c - 1, l_prev)) { ok = false; break; }
         }
       }
       if (!ok) break;
       l_prev = l_run;
+      pu = cu;
+      cu = nu;
     }
-    if (ok && my_units > 0) finish_unit(my_units - 1, my_units * KT - 1, l_prev);
+    if (ok && my_units > 0) finish_unit(pu, my_units * KT - 1, l_prev);
     if (lane == 0) tc::tma_store_wait_all<0>();
   }
 
