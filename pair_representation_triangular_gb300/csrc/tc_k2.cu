@@ -112,10 +112,11 @@ __device__ __forceinline__ void load_bias(uint32_t brow, uint4 (&bh)[8]) {
 // bits, sv) in log2 units (the reference of the exponentials is 0). Each key
 // pair of S is rounded to an fp16 pair, the fp16 bias pair added and 2^x taken
 // of both halves at once; P leaves as 32 fp16 pairs (the A operand of the P V
-// MMA) and the return value is their sum as one fp16 pair (a tree of pairwise
-// adds).
+// MMA) and the return value is their sum as one fp16 pair: four running sums,
+// each taking every fourth pair as it is produced, then added pairwise.
 __device__ __forceinline__ uint32_t p_tile_fast(const uint32_t (&sv)[2 * BK / 2], const uint4 (&bh)[8],
                                                 uint32_t (&pk)[BK / 2]) {
+  uint32_t acc[4];
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     const uint32_t hw[4] = {bh[q].x, bh[q].y, bh[q].z, bh[q].w};
@@ -123,16 +124,10 @@ __device__ __forceinline__ uint32_t p_tile_fast(const uint32_t (&sv)[2 * BK / 2]
     for (int e = 0; e < 4; ++e) {
       const int m = q * 4 + e;
       pk[m] = ex2_f16x2(hadd2(cvt_f16x2(__uint_as_float(sv[2 * m]), __uint_as_float(sv[2 * m + 1])), hw[e]));
+      acc[e] = q == 0 ? pk[m] : hadd2(acc[e], pk[m]);
     }
   }
-  uint32_t t[16];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) t[k] = hadd2(pk[2 * k], pk[2 * k + 1]);
-#pragma unroll
-  for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-    for (int k = 0; k < w; ++k) t[k] = hadd2(t[2 * k], t[2 * k + 1]);
-  return t[0];
+  return hadd2(hadd2(acc[0], acc[1]), hadd2(acc[2], acc[3]));
 }
 
 // P of a 64-key sub-tile row of a lane that is not live: 1 on every real key
