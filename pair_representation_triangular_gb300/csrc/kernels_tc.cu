@@ -130,6 +130,7 @@ struct TcState {
   float v_scale;             // v is stored in fp16 times this power of 2
   float* bias32;             // (B, h, N, N) fp32 pair bias in cell order (K1's output)
   unsigned char* row_any;    // (B*N) mask rows keeping some key
+  int* line_tiles;           // (B*N) leading key sub-tiles each mask row needs
   uint32_t* mbits;           // (B*N, words) mask bits
   int words;
   int num_sms;
@@ -162,8 +163,8 @@ size_t tri_tc_extra_bytes(int B, int N, int, int h) {
   // the attention's fp16 bias plane (rows padded to Nb) beside K1's fp32 one;
   // plus the mask summary
   const size_t Nb = (size_t)round_up(N, 8);
-  return (size_t)B * h * N * Nb * 2 + (size_t)B * N + (size_t)B * N * 2 * ((N + 63) / 64) * 4 +
-         512;
+  return (size_t)B * h * N * Nb * 2 + (size_t)B * N * 5 + (size_t)B * N * 2 * ((N + 63) / 64) * 4 +
+         1024;
 }
 
 cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const void* Wv,
@@ -185,6 +186,7 @@ cudaError_t tri_tc_init(tri_attn_s* t, const void* Wq, const void* Wk, const voi
   st->words = 2 * ((N + k2::BK - 1) / k2::BK);   // two 32-key words per 64-key tile
   st->R = k2_lines_per_unit(t->d);
   if (e == cudaSuccess) e = cudaMalloc((void**)&st->row_any, (size_t)B * N);
+  if (e == cudaSuccess) e = cudaMalloc((void**)&st->line_tiles, (size_t)B * N * 4);
   if (e == cudaSuccess) e = cudaMalloc((void**)&st->mbits, (size_t)B * N * st->words * 4);
   const size_t wbytes = (size_t)D * D * 2;
   const void* mats[4] = {Wq, Wk, Wv, Wg};
@@ -305,6 +307,7 @@ void tri_tc_release(tri_attn_s* t) {
   if (!st) return;
   if (st->bias32) cudaFree(st->bias32);
   if (st->row_any) cudaFree(st->row_any);
+  if (st->line_tiles) cudaFree(st->line_tiles);
   if (st->mbits) cudaFree(st->mbits);
   if (st->copy_in) cudaStreamDestroy(st->copy_in);
   if (st->copy_out) cudaStreamDestroy(st->copy_out);
@@ -339,7 +342,8 @@ cudaError_t launch_k1(tri_attn_s* t, cudaStream_t s, const CUtensorMap& map_x,
 cudaError_t launch_mask(tri_attn_s* t, cudaStream_t s, const int32_t* mask, int& mark) {
   TcState* st = (TcState*)t->tc;
   const cudaError_t e =
-      k2_mask_summary(mask, t->B, t->N, t->ending, st->words, st->mbits, st->row_any, s, !t->timing);
+      k2_mask_summary(mask, t->B, t->N, t->ending, st->words, st->mbits, st->row_any, st->line_tiles, s,
+                      !t->timing);
   tri_mark(t, s, mark++, t->ending ? "mask_summary_cols" : "mask_summary");
   return e;
 }
@@ -372,7 +376,7 @@ cudaError_t launch_k2(tri_attn_s* t, cudaStream_t s, int u0, int nu) {
   p2.unit0 = u0;
   p2.units = nu;
   p2.words = st->words;
-  p2.mbits = st->mbits; p2.row_any = st->row_any;
+  p2.mbits = st->mbits; p2.row_any = st->row_any; p2.line_tiles = st->line_tiles;
   p2.dev_err = t->dev_err;
   p2.polls = t->wait_limit;
   p2.q = (const __nv_bfloat16*)t->q;

@@ -36,6 +36,13 @@ struct Bars {
   uint64_t s_ready[R][2], p_full[R][2], p_free[R][2], o_free[R], drain[R];
   uint32_t tmem_base;
   int abort;
+  // Key sub-tiles of unit ui in slot ui & 7, written by the producer before the
+  // unit's first copies (the consumers read it after waiting on one of them:
+  // the MMA warps on the unit's Q, the softmax on its first bias sub-tile).
+  // The producer rewrites a slot only after the MMAs of the unit six places
+  // on have been issued, which needs the softmax four units on, so every
+  // reader of the slot is done with it.
+  int unit_kt[8];
 };
 
 struct Unit {
@@ -69,29 +76,43 @@ __device__ __forceinline__ void step_unit(Unit& u, const Params& p) {
   u.j0 = u.jt * BQ;
 }
 
+// Key sub-tiles of a unit: the row-key reading skips the trailing sub-tiles
+// that every line of the unit drops (a line that keeps no key needs all of
+// them); the query-key reading takes all KT.
+template <int R>
+__device__ __forceinline__ int unit_tiles(const Unit& u, const Params& p, int KT) {
+  if (p.mask_mode == TRI_ATTN_MASK_QUERY_KEY) return KT;
+  int t = 1;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int a = u.rg * R + r;
+    if (a < p.N) t = max(t, __ldg(p.line_tiles + (long long)u.b * p.N + a));
+  }
+  return t;
+}
+
 // Position in a stream of sub-tiles: global sub-tile c, its unit ui and key
 // sub-tile kt, the K/V stage slot and phase, and the bias slot and phase,
-// advanced without dividing.
+// advanced without dividing. KTu: the sub-tiles of unit ui.
 struct SubIt {
   int c, ui, kt, kvs, kvph, bs, bph;
 };
 template <int SPS, int KV_STAGES>
-__device__ __forceinline__ void advance(SubIt& it, int KT) {
+__device__ __forceinline__ void advance(SubIt& it, int KTu) {
   ++it.c;
-  const bool stage_end = (it.kt % SPS) == SPS - 1 || it.kt == KT - 1;
-  if (++it.kt == KT) { it.kt = 0; ++it.ui; }
+  const bool stage_end = (it.kt % SPS) == SPS - 1 || it.kt == KTu - 1;
+  if (++it.kt == KTu) { it.kt = 0; ++it.ui; }
   if (stage_end && ++it.kvs == KV_STAGES) { it.kvs = 0; it.kvph ^= 1; }
   if (++it.bs == B_STAGES) { it.bs = 0; it.bph ^= 1; }
 }
 
-// The softmax's position in its sub-tile stream: global sub-tile c, key
-// sub-tile kt and the bias slot and phase.
+// The softmax's position in its sub-tile stream: global sub-tile c and the
+// bias slot and phase.
 struct SoftIt {
-  int c, kt, bs, bph;
+  int c, bs, bph;
 };
-__device__ __forceinline__ void advance_soft(SoftIt& it, int KT) {
+__device__ __forceinline__ void advance_soft(SoftIt& it) {
   ++it.c;
-  if (++it.kt == KT) it.kt = 0;
   if (++it.bs == B_STAGES) { it.bs = 0; it.bph ^= 1; }
 }
 
@@ -316,8 +337,10 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       for (int ui = 0; ok && ui < my_units; ++ui, step_unit(un, p)) {
         const int a0 = un.rg * R;
         const int qb = ui & 1;
+        const int KTu = unit_tiles<R>(un, p, KT);
         if (ui >= 2 && !warp_wait_or_abort(&bars->q_empty[qb], ((ui >> 1) - 1) & 1, ab)) break;
         if (elect_one()) {
+          bars->unit_kt[ui & 7] = KTu;
           tc::mbar_arrive_expect_tx(&bars->q_full[qb], R * Q_BYTES);
           for (int r = 0; r < R; ++r)
             tc::tma_load_4d(smem + OFF_Q + (qb * R + r) * Q_BYTES, &map_q, &bars->q_full[qb],
@@ -325,7 +348,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         }
         __syncwarp();
         q_issued = ui + 1;
-        for (int kt = 0; kt < KT; ++kt) {
+        for (int kt = 0; kt < KTu; ++kt) {
           if (kt % SPS == 0) {
             if (kv_issued >= KV_STAGES && !warp_wait_or_abort(&bars->kv_empty[kvs], kvph ^ 1, ab)) {
               ok = false;
@@ -376,7 +399,9 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       const uint64_t dq0 = tc::smem_desc(tc::smem_addr(smem + OFF_Q + r * Q_BYTES), 16, 8 * SW, swz_mode(SW));
       const uint64_t dk0 =
           tc::smem_desc(tc::smem_addr(smem + OFF_KV + r * 2 * KVT_BYTES), 16, 8 * SW, swz_mode(SW));
-      const int total = my_units * KT;     // one item per key sub-tile
+      // The sub-tiles of a cursor's unit, published by the producer before the
+      // unit's Q copy, which the S cursor (never behind the P V one) has waited on.
+      auto unit_kt = [&](const SubIt& it) -> int { return *(volatile int*)&bars->unit_kt[it.ui & 7]; };
       auto qk = [&](const SubIt& it) -> bool {
         const int c = it.c;
         if (it.kt == 0 && !warp_wait_or_abort(&bars->q_full[it.ui & 1], (it.ui >> 1) & 1, ab)) return false;
@@ -389,7 +414,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
           for (int ks = 0; ks < DH / 16; ++ks)
             tc::mma_ss(tr + (c & 1) * TM_S1, qd + 2 * ks, kd + 2 * ks, id_qk, ks > 0);
           tc::mma_commit(&bars->s_ready[r][c & 1]);
-          if (it.kt == KT - 1) tc::mma_commit(&bars->q_empty[it.ui & 1]);
+          if (it.kt == unit_kt(it) - 1) tc::mma_commit(&bars->q_empty[it.ui & 1]);
         }
         __syncwarp();
         return true;
@@ -408,19 +433,19 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
             tc::mma_ts(tr + TM_O, tr + (c & 1) * TM_S1 + ks * 8, vd + SW * ks, id_pv,
                             (it.kt > 0 || ks > 0) ? 1u : 0u);
           tc::mma_commit(&bars->p_free[r][c & 1]);
-          if (it.kt % SPS == SPS - 1 || it.kt == KT - 1) tc::mma_commit(&bars->kv_empty[it.kvs]);
+          if (it.kt % SPS == SPS - 1 || it.kt == unit_kt(it) - 1) tc::mma_commit(&bars->kv_empty[it.kvs]);
         }
         __syncwarp();
         return true;
       };
       bool ok = true;
       SubIt itq{0, 0, 0, 0, 0, 0, 0}, itp{0, 0, 0, 0, 0, 0, 0};
-      for (; ok && itq.c < 2 && itq.c < total; advance<SPS, KV_STAGES>(itq, KT)) ok = qk(itq);
-      for (; ok && itp.c < total; advance<SPS, KV_STAGES>(itp, KT)) {
+      for (; ok && itq.c < 2 && itq.ui < my_units; advance<SPS, KV_STAGES>(itq, unit_kt(itq))) ok = qk(itq);
+      for (; ok && itp.ui < my_units; advance<SPS, KV_STAGES>(itp, unit_kt(itp))) {
         ok = pv(itp);
-        if (ok && itq.c < total) {
+        if (ok && itq.ui < my_units) {
           ok = qk(itq);
-          advance<SPS, KV_STAGES>(itq, KT);
+          advance<SPS, KV_STAGES>(itq, unit_kt(itq));
         }
       }
       if (elect_one()) tc::mma_commit(&bars->drain[r]);
@@ -520,7 +545,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       return true;
     };
     bool ok = true;
-    SoftIt its{0, 0, 0, 0};                         // this warp's sub-tile stream
+    SoftIt its{0, 0, 0};                            // this warp's sub-tile stream
     float l_prev = 0.f;
     for (int ui = 0; ok && ui < my_units; ++ui) {
       const bool uni = nx_any == 0u;
@@ -532,10 +557,12 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       float l_run = 0.f;
       // Warp-uniform unit state: whether any lane has a key-keeping query row.
       const bool unit_live = __any_sync(0xffffffffu, !uni);
-      for (int kt = 0; ok && kt < KT; ++kt, advance_soft(its, KT)) {
+      // The unit's key sub-tiles (KT until read after the first sub-tile's waits).
+      int KTu = KT;
+      for (int kt = 0; ok && kt < KTu; ++kt, advance_soft(its)) {
         const int c = its.c;
         const uint2 mb = nbits;
-        if (kt + 1 < KT) nbits = tc::ldg_nc_v2_early(mrow + 2 * (kt + 1));
+        if (kt + 1 < KTu) nbits = tc::ldg_nc_v2_early(mrow + 2 * (kt + 1));
         const int left = N - kt * BK;
         const uint32_t rl0 = real_bits(left, 0), rl1 = real_bits(left, 1);
         // Keys kept by this lane (query-key: its own query row; row-key: the
@@ -555,6 +582,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         if (!okk) okk = wait_or_abort_slow(&bars->b_full[its.bs], its.bph, ab);
         if (okk && !oks) oks = wait_or_abort_slow(&bars->s_ready[r][c & 1], (c >> 1) & 1, ab);
         if (!__all_sync(0xffffffffu, okk && oks)) { ok = false; break; }
+        if (kt == 0) KTu = *(volatile int*)&bars->unit_kt[ui & 7];
         const bool any_live = unit_live && tile_keys;
         tc::tc_fence_after();
         const uint32_t tsb = tb + (c & 1) * TM_S1;     // S(c), then P(c) over it
@@ -614,7 +642,7 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       pu = cu;
       cu = nu;
     }
-    if (ok && my_units > 0) finish_unit(pu, my_units * KT - 1, l_prev);
+    if (ok && my_units > 0) finish_unit(pu, its.c - 1, l_prev);
     if (lane == 0) tc::tma_store_wait_all<0>();
   }
 
@@ -708,22 +736,33 @@ bias_rows(const float* __restrict__ C, int N, int Nb, int ending, __half* __rest
 // One warp per mask row (b, r): bit k of word k/32 is pair_mask[b, r, k] != 0
 // for k < N (0 beyond, up to `words` words), and any[row] says whether the row
 // keeps some key.
+// Leading 64-key sub-tiles a mask row needs: through its last kept key (last,
+// -1 if none), or every sub-tile when it keeps none (its weights then spread
+// over all real keys).
+__device__ __forceinline__ int row_tiles(int last, int N) {
+  return last < 0 ? (N + BK - 1) / BK : last / BK + 1;
+}
+
 __global__ void mask_summary(const int32_t* __restrict__ mask, int N, long long rows, int words,
-                             uint32_t* __restrict__ bits, unsigned char* __restrict__ any) {
+                             uint32_t* __restrict__ bits, unsigned char* __restrict__ any,
+                             int* __restrict__ tiles) {
   pdl_trigger();
   pdl_wait();
   const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= rows) return;
   const int lane = threadIdx.x & 31;
-  unsigned found = 0;
+  int last = -1;
   for (int wd = 0; wd < words; ++wd) {
     const int k = wd * 32 + lane;
     const bool keep = k < N && mask[row * N + k] != 0;
     const unsigned w = __ballot_sync(0xffffffffu, keep);
-    found |= w;
+    if (w) last = wd * 32 + 31 - __clz(w);
     if (lane == 0) bits[row * words + wd] = w;
   }
-  if (lane == 0) any[row] = found != 0;
+  if (lane == 0) {
+    any[row] = last >= 0;
+    tiles[row] = row_tiles(last, N);
+  }
 }
 
 // Ending node: line (b, a) is column a of the mask (key k = grid row k). A
@@ -733,15 +772,15 @@ __global__ void mask_summary(const int32_t* __restrict__ mask, int N, long long 
 // and the block ORs them into the column's "keeps some key" flag.
 __global__ void __launch_bounds__(256)
 mask_summary_cols(const int32_t* __restrict__ mask, int N, int words, uint32_t* __restrict__ bits,
-                  unsigned char* __restrict__ any) {
-  __shared__ uint32_t found[8][32];
+                  unsigned char* __restrict__ any, int* __restrict__ tiles) {
+  __shared__ int found[8][32];
   pdl_trigger();
   pdl_wait();
   const int cblocks = (N + 31) >> 5;
   const long long b = blockIdx.x / cblocks;
   const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
   const int a = (int)(blockIdx.x % cblocks) * 32 + lane;
-  uint32_t acc = 0;
+  int last = -1;                       // last kept key among this warp's words
   if (a < N) {
     const int32_t* col = mask + b * N * N + a;
     for (int w = wp; w < words; w += 8) {
@@ -752,15 +791,16 @@ mask_summary_cols(const int32_t* __restrict__ mask, int N, int words, uint32_t* 
         if (k < N && col[(long long)k * N] != 0) word |= 1u << kk;
       }
       bits[(b * N + a) * words + w] = word;
-      acc |= word;
+      if (word) last = 32 * w + 31 - __clz(word);
     }
   }
-  found[wp][lane] = acc;
+  found[wp][lane] = last;
   __syncthreads();
   if (wp == 0 && a < N) {
 #pragma unroll
-    for (int i = 1; i < 8; ++i) acc |= found[i][lane];
-    any[b * N + a] = acc != 0;
+    for (int i = 1; i < 8; ++i) last = max(last, found[i][lane]);
+    any[b * N + a] = last >= 0;
+    tiles[b * N + a] = row_tiles(last, N);
   }
 }
 
@@ -804,13 +844,14 @@ cudaError_t k2_launch(int d, int grid, cudaStream_t s, bool pdl, const k2::Maps&
 }
 
 cudaError_t k2_mask_summary(const int32_t* mask, int B, int N, bool ending, int words,
-                            uint32_t* bits, unsigned char* any, cudaStream_t s, bool pdl) {
+                            uint32_t* bits, unsigned char* any, int* tiles, cudaStream_t s, bool pdl) {
   const long long rows = (long long)B * N;
   if (!ending)
     return launch_pdl(pdl, k2::mask_summary, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s, mask, N,
-                      rows, words, bits, any);
+                      rows, words, bits, any, tiles);
   const unsigned blocks = (unsigned)(B * (long long)((N + 31) / 32));
-  return launch_pdl(pdl, k2::mask_summary_cols, dim3(blocks), dim3(256), 0, s, mask, N, words, bits, any);
+  return launch_pdl(pdl, k2::mask_summary_cols, dim3(blocks), dim3(256), 0, s, mask, N, words, bits, any,
+                    tiles);
 }
 
 cudaError_t k2_bias_rows(const float* C, int B, int h, int N, int Nb, bool ending, __half* P,

@@ -60,6 +60,9 @@ struct Params {
   UnitStep step;                  // gridDim.x in unit digits
   const uint32_t* mbits;          // (B*N rows, words): bit k = pair_mask[b, r, k] != 0, k < N
   const unsigned char* row_any;   // (B*N rows): the mask row keeps some key
+  // (B*N rows): leading 64-key sub-tiles the row needs: up to its last kept
+  // key, or all of them when it keeps none (weight 1 on every real key)
+  const int* line_tiles;
   unsigned int* dev_err;
   long long polls;
   // The same q, k, v and bias plane as raw tensors, for the exact recomputation
@@ -136,7 +139,7 @@ int k2_keys_per_stage(int d);
 cudaError_t k2_launch(int d, int grid, cudaStream_t s, bool pdl, const k2::Maps& m,
                       const k2::Params& p);
 cudaError_t k2_mask_summary(const int32_t* mask, int B, int N, bool ending, int words,
-                            uint32_t* bits, unsigned char* any, cudaStream_t s, bool pdl);
+                            uint32_t* bits, unsigned char* any, int* tiles, cudaStream_t s, bool pdl);
 cudaError_t k2_bias_rows(const float* C, int B, int h, int N, int Nb, bool ending, __half* P,
                          cudaStream_t s, bool pdl);
 

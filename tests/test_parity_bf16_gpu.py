@@ -332,6 +332,32 @@ def test_bf16_value_weights_scaled_into_fp16_range(mode):
     H.assert_parity(w, got, O.forward(inp["x"], inp["pair_mask"], inp["params"], w.h, mode))
 
 
+@pytest.mark.parametrize("D,h", [(128, 4), (64, 1)])
+@pytest.mark.parametrize("mode", [0, 2, 1])
+def test_bf16_trailing_dropped_key_tiles(D, h, mode):
+    """Row-key reading: the attention skips the trailing 64-key sub-tiles that
+    every line of a work unit drops. Lines keep keys 0 .. e - 1 with e cycling
+    through tile edges and their neighbours, a line that keeps no key (weight
+    on every real key), and lines with holes, so that units mix lines needing
+    1 to 4 sub-tiles of N = 200 (and 1 to 2 of N = 100); the ending node reads
+    the same pattern along columns. The query-key reading (mode 1) takes every
+    sub-tile and is checked on the same mask."""
+    for B, N in ((2, 200), (1, 100)):
+        w = W.custom(B, N, D, h, "bf16", "bernoulli", seed=9700 + N + D + mode)
+        inp = W.make_inputs(w)
+        ext = [0, 1, 63, 64, 65, 127, 128, 129, 150, N, 7, 64]
+        keep = np.zeros((B, N, N), np.int32)
+        for b in range(B):
+            for i in range(N):
+                e = min(ext[(i + 5 * b) % len(ext)], N)
+                keep[b, i, :e] = 1
+                if i % 7 == 3 and e > 10:
+                    keep[b, i, 2:e:3] = 0           # holes inside the kept range
+        inp["pair_mask"] = keep.transpose(0, 2, 1).copy() if mode & tb.TRI_ATTN_ENDING_NODE else keep
+        got = H.run_forward(w, inp, mode)[0]
+        H.assert_parity(w, got, _oracle(inp, w, mode))
+
+
 # Every (D, h) the tensor-core kernels are built for: D in {32, 64, 128} and
 # d = D / h in {16, 32, 64} (R = 3 lines per attention unit for d = 16, 32;
 # R = 2 and 64-key K/V stages for d = 64).
