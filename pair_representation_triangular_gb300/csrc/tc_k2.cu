@@ -673,11 +673,14 @@ row_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
 // precise. A block takes 8 rows of one (b, t) plane, one warp per row, and
 // walks the keys 128 at a time (4 per lane), once for the row maximum and once
 // to write; for the ending node each step first moves a 128-key x 8-query
-// block of C (32 contiguous bytes per key) through shared memory. A row with
-// every key dropped stays -inf.
+// block of C (32 contiguous bytes per key) through shared memory. Rows of up
+// to 1024 keys are read once: every load of the row is issued before the
+// maximum is taken (the ending node's 8-query block moves through shared
+// memory whole). A row with every key dropped stays -inf.
+constexpr int kBiasRowChunks = 8;           // keys read in one pass: 8 x 128
 __global__ void __launch_bounds__(256)
 bias_rows(const float* __restrict__ C, int N, int Nb, int ending, __half* __restrict__ P) {
-  __shared__ float tile[8][132];
+  __shared__ float tile[8][kBiasRowChunks * 128 + 4];
   pdl_trigger();
   pdl_wait();
   const int a0 = blockIdx.x * 8;
@@ -686,6 +689,61 @@ bias_rows(const float* __restrict__ C, int N, int Nb, int ending, __half* __rest
   __half* Pp = P + plane * N * Nb;
   const int wq = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int a = a0 + wq;                          // this warp's row
+  // Writes keys k .. k + 3 of the row (entries v minus the row maximum m).
+  auto store4 = [&](int k, const float (&v)[4], float m) {
+    __half hv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) hv[e] = __float2half_rn(m == -INFINITY ? -INFINITY : v[e] - m);
+    if (k + 3 < N) {                              // 8-byte store: Nb and k are multiples of 4
+      *(uint2*)(Pp + (long long)a * Nb + k) = *(const uint2*)hv;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (k + e < N) Pp[(long long)a * Nb + k + e] = hv[e];
+    }
+  };
+  if (N <= kBiasRowChunks * 128) {
+    float v[kBiasRowChunks][4];
+    if (ending) {
+      // Thread i moves C[k][a0 + 4 (i & 1) .. + 3] for keys k = i / 2 + 128 c.
+      const int qa = 4 * (threadIdx.x & 1);
+#pragma unroll
+      for (int c = 0; c < kBiasRowChunks; ++c) {
+        const int kk = 128 * c + (threadIdx.x >> 1);
+        if (128 * c < N) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            tile[qa + e][kk] = (kk < N && a0 + qa + e < N) ? Cp[(long long)kk * N + a0 + qa + e] : -INFINITY;
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int c = 0; c < kBiasRowChunks; ++c)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          v[c][e] = 128 * c < N ? tile[wq][128 * c + 4 * lane + e] : -INFINITY;
+    } else {
+#pragma unroll
+      for (int c = 0; c < kBiasRowChunks; ++c)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int k = 128 * c + 4 * lane + e;
+          v[c][e] = (k < N && a < N) ? Cp[(long long)a * N + k] : -INFINITY;
+        }
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kBiasRowChunks; ++c)
+      m = fmaxf(fmaxf(m, fmaxf(v[c][0], v[c][1])), fmaxf(v[c][2], v[c][3]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (a < N) {
+#pragma unroll
+      for (int c = 0; c < kBiasRowChunks; ++c)
+        if (128 * c < N) store4(128 * c + 4 * lane, v[c], m);
+    }
+    return;
+  }
   float m = -INFINITY;
 #pragma unroll 1
   for (int pass = 0; pass < 2; ++pass) {
@@ -713,17 +771,7 @@ bias_rows(const float* __restrict__ C, int N, int Nb, int ending, __half* __rest
       if (pass == 0) {
         m = fmaxf(fmaxf(m, fmaxf(v[0], v[1])), fmaxf(v[2], v[3]));
       } else if (a < N) {
-        const int k = k0 + 4 * lane;
-        __half hv[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) hv[e] = __float2half_rn(m == -INFINITY ? -INFINITY : v[e] - m);
-        if (k + 3 < N) {                          // 8-byte store: Nb and k are multiples of 4
-          *(uint2*)(Pp + (long long)a * Nb + k) = *(const uint2*)hv;
-        } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (k + e < N) Pp[(long long)a * Nb + k + e] = hv[e];
-        }
+        store4(k0 + 4 * lane, v, m);
       }
     }
     if (pass == 0) {
@@ -733,9 +781,6 @@ bias_rows(const float* __restrict__ C, int N, int Nb, int ending, __half* __rest
   }
 }
 
-// One warp per mask row (b, r): bit k of word k/32 is pair_mask[b, r, k] != 0
-// for k < N (0 beyond, up to `words` words), and any[row] says whether the row
-// keeps some key.
 // Leading 64-key sub-tiles a mask row needs: through its last kept key (last,
 // -1 if none), or every sub-tile when it keeps none (its weights then spread
 // over all real keys).
@@ -743,6 +788,9 @@ __device__ __forceinline__ int row_tiles(int last, int N) {
   return last < 0 ? (N + BK - 1) / BK : last / BK + 1;
 }
 
+// One warp per mask row (b, r): bit k of word k/32 is pair_mask[b, r, k] != 0
+// for k < N (0 beyond, up to `words` words), any[row] says whether the row
+// keeps some key and tiles[row] how many leading sub-tiles it needs.
 __global__ void mask_summary(const int32_t* __restrict__ mask, int N, long long rows, int words,
                              uint32_t* __restrict__ bits, unsigned char* __restrict__ any,
                              int* __restrict__ tiles) {
