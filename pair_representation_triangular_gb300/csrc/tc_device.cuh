@@ -1,5 +1,5 @@
 // Device helpers shared by the bf16 tensor-core kernels: bounded waits with a
-// CTA-wide abort flag, special-function approximations, packed-fp16 adds and
+// CTA-wide abort flag, the gate's logistic function, packed-fp16 arithmetic and
 // swizzled shared-memory addressing.
 #pragma once
 
@@ -49,12 +49,6 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   tc::mbar_wait(bar, parity, 1ll << 40);
 }
 
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // Logistic function for the gate, 1/(1 + e^-z) = (1 + tanh(z/2)) / 2, with the
 // hardware tanh approximation (one special-function operation; its error is
 // well below the bf16 rounding the gate gets).
@@ -65,20 +59,6 @@ __device__ __forceinline__ float tanh_approx(float x) {
 }
 __device__ __forceinline__ float sigmoid_approx(float z) {
   return fmaf(0.5f, tanh_approx(0.5f * z), 0.5f);
-}
-
-// fp16 half of a packed pair plus an fp32 value, rounded once in fp32.
-__device__ __forceinline__ float add_f16lo_f32(uint32_t h2, float c) {
-  float d;
-  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, lo, %2;\n\t}"
-      : "=f"(d) : "r"(h2), "f"(c));
-  return d;
-}
-__device__ __forceinline__ float add_f16hi_f32(uint32_t h2, float c) {
-  float d;
-  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, hi, %2;\n\t}"
-      : "=f"(d) : "r"(h2), "f"(c));
-  return d;
 }
 
 // Packed fp16 arithmetic of the attention's softmax. cvt_f16x2: two fp32
