@@ -235,10 +235,11 @@ __device__ __noinline__ void exact_row(const __nv_bfloat16* qrow, const __nv_bfl
 
 // Persistent: CTA c serves work units unit0 + c, + G, ... A unit is (b, head
 // t, R lines, 128 queries), R = 3 (d = 16, 32) or 2 (d = 64, whose three
-// lines would not fit tensor memory); it streams 64-key sub-tiles. The K and
-// V tiles of the R lines arrive KVK keys at a time (128: one stage serves two
-// sub-tiles; 64 for d = 64, where shared memory is short); the fp16 bias
-// sub-tile they share has a ring of its own. Warpgroup 0: warp 0 TMA, warp
+// lines would not fit tensor memory); it streams 64-key sub-tiles, all of
+// them or, under the row-key reading, up to the last one that some line of the
+// unit keeps a key of. The K and V tiles of the R lines arrive one sub-tile per
+// stage, in a ring of four stages (two for d = 64, where shared memory is
+// short); the fp16 bias sub-tile they share has a ring of its own. Warpgroup 0: warp 0 TMA, warp
 // 1 + r issues the MMAs of line r (both roles run as whole warps; one elected
 // lane issues); warpgroup 1 + r runs the softmax of line r, with registers
 // moved to it from warpgroup 0 (setmaxnreg). Tensor memory per line: S0 | S1
