@@ -816,13 +816,15 @@ __global__ void mask_summary(const int32_t* __restrict__ mask, int N, long long 
 
 // Ending node: line (b, a) is column a of the mask (key k = grid row k). A
 // block takes 32 columns of one batch, lane = column a; warp wp forms the
-// words w = wp, wp + 8, ... (bit kk of word w: pair_mask[b, 32 w + kk, a] != 0,
+// words w = wp, wp + 32, ... (bit kk of word w: pair_mask[b, 32 w + kk, a] != 0,
 // each of its 32 loads one coalesced 128-byte row segment across the warp),
-// and the block ORs them into the column's "keeps some key" flag.
-__global__ void __launch_bounds__(256)
+// and the block combines the warps' last kept keys in shared memory. There are
+// few blocks (one per 32 columns), so each has 32 warps.
+constexpr int kMaskColWarps = 32;
+__global__ void __launch_bounds__(32 * kMaskColWarps)
 mask_summary_cols(const int32_t* __restrict__ mask, int N, int words, uint32_t* __restrict__ bits,
                   unsigned char* __restrict__ any, int* __restrict__ tiles) {
-  __shared__ int found[8][32];
+  __shared__ int found[kMaskColWarps][32];
   pdl_trigger();
   pdl_wait();
   const int cblocks = (N + 31) >> 5;
@@ -832,7 +834,7 @@ mask_summary_cols(const int32_t* __restrict__ mask, int N, int words, uint32_t* 
   int last = -1;                       // last kept key among this warp's words
   if (a < N) {
     const int32_t* col = mask + b * N * N + a;
-    for (int w = wp; w < words; w += 8) {
+    for (int w = wp; w < words; w += kMaskColWarps) {
       uint32_t word = 0;
 #pragma unroll
       for (int kk = 0; kk < 32; ++kk) {
@@ -847,7 +849,7 @@ mask_summary_cols(const int32_t* __restrict__ mask, int N, int words, uint32_t* 
   __syncthreads();
   if (wp == 0 && a < N) {
 #pragma unroll
-    for (int i = 1; i < 8; ++i) last = max(last, found[i][lane]);
+    for (int i = 1; i < kMaskColWarps; ++i) last = max(last, found[i][lane]);
     any[b * N + a] = last >= 0;
     tiles[b * N + a] = row_tiles(last, N);
   }
@@ -899,8 +901,8 @@ cudaError_t k2_mask_summary(const int32_t* mask, int B, int N, bool ending, int 
     return launch_pdl(pdl, k2::mask_summary, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s, mask, N,
                       rows, words, bits, any, tiles);
   const unsigned blocks = (unsigned)(B * (long long)((N + 31) / 32));
-  return launch_pdl(pdl, k2::mask_summary_cols, dim3(blocks), dim3(256), 0, s, mask, N, words, bits, any,
-                    tiles);
+  return launch_pdl(pdl, k2::mask_summary_cols, dim3(blocks), dim3(32 * k2::kMaskColWarps), 0, s, mask, N,
+                    words, bits, any, tiles);
 }
 
 cudaError_t k2_bias_rows(const float* C, int B, int h, int N, int Nb, bool ending, __half* P,
