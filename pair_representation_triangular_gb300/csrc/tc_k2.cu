@@ -789,26 +789,36 @@ __device__ __forceinline__ int row_tiles(int last, int N) {
   return last < 0 ? (N + BK - 1) / BK : last / BK + 1;
 }
 
-// One warp per mask row (b, r): bit k of word k/32 is pair_mask[b, r, k] != 0
-// for k < N (0 beyond, up to `words` words), any[row] says whether the row
-// keeps some key and tiles[row] how many leading sub-tiles it needs.
-__global__ void mask_summary(const int32_t* __restrict__ mask, int N, long long rows, int words,
-                             uint32_t* __restrict__ bits, unsigned char* __restrict__ any,
-                             int* __restrict__ tiles) {
+// Mask rows (b, r): bit k of word k/32 is pair_mask[b, r, k] != 0 for k < N
+// (0 beyond, up to `words` words), any[row] says whether the row keeps some key
+// and tiles[row] how many leading sub-tiles it needs. A block takes 8 rows with
+// 4 warps each (warp part p forms the words p, p + 4, ...); the parts' last
+// kept keys are combined in shared memory.
+constexpr int kMaskRowParts = 4;
+__global__ void __launch_bounds__(256 * kMaskRowParts)
+mask_summary(const int32_t* __restrict__ mask, int N, long long rows, int words,
+             uint32_t* __restrict__ bits, unsigned char* __restrict__ any, int* __restrict__ tiles) {
+  __shared__ int found[8][kMaskRowParts];
   pdl_trigger();
   pdl_wait();
-  const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (row >= rows) return;
-  const int lane = threadIdx.x & 31;
+  const int wp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rl = wp / kMaskRowParts, part = wp % kMaskRowParts;
+  const long long row = (long long)blockIdx.x * 8 + rl;
   int last = -1;
-  for (int wd = 0; wd < words; ++wd) {
-    const int k = wd * 32 + lane;
-    const bool keep = k < N && mask[row * N + k] != 0;
-    const unsigned w = __ballot_sync(0xffffffffu, keep);
-    if (w) last = wd * 32 + 31 - __clz(w);
-    if (lane == 0) bits[row * words + wd] = w;
+  if (row < rows) {
+    for (int wd = part; wd < words; wd += kMaskRowParts) {
+      const int k = wd * 32 + lane;
+      const bool keep = k < N && mask[row * N + k] != 0;
+      const unsigned w = __ballot_sync(0xffffffffu, keep);
+      if (w) last = wd * 32 + 31 - __clz(w);
+      if (lane == 0) bits[row * words + wd] = w;
+    }
   }
-  if (lane == 0) {
+  if (lane == 0) found[rl][part] = last;
+  __syncthreads();
+  if (part == 0 && lane == 0 && row < rows) {
+#pragma unroll
+    for (int i = 1; i < kMaskRowParts; ++i) last = max(last, found[rl][i]);
     any[row] = last >= 0;
     tiles[row] = row_tiles(last, N);
   }
@@ -898,8 +908,8 @@ cudaError_t k2_mask_summary(const int32_t* mask, int B, int N, bool ending, int 
                             uint32_t* bits, unsigned char* any, int* tiles, cudaStream_t s, bool pdl) {
   const long long rows = (long long)B * N;
   if (!ending)
-    return launch_pdl(pdl, k2::mask_summary, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s, mask, N,
-                      rows, words, bits, any, tiles);
+    return launch_pdl(pdl, k2::mask_summary, dim3((unsigned)((rows + 7) / 8)), dim3(256 * k2::kMaskRowParts),
+                      0, s, mask, N, rows, words, bits, any, tiles);
   const unsigned blocks = (unsigned)(B * (long long)((N + 31) / 32));
   return launch_pdl(pdl, k2::mask_summary_cols, dim3(blocks), dim3(32 * k2::kMaskColWarps), 0, s, mask, N,
                     words, bits, any, tiles);
